@@ -1,0 +1,38 @@
+"""torch.autograd.Function over the C ABI.
+
+Mirrors the wrapper on "Triton 05: Flash Attention", section torch.autograd.Function
+래핑: the forward saves q, k, v, o and the logsumexp (never S or P), the backward
+returns dq, dk, dv and None for the causal flag; sm_scale defaults to d ** -0.5.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import torch
+
+from . import binding
+
+
+class FlashAttentionFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, causal: bool = False, scale: Optional[float] = None):
+        scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
+        o, lse = binding.attn_fwd(q, k, v, causal=causal, scale=scale)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.causal = causal
+        ctx.scale = scale
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse = ctx.saved_tensors
+        dq, dk, dv = binding.attn_bwd(q, k, v, o, lse, do.contiguous(), causal=ctx.causal,
+                                      scale=ctx.scale)
+        return dq, dk, dv, None, None
+
+
+def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+              scale: Optional[float] = None) -> torch.Tensor:
+    """Differentiable exact attention over [B, H, N, d] fp16/bf16 CUDA tensors."""
+    return FlashAttentionFunction.apply(q, k, v, causal, scale)

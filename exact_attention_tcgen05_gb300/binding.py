@@ -1,0 +1,179 @@
+"""ctypes binding of libattn.so: argument marshalling only.
+
+Every function here checks that the tensors are what the C ABI expects (CUDA,
+contiguous, [B, H, N, d], one 16-bit dtype), allocates outputs with torch when the
+caller passes none, and calls the library on torch's current stream. All arithmetic
+runs in the library's kernels; there is no fallback of any kind: if the library is
+missing or fails, these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+from .build import LIB_PATH
+
+ATTN_OK = 0
+STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
+                3: "ATTN_ERR_CUDA", 4: "ATTN_ERR_TIMEOUT"}
+_DTYPE_CODES = {torch.float16: 0, torch.bfloat16: 1}
+
+# Public entry points declared in include/attn.h and their ctypes signatures.
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+SIGNATURES = {
+    "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I]),
+    "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_bwd_preprocess": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "attn_status_str": (ctypes.c_char_p, [_I]),
+    "attn_last_kernel_status": (_I, [_P, ctypes.POINTER(_I)]),
+}
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {STATUS_NAMES.get(code, code)}")
+        self.code = code
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libattn.so (once). Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -c \"import __graft_entry__ as g; "
+                f"g.build()\"` (nvcc, sm_103a). There is no fallback implementation.")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check(fn: str, code: int) -> None:
+    if code != ATTN_OK:
+        raise AttnError(fn, code)
+
+
+def _shape_of(x: torch.Tensor, name: str) -> tuple[int, int, int, int]:
+    if not isinstance(x, torch.Tensor) or x.dim() != 4:
+        raise ValueError(f"{name} must be a [B, H, N, d] tensor")
+    if not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not x.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if x.dtype not in _DTYPE_CODES:
+        raise ValueError(f"{name} must be float16 or bfloat16")
+    return tuple(x.shape)  # type: ignore[return-value]
+
+
+def _same(ref: torch.Tensor, x: torch.Tensor, name: str) -> None:
+    _shape_of(x, name)
+    if x.shape != ref.shape or x.dtype != ref.dtype or x.device != ref.device:
+        raise ValueError(f"{name} must match q in shape, dtype and device")
+
+
+def _lse_like(q: torch.Tensor, x: Optional[torch.Tensor], name: str) -> torch.Tensor:
+    B, H, N, _ = q.shape
+    if x is None:
+        return torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if x.shape != (B, H, N) or x.dtype != torch.float32 or not x.is_contiguous() \
+            or x.device != q.device:
+        raise ValueError(f"{name} must be a contiguous float32 [B, H, N] tensor on q's device")
+    return x
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+             scale: Optional[float] = None, o: Optional[torch.Tensor] = None,
+             lse: Optional[torch.Tensor] = None,
+             stream: Optional[torch.cuda.Stream] = None) -> tuple[torch.Tensor, torch.Tensor]:
+    """O = softmax(scale q k^T [causal]) v and the natural-log LSE, via libattn.so."""
+    B, H, N, d = _shape_of(q, "q")
+    _same(q, k, "k")
+    _same(q, v, "v")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if o is None:
+        o = torch.empty_like(q)
+    else:
+        _same(q, o, "o")
+    lse = _lse_like(q, lse, "lse")
+    with torch.cuda.device(q.device):
+        code = load().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               lse.data_ptr(), B, H, N, d, _DTYPE_CODES[q.dtype], int(causal),
+                               scale, _stream_handle(stream))
+    _check("attn_fwd", code)
+    return o, lse
+
+
+def attn_bwd_workspace_bytes(B: int, H: int, N: int) -> int:
+    return int(load().attn_bwd_workspace_bytes(B, H, N))
+
+
+def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+             lse: torch.Tensor, do: torch.Tensor, causal: bool = False,
+             scale: Optional[float] = None, dq: Optional[torch.Tensor] = None,
+             dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
+             workspace: Optional[torch.Tensor] = None,
+             stream: Optional[torch.cuda.Stream] = None
+             ) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """dq, dk, dv of sum(do * o), recomputing P from lse, via libattn.so."""
+    B, H, N, d = _shape_of(q, "q")
+    for name, x in (("k", k), ("v", v), ("o", o), ("do", do)):
+        _same(q, x, name)
+    lse = _lse_like(q, lse, "lse")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for name, x in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _same(q, x, name)
+    workspace = _lse_like(q, workspace, "workspace")
+    with torch.cuda.device(q.device):
+        code = load().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                               dv.data_ptr(), workspace.data_ptr(), B, H, N, d,
+                               _DTYPE_CODES[q.dtype], int(causal), scale,
+                               _stream_handle(stream))
+    _check("attn_bwd", code)
+    return dq, dk, dv
+
+
+def attn_bwd_preprocess(o: torch.Tensor, do: torch.Tensor,
+                        delta: Optional[torch.Tensor] = None,
+                        stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """delta = rowsum(do * o) in float32, via libattn.so."""
+    B, H, N, d = _shape_of(o, "o")
+    _same(o, do, "do")
+    delta = _lse_like(o, delta, "delta")
+    with torch.cuda.device(o.device):
+        code = load().attn_bwd_preprocess(o.data_ptr(), do.data_ptr(), delta.data_ptr(), B, H,
+                                          N, d, _DTYPE_CODES[o.dtype], _stream_handle(stream))
+    _check("attn_bwd_preprocess", code)
+    return delta
+
+
+def attn_last_kernel_status(stream: Optional[torch.cuda.Stream] = None) -> tuple[int, int]:
+    """(status, where): ATTN_ERR_TIMEOUT and the wait's code if a bounded wait ran out."""
+    where = ctypes.c_int(0)
+    code = load().attn_last_kernel_status(_stream_handle(stream), ctypes.byref(where))
+    return int(code), int(where.value)
+
+
+def status_str(code: int) -> str:
+    return load().attn_status_str(code).decode()

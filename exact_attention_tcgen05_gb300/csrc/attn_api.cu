@@ -1,0 +1,224 @@
+// attn_api.cu - the C ABI declared in include/attn.h: argument validation (host only,
+// before any CUDA call), TMA descriptor encoding and kernel launches on the caller's
+// stream. The library allocates no device memory and keeps no per-call state.
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "attn.h"
+#include "launch.h"
+
+namespace {
+
+using attn::Maps;
+using attn::Shape;
+
+constexpr int kMaxN = 1 << 20;
+constexpr long long kMaxBH = 65535;  // grid.y limit
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+  uintptr_t lo, hi;
+};
+Range range_of(const void* p, size_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return Range{a, a + bytes};
+}
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+attn_status check_shape(int B, int H, int N, int d, attn_dtype dtype) {
+  if (B < 1 || H < 1 || N < 1 || N > kMaxN) return ATTN_ERR_INVALID_ARG;
+  if ((long long)B * H > kMaxBH) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_FP16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+attn_status check_scale(float scale) {
+  return (std::isfinite(scale) && scale > 0.f) ? ATTN_OK : ATTN_ERR_INVALID_ARG;
+}
+
+unsigned long long wait_limit_cycles() {
+  static const unsigned long long v = [] {
+    const char* e = std::getenv("ATTN_WAIT_LIMIT_CYCLES");
+    if (e != nullptr) {
+      char* end = nullptr;
+      const unsigned long long x = std::strtoull(e, &end, 10);
+      if (end != e && x > 0) return x;
+    }
+    return 1ull << 31;  // about one second at the GB300's maximum SM clock
+  }();
+  return v;
+}
+
+// cuTensorMapEncodeTiled, fetched once through the runtime (no link against libcuda).
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn get_encode() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  });
+  return fn;
+}
+
+// [BH, N, d] 16-bit tensor, read as [64-column x 128-row] boxes with 128-byte swizzle;
+// rows past N read as zero.
+attn_status encode_map(CUtensorMap* m, const void* base, int BH, int N, int d, bool bf16) {
+  EncodeFn enc = get_encode();
+  if (enc == nullptr) return ATTN_ERR_CUDA;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * (cuuint64_t)d * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r =
+      enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+Shape make_shape(int B, int H, int N, int d, attn_dtype dtype, int causal, float scale) {
+  Shape s;
+  s.BH = B * H;
+  s.N = N;
+  s.d = d;
+  s.bf16 = dtype == ATTN_BF16;
+  s.causal = causal != 0;
+  s.scale = scale;
+  s.wait_limit = wait_limit_cycles();
+  return s;
+}
+
+attn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_status_str(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+  }
+  return "ATTN_ERR_UNKNOWN";
+}
+
+size_t attn_bwd_workspace_bytes(int B, int H, int N) {
+  if (B <= 0 || H <= 0 || N <= 0) return 0;
+  return (size_t)4 * (size_t)B * (size_t)H * (size_t)N;
+}
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int N, int d, attn_dtype dtype, int causal, float scale,
+                     void* cuda_stream) {
+  attn_status st = check_shape(B, H, N, d, dtype);
+  if (st != ATTN_OK) return st;
+  if ((st = check_scale(scale)) != ATTN_OK) return st;
+  const void* ptrs[5] = {q, k, v, o, lse};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return ATTN_ERR_INVALID_ARG;
+  const size_t tb = (size_t)B * H * N * d * 2;
+  const size_t lb = (size_t)B * H * N * 4;
+  const Range rq = range_of(q, tb), rk = range_of(k, tb), rv = range_of(v, tb);
+  const Range ro = range_of(o, tb), rl = range_of(lse, lb);
+  for (Range out : {ro, rl})
+    for (Range in : {rq, rk, rv})
+      if (overlap(out, in)) return ATTN_ERR_INVALID_ARG;
+  if (overlap(ro, rl)) return ATTN_ERR_INVALID_ARG;
+
+  const Shape s = make_shape(B, H, N, d, dtype, causal, scale);
+  Maps m;
+  if ((st = encode_map(&m.q, q, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
+  if ((st = encode_map(&m.k, k, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
+  if ((st = encode_map(&m.v, v, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
+  m.d_o = m.v;
+  return from_cuda(attn::launch_fwd(m, s, o, lse, static_cast<cudaStream_t>(cuda_stream)));
+}
+
+attn_status attn_bwd_preprocess(const void* o, const void* dO, float* delta, int B, int H,
+                                int N, int d, attn_dtype dtype, void* cuda_stream) {
+  attn_status st = check_shape(B, H, N, d, dtype);
+  if (st != ATTN_OK) return st;
+  const void* ptrs[3] = {o, dO, delta};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return ATTN_ERR_INVALID_ARG;
+  const size_t tb = (size_t)B * H * N * d * 2;
+  const Range rd = range_of(delta, (size_t)B * H * N * 4);
+  if (overlap(rd, range_of(o, tb)) || overlap(rd, range_of(dO, tb))) return ATTN_ERR_INVALID_ARG;
+  const Shape s = make_shape(B, H, N, d, dtype, 0, 1.f);
+  return from_cuda(attn::launch_delta(s, o, dO, delta, static_cast<cudaStream_t>(cuda_stream)));
+}
+
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                     void* workspace, int B, int H, int N, int d, attn_dtype dtype, int causal,
+                     float scale, void* cuda_stream) {
+  attn_status st = check_shape(B, H, N, d, dtype);
+  if (st != ATTN_OK) return st;
+  if ((st = check_scale(scale)) != ATTN_OK) return st;
+  const void* ptrs[10] = {q, k, v, o, lse, dO, dq, dk, dv, workspace};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return ATTN_ERR_INVALID_ARG;
+  const size_t tb = (size_t)B * H * N * d * 2;
+  const size_t lb = (size_t)B * H * N * 4;
+  const Range ins[6] = {range_of(q, tb), range_of(k, tb), range_of(v, tb),
+                        range_of(o, tb), range_of(lse, lb), range_of(dO, tb)};
+  const Range outs[4] = {range_of(dq, tb), range_of(dk, tb), range_of(dv, tb),
+                         range_of(workspace, lb)};
+  for (int a = 0; a < 4; ++a) {
+    for (const Range& in : ins)
+      if (overlap(outs[a], in)) return ATTN_ERR_INVALID_ARG;
+    for (int b = a + 1; b < 4; ++b)
+      if (overlap(outs[a], outs[b])) return ATTN_ERR_INVALID_ARG;
+  }
+
+  const Shape s = make_shape(B, H, N, d, dtype, causal, scale);
+  Maps m;
+  if ((st = encode_map(&m.q, q, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
+  if ((st = encode_map(&m.k, k, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
+  if ((st = encode_map(&m.v, v, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
+  if ((st = encode_map(&m.d_o, dO, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(cuda_stream);
+  float* delta = static_cast<float*>(workspace);
+  cudaError_t e = attn::launch_delta(s, o, dO, delta, cs);
+  if (e == cudaSuccess) e = attn::launch_dkv(m, s, lse, delta, dk, dv, cs);
+  if (e == cudaSuccess) e = attn::launch_dq(m, s, lse, delta, dq, cs);
+  return from_cuda(e);
+}
+
+attn_status attn_last_kernel_status(void* cuda_stream, int* where) {
+  cudaStream_t cs = static_cast<cudaStream_t>(cuda_stream);
+  int first = 0;
+  using Reader = int (*)(cudaStream_t, cudaError_t*);
+  const Reader readers[4] = {attn::status_fwd, attn::status_delta, attn::status_dq,
+                             attn::status_dkv};
+  for (Reader r : readers) {
+    cudaError_t e = cudaSuccess;
+    const int w = r(cs, &e);
+    if (e != cudaSuccess) return ATTN_ERR_CUDA;
+    if (first == 0 && w != 0) first = w;
+  }
+  if (where != nullptr) *where = first;
+  return first == 0 ? ATTN_OK : ATTN_ERR_TIMEOUT;
+}
+
+}  // extern "C"

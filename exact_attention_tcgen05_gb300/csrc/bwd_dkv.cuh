@@ -1,0 +1,310 @@
+// bwd_dkv.cuh - backward, dK/dV kernel: the grid runs over blocks of 128 keys; each CTA
+// owns dK_j and dV_j, keeps K_j and V_j on chip and streams every query block that sees
+// them ("Triton 05: Flash Attention", section 3단계 커널 구조, [2단계] dKV 커널: K_j, V_j
+// fixed in SRAM, loop over all Q_i; no atomics because each CTA owns its outputs).
+//
+// It works in the transposed orientation so that the key index runs down the tensor
+// memory lanes: per query block i
+//   S^T = scale K_j Q_i^T,  P^T = exp(S^T - L_i),  dV_j += P^T dO_i,
+//   dP^T = V_j dO_i^T,      dS^T = P^T * (dP^T - D_i),  dK_j += scale * dS^T Q_i.
+// P^T and dS^T are written back over S^T and dP^T as 16-bit pairs and used as the A
+// operand of the two accumulating products straight from tensor memory.
+// Tensor memory: S^T (128 cols), dP^T (128), dV (d), dK (d).
+#pragma once
+
+#include "bwd_dq.cuh"
+
+namespace attn {
+
+template <int D>
+struct DkvCfg : BwdCfg<D> {
+  using B = BwdCfg<D>;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + B::kTileBytes;
+  static constexpr int kOffQ = kOffV + B::kTileBytes;
+  static constexpr int kOffDO = kOffQ + B::kStages * B::kTileBytes;
+  static constexpr int kOffStats = kOffDO + B::kStages * B::kTileBytes;  // 2 x (128 + 128) f32
+  static constexpr int kOffBar = kOffStats + 2 * 256 * 4;
+  // kv_full, q_full[S], do_full[S], qdo_empty[S], s_full, p_full, dp_full, ds_full,
+  // acc_done, drain, stats_ready[2]
+  static constexpr int kNumBars = 1 + 3 * B::kStages + 8;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes =
+      (kOffMisc + 16 + 1024) > B::kMinSmem ? (kOffMisc + 16 + 1024) : B::kMinSmem;
+};
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(192, 1)
+    attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q,
+                        const __grid_constant__ CUtensorMap map_k,
+                        const __grid_constant__ CUtensorMap map_v,
+                        const __grid_constant__ CUtensorMap map_do, const BwdParams p) {
+  using C = DkvCfg<D>;
+  constexpr int NS = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* kv_full = bars;
+  uint64_t* q_full = bars + 1;
+  uint64_t* do_full = q_full + NS;
+  uint64_t* qdo_empty = do_full + NS;
+  uint64_t* s_full = qdo_empty + NS;
+  uint64_t* p_full = s_full + 1;
+  uint64_t* dp_full = p_full + 1;
+  uint64_t* ds_full = dp_full + 1;
+  uint64_t* acc_done = ds_full + 1;
+  uint64_t* drain = acc_done + 1;
+  uint64_t* stats_ready = drain + 1;  // [2], one per statistics buffer
+  float* stats = reinterpret_cast<float*>(smem + C::kOffStats);  // [2][-L*log2e x128, D x128]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+  const int bh = blockIdx.y;
+  const int jb = blockIdx.x;  // causal: block 0 sees the most query blocks, so runs first
+  const int j0 = jb * kTileN;
+  const int N = p.N;
+  const int i_first = p.causal ? jb : 0;
+  const int n = p.nb - i_first;  // query blocks i_first .. nb-1
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&do_full[s], 1);
+      mbar_init(&qdo_empty[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(dp_full, 1);
+    mbar_init(ds_full, 128);
+    mbar_init(acc_done, 1);
+    mbar_init(drain, 1);
+    mbar_init(&stats_ready[0], 128);
+    mbar_init(&stats_ready[1], 128);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_holder, C::kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint64_t limit = p.wait_limit;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      tma_prefetch_map(&map_q);
+      tma_prefetch_map(&map_k);
+      tma_prefetch_map(&map_v);
+      tma_prefetch_map(&map_do);
+      mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
+      for (int c = 0; c < C::kChunks; ++c) {
+        tma_load_3d(smem + C::kOffK + c * kBoxBytes, &map_k, kv_full, c * kBoxCols, j0, bh);
+        tma_load_3d(smem + C::kOffV + c * kBoxBytes, &map_v, kv_full, c * kBoxCols, j0, bh);
+      }
+      int issued = 0;
+      for (int it = 0; it < n; ++it) {
+        const int s = it % NS;
+        const int i = i_first + it;
+        if (it >= NS &&
+            !mbar_wait(&qdo_empty[s], ((it / NS) - 1) & 1, limit, abort_flag, kWaitDkvEmpty))
+          break;
+        mbar_arrive_expect_tx(&q_full[s], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(smem + C::kOffQ + s * C::kTileBytes + c * kBoxBytes, &map_q, &q_full[s],
+                      c * kBoxCols, i * kTileM, bh);
+        mbar_arrive_expect_tx(&do_full[s], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(smem + C::kOffDO + s * C::kTileBytes + c * kBoxBytes, &map_do,
+                      &do_full[s], c * kBoxCols, i * kTileM, bh);
+        issued = it + 1;
+      }
+      if (*abort_flag) {
+        mbar_wait(kv_full, 0, limit, nullptr, kWaitDkvDrain);
+        for (int it = max(0, issued - NS); it < issued; ++it) {
+          mbar_wait(&q_full[it % NS], (it / NS) & 1, limit, nullptr, kWaitDkvDrain);
+          mbar_wait(&do_full[it % NS], (it / NS) & 1, limit, nullptr, kWaitDkvDrain);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      const uint32_t idesc_st = make_idesc(BF16, 128, kTileM, false, false);
+      const uint32_t idesc_acc = make_idesc(BF16, 128, D, false, true);
+      const uint32_t sk = smem_u32(smem + C::kOffK);
+      const uint32_t sv = smem_u32(smem + C::kOffV);
+      const uint32_t sq = smem_u32(smem + C::kOffQ);
+      const uint32_t sdo = smem_u32(smem + C::kOffDO);
+      bool ok = mbar_wait(kv_full, 0, limit, abort_flag, kWaitDkvKV) &&
+                mbar_wait(&q_full[0], 0, limit, abort_flag, kWaitDkvQ);
+      if (ok) {
+        tc_fence_after();
+        issue_rowdot<D>(tmem + C::kColS, sk, sq, idesc_st);
+        mma_commit(s_full);
+        ok = mbar_wait(&do_full[0], 0, limit, abort_flag, kWaitDkvDO);
+      }
+      if (ok) {
+        tc_fence_after();
+        issue_rowdot<D>(tmem + C::kColDP, sv, sdo, idesc_st);
+        mma_commit(dp_full);
+      }
+      for (int it = 0; ok && it < n; ++it) {
+        const int s = it % NS;
+        const int in = it + 1;
+        const int sn = in % NS;
+        if (!(ok = mbar_wait(p_full, it & 1, limit, abort_flag, kWaitDkvP))) break;
+        tc_fence_after();
+        // dV_j += P^T dO_i
+        issue_tmem_a(tmem + C::kColAcc0, tmem + C::kColS, sdo + s * C::kTileBytes, idesc_acc,
+                     it > 0);
+        if (in < n) {
+          if (!(ok = mbar_wait(&q_full[sn], (in / NS) & 1, limit, abort_flag, kWaitDkvQ))) break;
+          tc_fence_after();
+          issue_rowdot<D>(tmem + C::kColS, sk, sq + sn * C::kTileBytes, idesc_st);
+          mma_commit(s_full);
+        }
+        if (!(ok = mbar_wait(ds_full, it & 1, limit, abort_flag, kWaitDkvDS))) break;
+        tc_fence_after();
+        // dK_j += dS^T Q_i
+        issue_tmem_a(tmem + C::kColAcc1, tmem + C::kColDP, sq + s * C::kTileBytes, idesc_acc,
+                     it > 0);
+        if (in < n) {
+          if (!(ok = mbar_wait(&do_full[sn], (in / NS) & 1, limit, abort_flag, kWaitDkvDO)))
+            break;
+          tc_fence_after();
+          issue_rowdot<D>(tmem + C::kColDP, sv, sdo + sn * C::kTileBytes, idesc_st);
+          mma_commit(dp_full);
+        }
+        mma_commit(&qdo_empty[s]);
+      }
+      if (ok) mma_commit(acc_done);
+      mma_commit(drain);
+      mbar_wait(drain, 0, limit, nullptr, kWaitDkvDrain);
+    }
+  } else {
+    // warps 0-3: one thread per key row
+    const int wq = warp;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + C::kColS;
+    const uint32_t t_dp = tmem + lane_base + C::kColDP;
+    const int tid = threadIdx.x;        // 0..127
+    const int key = j0 + tid;           // key index of this thread
+    const float sl2 = p.scale_log2;
+    const float* lse_bh = p.lse + (size_t)bh * N;
+    const float* dl_bh = p.delta + (size_t)bh * N;
+    // Prefetch the statistics of the first query block.
+    auto load_stats = [&](int i, float& nl2, float& dl) {
+      const int q = i * kTileM + tid;
+      nl2 = -INFINITY;
+      dl = 0.f;
+      if (q < N) {
+        nl2 = -lse_bh[q] * kLog2e;
+        dl = dl_bh[q];
+      }
+    };
+    float nl2_next, dl_next;
+    load_stats(i_first, nl2_next, dl_next);
+    bool ok = true;
+    for (int it = 0; it < n; ++it) {
+      const int i = i_first + it;
+      // Double-buffered statistics: buffer it&1 was last read in iteration it-2, and
+      // every thread has passed iteration it-1's stats_ready wait, which needs all 128
+      // arrivals, so nobody still reads it.
+      float* st = stats + (it & 1) * 256;
+      st[tid] = nl2_next;
+      st[128 + tid] = dl_next;
+      mbar_arrive(&stats_ready[it & 1]);
+      if (it + 1 < n) load_stats(i + 1, nl2_next, dl_next);
+      if (!(ok = warp_wait(&stats_ready[it & 1], (it >> 1) & 1, limit, abort_flag,
+                           kWaitDkvStats)))
+        break;
+
+      if (!(ok = warp_wait(s_full, it & 1, limit, abort_flag, kWaitDkvS))) break;
+      tc_fence_after();
+      float pr[kTileM];
+#pragma unroll
+      for (int c4 = 0; c4 < kTileM / 32; ++c4) {
+        uint32_t r[32];
+        tmem_ld32(t_s + c4 * 32, r);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pr[c4 * 32 + c] = __uint_as_float(r[c]);
+      }
+      // Causal: on the diagonal block query q = i*128 + c sees this key iff q >= key.
+      const int lo = (p.causal && i == jb) ? (key - i * kTileM) : 0;  // first visible c
+      const float4* nl4 = reinterpret_cast<const float4*>(st);
+#pragma unroll
+      for (int c4 = 0; c4 < kTileM / 4; ++c4) {
+        const float4 nl = nl4[c4];
+        const float nlv[4] = {nl.x, nl.y, nl.z, nl.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = c4 * 4 + u;
+          pr[c] = (c < lo) ? 0.f : ex2(fmaf(pr[c], sl2, nlv[u]));
+        }
+      }
+#pragma unroll
+      for (int c4 = 0; c4 < kTileM / 32; ++c4) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) pk[u] = pack2<BF16>(pr[c4 * 32 + 2 * u], pr[c4 * 32 + 2 * u + 1]);
+        tmem_st16(t_s + c4 * 16, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(p_full);
+
+      if (!(ok = warp_wait(dp_full, it & 1, limit, abort_flag, kWaitDkvDP))) break;
+      tc_fence_after();
+      const float4* dl4 = reinterpret_cast<const float4*>(st + 128);
+#pragma unroll
+      for (int c4 = 0; c4 < kTileM / 32; ++c4) {
+        uint32_t r[32];
+        tmem_ld32(t_dp + c4 * 32, r);
+        uint32_t pk[16];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float4 dl = dl4[c4 * 8 + u];
+          const int c = c4 * 32 + 4 * u;
+          const float d0 = pr[c + 0] * (__uint_as_float(r[4 * u + 0]) - dl.x);
+          const float d1 = pr[c + 1] * (__uint_as_float(r[4 * u + 1]) - dl.y);
+          const float d2 = pr[c + 2] * (__uint_as_float(r[4 * u + 2]) - dl.z);
+          const float d3 = pr[c + 3] * (__uint_as_float(r[4 * u + 3]) - dl.w);
+          pk[2 * u] = pack2<BF16>(d0, d1);
+          pk[2 * u + 1] = pack2<BF16>(d2, d3);
+        }
+        tmem_st16(t_dp + c4 * 16, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(ds_full);
+    }
+    if (ok && warp_wait(acc_done, 0, limit, abort_flag, kWaitDkvDone)) {
+      tc_fence_after();
+      const size_t off = ((size_t)bh * N + key) * (size_t)(D * 2);
+      uint8_t* dk_row = reinterpret_cast<uint8_t*>(p.out0) + off;
+      uint8_t* dv_row = reinterpret_cast<uint8_t*>(p.out1) + off;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_base + C::kColAcc0 + cc * 32, r);
+        if (key < N) store_row32<BF16>(dv_row + cc * 64, r, 1.f);
+        tmem_ld32(tmem + lane_base + C::kColAcc1 + cc * 32, r);
+        if (key < N) store_row32<BF16>(dk_row + cc * 64, r, p.scale);
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace attn

@@ -1,0 +1,314 @@
+// bwd_dq.cuh - backward, dQ kernel: the grid runs over blocks of 128 query rows; each
+// CTA owns dQ_i, streams every visible block of keys/values and accumulates
+//   S = scale Q_i K_j^T, P = exp(S - L_i), dP = dO_i V_j^T, dS = P * (dP - D_i),
+//   dQ_i += scale * dS K_j
+// with no atomics ("Triton 05: Flash Attention", section 3단계 커널 구조, [3단계] dQ
+// 커널: Q_i held on chip, loop over K_j, V_j; sections LSE로 P 재계산 and Softmax
+// Gradient for the recomputation and the gradient). D_i comes from the preprocess
+// kernel. The factor scale on dQ follows from S = scale Q K^T.
+//
+// GB300 design: warps 0-3 turn S / dP (fp32 in tensor memory) into dS, warp 4 is the TMA
+// producer (Q_i and dO_i once, then a ring of K_j / V_j blocks), warp 5 issues the
+// tcgen05 MMAs. Tensor memory: S (128 cols), dP (128 cols), dQ accumulator (d cols).
+// dS is written back over dP as 16-bit pairs and feeds dS K_j from tensor memory; S of
+// the next block is computed while the softmax warps work on dP of this one.
+#pragma once
+
+#include "common.cuh"
+
+namespace attn {
+
+struct BwdParams {
+  const float* lse;    // [BH, N] natural-log L
+  const float* delta;  // [BH, N] D
+  void* out0;          // dQ (dQ kernel) or dK (dKV kernel)
+  void* out1;          // dV (dKV kernel)
+  int N;
+  int nb;              // number of 128-row blocks
+  int causal;
+  float scale;
+  float scale_log2;    // scale * log2(e)
+  unsigned long long wait_limit;
+};
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kChunks = D / kBoxCols;
+  static constexpr int kTileBytes = kChunks * kBoxBytes;
+  static constexpr int kStages = 2;
+  static constexpr int kThreads = 192;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
+  // Each CTA takes all 512 tensor-memory columns, so at most one may be resident per SM:
+  // shared memory is padded past half of the SM's 228 KiB to guarantee that.
+  static constexpr int kMinSmem = 120 * 1024;
+};
+
+template <int D>
+struct DqCfg : BwdCfg<D> {
+  using B = BwdCfg<D>;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffDO = kOffQ + B::kTileBytes;
+  static constexpr int kOffK = kOffDO + B::kTileBytes;
+  static constexpr int kOffV = kOffK + B::kStages * B::kTileBytes;
+  static constexpr int kOffBar = kOffV + B::kStages * B::kTileBytes;
+  // qdo_full, k_full[S], v_full[S], kv_empty[S], s_full, s_free, dp_full, ds_full,
+  // acc_done, drain
+  static constexpr int kNumBars = 1 + 3 * B::kStages + 6;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes =
+      (kOffMisc + 16 + 1024) > B::kMinSmem ? (kOffMisc + 16 + 1024) : B::kMinSmem;
+};
+
+// Writes 32 fp32 accumulator values, multiplied by `mul`, as 16-bit to a global row.
+template <bool BF16>
+__device__ __forceinline__ void store_row32(uint8_t* dst, const uint32_t (&r)[32], float mul) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    pk[i] = pack2<BF16>(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+}
+
+// K-major x K-major product over the head dimension: D[128 x 128] = A[128 x d] B[128 x d]^T.
+template <int D>
+__device__ __forceinline__ void issue_rowdot(uint32_t d_tmem, uint32_t a0, uint32_t b0,
+                                             uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+    mma_ss(d_tmem, make_sdesc_sw128(a0 + off, 16, 1024), make_sdesc_sw128(b0 + off, 16, 1024),
+           idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// Tensor-memory A [128 x 128] (16-bit pairs) times an MN-major [128 x d] tile in shared
+// memory: D[128 x d] (+)= A B.
+__device__ __forceinline__ void issue_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint32_t b0,
+                                             uint32_t idesc, bool acc) {
+#pragma unroll
+  for (int kk = 0; kk < 128 / 16; ++kk)
+    mma_ts(d_tmem, a_tmem + kk * 8, make_sdesc_sw128(b0 + kk * 2048, kBoxBytes, 1024), idesc,
+           (acc || kk > 0) ? 1u : 0u);
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(192, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q,
+                       const __grid_constant__ CUtensorMap map_k,
+                       const __grid_constant__ CUtensorMap map_v,
+                       const __grid_constant__ CUtensorMap map_do, const BwdParams p) {
+  using C = DqCfg<D>;
+  constexpr int NS = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* qdo_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* v_full = k_full + NS;
+  uint64_t* kv_empty = v_full + NS;
+  uint64_t* s_full = kv_empty + NS;
+  uint64_t* s_free = s_full + 1;
+  uint64_t* dp_full = s_free + 1;
+  uint64_t* ds_full = dp_full + 1;
+  uint64_t* acc_done = ds_full + 1;
+  uint64_t* drain = acc_done + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+  const int bh = blockIdx.y;
+  const int ib = p.causal ? (p.nb - 1 - blockIdx.x) : blockIdx.x;  // longest first
+  const int i0 = ib * kTileM;
+  const int N = p.N;
+  const int n = p.causal ? ib + 1 : p.nb;  // key blocks 0 .. n-1
+
+  if (threadIdx.x == 0) {
+    mbar_init(qdo_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 128);
+    mbar_init(dp_full, 1);
+    mbar_init(ds_full, 128);
+    mbar_init(acc_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_holder, C::kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint64_t limit = p.wait_limit;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      tma_prefetch_map(&map_q);
+      tma_prefetch_map(&map_k);
+      tma_prefetch_map(&map_v);
+      tma_prefetch_map(&map_do);
+      mbar_arrive_expect_tx(qdo_full, 2 * C::kTileBytes);
+      for (int c = 0; c < C::kChunks; ++c) {
+        tma_load_3d(smem + C::kOffQ + c * kBoxBytes, &map_q, qdo_full, c * kBoxCols, i0, bh);
+        tma_load_3d(smem + C::kOffDO + c * kBoxBytes, &map_do, qdo_full, c * kBoxCols, i0, bh);
+      }
+      int issued = 0;
+      for (int j = 0; j < n; ++j) {
+        const int s = j % NS;
+        if (j >= NS &&
+            !mbar_wait(&kv_empty[s], ((j / NS) - 1) & 1, limit, abort_flag, kWaitDqEmpty))
+          break;
+        mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(smem + C::kOffK + s * C::kTileBytes + c * kBoxBytes, &map_k, &k_full[s],
+                      c * kBoxCols, j * kTileN, bh);
+        mbar_arrive_expect_tx(&v_full[s], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(smem + C::kOffV + s * C::kTileBytes + c * kBoxBytes, &map_v, &v_full[s],
+                      c * kBoxCols, j * kTileN, bh);
+        issued = j + 1;
+      }
+      if (*abort_flag) {
+        mbar_wait(qdo_full, 0, limit, nullptr, kWaitDqDrain);
+        for (int j = max(0, issued - NS); j < issued; ++j) {
+          mbar_wait(&k_full[j % NS], (j / NS) & 1, limit, nullptr, kWaitDqDrain);
+          mbar_wait(&v_full[j % NS], (j / NS) & 1, limit, nullptr, kWaitDqDrain);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      const uint32_t idesc_sq = make_idesc(BF16, 128, kTileN, false, false);
+      const uint32_t idesc_acc = make_idesc(BF16, 128, D, false, true);
+      const uint32_t sq = smem_u32(smem + C::kOffQ);
+      const uint32_t sdo = smem_u32(smem + C::kOffDO);
+      const uint32_t sk = smem_u32(smem + C::kOffK);
+      const uint32_t sv = smem_u32(smem + C::kOffV);
+      bool ok = mbar_wait(qdo_full, 0, limit, abort_flag, kWaitDqQ) &&
+                mbar_wait(&k_full[0], 0, limit, abort_flag, kWaitDqK);
+      if (ok) {
+        tc_fence_after();
+        issue_rowdot<D>(tmem + C::kColS, sq, sk, idesc_sq);
+        mma_commit(s_full);
+        ok = mbar_wait(&v_full[0], 0, limit, abort_flag, kWaitDqV);
+      }
+      if (ok) {
+        tc_fence_after();
+        issue_rowdot<D>(tmem + C::kColDP, sdo, sv, idesc_sq);
+        mma_commit(dp_full);
+      }
+      for (int j = 0; ok && j < n; ++j) {
+        const int s = j % NS;
+        const int jn = j + 1;
+        const int sn = jn % NS;
+        if (jn < n) {
+          if (!(ok = mbar_wait(&k_full[sn], (jn / NS) & 1, limit, abort_flag, kWaitDqK) &&
+                     mbar_wait(s_free, j & 1, limit, abort_flag, kWaitDqSC)))
+            break;
+          tc_fence_after();
+          issue_rowdot<D>(tmem + C::kColS, sq, sk + sn * C::kTileBytes, idesc_sq);
+          mma_commit(s_full);
+        }
+        if (!(ok = mbar_wait(ds_full, j & 1, limit, abort_flag, kWaitDqDS))) break;
+        tc_fence_after();
+        issue_tmem_a(tmem + C::kColAcc0, tmem + C::kColDP, sk + s * C::kTileBytes, idesc_acc,
+                     j > 0);
+        if (jn < n) {
+          if (!(ok = mbar_wait(&v_full[sn], (jn / NS) & 1, limit, abort_flag, kWaitDqV))) break;
+          tc_fence_after();
+          issue_rowdot<D>(tmem + C::kColDP, sdo, sv + sn * C::kTileBytes, idesc_sq);
+          mma_commit(dp_full);
+        }
+        mma_commit(&kv_empty[s]);
+      }
+      if (ok) mma_commit(acc_done);
+      mma_commit(drain);
+      mbar_wait(drain, 0, limit, nullptr, kWaitDqDrain);
+    }
+  } else {
+    // warps 0-3: one thread per query row
+    const int wq = warp;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + C::kColS;
+    const uint32_t t_dp = tmem + lane_base + C::kColDP;
+    const uint32_t t_acc = tmem + lane_base + C::kColAcc0;
+    const int row = i0 + wq * 32 + lane;
+    const float sl2 = p.scale_log2;
+    float neg_l2 = -INFINITY;  // -L * log2(e); rows past N get P = 0
+    float dlt = 0.f;
+    if (row < N) {
+      neg_l2 = -p.lse[(size_t)bh * N + row] * kLog2e;
+      dlt = p.delta[(size_t)bh * N + row];
+    }
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      if (!(ok = warp_wait(s_full, j & 1, limit, abort_flag, kWaitDqS))) break;
+      tc_fence_after();
+      float pr[kTileN];
+#pragma unroll
+      for (int c4 = 0; c4 < kTileN / 32; ++c4) {
+        uint32_t r[32];
+        tmem_ld32(t_s + c4 * 32, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pr[c4 * 32 + i] = __uint_as_float(r[i]);
+      }
+      tc_fence_before();
+      mbar_arrive(s_free);
+      const int kbase = j * kTileN;
+      int lim = kTileN - 1;
+      if (kbase + kTileN > N) lim = N - 1 - kbase;
+      if (p.causal && kbase + kTileN - 1 > i0) lim = min(lim, row - kbase);
+#pragma unroll
+      for (int c = 0; c < kTileN; ++c)
+        pr[c] = (c > lim) ? 0.f : ex2(fmaf(pr[c], sl2, neg_l2));
+      if (!(ok = warp_wait(dp_full, j & 1, limit, abort_flag, kWaitDqDP))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c4 = 0; c4 < kTileN / 32; ++c4) {
+        uint32_t r[32];
+        tmem_ld32(t_dp + c4 * 32, r);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float d0 = pr[c4 * 32 + 2 * i] * (__uint_as_float(r[2 * i]) - dlt);
+          const float d1 = pr[c4 * 32 + 2 * i + 1] * (__uint_as_float(r[2 * i + 1]) - dlt);
+          pk[i] = pack2<BF16>(d0, d1);
+        }
+        tmem_st16(t_dp + c4 * 16, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(ds_full);
+    }
+    if (ok && warp_wait(acc_done, 0, limit, abort_flag, kWaitDqDone)) {
+      tc_fence_after();
+      uint8_t* drow = reinterpret_cast<uint8_t*>(p.out0) + ((size_t)bh * N + row) * (size_t)(D * 2);
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32(t_acc + cc * 32, r);
+        if (row < N) store_row32<BF16>(drow + cc * 64, r, p.scale);
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace attn

@@ -1,0 +1,41 @@
+// common.cuh - shapes and tile geometry shared by the attention kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "ptx.cuh"
+
+namespace attn {
+
+constexpr int kTileM = 128;           // query rows per MMA tile (TMEM lanes)
+constexpr int kTileN = 128;           // keys per key/value block
+constexpr int kBoxCols = 64;          // 16-bit elements per 128-byte swizzled row
+constexpr int kBoxBytes = 128 * 128;  // one [128 rows x 64 cols] 16-bit box = 16 KiB
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Codes recorded in the status word when a bounded wait gives up (kernel * 16 + site).
+enum WaitSite : int {
+  kWaitFwdQ = 0x11, kWaitFwdK, kWaitFwdV, kWaitFwdEmpty, kWaitFwdS, kWaitFwdP, kWaitFwdO,
+  kWaitFwdDrain,
+  kWaitDqQ = 0x21, kWaitDqK, kWaitDqV, kWaitDqEmpty, kWaitDqS, kWaitDqDP, kWaitDqDS,
+  kWaitDqDone, kWaitDqDrain, kWaitDqSC,
+  kWaitDkvKV = 0x31, kWaitDkvQ, kWaitDkvDO, kWaitDkvEmpty, kWaitDkvS, kWaitDkvDP,
+  kWaitDkvP, kWaitDkvDS, kWaitDkvDone, kWaitDkvDrain, kWaitDkvStats
+};
+
+// Rounds a shared-memory pointer up to 1024 bytes (the swizzle-atom alignment).
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  const uint32_t a = smem_u32(p);
+  return p + (((a + 1023u) & ~1023u) - a);
+}
+
+// Warp-uniform bounded wait: every lane waits; the result is true only if all did.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t limit,
+                                          volatile int* abort, int where) {
+  const bool ok = mbar_wait(bar, parity, limit, abort, where);
+  return __all_sync(0xffffffffu, ok);
+}
+
+}  // namespace attn

@@ -1,0 +1,355 @@
+// fwd.cuh - attention forward on sm_103a: O = softmax(scale Q K^T [causal]) V and the
+// per-row logsumexp L, with the online-softmax recurrence.
+//
+// Method ("Triton 05: Flash Attention", sections Online Softmax and 코드 라인별 설명
+// (Forward); "FlashAttention·FA4·FP4", section 온라인 softmax가 블록 사이의 값을 어떻게
+// 이어 주나): for each block of keys, S = scale Q K_j^T, m' = max(m, rowmax S),
+// l' = exp(m - m') l + rowsum exp(S - m'), O' = exp(m - m') O + exp(S - m') V_j; after
+// the last block O / l once, and L = m + ln l. The scores never leave the chip.
+//
+// GB300 design (the pages' kernels were written for A100 / Ada / B200: prior art):
+//  * One CTA = one (b, h) slice x 256 query rows, split into two 128-row tiles that
+//    ping-pong: while one tile's softmax runs on the CUDA cores, the tensor core works
+//    on the other tile (the two-tile schedule described for Blackwell on
+//    "FlashAttention·FA4·FP4", section HBM을 아낀 뒤에는 무엇이 기다리는가).
+//  * Warp roles: warps 0-3 softmax of tile 0, warps 4-7 softmax of tile 1, warp 8 TMA
+//    producer, warp 9 MMA issuer (one thread) and TMEM owner.
+//  * Q tiles, and a ring of K/V blocks, are TMA-copied into 128B-swizzled shared
+//    memory; S = Q K^T and O += P V run on tcgen05 with fp32 accumulators in tensor
+//    memory (S_t: 128 columns, O_t: d columns per tile). P is written back over S_t as
+//    16-bit pairs and fed to the P V product straight from tensor memory.
+//  * exp is exp2 with scale*log2(e) folded into one FFMA per score ("Triton 05",
+//    section 2. exp -> exp2 트릭); L is exported in the natural log.
+//  * The O rescale is conditional: the running max used for exp2 is only moved when
+//    the row max grows by more than 8 (a factor 256), otherwise the stale max is kept
+//    for both the numerator and l, which leaves O = acc / l exact ("FlashAttention·
+//    FA4·FP4", section HBM을 아낀 뒤에는 무엇이 기다리는가, the rescale skip).
+//  * Causal: key blocks after a tile's diagonal block are skipped; only the diagonal
+//    block (and a ragged last block) is masked. The CTAs of one head are adjacent in
+//    launch order (K/V of the head stay in L2) and run longest-first.
+#pragma once
+
+#include "common.cuh"
+
+namespace attn {
+
+struct FwdParams {
+  void* o;
+  float* lse;
+  int N;
+  int nkb;          // number of 128-key blocks
+  int nqb;          // number of 256-row query blocks
+  int causal;
+  float scale_log2; // scale * log2(e)
+  unsigned long long wait_limit;
+};
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kChunks = D / kBoxCols;            // 64-column boxes per row
+  static constexpr int kTileBytes = kChunks * kBoxBytes;  // one 128 x D tile
+  static constexpr int kStages = (D == 128) ? 2 : 4;      // K/V ring depth
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  // barriers: q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2],
+  // o_done[2], drain
+  static constexpr int kNumBars = 1 + 3 * kStages + 6 + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+  // All 512 tensor-memory columns per CTA: one CTA per SM, which the shared memory
+  // footprint (> 114 KiB for both head dims) already guarantees.
+  static_assert(kSmemBytes > 114 * 1024, "two CTAs could share an SM");
+  static constexpr int kThreads = 320;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+};
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(320, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
+                    const __grid_constant__ CUtensorMap map_k,
+                    const __grid_constant__ CUtensorMap map_v, const FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* v_full = k_full + C::kStages;
+  uint64_t* kv_empty = v_full + C::kStages;
+  uint64_t* s_full = kv_empty + C::kStages;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_done = p_full + 2;
+  uint64_t* drain = o_done + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+  const int bh = blockIdx.y;
+  const int qb = p.nqb - 1 - blockIdx.x;  // within a head, longest (most key blocks) first
+  const int q0 = qb * 256;
+  const int N = p.N;
+  const int ntiles = (q0 + kTileM < N) ? 2 : 1;
+  int nkv[2];
+  for (int t = 0; t < 2; ++t) {
+    nkv[t] = (t < ntiles) ? (p.causal ? min(p.nkb, q0 / kTileN + t + 1) : p.nkb) : 0;
+  }
+  const int n_kv = max(nkv[0], nkv[1]);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 128);
+      mbar_init(&o_done[t], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_holder, C::kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint64_t limit = p.wait_limit;
+
+  if (warp == 8) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      tma_prefetch_map(&map_q);
+      tma_prefetch_map(&map_k);
+      tma_prefetch_map(&map_v);
+      mbar_arrive_expect_tx(q_full, ntiles * C::kTileBytes);
+      for (int t = 0; t < ntiles; ++t)
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(smem + C::kOffQ + t * C::kTileBytes + c * kBoxBytes, &map_q, q_full,
+                      c * kBoxCols, q0 + t * kTileM, bh);
+      int issued = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        const int s = j % C::kStages;
+        if (j >= C::kStages &&
+            !mbar_wait(&kv_empty[s], ((j / C::kStages) - 1) & 1, limit, abort_flag,
+                       kWaitFwdEmpty))
+          break;
+        mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(smem + C::kOffK + s * C::kTileBytes + c * kBoxBytes, &map_k,
+                      &k_full[s], c * kBoxCols, j * kTileN, bh);
+        mbar_arrive_expect_tx(&v_full[s], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(smem + C::kOffV + s * C::kTileBytes + c * kBoxBytes, &map_v,
+                      &v_full[s], c * kBoxCols, j * kTileN, bh);
+        issued = j + 1;
+      }
+      if (*abort_flag) {
+        // Let every copy this CTA started land before its shared memory is released.
+        mbar_wait(q_full, 0, limit, nullptr, kWaitFwdDrain);
+        for (int j = max(0, issued - C::kStages); j < issued; ++j) {
+          const int s = j % C::kStages;
+          mbar_wait(&k_full[s], (j / C::kStages) & 1, limit, nullptr, kWaitFwdDrain);
+          mbar_wait(&v_full[s], (j / C::kStages) & 1, limit, nullptr, kWaitFwdDrain);
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------ MMA issuer --------------------------------
+    if (lane == 0) {
+      const uint32_t idesc_s = make_idesc(BF16, 128, kTileN, false, false);
+      const uint32_t idesc_o = make_idesc(BF16, 128, D, false, true);
+      const uint32_t sq = smem_u32(smem + C::kOffQ);
+      const uint32_t sk = smem_u32(smem + C::kOffK);
+      const uint32_t sv = smem_u32(smem + C::kOffV);
+      const uint32_t col_s[2] = {C::kColS0, C::kColS1};
+      const uint32_t col_o[2] = {C::kColO0, C::kColO1};
+
+      auto issue_s = [&](int t, int stage) {
+        const uint32_t a0 = sq + t * C::kTileBytes;
+        const uint32_t b0 = sk + stage * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+          mma_ss(tmem + col_s[t], make_sdesc_sw128(a0 + off, 16, 1024),
+                 make_sdesc_sw128(b0 + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int t, int stage, bool acc) {
+        const uint32_t b0 = sv + stage * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk) {
+          mma_ts(tmem + col_o[t], tmem + col_s[t] + kk * 8,
+                 make_sdesc_sw128(b0 + kk * 2048, kBoxBytes, 1024), idesc_o,
+                 (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+
+      bool ok = mbar_wait(q_full, 0, limit, abort_flag, kWaitFwdQ);
+      if (ok) ok = mbar_wait(&k_full[0], 0, limit, abort_flag, kWaitFwdK);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t)
+          if (nkv[t] > 0) {
+            issue_s(t, 0);
+            mma_commit(&s_full[t]);
+          }
+      }
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int s = j % C::kStages;
+        if (!(ok = mbar_wait(&v_full[s], (j / C::kStages) & 1, limit, abort_flag,
+                             kWaitFwdV)))
+          break;
+        tc_fence_after();
+        const int jn = j + 1;
+        const int sn = jn % C::kStages;
+        bool next_k_ready = false;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= nkv[t]) continue;
+          if (!(ok = mbar_wait(&p_full[t], j & 1, limit, abort_flag, kWaitFwdP))) break;
+          tc_fence_after();
+          issue_pv(t, s, j > 0);
+          mma_commit(&o_done[t]);
+          if (jn < nkv[t]) {
+            if (!next_k_ready) {
+              if (!(ok = mbar_wait(&k_full[sn], (jn / C::kStages) & 1, limit, abort_flag,
+                                   kWaitFwdK)))
+                break;
+              tc_fence_after();
+              next_k_ready = true;
+            }
+            issue_s(t, sn);
+            mma_commit(&s_full[t]);
+          }
+        }
+        if (ok) mma_commit(&kv_empty[s]);
+      }
+      // Every MMA this thread issued must finish before tensor memory is released.
+      mma_commit(drain);
+      mbar_wait(drain, 0, limit, nullptr, kWaitFwdDrain);
+    }
+  } else {
+    // ------------------------------ softmax (tile t) --------------------------
+    const int t = warp >> 2;
+    const int wq = warp & 3;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + (t == 0 ? C::kColS0 : C::kColS1);
+    const uint32_t t_o = tmem + lane_base + (t == 0 ? C::kColO0 : C::kColO1);
+    const int row = q0 + t * kTileM + wq * 32 + lane;  // query index of this thread
+    const int tile_row0 = q0 + t * kTileM;
+    const float sl2 = p.scale_log2;
+    float m = -INFINITY;  // running max of scale*log2(e)*S (possibly stale by <= 8)
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkv[t]; ++j) {
+      if (!(ok = warp_wait(&s_full[t], j & 1, limit, abort_flag, kWaitFwdS))) break;
+      tc_fence_after();
+      float s[kTileN];
+#pragma unroll
+      for (int c4 = 0; c4 < kTileN / 32; ++c4) {
+        uint32_t r[32];
+        tmem_ld32(t_s + c4 * 32, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c4 * 32 + i] = __uint_as_float(r[i]);
+      }
+      const int kbase = j * kTileN;
+      const bool diag = p.causal && (kbase + kTileN - 1 > tile_row0);
+      if (diag || kbase + kTileN > N) {
+        int lim = N - 1 - kbase;                       // last key in range
+        if (p.causal) lim = min(lim, row - kbase);     // last key visible to this row
+#pragma unroll
+        for (int c = 0; c < kTileN; ++c)
+          if (c > lim) s[c] = -INFINITY;
+      }
+      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+      for (int c = 4; c < kTileN; c += 4) {
+        mx0 = fmaxf(mx0, s[c]);
+        mx1 = fmaxf(mx1, s[c + 1]);
+        mx2 = fmaxf(mx2, s[c + 2]);
+        mx3 = fmaxf(mx3, s[c + 3]);
+      }
+      const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const bool need = m_cand > m + 8.0f;
+      float alpha = 1.f;
+      if (need) {
+        alpha = ex2(m - m_cand);  // 0 on the first block (m = -inf)
+        m = m_cand;
+      }
+      const float neg_m = -m;
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int c4 = 0; c4 < kTileN / 32; ++c4) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2(fmaf(s[c4 * 32 + 2 * i], sl2, neg_m));
+          const float p1 = ex2(fmaf(s[c4 * 32 + 2 * i + 1], sl2, neg_m));
+          sum0 += p0;
+          sum1 += p1;
+          pk[i] = pack2<BF16>(p0, p1);
+        }
+        tmem_st16(t_s + c4 * 16, pk);
+      }
+      l = l * alpha + (sum0 + sum1);
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // Bring O to the new max: wait until the previous P V product has landed.
+        if (!(ok = warp_wait(&o_done[t], (j - 1) & 1, limit, abort_flag, kWaitFwdO))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t r[32];
+          tmem_ld32(t_o + cc * 32, r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          tmem_st32(t_o + cc * 32, r);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&p_full[t]);
+    }
+    if (ok && nkv[t] > 0 &&
+        warp_wait(&o_done[t], (nkv[t] - 1) & 1, limit, abort_flag, kWaitFwdO)) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
+                      ((size_t)bh * N + (size_t)row) * (size_t)(D * 2);
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32(t_o + cc * 32, r);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack2<BF16>(__uint_as_float(r[2 * i]) * inv_l,
+                              __uint_as_float(r[2 * i + 1]) * inv_l);
+        if (row < N) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 64);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+      if (row < N) p.lse[(size_t)bh * N + row] = (m + log2f(l)) * kLn2;
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace attn

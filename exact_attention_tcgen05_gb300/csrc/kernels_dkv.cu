@@ -1,0 +1,41 @@
+// kernels_dkv.cu - instantiation and launch of the backward dK/dV kernel.
+#include "bwd_dkv.cuh"
+#include "launch.h"
+
+namespace attn {
+
+template <int D, bool BF16>
+static cudaError_t launch_dkv_t(const Maps& m, const Shape& s, const float* lse,
+                                const float* delta, void* dk, void* dv, cudaStream_t st) {
+  using C = DkvCfg<D>;
+  auto kern = attn_bwd_dkv_kernel<D, BF16>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  BwdParams p;
+  p.lse = lse;
+  p.delta = delta;
+  p.out0 = dk;
+  p.out1 = dv;
+  p.N = s.N;
+  p.nb = (s.N + kTileM - 1) / kTileM;
+  p.causal = s.causal ? 1 : 0;
+  p.scale = s.scale;
+  p.scale_log2 = s.scale * kLog2e;
+  p.wait_limit = s.wait_limit;
+  dim3 grid(p.nb, s.BH);
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(m.q, m.k, m.v, m.d_o, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dkv(const Maps& m, const Shape& s, const float* lse, const float* delta,
+                       void* dk, void* dv, cudaStream_t st) {
+  if (s.d == 128) return s.bf16 ? launch_dkv_t<128, true>(m, s, lse, delta, dk, dv, st)
+                                : launch_dkv_t<128, false>(m, s, lse, delta, dk, dv, st);
+  return s.bf16 ? launch_dkv_t<64, true>(m, s, lse, delta, dk, dv, st)
+                : launch_dkv_t<64, false>(m, s, lse, delta, dk, dv, st);
+}
+
+ATTN_DEFINE_STATUS_READER(status_dkv)
+
+}  // namespace attn

@@ -1,0 +1,41 @@
+// kernels_dq.cu - instantiation and launch of the backward dQ kernel.
+#include "bwd_dq.cuh"
+#include "launch.h"
+
+namespace attn {
+
+template <int D, bool BF16>
+static cudaError_t launch_dq_t(const Maps& m, const Shape& s, const float* lse,
+                               const float* delta, void* dq, cudaStream_t st) {
+  using C = DqCfg<D>;
+  auto kern = attn_bwd_dq_kernel<D, BF16>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  BwdParams p;
+  p.lse = lse;
+  p.delta = delta;
+  p.out0 = dq;
+  p.out1 = nullptr;
+  p.N = s.N;
+  p.nb = (s.N + kTileM - 1) / kTileM;
+  p.causal = s.causal ? 1 : 0;
+  p.scale = s.scale;
+  p.scale_log2 = s.scale * kLog2e;
+  p.wait_limit = s.wait_limit;
+  dim3 grid(p.nb, s.BH);
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(m.q, m.k, m.v, m.d_o, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq(const Maps& m, const Shape& s, const float* lse, const float* delta,
+                      void* dq, cudaStream_t st) {
+  if (s.d == 128) return s.bf16 ? launch_dq_t<128, true>(m, s, lse, delta, dq, st)
+                                : launch_dq_t<128, false>(m, s, lse, delta, dq, st);
+  return s.bf16 ? launch_dq_t<64, true>(m, s, lse, delta, dq, st)
+                : launch_dq_t<64, false>(m, s, lse, delta, dq, st);
+}
+
+ATTN_DEFINE_STATUS_READER(status_dq)
+
+}  // namespace attn

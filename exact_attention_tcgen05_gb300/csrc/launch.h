@@ -1,0 +1,52 @@
+// launch.h - internal interface between the C ABI (attn_api.cu) and the translation
+// units that hold the kernels. Not part of the public header.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+// TMA descriptors of the [B*H, N, d] 16-bit tensors a kernel reads.
+struct Maps {
+  CUtensorMap q, k, v, d_o;
+};
+
+struct Shape {
+  int BH, N, d;
+  bool bf16, causal;
+  float scale;
+  unsigned long long wait_limit;  // SM cycles one pipeline wait may take
+};
+
+cudaError_t launch_fwd(const Maps& m, const Shape& s, void* o, float* lse, cudaStream_t st);
+cudaError_t launch_delta(const Shape& s, const void* o, const void* dO, float* delta,
+                         cudaStream_t st);
+cudaError_t launch_dq(const Maps& m, const Shape& s, const float* lse, const float* delta,
+                      void* dq, cudaStream_t st);
+cudaError_t launch_dkv(const Maps& m, const Shape& s, const float* lse, const float* delta,
+                       void* dk, void* dv, cudaStream_t st);
+
+// Each kernel translation unit has its own device status word; these read (after the
+// work queued on `st`, blocking) and clear it. Return the word (0 = no timeout).
+int status_fwd(cudaStream_t st, cudaError_t* err);
+int status_delta(cudaStream_t st, cudaError_t* err);
+int status_dq(cudaStream_t st, cudaError_t* err);
+int status_dkv(cudaStream_t st, cudaError_t* err);
+
+}  // namespace attn
+
+// Defines the status reader of one translation unit.
+#define ATTN_DEFINE_STATUS_READER(fn)                                                      \
+  int fn(cudaStream_t st, cudaError_t* err) {                                             \
+    int h = 0;                                                                             \
+    const int zero = 0;                                                                    \
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&h, g_kernel_status, sizeof(int), 0,        \
+                                              cudaMemcpyDeviceToHost, st);                 \
+    if (e == cudaSuccess)                                                                  \
+      e = cudaMemcpyToSymbolAsync(g_kernel_status, &zero, sizeof(int), 0,                 \
+                                  cudaMemcpyHostToDevice, st);                             \
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);                                   \
+    *err = e;                                                                              \
+    return h;                                                                              \
+  }

@@ -1,0 +1,130 @@
+/*
+ * attn.h - C ABI of libattn.so: exact scaled-dot-product attention on GB300 (sm_103a).
+ *
+ * Forward:  O = softmax(scale * Q K^T [causal mask]) V, plus the per-row logsumexp L.
+ * Backward: dQ, dK, dV of sum(dO * O), recomputing the probabilities from L.
+ *
+ * The operations are the ones described on these pages:
+ *   - "Triton 05: Flash Attention" (wonbeomjang.kr): sections Online Softmax,
+ *     코드 라인별 설명 (Forward), Backward 구현 (LSE로 P 재계산, Softmax Gradient,
+ *     3단계 커널 구조) and torch.autograd.Function 래핑, which fixes the interface
+ *     forward(q, k, v, causal) -> o (saving q, k, v, o, lse) and
+ *     backward(do) -> dq, dk, dv with sm_scale = d ** -0.5.
+ *   - "FlashAttentionを1から — 計算を増やして速くする逆説": sections オンラインsoftmax
+ *     and 逆伝播で、わざと計算し直す (recompute P in the backward instead of storing it).
+ *
+ * Conventions shared by every entry point
+ *   Layout   q, k, v, o, dO, dq, dk, dv are contiguous [B, H, N, d] tensors of 16-bit
+ *            floats (fp16 or bf16, one type for all of them), row-major, d innermost.
+ *            lse and the backward workspace are contiguous [B, H, N] float32.
+ *            Every pointer is a DEVICE pointer, 16-byte aligned.
+ *   Sizes    B >= 1, H >= 1, 1 <= N <= 1048576, d in {64, 128}; B*H <= 65535.
+ *   Mask     causal != 0 masks key j for query i when j > i (top-left aligned,
+ *            N_q = N_k, diagonal kept), so no row is ever fully masked.
+ *   scale    the factor applied to Q K^T; finite and > 0 (the usual value is
+ *            1/sqrt(d)).
+ *   Streams  cuda_stream is a cudaStream_t (NULL = legacy default stream). All work
+ *            is enqueued on it; the calls never synchronise the device and return
+ *            as soon as the launches are queued.
+ *   Ownership the caller allocates and owns every buffer and the stream. The library
+ *            allocates no device memory, keeps no state between calls (tensor maps
+ *            are encoded per call) and is safe to call from several host threads.
+ *   Errors   ATTN_ERR_INVALID_ARG for a bad size, pointer, alignment, scale or an
+ *            output that overlaps an input (checked on the host before any CUDA
+ *            call); ATTN_ERR_UNSUPPORTED for a head dimension or type the kernels do
+ *            not implement; ATTN_ERR_CUDA when a launch or a tensor-map encoding
+ *            fails (the CUDA error is then also left for cudaGetLastError).
+ *            Faults inside a kernel surface, as with any CUDA library, at the
+ *            caller's next synchronisation. Every pipeline wait inside the kernels
+ *            is bounded; a wait that runs out records ATTN_ERR_TIMEOUT in the
+ *            status word read by attn_last_kernel_status().
+ */
+#ifndef ATTN_H
+#define ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,
+  ATTN_ERR_UNSUPPORTED = 2,
+  ATTN_ERR_CUDA = 3,
+  ATTN_ERR_TIMEOUT = 4
+} attn_status;
+
+typedef enum { ATTN_FP16 = 0, ATTN_BF16 = 1 } attn_dtype;
+
+/*
+ * attn_fwd - forward pass.
+ * Computes, for every (b, h) slice and query row i,
+ *   S_ij = scale * q_i . k_j  (S_ij = -inf for j > i when causal),
+ *   O_i  = sum_j softmax(S_i)_j v_j,   L_i = max_j S_ij + ln sum_j exp(S_ij - max_j S_ij),
+ * tile by tile with the online-softmax recurrence (running max m, denominator l,
+ * unnormalised accumulator rescaled by exp(m_old - m_new), one final divide by l), so
+ * that the N x N scores never reach device memory ("Triton 05: Flash Attention",
+ * sections Online Softmax and 코드 라인별 설명 (Forward); "FlashAttention·FA4·FP4",
+ * section 온라인 softmax가 블록 사이의 값을 어떻게 이어 주나).
+ *   q, k, v  in:  [B, H, N, d] 16-bit.
+ *   o        out: [B, H, N, d] same type as q.
+ *   lse      out: [B, H, N] float32, natural-log L_i (the value attn_bwd consumes).
+ * o and lse must not overlap q, k, v or each other.
+ */
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int H, int N, int d, attn_dtype dtype, int causal,
+                     float scale, void* cuda_stream);
+
+/*
+ * attn_bwd_workspace_bytes - bytes of the float32 workspace attn_bwd needs:
+ * 4 * B * H * N (one D_i per query row). Returns 0 for non-positive sizes.
+ */
+size_t attn_bwd_workspace_bytes(int B, int H, int N);
+
+/*
+ * attn_bwd - backward pass, three kernels on cuda_stream with no atomics
+ * ("Triton 05: Flash Attention", section 3단계 커널 구조):
+ *   1. D_i = rowsum(dO_i * O_i) into the workspace (section Softmax Gradient);
+ *   2. per block of keys j: P_ij = exp(S_ij - L_i), dV_j = sum_i P_ij dO_i,
+ *      dS_ij = P_ij (dO_i . v_j - D_i), dK_j = scale * sum_i dS_ij q_i;
+ *   3. per block of queries i: dQ_i = scale * sum_j dS_ij k_j.
+ *   q, k, v, o, dO in: [B, H, N, d] 16-bit; lse in: [B, H, N] float32 from attn_fwd
+ *                      with the same q, k, v, causal and scale.
+ *   dq, dk, dv    out: [B, H, N, d] same type as q.
+ *   workspace     scratch of attn_bwd_workspace_bytes(B, H, N) bytes, device memory
+ *                 owned by the caller; its contents on entry do not matter.
+ * Outputs must not overlap the inputs, each other or the workspace.
+ */
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                     void* workspace, int B, int H, int N, int d, attn_dtype dtype,
+                     int causal, float scale, void* cuda_stream);
+
+/*
+ * attn_bwd_preprocess - step 1 of attn_bwd alone: delta[b,h,i] = sum_c dO[b,h,i,c] *
+ * o[b,h,i,c] in float32 ("Triton 05: Flash Attention", section 3단계 커널 구조,
+ * [1단계] Preprocess). o, dO: [B, H, N, d] 16-bit device; delta: [B, H, N] float32
+ * device, must not overlap o or dO.
+ */
+attn_status attn_bwd_preprocess(const void* o, const void* dO, float* delta, int B, int H,
+                                int N, int d, attn_dtype dtype, void* cuda_stream);
+
+/* attn_status_str - static, NUL-terminated name of a status code. */
+const char* attn_status_str(attn_status s);
+
+/*
+ * attn_last_kernel_status - reads (with a blocking device-to-host copy on
+ * cuda_stream, after the work queued before it) and clears the status word the
+ * kernels set when a bounded pipeline wait runs out. Returns ATTN_OK when no wait
+ * ran out since the last call, ATTN_ERR_TIMEOUT otherwise, ATTN_ERR_CUDA if the
+ * copy fails. *where (may be NULL) receives the code of the first wait that gave up.
+ */
+attn_status attn_last_kernel_status(void* cuda_stream, int* where);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H */

@@ -1,0 +1,98 @@
+"""Shared helpers for the GPU parity tests: run the CUDA path through the C ABI on seeded
+inputs, run the fp64 oracle on the same rounded inputs, and compare.
+
+Tolerances (the bar the CUDA path must meet against the oracle):
+  O    max-abs <= 1e-2 where |O_ref| < 4; where |O_ref| >= 4, one output-dtype ulp of
+       O_ref is added (bf16 storage rounding alone is 0.0156 there);
+  LSE  max-abs <= 1e-3;
+  dQ, dK, dV  relative Frobenius error <= 3e-2 per (b, h) slice.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import torch
+
+import oracle.attention as OA
+from exact_attention_tcgen05_gb300 import binding
+from exact_attention_tcgen05_gb300 import inputs as I
+
+O_TOL = 1e-2
+LSE_TOL = 1e-3
+GRAD_TOL = 3e-2
+
+
+@dataclasses.dataclass
+class GpuRun:
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    do: torch.Tensor
+    o: torch.Tensor
+    lse: torch.Tensor
+    dq: torch.Tensor
+    dk: torch.Tensor
+    dv: torch.Tensor
+
+
+def make_inputs(w: I.Workload, device="cuda"):
+    return tuple(I.make_tensor(w, t).to(device) for t in ("q", "k", "v", "do"))
+
+
+def run_gpu(w: I.Workload, tensors=None, backward=True) -> GpuRun:
+    q, k, v, do = make_inputs(w) if tensors is None else tensors
+    o, lse = binding.attn_fwd(q, k, v, causal=w.causal, scale=w.scale)
+    if backward:
+        dq, dk, dv = binding.attn_bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.scale)
+    else:
+        dq = dk = dv = None
+    torch.cuda.synchronize()
+    return GpuRun(q, k, v, do, o, lse, dq, dk, dv)
+
+
+def ulp(x: np.ndarray, dtype: torch.dtype) -> np.ndarray:
+    mant = 7 if dtype == torch.bfloat16 else 10
+    e = np.floor(np.log2(np.maximum(np.abs(x), 1e-30)))
+    return np.exp2(e - mant)
+
+
+def o_error(o_gpu: np.ndarray, o_ref: np.ndarray, dtype) -> tuple[float, float]:
+    """(max raw error, max excess over the allowed bound); pass iff excess <= 0."""
+    err = np.abs(o_gpu - o_ref)
+    allowed = np.where(np.abs(o_ref) < 4.0, O_TOL, O_TOL + ulp(o_ref, dtype))
+    return float(err.max()), float((err - allowed).max())
+
+
+def rel_fro(a: np.ndarray, b: np.ndarray) -> float:
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def compare_slice(w: I.Workload, run: GpuRun, b: int, h: int, backward=True) -> dict:
+    """Oracle on slice (b, h) from the same rounded inputs; returns the errors."""
+    q, k, v, do = (I.to_f64(x[b, h]) for x in (run.q, run.k, run.v, run.do))
+    if backward:
+        ref = OA.attention_backward(q, k, v, do, w.causal, w.scale)
+    else:
+        o_ref, lse_ref = OA.attention_forward(q, k, v, w.causal, w.scale)
+        ref = dict(o=o_ref, lse=lse_ref)
+    res = {}
+    res["o_max"], res["o_excess"] = o_error(I.to_f64(run.o[b, h]), ref["o"], w.torch_dtype)
+    res["lse_max"] = float(np.abs(run.lse[b, h].double().cpu().numpy() - ref["lse"]).max())
+    if backward:
+        for name in ("dq", "dk", "dv"):
+            res[name] = rel_fro(I.to_f64(getattr(run, name)[b, h]), ref[name])
+    return res
+
+
+def assert_within(res: dict, where: str) -> None:
+    assert res["o_excess"] <= 0.0, f"{where}: O error {res['o_max']:.3e} above bound"
+    assert res["lse_max"] <= LSE_TOL, f"{where}: LSE error {res['lse_max']:.3e}"
+    for name in ("dq", "dk", "dv"):
+        if name in res:
+            assert res[name] <= GRAD_TOL, f"{where}: {name} rel. Frobenius {res[name]:.3e}"
+
+
+def all_finite(run: GpuRun) -> bool:
+    ts = [run.o, run.lse] + ([run.dq, run.dk, run.dv] if run.dq is not None else [])
+    return all(bool(torch.isfinite(t).all()) for t in ts)

@@ -1,0 +1,125 @@
+"""The C ABI without a GPU: the library builds, exports every function include/attn.h
+declares, and rejects bad arguments on the host before making any CUDA call."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_tcgen05_gb300 import binding
+    from exact_attention_tcgen05_gb300 import build as B
+    B.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes",
+                     "attn_bwd_preprocess", "attn_status_str", "attn_last_kernel_status"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from exact_attention_tcgen05_gb300 import build as B
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (\w+)", out))
+    for name in declared_functions():
+        assert name in exported, name
+        getattr(lib, name)
+
+
+def test_binding_covers_the_header():
+    from exact_attention_tcgen05_gb300 import binding
+    assert sorted(binding.SIGNATURES) == declared_functions()
+
+
+def test_status_strings(lib):
+    assert lib.attn_status_str(0) == b"ATTN_OK"
+    assert lib.attn_status_str(4) == b"ATTN_ERR_TIMEOUT"
+    assert lib.attn_status_str(77) == b"ATTN_ERR_UNKNOWN"
+
+
+def test_workspace_bytes(lib):
+    assert lib.attn_bwd_workspace_bytes(4, 32, 4096) == 4 * 4 * 32 * 4096
+    assert lib.attn_bwd_workspace_bytes(0, 1, 1) == 0
+    assert lib.attn_bwd_workspace_bytes(1, 1, -5) == 0
+
+
+# Fake, 16-byte aligned, non-overlapping "device" addresses: validation must reject the
+# call before any of them is dereferenced or passed to CUDA.
+MB = 1 << 20
+Q, K, V, O, L, DO, DQ, DK, DV, WS = (0x10000000 + i * 64 * MB for i in range(10))
+
+
+def fwd(lib, q=Q, k=K, v=V, o=O, lse=L, B=1, H=1, N=256, d=128, dt=1, causal=0, scale=0.1):
+    return lib.attn_fwd(q, k, v, o, lse, B, H, N, d, dt, causal, scale, None)
+
+
+def bwd(lib, dq=DQ, ws=WS, q=Q, B=1, H=1, N=256, d=128, dt=1, scale=0.1):
+    return lib.attn_bwd(q, K, V, O, L, DO, dq, DK, DV, ws, B, H, N, d, dt, 0, scale, None)
+
+
+INVALID, UNSUPPORTED = 1, 2
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), INVALID), (dict(o=0), INVALID), (dict(lse=L + 4), INVALID),
+    (dict(k=K + 2), INVALID), (dict(B=0), INVALID), (dict(H=-1), INVALID),
+    (dict(N=0), INVALID), (dict(N=(1 << 20) + 1), INVALID), (dict(B=300, H=300), INVALID),
+    (dict(d=96), UNSUPPORTED), (dict(d=256), UNSUPPORTED), (dict(dt=2), INVALID),
+    (dict(scale=0.0), INVALID), (dict(scale=-1.0), INVALID), (dict(scale=float("nan")), INVALID),
+    (dict(scale=float("inf")), INVALID), (dict(o=Q), INVALID), (dict(o=K + 16), INVALID),
+    (dict(lse=O + 1024), INVALID),
+])
+def test_fwd_rejects_bad_arguments(lib, kw, code):
+    assert fwd(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dq=0), INVALID), (dict(ws=0), INVALID), (dict(dq=DK), INVALID), (dict(ws=Q), INVALID),
+    (dict(dq=O + 32), INVALID), (dict(d=32), UNSUPPORTED), (dict(scale=0.0), INVALID),
+    (dict(ws=WS + 8), INVALID),
+])
+def test_bwd_rejects_bad_arguments(lib, kw, code):
+    assert bwd(lib, **kw) == code
+
+
+def test_preprocess_rejects_bad_arguments(lib):
+    assert lib.attn_bwd_preprocess(O, DO, 0, 1, 1, 16, 64, 0, None) == INVALID
+    assert lib.attn_bwd_preprocess(O, DO, O, 1, 1, 16, 64, 0, None) == INVALID
+    assert lib.attn_bwd_preprocess(O, DO, WS, 1, 1, 16, 48, 0, None) == UNSUPPORTED
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    from exact_attention_tcgen05_gb300 import binding
+    x = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        binding.attn_fwd(x, x, x)
+
+
+def test_product_path_has_no_oracle_or_fallback():
+    """The package never imports the oracle and has no CPU implementation."""
+    pkg = os.path.join(ROOT, "exact_attention_tcgen05_gb300")
+    for fn in os.listdir(pkg):
+        if fn.endswith(".py"):
+            src = open(os.path.join(pkg, fn)).read()
+            assert not re.search(r"^\s*(import|from)\s+oracle", src, flags=re.M), fn
+            code = re.sub(r'""".*?"""', "", src, flags=re.S)
+            code = re.sub(r"#.*", "", code)
+            for banned in ("softmax(", "scaled_dot_product", ".exp(", "matmul(", " @ "):
+                assert banned not in code, (fn, banned)
