@@ -1,0 +1,393 @@
+"""Throughput of the exact-attention hot path on GB300: one step = forward + backward
+(D preprocess, dK/dV, dQ) over one batch of seeded synthetic inputs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0. `value` is whole-job TFLOPS with inputs resident in HBM
+(counted FLOPs: forward 4·B·H·N²·d, backward 10·B·H·N²·d, both halved when causal);
+`e2e` is the same metric through the C ABI with host buffers (pinned host -> device
+copies of q, k, v, dO and device -> host copies of o, lse, dq, dk, dv inside the timed
+region). `--impl reference` times the fp64 CPU oracle on bounded samples instead.
+N > 1 (torchrun): every rank runs an independent replica of the workload on its own
+GPU (weak scaling, no collective on the data path); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "B4_H32_N4096_d128_bf16_causal"
+METRIC = "attention fwd/bwd TFLOPS (causal-adjusted) and % of GB300 dense BF16 peak"
+L2_BYTES = 126 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "source": "fallback"}
+
+
+def flops(w, part: str) -> float:
+    """Counted FLOPs of one pass over the whole workload."""
+    base = 4.0 * w.B * w.H * w.N * w.N * w.d
+    f = {"fwd": base, "bwd": 2.5 * base, "dkv": 2.0 * base, "dq": 1.5 * base}[part]
+    return f / 2 if w.causal else f
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        p["source"] = "measured"
+        return p
+    return dict(FALLBACK_PEAKS)
+
+
+# ------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"attn_bench_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[4:8]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def cpu_baseline(w, budget_s: float = 12.0, max_slices: int = 32) -> dict:
+    """The fp64 oracle on (b, h) slices of the workload, in a fresh process (so its BLAS
+    thread count is set before numpy loads), until about `budget_s` seconds."""
+    cores = os.cpu_count() or 1
+    code = f"""
+import json, sys, time
+sys.path.insert(0, {ROOT!r})
+from exact_attention_tcgen05_gb300 import inputs as I
+import oracle.attention as OA
+w = I.BY_NAME[{w.name!r}]
+slices = I.sampled_slices(w, min(w.BH, {max_slices}))
+done, t_total = 0, 0.0
+for b, h in slices:
+    q, k, v, do = (I.to_f64(I.make_slice(w, b, h, t)) for t in ("q", "k", "v", "do"))
+    t0 = time.perf_counter()
+    OA.attention_forward(q, k, v, w.causal, w.scale)
+    OA.attention_backward(q, k, v, do, w.causal, w.scale)
+    t_total += time.perf_counter() - t0
+    done += 1
+    if t_total > {budget_s}:
+        break
+print(json.dumps({{"slices": done, "seconds": t_total}}))
+"""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS=str(cores), OMP_NUM_THREADS=str(cores),
+               MKL_NUM_THREADS=str(cores))
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                         timeout=600)
+    if res.returncode != 0:
+        return {"value": None, "error": res.stderr.strip().splitlines()[-1:]}
+    r = json.loads(res.stdout.strip().splitlines()[-1])
+    per_slice = (flops(w, "fwd") + flops(w, "bwd")) / w.BH
+    return {"value": per_slice * r["slices"] / r["seconds"] / 1e12, "unit": "TFLOPS",
+            "cores": cores, "kind": "oracle",
+            "sample": f"{r['slices']} (b,h) slices of {w.name}, forward + backward in fp64 "
+                      f"(numpy; BLAS on {cores} threads, elementwise steps single-threaded), "
+                      f"{r['seconds']:.1f} s"}
+
+
+def run_ours(args) -> None:
+    import torch
+    from exact_attention_tcgen05_gb300 import binding
+    from exact_attention_tcgen05_gb300 import inputs as I
+
+    rank, world, local = dist_setup()
+    w = I.BY_NAME[args.workload]
+    if world > 1:  # each rank: its own replica of the workload (weak scaling)
+        w = I.Workload(w.name, w.B, w.H, w.N, w.d, w.dtype, w.causal, w.seed + 7919 * rank,
+                       w.qk_gain, w.spike, w.spike_frac, w.oracle_slices)
+    binding.load()
+    host = {t: I.make_tensor(w, t).pin_memory() for t in ("q", "k", "v", "do")}
+    dev = {t: x.cuda(non_blocking=True) for t, x in host.items()}
+    q, k, v, do = dev["q"], dev["k"], dev["v"], dev["do"]
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    delta = torch.empty_like(lse)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        binding.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, o=o, lse=lse)
+        binding.attn_bwd_preprocess(o, do, delta)
+        binding.attn_bwd_dkv(q, k, v, lse, delta, do, causal=w.causal, scale=w.scale, dk=dk,
+                             dv=dv)
+        binding.attn_bwd_dq(q, k, v, lse, delta, do, causal=w.causal, scale=w.scale, dq=dq)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # --- device-timed region: inputs resident, per-kernel events on the launch stream.
+    names = ("fwd", "delta", "dkv", "dq")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        e = ev[i]
+        e[0].record(stream)
+        binding.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, o=o, lse=lse)
+        e[1].record(stream)
+        binding.attn_bwd_preprocess(o, do, delta)
+        e[2].record(stream)
+        binding.attn_bwd_dkv(q, k, v, lse, delta, do, causal=w.causal, scale=w.scale, dk=dk,
+                             dv=dv)
+        e[3].record(stream)
+        binding.attn_bwd_dq(q, k, v, lse, delta, do, causal=w.causal, scale=w.scale, dq=dq)
+        e[4].record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    barrier(world)
+    total_ms = ev[0][0].elapsed_time(ev[-1][4])
+    per_kernel = {n: [ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)]
+                  for j, n in enumerate(names)}
+    code, where = binding.attn_last_kernel_status()
+    if code != binding.ATTN_OK:
+        raise RuntimeError(f"a bounded wait ran out inside a kernel (site {where:#x})")
+    total_ms = max_over_ranks(total_ms, world)
+    ms_step = total_ms / args.steps
+    f_fwd, f_bwd = flops(w, "fwd"), flops(w, "bwd")
+    value = world * (f_fwd + f_bwd) * args.steps / (total_ms * 1e-3) / 1e12
+
+    # --- end to end through the C ABI with host buffers.
+    e2e = None
+    if not args.no_e2e:
+        out_host = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                    for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+        h2d = sum(x.numel() * x.element_size() for x in host.values())
+        d2h = sum(x.numel() * x.element_size() for x in out_host.values())
+        e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        e_start.record(stream)
+        for _ in range(args.steps):
+            for t in ("q", "k", "v", "do"):
+                dev[t].copy_(host[t], non_blocking=True)
+            step()
+            for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+                out_host[n].copy_(t, non_blocking=True)
+        e_end.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), world)
+        e2e = {"value": world * (f_fwd + f_bwd) * args.steps / (e2e_ms * 1e-3) / 1e12,
+               "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms / args.steps}
+
+    if rank != 0:
+        return
+    peaks = load_peaks()
+    avg = {n: sum(x) / len(x) for n, x in per_kernel.items()}
+    share = {n: avg[n] / ms_step for n in names}
+    dominant = max(("fwd", "dkv", "dq"), key=lambda n: avg[n])
+    dom_flops = flops(w, dominant)
+    achieved = dom_flops / (avg[dominant] * 1e-3) / 1e12
+    sustained = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    fwd_t = f_fwd / (avg["fwd"] * 1e-3) / 1e12
+    bwd_ms = avg["delta"] + avg["dkv"] + avg["dq"]
+    bwd_t = f_bwd / (bwd_ms * 1e-3) / 1e12
+    delta_bytes = 2 * w.B * w.H * w.N * w.d * 2 + w.B * w.H * w.N * 4
+    traffic = load_traffic(dominant, w.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1) inputs, see exact_attention_tcgen05_gb300/inputs.py)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "scale": w.scale,
+                   "counted_tflop_per_step": (f_fwd + f_bwd) / 1e12,
+                   "l2": f"inputs larger than L2: each of q,k,v,dO is "
+                         f"{w.B * w.H * w.N * w.d * 2 / 2**20:.0f} MiB > {L2_BYTES / 2**20:.0f} MiB",
+                   "parallelism": f"replicas x{world}"},
+        "fwd_tflops": fwd_t, "bwd_tflops": bwd_t,
+        "frac_of_peak": {"fwd": fwd_t / peaks["bf16_tflops"], "bwd": bwd_t / peaks["bf16_tflops"],
+                         "peak_tflops": peaks["bf16_tflops"], "peak_source": peaks["source"],
+                         "fwd_of_sustained": fwd_t / sustained, "bwd_of_sustained": bwd_t / sustained},
+        "kernels": {n: {"ms": avg[n], "share": share[n]} for n in names},
+        "delta_kernel": {"achieved_gbs": delta_bytes / (avg["delta"] * 1e-3) / 1e9,
+                         "peak_gbs": peaks["hbm_gbs"],
+                         "frac": delta_bytes / (avg["delta"] * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+        "roofline": {"kernel": dominant, "bound": "tensor", "achieved": achieved,
+                     "peak": sustained, "unit": "TFLOP/s", "frac": achieved / sustained,
+                     "peak_kind": f"bf16 sustained ({peaks['source']})",
+                     "algorithmic_tflop_per_launch": dom_flops / 1e12, "traffic": traffic},
+        "e2e": e2e, "clocks": clock_info, "gpu_launches": 4 * args.steps,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+
+
+def load_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches this kernel
+    and workload (profiles/traffic.json); else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    entry = t.get(kernel, {})
+    if entry.get("workload") == workload and entry.get("source_hash") == source_hash():
+        return entry.get("dram_bytes_per_launch")
+    return None
+
+
+def source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_tcgen05_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+# ------------------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores
+# ------------------------------------------------------------------------------------
+def run_reference(args) -> None:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from exact_attention_tcgen05_gb300 import inputs as I
+    import oracle.attention as OA
+    w = I.BY_NAME[args.workload]
+    slices = I.sampled_slices(w, min(w.BH, args.steps + args.warmup))
+    per_slice = (flops(w, "fwd") + flops(w, "bwd")) / w.BH
+    times = []
+    for i, (b, h) in enumerate(slices[: args.warmup + args.steps]):
+        q, k, v, do = (I.to_f64(I.make_slice(w, b, h, t)) for t in ("q", "k", "v", "do"))
+        t0 = time.perf_counter()
+        OA.attention_forward(q, k, v, w.causal, w.scale)
+        OA.attention_backward(q, k, v, do, w.causal, w.scale)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = per_slice * len(times) / total / 1e12
+    cores = os.cpu_count() or 1
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": 1,
+        "steps": len(times), "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, same generator as the CUDA arm)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "step": "one (b,h) slice, forward + backward"},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                         "sample": f"{len(times)} (b,h) slices of {w.name}, fp64 numpy oracle"},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

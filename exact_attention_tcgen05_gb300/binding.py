@@ -31,6 +31,8 @@ SIGNATURES = {
     "attn_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_bwd_preprocess": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "attn_bwd_dkv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_bwd_dq": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_status_str": (ctypes.c_char_p, [_I]),
     "attn_last_kernel_status": (_I, [_P, ctypes.POINTER(_I)]),
 }
@@ -166,6 +168,54 @@ def attn_bwd_preprocess(o: torch.Tensor, do: torch.Tensor,
                                           N, d, _DTYPE_CODES[o.dtype], _stream_handle(stream))
     _check("attn_bwd_preprocess", code)
     return delta
+
+
+def attn_bwd_dkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, lse: torch.Tensor,
+                 delta: torch.Tensor, do: torch.Tensor, causal: bool = False,
+                 scale: Optional[float] = None, dk: Optional[torch.Tensor] = None,
+                 dv: Optional[torch.Tensor] = None,
+                 stream: Optional[torch.cuda.Stream] = None
+                 ) -> tuple[torch.Tensor, torch.Tensor]:
+    """dk, dv from the dK/dV kernel alone (delta from attn_bwd_preprocess)."""
+    B, H, N, d = _shape_of(q, "q")
+    for name, x in (("k", k), ("v", v), ("do", do)):
+        _same(q, x, name)
+    lse = _lse_like(q, lse, "lse")
+    delta = _lse_like(q, delta, "delta")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    _same(q, dk, "dk")
+    _same(q, dv, "dv")
+    with torch.cuda.device(q.device):
+        code = load().attn_bwd_dkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), lse.data_ptr(),
+                                   delta.data_ptr(), do.data_ptr(), dk.data_ptr(),
+                                   dv.data_ptr(), B, H, N, d, _DTYPE_CODES[q.dtype],
+                                   int(causal), scale, _stream_handle(stream))
+    _check("attn_bwd_dkv", code)
+    return dk, dv
+
+
+def attn_bwd_dq(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, lse: torch.Tensor,
+                delta: torch.Tensor, do: torch.Tensor, causal: bool = False,
+                scale: Optional[float] = None, dq: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """dq from the dQ kernel alone (delta from attn_bwd_preprocess)."""
+    B, H, N, d = _shape_of(q, "q")
+    for name, x in (("k", k), ("v", v), ("do", do)):
+        _same(q, x, name)
+    lse = _lse_like(q, lse, "lse")
+    delta = _lse_like(q, delta, "delta")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    _same(q, dq, "dq")
+    with torch.cuda.device(q.device):
+        code = load().attn_bwd_dq(q.data_ptr(), k.data_ptr(), v.data_ptr(), lse.data_ptr(),
+                                  delta.data_ptr(), do.data_ptr(), dq.data_ptr(), B, H, N, d,
+                                  _DTYPE_CODES[q.dtype], int(causal), scale,
+                                  _stream_handle(stream))
+    _check("attn_bwd_dq", code)
+    return dq
 
 
 def attn_last_kernel_status(stream: Optional[torch.cuda.Stream] = None) -> tuple[int, int]:

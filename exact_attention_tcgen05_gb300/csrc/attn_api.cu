@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
+#include <initializer_list>
 #include <mutex>
 
 #include <cuda.h>
@@ -168,6 +169,76 @@ attn_status attn_bwd_preprocess(const void* o, const void* dO, float* delta, int
   return from_cuda(attn::launch_delta(s, o, dO, delta, static_cast<cudaStream_t>(cuda_stream)));
 }
 
+namespace {
+
+// Validation shared by the backward entry points. `outs` must not overlap `ins` or
+// each other.
+attn_status check_ranges(const Range* ins, int n_in, const Range* outs, int n_out) {
+  for (int a = 0; a < n_out; ++a) {
+    for (int i = 0; i < n_in; ++i)
+      if (overlap(outs[a], ins[i])) return ATTN_ERR_INVALID_ARG;
+    for (int b = a + 1; b < n_out; ++b)
+      if (overlap(outs[a], outs[b])) return ATTN_ERR_INVALID_ARG;
+  }
+  return ATTN_OK;
+}
+
+attn_status check_ptrs(std::initializer_list<const void*> ptrs) {
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+attn_status encode_bwd_maps(Maps* m, const void* q, const void* k, const void* v,
+                            const void* dO, const Shape& s) {
+  attn_status st;
+  if ((st = encode_map(&m->q, q, s.BH, s.N, s.d, s.bf16)) != ATTN_OK) return st;
+  if ((st = encode_map(&m->k, k, s.BH, s.N, s.d, s.bf16)) != ATTN_OK) return st;
+  if ((st = encode_map(&m->v, v, s.BH, s.N, s.d, s.bf16)) != ATTN_OK) return st;
+  return encode_map(&m->d_o, dO, s.BH, s.N, s.d, s.bf16);
+}
+
+}  // namespace
+
+attn_status attn_bwd_dkv(const void* q, const void* k, const void* v, const float* lse,
+                         const float* delta, const void* dO, void* dk, void* dv, int B, int H,
+                         int N, int d, attn_dtype dtype, int causal, float scale,
+                         void* cuda_stream) {
+  attn_status st = check_shape(B, H, N, d, dtype);
+  if (st != ATTN_OK) return st;
+  if ((st = check_scale(scale)) != ATTN_OK) return st;
+  if ((st = check_ptrs({q, k, v, lse, delta, dO, dk, dv})) != ATTN_OK) return st;
+  const size_t tb = (size_t)B * H * N * d * 2, lb = (size_t)B * H * N * 4;
+  const Range ins[6] = {range_of(q, tb),   range_of(k, tb),     range_of(v, tb),
+                        range_of(lse, lb), range_of(delta, lb), range_of(dO, tb)};
+  const Range outs[2] = {range_of(dk, tb), range_of(dv, tb)};
+  if ((st = check_ranges(ins, 6, outs, 2)) != ATTN_OK) return st;
+  const Shape s = make_shape(B, H, N, d, dtype, causal, scale);
+  Maps m;
+  if ((st = encode_bwd_maps(&m, q, k, v, dO, s)) != ATTN_OK) return st;
+  return from_cuda(
+      attn::launch_dkv(m, s, lse, delta, dk, dv, static_cast<cudaStream_t>(cuda_stream)));
+}
+
+attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const float* lse,
+                        const float* delta, const void* dO, void* dq, int B, int H, int N,
+                        int d, attn_dtype dtype, int causal, float scale, void* cuda_stream) {
+  attn_status st = check_shape(B, H, N, d, dtype);
+  if (st != ATTN_OK) return st;
+  if ((st = check_scale(scale)) != ATTN_OK) return st;
+  if ((st = check_ptrs({q, k, v, lse, delta, dO, dq})) != ATTN_OK) return st;
+  const size_t tb = (size_t)B * H * N * d * 2, lb = (size_t)B * H * N * 4;
+  const Range ins[6] = {range_of(q, tb),   range_of(k, tb),     range_of(v, tb),
+                        range_of(lse, lb), range_of(delta, lb), range_of(dO, tb)};
+  const Range outs[1] = {range_of(dq, tb)};
+  if ((st = check_ranges(ins, 6, outs, 1)) != ATTN_OK) return st;
+  const Shape s = make_shape(B, H, N, d, dtype, causal, scale);
+  Maps m;
+  if ((st = encode_bwd_maps(&m, q, k, v, dO, s)) != ATTN_OK) return st;
+  return from_cuda(
+      attn::launch_dq(m, s, lse, delta, dq, static_cast<cudaStream_t>(cuda_stream)));
+}
+
 attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                      const float* lse, const void* dO, void* dq, void* dk, void* dv,
                      void* workspace, int B, int H, int N, int d, attn_dtype dtype, int causal,
@@ -175,28 +246,17 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   attn_status st = check_shape(B, H, N, d, dtype);
   if (st != ATTN_OK) return st;
   if ((st = check_scale(scale)) != ATTN_OK) return st;
-  const void* ptrs[10] = {q, k, v, o, lse, dO, dq, dk, dv, workspace};
-  for (const void* p : ptrs)
-    if (p == nullptr || !aligned16(p)) return ATTN_ERR_INVALID_ARG;
-  const size_t tb = (size_t)B * H * N * d * 2;
-  const size_t lb = (size_t)B * H * N * 4;
-  const Range ins[6] = {range_of(q, tb), range_of(k, tb), range_of(v, tb),
+  if ((st = check_ptrs({q, k, v, o, lse, dO, dq, dk, dv, workspace})) != ATTN_OK) return st;
+  const size_t tb = (size_t)B * H * N * d * 2, lb = (size_t)B * H * N * 4;
+  const Range ins[6] = {range_of(q, tb), range_of(k, tb),   range_of(v, tb),
                         range_of(o, tb), range_of(lse, lb), range_of(dO, tb)};
   const Range outs[4] = {range_of(dq, tb), range_of(dk, tb), range_of(dv, tb),
                          range_of(workspace, lb)};
-  for (int a = 0; a < 4; ++a) {
-    for (const Range& in : ins)
-      if (overlap(outs[a], in)) return ATTN_ERR_INVALID_ARG;
-    for (int b = a + 1; b < 4; ++b)
-      if (overlap(outs[a], outs[b])) return ATTN_ERR_INVALID_ARG;
-  }
+  if ((st = check_ranges(ins, 6, outs, 4)) != ATTN_OK) return st;
 
   const Shape s = make_shape(B, H, N, d, dtype, causal, scale);
   Maps m;
-  if ((st = encode_map(&m.q, q, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
-  if ((st = encode_map(&m.k, k, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
-  if ((st = encode_map(&m.v, v, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
-  if ((st = encode_map(&m.d_o, dO, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
+  if ((st = encode_bwd_maps(&m, q, k, v, dO, s)) != ATTN_OK) return st;
   cudaStream_t cs = static_cast<cudaStream_t>(cuda_stream);
   float* delta = static_cast<float*>(workspace);
   cudaError_t e = attn::launch_delta(s, o, dO, delta, cs);

@@ -27,8 +27,9 @@
  *            is enqueued on it; the calls never synchronise the device and return
  *            as soon as the launches are queued.
  *   Ownership the caller allocates and owns every buffer and the stream. The library
- *            allocates no device memory, keeps no state between calls (tensor maps
- *            are encoded per call) and is safe to call from several host threads.
+ *            allocates no device memory and keeps no state between calls (tensor
+ *            maps are encoded per call); its only device globals are the status
+ *            words described under Errors. Safe to call from several host threads.
  *   Errors   ATTN_ERR_INVALID_ARG for a bad size, pointer, alignment, scale or an
  *            output that overlaps an input (checked on the host before any CUDA
  *            call); ATTN_ERR_UNSUPPORTED for a head dimension or type the kernels do
@@ -110,6 +111,31 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
  */
 attn_status attn_bwd_preprocess(const void* o, const void* dO, float* delta, int B, int H,
                                 int N, int d, attn_dtype dtype, void* cuda_stream);
+
+/*
+ * attn_bwd_dkv - step 2 of attn_bwd alone ("Triton 05: Flash Attention", section
+ * 3단계 커널 구조, [2단계] dKV 커널): one CTA per block of 128 keys of one (b, h) slice
+ * holds K_j, V_j on chip and loops over the query blocks that see them:
+ *   P_ij = exp(S_ij - L_i), dV_j = sum_i P_ij dO_i, dS_ij = P_ij (dO_i . v_j - D_i),
+ *   dK_j = scale * sum_i dS_ij q_i.
+ * q, k, v, dO: [B, H, N, d] 16-bit; lse, delta: [B, H, N] float32 (delta from
+ * attn_bwd_preprocess); dk, dv: [B, H, N, d] outputs, must not overlap any input or
+ * each other. All device pointers, 16-byte aligned.
+ */
+attn_status attn_bwd_dkv(const void* q, const void* k, const void* v, const float* lse,
+                         const float* delta, const void* dO, void* dk, void* dv, int B, int H,
+                         int N, int d, attn_dtype dtype, int causal, float scale,
+                         void* cuda_stream);
+
+/*
+ * attn_bwd_dq - step 3 of attn_bwd alone ("Triton 05: Flash Attention", section
+ * 3단계 커널 구조, [3단계] dQ 커널): one CTA per block of 128 query rows holds Q_i and
+ * dO_i on chip and loops over the visible key blocks: dQ_i = scale * sum_j dS_ij k_j.
+ * Same inputs as attn_bwd_dkv; dq: [B, H, N, d] output that must not overlap them.
+ */
+attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const float* lse,
+                        const float* delta, const void* dO, void* dq, int B, int H, int N,
+                        int d, attn_dtype dtype, int causal, float scale, void* cuda_stream);
 
 /* attn_status_str - static, NUL-terminated name of a status code. */
 const char* attn_status_str(attn_status s);

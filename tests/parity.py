@@ -5,7 +5,9 @@ Tolerances (the bar the CUDA path must meet against the oracle):
   O    max-abs <= 1e-2 where |O_ref| < 4; where |O_ref| >= 4, one output-dtype ulp of
        O_ref is added (bf16 storage rounding alone is 0.0156 there);
   LSE  max-abs <= 1e-3;
-  dQ, dK, dV  relative Frobenius error <= 3e-2 per (b, h) slice.
+  dQ, dK, dV  relative Frobenius error <= 3e-2 per (b, h) slice, with an absolute
+       floor of 1e-5 RMS for gradients that vanish exactly (e.g. N = 1 causal, where
+       dS = P (dP - D) = 0, so dQ = dK = 0 and only fp32 rounding is left).
 """
 from __future__ import annotations
 
@@ -21,6 +23,7 @@ from exact_attention_tcgen05_gb300 import inputs as I
 O_TOL = 1e-2
 LSE_TOL = 1e-3
 GRAD_TOL = 3e-2
+GRAD_RMS_FLOOR = 1e-5
 
 
 @dataclasses.dataclass
@@ -65,7 +68,9 @@ def o_error(o_gpu: np.ndarray, o_ref: np.ndarray, dtype) -> tuple[float, float]:
 
 
 def rel_fro(a: np.ndarray, b: np.ndarray) -> float:
-    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+    """||a - b||_F / max(||b||_F, floor * sqrt(numel))."""
+    floor = GRAD_RMS_FLOOR * np.sqrt(b.size)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), floor))
 
 
 def compare_slice(w: I.Workload, run: GpuRun, b: int, h: int, backward=True) -> dict:

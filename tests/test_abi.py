@@ -28,7 +28,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes",
-                     "attn_bwd_preprocess", "attn_status_str", "attn_last_kernel_status"):
+                     "attn_bwd_preprocess", "attn_bwd_dkv", "attn_bwd_dq", "attn_status_str",
+                     "attn_last_kernel_status"):
         assert required in names
 
 
@@ -96,6 +97,20 @@ def test_fwd_rejects_bad_arguments(lib, kw, code):
 ])
 def test_bwd_rejects_bad_arguments(lib, kw, code):
     assert bwd(lib, **kw) == code
+
+
+def test_stage_entry_points_reject_bad_arguments(lib):
+    dkv = lambda dk=DK, dv=DV, d=128, lse=L: lib.attn_bwd_dkv(Q, K, V, lse, WS, DO, dk, dv, 1, 1,
+                                                              256, d, 1, 1, 0.1, None)
+    assert dkv(dk=DV) == INVALID
+    assert dkv(dk=Q) == INVALID
+    assert dkv(lse=0) == INVALID
+    assert dkv(d=80) == UNSUPPORTED
+    dq = lambda out=DQ, scale=0.1: lib.attn_bwd_dq(Q, K, V, L, WS, DO, out, 1, 1, 256, 64, 0, 0,
+                                                   scale, None)
+    assert dq(out=WS) == INVALID
+    assert dq(out=DQ + 4) == INVALID
+    assert dq(scale=-2.0) == INVALID
 
 
 def test_preprocess_rejects_bad_arguments(lib):
