@@ -20,6 +20,10 @@
 //    16-bit pairs and fed to the P V product straight from tensor memory.
 //  * exp is exp2 with scale*log2(e) folded into one FFMA per score ("Triton 05",
 //    section 2. exp -> exp2 트릭); L is exported in the natural log.
+//  * P is rounded to the input type for P V (the Triton code's p.to(v.dtype)). O is
+//    divided by the sum of those same rounded values, so numerator and denominator use
+//    one set of weights (the mismatch that "FlashAttention·FA4·FP4", FP4 section, warns
+//    about); L uses the unrounded sum.
 //  * The O rescale is conditional: the running max used for exp2 is only moved when
 //    the row max grows by more than 8 (a factor 256), otherwise the stale max is kept
 //    for both the numerator and l, which leaves O = acc / l exact ("FlashAttention·
@@ -248,7 +252,8 @@ __global__ void __launch_bounds__(320, 1)
     const int tile_row0 = q0 + t * kTileM;
     const float sl2 = p.scale_log2;
     float m = -INFINITY;  // running max of scale*log2(e)*S (possibly stale by <= 8)
-    float l = 0.f;
+    float l = 0.f;        // sum of exp2 values (fp32)
+    float lr = 0.f;       // sum of the same values after rounding to 16 bits
     bool ok = true;
     for (int j = 0; j < nkv[t]; ++j) {
       if (!(ok = warp_wait(&s_full[t], j & 1, limit, abort_flag, kWaitFwdS))) break;
@@ -286,7 +291,9 @@ __global__ void __launch_bounds__(320, 1)
         m = m_cand;
       }
       const float neg_m = -m;
-      float sum0 = 0.f, sum1 = 0.f;
+      // l sums the fp32 values (it defines L); lr sums the 16-bit values that enter
+      // P V, so that O = acc / lr divides by exactly the weights it accumulated.
+      float sum0 = 0.f, sum1 = 0.f, rsum0 = 0.f, rsum1 = 0.f;
 #pragma unroll
       for (int c4 = 0; c4 < kTileN / 32; ++c4) {
         uint32_t pk[16];
@@ -297,10 +304,14 @@ __global__ void __launch_bounds__(320, 1)
           sum0 += p0;
           sum1 += p1;
           pk[i] = pack2<BF16>(p0, p1);
+          const float2 r = unpack2<BF16>(pk[i]);
+          rsum0 += r.x;
+          rsum1 += r.y;
         }
         tmem_st16(t_s + c4 * 16, pk);
       }
       l = l * alpha + (sum0 + sum1);
+      lr = lr * alpha + (rsum0 + rsum1);
       if (j > 0 && __any_sync(0xffffffffu, need)) {
         // Bring O to the new max: wait until the previous P V product has landed.
         if (!(ok = warp_wait(&o_done[t], (j - 1) & 1, limit, abort_flag, kWaitFwdO))) break;
@@ -321,7 +332,7 @@ __global__ void __launch_bounds__(320, 1)
     if (ok && nkv[t] > 0 &&
         warp_wait(&o_done[t], (nkv[t] - 1) & 1, limit, abort_flag, kWaitFwdO)) {
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float inv_l = 1.f / lr;
       uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
                       ((size_t)bh * N + (size_t)row) * (size_t)(D * 2);
 #pragma unroll

@@ -2,8 +2,10 @@
 inputs, run the fp64 oracle on the same rounded inputs, and compare.
 
 Tolerances (the bar the CUDA path must meet against the oracle):
-  O    max-abs <= 1e-2 where |O_ref| < 4; where |O_ref| >= 4, one output-dtype ulp of
-       O_ref is added (bf16 storage rounding alone is 0.0156 there);
+  O    |O_gpu - O_ref| <= 1e-2 + half an ulp of the output type at |O_ref|: 1e-2 is
+       the computation's budget and the output's own storage rounding (bf16: up to
+       0.0078 for |O| in [2, 4)) comes on top, since no kernel that stores 16-bit
+       outputs can avoid it;
   LSE  max-abs <= 1e-3;
   dQ, dK, dV  relative Frobenius error <= 3e-2 per (b, h) slice, with an absolute
        floor of 1e-5 RMS for gradients that vanish exactly (e.g. N = 1 causal, where
@@ -63,7 +65,7 @@ def ulp(x: np.ndarray, dtype: torch.dtype) -> np.ndarray:
 def o_error(o_gpu: np.ndarray, o_ref: np.ndarray, dtype) -> tuple[float, float]:
     """(max raw error, max excess over the allowed bound); pass iff excess <= 0."""
     err = np.abs(o_gpu - o_ref)
-    allowed = np.where(np.abs(o_ref) < 4.0, O_TOL, O_TOL + ulp(o_ref, dtype))
+    allowed = O_TOL + 0.5 * ulp(o_ref, dtype)
     return float(err.max()), float((err - allowed).max())
 
 
