@@ -33,6 +33,8 @@ SIGNATURES = {
     "attn_bwd_preprocess": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "attn_bwd_dkv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_bwd_dq": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F,
+                              _P]),
     "attn_status_str": (ctypes.c_char_p, [_I]),
     "attn_last_kernel_status": (_I, [_P, ctypes.POINTER(_I)]),
 }
@@ -153,6 +155,39 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
                                _DTYPE_CODES[q.dtype], int(causal), scale,
                                _stream_handle(stream))
     _check("attn_bwd", code)
+    return dq, dk, dv
+
+
+NOALLOC_MAX_ROWS = 4194304  # ATTN_NOALLOC_MAX_ROWS in include/attn.h
+
+
+def attn_bwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                     lse: torch.Tensor, do: torch.Tensor, causal: bool = False,
+                     scale: Optional[float] = None, dq: Optional[torch.Tensor] = None,
+                     dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
+                     stream: Optional[torch.cuda.Stream] = None
+                     ) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """attn_bwd for callers that cannot allocate a workspace: the library's own
+    fixed-size scratch array holds the per-row D values (B*H*N <= NOALLOC_MAX_ROWS).
+    Calls that overlap on the GPU share that array and race; serialise them. This
+    wrapper still lets torch allocate dq, dk, dv when they are not passed in."""
+    B, H, N, d = _shape_of(q, "q")
+    for name, x in (("k", k), ("v", v), ("o", o), ("do", do)):
+        _same(q, x, name)
+    lse = _lse_like(q, lse, "lse")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for name, x in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _same(q, x, name)
+    with torch.cuda.device(q.device):
+        code = load().attn_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                       lse.data_ptr(), do.data_ptr(), dq.data_ptr(),
+                                       dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+                                       _DTYPE_CODES[q.dtype], int(causal), scale,
+                                       _stream_handle(stream))
+    _check("attn_bwd_noalloc", code)
     return dq, dk, dv
 
 

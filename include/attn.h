@@ -137,6 +137,30 @@ attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const float
                         const float* delta, const void* dO, void* dq, int B, int H, int N,
                         int d, attn_dtype dtype, int causal, float scale, void* cuda_stream);
 
+/*
+ * attn_bwd_noalloc - attn_bwd for callers that cannot allocate device memory, such as a
+ * plugin inside a host engine that owns all device memory and offers no allocator or
+ * workspace, or a serving loop that forbids cudaMalloc after start-up because it can
+ * synchronise the device and stall other streams. The pages have no counterpart: this
+ * entry point exists only for such callers.
+ * Same arguments, layouts, results and errors as attn_bwd, minus `workspace`: the D
+ * values live in a float32 array of ATTN_NOALLOC_MAX_ROWS entries (16 MiB) inside the
+ * library, in device memory that every GPU which loads the library reserves until the
+ * process exits. B * H * N above ATTN_NOALLOC_MAX_ROWS returns ATTN_ERR_INVALID_ARG.
+ * Neither the library nor this call allocates anything.
+ * The first call on a device looks up that device's address of the array (a
+ * cudaGetSymbolAddress with the device current); make that first call before any stream
+ * capture on the device. Every call shares the one array and it keeps the last call's
+ * values: calls whose work can overlap on the GPU (other streams, or host threads with
+ * no ordering between them) race on it and produce wrong gradients, so serialise them.
+ * Nothing in it has to start at zero: each call writes every entry it reads.
+ */
+#define ATTN_NOALLOC_MAX_ROWS 4194304
+attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                             const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                             int B, int H, int N, int d, attn_dtype dtype, int causal,
+                             float scale, void* cuda_stream);
+
 /* attn_status_str - static, NUL-terminated name of a status code. */
 const char* attn_status_str(attn_status s);
 
