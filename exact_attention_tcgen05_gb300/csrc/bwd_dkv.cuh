@@ -9,6 +9,12 @@
 //   dP^T = V_j dO_i^T,      dS^T = P^T * (dP^T - D_i),  dK_j += scale * dS^T Q_i.
 // P^T and dS^T are written back over S^T and dP^T as 16-bit pairs and used as the A
 // operand of the two accumulating products straight from tensor memory.
+//
+// Roles (10 warps): warps 0-3 and 4-7 are two softmax warpgroups that share each key row
+// (thread = key row = TMEM lane); group g handles queries [64g, 64g + 64) of the block, so
+// a thread does 64 exponentials per block and every SM sub-partition runs two softmax
+// warps. Group g writes its 16-bit pairs into columns [64g, 64g + 32) of the region it
+// read, where no other thread reads. Warp 8: TMA producer; warp 9: MMA issuer.
 // Tensor memory: S^T (128 cols), dP^T (128), dV (d), dK (d).
 #pragma once
 
@@ -19,6 +25,7 @@ namespace attn {
 template <int D>
 struct DkvCfg : BwdCfg<D> {
   using B = BwdCfg<D>;
+  static constexpr int kThreads = 320;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + B::kTileBytes;
   static constexpr int kOffQ = kOffV + B::kTileBytes;
@@ -34,7 +41,7 @@ struct DkvCfg : BwdCfg<D> {
 };
 
 template <int D, bool BF16>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k,
                         const __grid_constant__ CUtensorMap map_v,
@@ -76,17 +83,17 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&qdo_empty[s], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, 128);
+    mbar_init(p_full, 256);
     mbar_init(dp_full, 1);
-    mbar_init(ds_full, 128);
+    mbar_init(ds_full, 256);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
-    mbar_init(&stats_ready[0], 128);
-    mbar_init(&stats_ready[1], 128);
+    mbar_init(&stats_ready[0], 256);
+    mbar_init(&stats_ready[1], 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_holder, C::kTmemCols);
     tmem_relinquish();
     tc_fence_before();
@@ -96,7 +103,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = *tmem_holder;
   const uint64_t limit = p.wait_limit;
 
-  if (warp == 4) {
+  if (warp == 8) {
     if (lane == 0) {
       tma_prefetch_map(&map_q);
       tma_prefetch_map(&map_k);
@@ -132,7 +139,7 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     if (lane == 0) {
       const uint32_t idesc_st = make_idesc(BF16, 128, kTileM, false, false);
       const uint32_t idesc_acc = make_idesc(BF16, 128, D, false, true);
@@ -160,8 +167,8 @@ __global__ void __launch_bounds__(192, 1)
         if (!(ok = mbar_wait(p_full, it & 1, limit, abort_flag, kWaitDkvP))) break;
         tc_fence_after();
         // dV_j += P^T dO_i
-        issue_tmem_a(tmem + C::kColAcc0, tmem + C::kColS, sdo + s * C::kTileBytes, idesc_acc,
-                     it > 0);
+        issue_tmem_a_split(tmem + C::kColAcc0, tmem + C::kColS, sdo + s * C::kTileBytes,
+                           idesc_acc, it > 0);
         if (in < n) {
           if (!(ok = mbar_wait(&q_full[sn], (in / NS) & 1, limit, abort_flag, kWaitDkvQ))) break;
           tc_fence_after();
@@ -171,8 +178,8 @@ __global__ void __launch_bounds__(192, 1)
         if (!(ok = mbar_wait(ds_full, it & 1, limit, abort_flag, kWaitDkvDS))) break;
         tc_fence_after();
         // dK_j += dS^T Q_i
-        issue_tmem_a(tmem + C::kColAcc1, tmem + C::kColDP, sq + s * C::kTileBytes, idesc_acc,
-                     it > 0);
+        issue_tmem_a_split(tmem + C::kColAcc1, tmem + C::kColDP, sq + s * C::kTileBytes,
+                           idesc_acc, it > 0);
         if (in < n) {
           if (!(ok = mbar_wait(&do_full[sn], (in / NS) & 1, limit, abort_flag, kWaitDkvDO)))
             break;
@@ -187,97 +194,103 @@ __global__ void __launch_bounds__(192, 1)
       mbar_wait(drain, 0, limit, nullptr, kWaitDkvDrain);
     }
   } else {
-    // warps 0-3: one thread per key row
-    const int wq = warp;
+    // warps 0-7: thread = key row (TMEM lane); group g covers queries [64g, 64g + 64)
+    const int g = warp >> 2;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;  // 0..127
+    const int key = j0 + row;
+    const int c0 = g * 64;           // first query column of this group
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    const uint32_t t_s = tmem + lane_base + C::kColS;
-    const uint32_t t_dp = tmem + lane_base + C::kColDP;
-    const int tid = threadIdx.x;        // 0..127
-    const int key = j0 + tid;           // key index of this thread
-    const float sl2 = p.scale_log2;
-    const float* lse_bh = p.lse + (size_t)bh * N;
-    const float* dl_bh = p.delta + (size_t)bh * N;
-    // Prefetch the statistics of the first query block.
-    auto load_stats = [&](int i, float& nl2, float& dl) {
-      const int q = i * kTileM + tid;
-      nl2 = -INFINITY;
-      dl = 0.f;
-      if (q < N) {
-        nl2 = -lse_bh[q] * kLog2e;
-        dl = dl_bh[q];
-      }
+    const uint32_t t_s = tmem + lane_base + C::kColS + c0;
+    const uint32_t t_dp = tmem + lane_base + C::kColDP + c0;
+    const float2 sl2x2 = make_float2(p.scale_log2, p.scale_log2);
+    // Group 0 stages -L*log2(e), group 1 stages D: one value per thread per query block.
+    const float* src = (g == 0 ? p.lse : p.delta) + (size_t)bh * N;
+    auto load_stat = [&](int i) -> float {
+      const int q = i * kTileM + row;
+      if (q >= N) return g == 0 ? -INFINITY : 0.f;  // padding queries: P = 0, D = 0
+      const float x = src[q];
+      return g == 0 ? -x * kLog2e : x;
     };
-    float nl2_next, dl_next;
-    load_stats(i_first, nl2_next, dl_next);
+    float stat_next = load_stat(i_first);
     bool ok = true;
     for (int it = 0; it < n; ++it) {
       const int i = i_first + it;
       // Double-buffered statistics: buffer it&1 was last read in iteration it-2, and
-      // every thread has passed iteration it-1's stats_ready wait, which needs all 128
+      // every thread has passed iteration it-1's stats_ready wait, which needs all 256
       // arrivals, so nobody still reads it.
       float* st = stats + (it & 1) * 256;
-      st[tid] = nl2_next;
-      st[128 + tid] = dl_next;
+      st[g * 128 + row] = stat_next;
       mbar_arrive(&stats_ready[it & 1]);
-      if (it + 1 < n) load_stats(i + 1, nl2_next, dl_next);
+      if (it + 1 < n) stat_next = load_stat(i + 1);
       if (!(ok = warp_wait(&stats_ready[it & 1], (it >> 1) & 1, limit, abort_flag,
                            kWaitDkvStats)))
         break;
 
+      // ---- P^T = exp2(S^T * scale * log2(e) - L * log2(e)), 16-bit pairs over S^T
       if (!(ok = warp_wait(s_full, it & 1, limit, abort_flag, kWaitDkvS))) break;
       tc_fence_after();
-      float pr[kTileM];
+      uint32_t sr[64];
+      tmem_ld64(t_s, sr);
+      float* pr = reinterpret_cast<float*>(sr);
+      const float4* nl4 = reinterpret_cast<const float4*>(st + c0);
 #pragma unroll
-      for (int c4 = 0; c4 < kTileM / 32; ++c4) {
-        uint32_t r[32];
-        tmem_ld32(t_s + c4 * 32, r);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) pr[c4 * 32 + c] = __uint_as_float(r[c]);
-      }
-      // Causal: on the diagonal block query q = i*128 + c sees this key iff q >= key.
-      const int lo = (p.causal && i == jb) ? (key - i * kTileM) : 0;  // first visible c
-      const float4* nl4 = reinterpret_cast<const float4*>(st);
-#pragma unroll
-      for (int c4 = 0; c4 < kTileM / 4; ++c4) {
+      for (int c4 = 0; c4 < 16; ++c4) {
         const float4 nl = nl4[c4];
-        const float nlv[4] = {nl.x, nl.y, nl.z, nl.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int c = c4 * 4 + u;
-          pr[c] = (c < lo) ? 0.f : ex2(fmaf(pr[c], sl2, nlv[u]));
-        }
+        const float2 a = fma2(make_float2(pr[4 * c4], pr[4 * c4 + 1]), sl2x2,
+                              make_float2(nl.x, nl.y));
+        const float2 b = fma2(make_float2(pr[4 * c4 + 2], pr[4 * c4 + 3]), sl2x2,
+                              make_float2(nl.z, nl.w));
+        pr[4 * c4] = ex2(a.x);
+        pr[4 * c4 + 1] = ex2(a.y);
+        pr[4 * c4 + 2] = ex2(b.x);
+        pr[4 * c4 + 3] = ex2(b.y);
       }
+      if (p.causal && i == jb) {
+        // Diagonal block: query column c0 + c sees this key iff c0 + c >= row.
 #pragma unroll
-      for (int c4 = 0; c4 < kTileM / 32; ++c4) {
-        uint32_t pk[16];
+        for (int c = 0; c < 64; ++c)
+          if (c0 + c < row) pr[c] = 0.f;
+      }
+      {
+        uint32_t pk[32];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) pk[u] = pack2<BF16>(pr[c4 * 32 + 2 * u], pr[c4 * 32 + 2 * u + 1]);
-        tmem_st16(t_s + c4 * 16, pk);
+        for (int u = 0; u < 32; ++u) pk[u] = pack2<BF16>(pr[2 * u], pr[2 * u + 1]);
+        uint32_t (&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&pk[0]);
+        uint32_t (&hi)[16] = *reinterpret_cast<uint32_t(*)[16]>(&pk[16]);
+        tmem_st16(t_s, lo);
+        tmem_st16(t_s + 16, hi);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_full);
 
+      // ---- dS^T = P^T * (dP^T - D), 16-bit pairs over dP^T
       if (!(ok = warp_wait(dp_full, it & 1, limit, abort_flag, kWaitDkvDP))) break;
       tc_fence_after();
-      const float4* dl4 = reinterpret_cast<const float4*>(st + 128);
+      uint32_t r[64];
+      tmem_ld64(t_dp, r);
+      const float4* dl4 = reinterpret_cast<const float4*>(st + 128 + c0);
 #pragma unroll
-      for (int c4 = 0; c4 < kTileM / 32; ++c4) {
-        uint32_t r[32];
-        tmem_ld32(t_dp + c4 * 32, r);
-        uint32_t pk[16];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float4 dl = dl4[c4 * 8 + u];
-          const int c = c4 * 32 + 4 * u;
-          const float d0 = pr[c + 0] * (__uint_as_float(r[4 * u + 0]) - dl.x);
-          const float d1 = pr[c + 1] * (__uint_as_float(r[4 * u + 1]) - dl.y);
-          const float d2 = pr[c + 2] * (__uint_as_float(r[4 * u + 2]) - dl.z);
-          const float d3 = pr[c + 3] * (__uint_as_float(r[4 * u + 3]) - dl.w);
-          pk[2 * u] = pack2<BF16>(d0, d1);
-          pk[2 * u + 1] = pack2<BF16>(d2, d3);
-        }
-        tmem_st16(t_dp + c4 * 16, pk);
+      for (int u = 0; u < 16; ++u) {
+        const float4 dl = dl4[u];
+        const float2 d01 = mul2(make_float2(pr[4 * u], pr[4 * u + 1]),
+                                add2(make_float2(__uint_as_float(r[4 * u]),
+                                                 __uint_as_float(r[4 * u + 1])),
+                                     make_float2(-dl.x, -dl.y)));
+        const float2 d23 = mul2(make_float2(pr[4 * u + 2], pr[4 * u + 3]),
+                                add2(make_float2(__uint_as_float(r[4 * u + 2]),
+                                                 __uint_as_float(r[4 * u + 3])),
+                                     make_float2(-dl.z, -dl.w)));
+        // Pack in place: r[2u] and r[2u+1] were read in this step (u = 0) or earlier.
+        r[2 * u] = pack2<BF16>(d01.x, d01.y);
+        r[2 * u + 1] = pack2<BF16>(d23.x, d23.y);
+      }
+      {
+        uint32_t (&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&r[0]);
+        uint32_t (&hi)[16] = *reinterpret_cast<uint32_t(*)[16]>(&r[16]);
+        tmem_st16(t_dp, lo);
+        tmem_st16(t_dp + 16, hi);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -285,23 +298,23 @@ __global__ void __launch_bounds__(192, 1)
     }
     if (ok && warp_wait(acc_done, 0, limit, abort_flag, kWaitDkvDone)) {
       tc_fence_after();
+      // Group 0 writes dV, group 1 writes dK (scaled).
       const size_t off = ((size_t)bh * N + key) * (size_t)(D * 2);
-      uint8_t* dk_row = reinterpret_cast<uint8_t*>(p.out0) + off;
-      uint8_t* dv_row = reinterpret_cast<uint8_t*>(p.out1) + off;
+      uint8_t* dst = reinterpret_cast<uint8_t*>(g == 0 ? p.out1 : p.out0) + off;
+      const uint32_t t_acc = tmem + lane_base + (g == 0 ? C::kColAcc0 : C::kColAcc1);
+      const float mul = (g == 0) ? 1.f : p.scale;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_base + C::kColAcc0 + cc * 32, r);
-        if (key < N) store_row32<BF16>(dv_row + cc * 64, r, 1.f);
-        tmem_ld32(tmem + lane_base + C::kColAcc1 + cc * 32, r);
-        if (key < N) store_row32<BF16>(dk_row + cc * 64, r, p.scale);
+        uint32_t a[32];
+        tmem_ld32(t_acc + cc * 32, a);
+        if (key < N) store_row32<BF16>(dst + cc * 64, a, mul);
       }
     }
     tc_fence_before();
   }
 
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }

@@ -7,11 +7,13 @@
 // Gradient for the recomputation and the gradient). D_i comes from the preprocess
 // kernel. The factor scale on dQ follows from S = scale Q K^T.
 //
-// GB300 design: warps 0-3 turn S / dP (fp32 in tensor memory) into dS, warp 4 is the TMA
-// producer (Q_i and dO_i once, then a ring of K_j / V_j blocks), warp 5 issues the
-// tcgen05 MMAs. Tensor memory: S (128 cols), dP (128 cols), dQ accumulator (d cols).
-// dS is written back over dP as 16-bit pairs and feeds dS K_j from tensor memory; S of
-// the next block is computed while the softmax warps work on dP of this one.
+// GB300 design: warps 0-3 and 4-7 are two softmax warpgroups that share each query row
+// (thread = row = TMEM lane), group g taking keys [64g, 64g + 64) of a block; they turn
+// S and dP (fp32 in tensor memory) into dS. Warp 8 is the TMA producer (Q_i and dO_i
+// once, then a ring of K_j / V_j blocks), warp 9 issues the tcgen05 MMAs. Tensor memory:
+// S (128 cols), dP (128 cols), dQ accumulator (d cols). Group g writes its dS pairs over
+// dP columns [64g, 64g + 32), which feed dS K_j from tensor memory; S of the next block
+// is computed while the softmax warps work on dP of this one.
 #pragma once
 
 #include "common.cuh"
@@ -36,7 +38,7 @@ struct BwdCfg {
   static constexpr int kChunks = D / kBoxCols;
   static constexpr int kTileBytes = kChunks * kBoxBytes;
   static constexpr int kStages = 2;
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = 320;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
   // Each CTA takes all 512 tensor-memory columns, so at most one may be resident per SM:
@@ -94,8 +96,21 @@ __device__ __forceinline__ void issue_tmem_a(uint32_t d_tmem, uint32_t a_tmem, u
            (acc || kk > 0) ? 1u : 0u);
 }
 
+// A operand in tensor memory whose 16-bit pairs sit in two halves: columns [0, 64) of A in
+// [base, base + 32) and columns [64, 128) in [base + 64, base + 96). B is an MN-major
+// [128 x d] tile in shared memory. D[128 x d] (+)= A B.
+__device__ __forceinline__ void issue_tmem_a_split(uint32_t d_tmem, uint32_t a_tmem,
+                                                   uint32_t b0, uint32_t idesc, bool acc) {
+#pragma unroll
+  for (int kk = 0; kk < 128 / 16; ++kk) {
+    const uint32_t a_col = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
+    mma_ts(d_tmem, a_tmem + a_col, make_sdesc_sw128(b0 + kk * 2048, kBoxBytes, 1024), idesc,
+           (acc || kk > 0) ? 1u : 0u);
+  }
+}
+
 template <int D, bool BF16>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q,
                        const __grid_constant__ CUtensorMap map_k,
                        const __grid_constant__ CUtensorMap map_v,
@@ -134,15 +149,15 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&kv_empty[s], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(s_free, 128);
+    mbar_init(s_free, 256);
     mbar_init(dp_full, 1);
-    mbar_init(ds_full, 128);
+    mbar_init(ds_full, 256);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_holder, C::kTmemCols);
     tmem_relinquish();
     tc_fence_before();
@@ -152,7 +167,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = *tmem_holder;
   const uint64_t limit = p.wait_limit;
 
-  if (warp == 4) {
+  if (warp == 8) {
     if (lane == 0) {
       tma_prefetch_map(&map_q);
       tma_prefetch_map(&map_k);
@@ -187,7 +202,7 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     if (lane == 0) {
       const uint32_t idesc_sq = make_idesc(BF16, 128, kTileN, false, false);
       const uint32_t idesc_acc = make_idesc(BF16, 128, D, false, true);
@@ -213,6 +228,7 @@ __global__ void __launch_bounds__(192, 1)
         const int jn = j + 1;
         const int sn = jn % NS;
         if (jn < n) {
+          // S of the next block overwrites S once the softmax warps have read it.
           if (!(ok = mbar_wait(&k_full[sn], (jn / NS) & 1, limit, abort_flag, kWaitDqK) &&
                      mbar_wait(s_free, j & 1, limit, abort_flag, kWaitDqSC)))
             break;
@@ -222,8 +238,9 @@ __global__ void __launch_bounds__(192, 1)
         }
         if (!(ok = mbar_wait(ds_full, j & 1, limit, abort_flag, kWaitDqDS))) break;
         tc_fence_after();
-        issue_tmem_a(tmem + C::kColAcc0, tmem + C::kColDP, sk + s * C::kTileBytes, idesc_acc,
-                     j > 0);
+        // dQ_i += dS K_j (dS read from tensor memory, over dP)
+        issue_tmem_a_split(tmem + C::kColAcc0, tmem + C::kColDP, sk + s * C::kTileBytes,
+                           idesc_acc, j > 0);
         if (jn < n) {
           if (!(ok = mbar_wait(&v_full[sn], (jn / NS) & 1, limit, abort_flag, kWaitDqV))) break;
           tc_fence_after();
@@ -237,55 +254,65 @@ __global__ void __launch_bounds__(192, 1)
       mbar_wait(drain, 0, limit, nullptr, kWaitDqDrain);
     }
   } else {
-    // warps 0-3: one thread per query row
-    const int wq = warp;
+    // warps 0-7: thread = query row (TMEM lane); group g covers keys [64g, 64g + 64)
+    const int g = warp >> 2;
+    const int wq = warp & 3;
+    const int c0 = g * 64;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    const uint32_t t_s = tmem + lane_base + C::kColS;
-    const uint32_t t_dp = tmem + lane_base + C::kColDP;
-    const uint32_t t_acc = tmem + lane_base + C::kColAcc0;
+    const uint32_t t_s = tmem + lane_base + C::kColS + c0;
+    const uint32_t t_dp = tmem + lane_base + C::kColDP + c0;
     const int row = i0 + wq * 32 + lane;
-    const float sl2 = p.scale_log2;
+    const float2 sl2x2 = make_float2(p.scale_log2, p.scale_log2);
     float neg_l2 = -INFINITY;  // -L * log2(e); rows past N get P = 0
     float dlt = 0.f;
     if (row < N) {
       neg_l2 = -p.lse[(size_t)bh * N + row] * kLog2e;
       dlt = p.delta[(size_t)bh * N + row];
     }
+    const float2 nl2x2 = make_float2(neg_l2, neg_l2);
+    const float2 ndl2 = make_float2(-dlt, -dlt);
     bool ok = true;
     for (int j = 0; j < n; ++j) {
+      // ---- P = exp2(S * scale * log2(e) - L * log2(e)) for keys [c0, c0 + 64)
       if (!(ok = warp_wait(s_full, j & 1, limit, abort_flag, kWaitDqS))) break;
       tc_fence_after();
-      float pr[kTileN];
-#pragma unroll
-      for (int c4 = 0; c4 < kTileN / 32; ++c4) {
-        uint32_t r[32];
-        tmem_ld32(t_s + c4 * 32, r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pr[c4 * 32 + i] = __uint_as_float(r[i]);
-      }
+      uint32_t sr[64];
+      tmem_ld64(t_s, sr);
       tc_fence_before();
       mbar_arrive(s_free);
-      const int kbase = j * kTileN;
-      int lim = kTileN - 1;
-      if (kbase + kTileN > N) lim = N - 1 - kbase;
-      if (p.causal && kbase + kTileN - 1 > i0) lim = min(lim, row - kbase);
+      float* pr = reinterpret_cast<float*>(sr);
 #pragma unroll
-      for (int c = 0; c < kTileN; ++c)
-        pr[c] = (c > lim) ? 0.f : ex2(fmaf(pr[c], sl2, neg_l2));
+      for (int c = 0; c < 64; c += 2) {
+        const float2 x = fma2(make_float2(pr[c], pr[c + 1]), sl2x2, nl2x2);
+        pr[c] = ex2(x.x);
+        pr[c + 1] = ex2(x.y);
+      }
+      const int kbase = j * kTileN + c0;  // key index of column 0 of this group
+      if ((p.causal && kbase + 63 > i0) || kbase + 64 > N) {  // diagonal or ragged
+        int lim = N - 1 - kbase;                    // last key in range
+        if (p.causal) lim = min(lim, row - kbase);  // last key this row sees
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c > lim) pr[c] = 0.f;
+      }
+      // ---- dS = P * (dP - D), 16-bit pairs over dP
       if (!(ok = warp_wait(dp_full, j & 1, limit, abort_flag, kWaitDqDP))) break;
       tc_fence_after();
+      uint32_t r[64];
+      tmem_ld64(t_dp, r);
 #pragma unroll
-      for (int c4 = 0; c4 < kTileN / 32; ++c4) {
-        uint32_t r[32];
-        tmem_ld32(t_dp + c4 * 32, r);
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float d0 = pr[c4 * 32 + 2 * i] * (__uint_as_float(r[2 * i]) - dlt);
-          const float d1 = pr[c4 * 32 + 2 * i + 1] * (__uint_as_float(r[2 * i + 1]) - dlt);
-          pk[i] = pack2<BF16>(d0, d1);
-        }
-        tmem_st16(t_dp + c4 * 16, pk);
+      for (int u = 0; u < 32; ++u) {
+        const float2 d = mul2(make_float2(pr[2 * u], pr[2 * u + 1]),
+                              add2(make_float2(__uint_as_float(r[2 * u]),
+                                               __uint_as_float(r[2 * u + 1])),
+                                   ndl2));
+        r[u] = pack2<BF16>(d.x, d.y);  // in place: r[u] was read in this step or earlier
+      }
+      {
+        uint32_t (&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&r[0]);
+        uint32_t (&hi)[16] = *reinterpret_cast<uint32_t(*)[16]>(&r[16]);
+        tmem_st16(t_dp, lo);
+        tmem_st16(t_dp + 16, hi);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -293,19 +320,22 @@ __global__ void __launch_bounds__(192, 1)
     }
     if (ok && warp_wait(acc_done, 0, limit, abort_flag, kWaitDqDone)) {
       tc_fence_after();
-      uint8_t* drow = reinterpret_cast<uint8_t*>(p.out0) + ((size_t)bh * N + row) * (size_t)(D * 2);
+      // Group g writes columns [g*d/2, (g+1)*d/2) of dQ, scaled.
+      uint8_t* drow = reinterpret_cast<uint8_t*>(p.out0) +
+                      ((size_t)bh * N + row) * (size_t)(D * 2) + g * D;
+      const uint32_t t_acc = tmem + lane_base + C::kColAcc0 + g * (D / 2);
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t r[32];
-        tmem_ld32(t_acc + cc * 32, r);
-        if (row < N) store_row32<BF16>(drow + cc * 64, r, p.scale);
+      for (int cc = 0; cc < D / 64; ++cc) {
+        uint32_t a[32];
+        tmem_ld32(t_acc + cc * 32, a);
+        if (row < N) store_row32<BF16>(drow + cc * 64, a, p.scale);
       }
     }
     tc_fence_before();
   }
 
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }

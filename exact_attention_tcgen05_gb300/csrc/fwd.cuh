@@ -258,14 +258,10 @@ __global__ void __launch_bounds__(320, 1)
     for (int j = 0; j < nkv[t]; ++j) {
       if (!(ok = warp_wait(&s_full[t], j & 1, limit, abort_flag, kWaitFwdS))) break;
       tc_fence_after();
-      float s[kTileN];
-#pragma unroll
-      for (int c4 = 0; c4 < kTileN / 32; ++c4) {
-        uint32_t r[32];
-        tmem_ld32(t_s + c4 * 32, r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c4 * 32 + i] = __uint_as_float(r[i]);
-      }
+      // One wide load of the whole score row, then a single wait.
+      uint32_t sr[kTileN];
+      tmem_ld128(t_s, sr);
+      float* s = reinterpret_cast<float*>(sr);
       const int kbase = j * kTileN;
       const bool diag = p.causal && (kbase + kTileN - 1 > tile_row0);
       if (diag || kbase + kTileN > N) {
@@ -275,41 +271,39 @@ __global__ void __launch_bounds__(320, 1)
         for (int c = 0; c < kTileN; ++c)
           if (c > lim) s[c] = -INFINITY;
       }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+      float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
 #pragma unroll
-      for (int c = 4; c < kTileN; c += 4) {
-        mx0 = fmaxf(mx0, s[c]);
-        mx1 = fmaxf(mx1, s[c + 1]);
-        mx2 = fmaxf(mx2, s[c + 2]);
-        mx3 = fmaxf(mx3, s[c + 3]);
+      for (int c = 6; c < kTileN - 2; c += 4) {
+        mx0 = fmax3(mx0, s[c], s[c + 1]);
+        mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
       }
-      const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const float m_cand = fmax3(mx0, mx1, fmaxf(s[kTileN - 2], s[kTileN - 1])) * sl2;
       const bool need = m_cand > m + 8.0f;
       float alpha = 1.f;
       if (need) {
         alpha = ex2(m - m_cand);  // 0 on the first block (m = -inf)
         m = m_cand;
       }
-      const float neg_m = -m;
+      const float2 sl2x2 = make_float2(sl2, sl2);
+      const float2 neg_m2 = make_float2(-m, -m);
       // l sums the fp32 values (it defines L); lr sums the 16-bit values that enter
       // P V, so that O = acc / lr divides by exactly the weights it accumulated.
-      float sum0 = 0.f, sum1 = 0.f, rsum0 = 0.f, rsum1 = 0.f;
+      float2 sum = make_float2(0.f, 0.f), rsum = make_float2(0.f, 0.f);
 #pragma unroll
       for (int c4 = 0; c4 < kTileN / 32; ++c4) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(fmaf(s[c4 * 32 + 2 * i], sl2, neg_m));
-          const float p1 = ex2(fmaf(s[c4 * 32 + 2 * i + 1], sl2, neg_m));
-          sum0 += p0;
-          sum1 += p1;
-          pk[i] = pack2<BF16>(p0, p1);
-          const float2 r = unpack2<BF16>(pk[i]);
-          rsum0 += r.x;
-          rsum1 += r.y;
+          const float2 x = fma2(make_float2(s[c4 * 32 + 2 * i], s[c4 * 32 + 2 * i + 1]), sl2x2,
+                                neg_m2);
+          const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+          sum = add2(sum, pp);
+          pk[i] = pack2<BF16>(pp.x, pp.y);
+          rsum = add2(rsum, unpack2<BF16>(pk[i]));
         }
         tmem_st16(t_s + c4 * 16, pk);
       }
+      const float sum0 = sum.x, sum1 = sum.y, rsum0 = rsum.x, rsum1 = rsum.y;
       l = l * alpha + (sum0 + sum1);
       lr = lr * alpha + (rsum0 + rsum1);
       if (j > 0 && __any_sync(0xffffffffu, need)) {
@@ -317,12 +311,15 @@ __global__ void __launch_bounds__(320, 1)
         if (!(ok = warp_wait(&o_done[t], (j - 1) & 1, limit, abort_flag, kWaitFwdO))) break;
         tc_fence_after();
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t r[32];
-          tmem_ld32(t_o + cc * 32, r);
+        for (int cc = 0; cc < D / 64; ++cc) {
+          uint32_t r[64];
+          tmem_ld64(t_o + cc * 64, r);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-          tmem_st32(t_o + cc * 32, r);
+          for (int i = 0; i < 64; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
+          uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[32]);
+          tmem_st32(t_o + cc * 64, lo);
+          tmem_st32(t_o + cc * 64 + 32, hi);
         }
       }
       tmem_st_wait();
@@ -336,18 +333,18 @@ __global__ void __launch_bounds__(320, 1)
       uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
                       ((size_t)bh * N + (size_t)row) * (size_t)(D * 2);
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t r[32];
-        tmem_ld32(t_o + cc * 32, r);
-        uint32_t pk[16];
+      for (int cc = 0; cc < D / 64; ++cc) {
+        uint32_t r[64];
+        tmem_ld64(t_o + cc * 64, r);
+        uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
+        for (int i = 0; i < 32; ++i)
           pk[i] = pack2<BF16>(__uint_as_float(r[2 * i]) * inv_l,
                               __uint_as_float(r[2 * i + 1]) * inv_l);
         if (row < N) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 64);
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 128);
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
+          for (int v = 0; v < 8; ++v)
             dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
