@@ -271,13 +271,16 @@ __global__ void __launch_bounds__(320, 1)
         for (int c = 0; c < kTileN; ++c)
           if (c > lim) s[c] = -INFINITY;
       }
-      float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
+      // Row max in four independent chains of 3-input max (short dependency chains).
+      float mx[4];
 #pragma unroll
-      for (int c = 6; c < kTileN - 2; c += 4) {
-        mx0 = fmax3(mx0, s[c], s[c + 1]);
-        mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+      for (int u = 0; u < 4; ++u) mx[u] = fmaxf(s[2 * u], s[2 * u + 1]);  // columns 0..7
+#pragma unroll
+      for (int c = 8; c < kTileN; c += 8) {  // columns 8..127
+#pragma unroll
+        for (int u = 0; u < 4; ++u) mx[u] = fmax3(mx[u], s[c + 2 * u], s[c + 2 * u + 1]);
       }
-      const float m_cand = fmax3(mx0, mx1, fmaxf(s[kTileN - 2], s[kTileN - 1])) * sl2;
+      const float m_cand = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
       const bool need = m_cand > m + 8.0f;
       float alpha = 1.f;
       if (need) {
@@ -288,7 +291,10 @@ __global__ void __launch_bounds__(320, 1)
       const float2 neg_m2 = make_float2(-m, -m);
       // l sums the fp32 values (it defines L); lr sums the 16-bit values that enter
       // P V, so that O = acc / lr divides by exactly the weights it accumulated.
-      float2 sum = make_float2(0.f, 0.f), rsum = make_float2(0.f, 0.f);
+      // Two sums, each in four independent packed accumulators.
+      float2 sum[4], rsum[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) sum[u] = rsum[u] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int c4 = 0; c4 < kTileN / 32; ++c4) {
         uint32_t pk[16];
@@ -297,13 +303,15 @@ __global__ void __launch_bounds__(320, 1)
           const float2 x = fma2(make_float2(s[c4 * 32 + 2 * i], s[c4 * 32 + 2 * i + 1]), sl2x2,
                                 neg_m2);
           const float2 pp = make_float2(ex2(x.x), ex2(x.y));
-          sum = add2(sum, pp);
+          sum[i & 3] = add2(sum[i & 3], pp);
           pk[i] = pack2<BF16>(pp.x, pp.y);
-          rsum = add2(rsum, unpack2<BF16>(pk[i]));
+          rsum[i & 3] = add2(rsum[i & 3], unpack2<BF16>(pk[i]));
         }
         tmem_st16(t_s + c4 * 16, pk);
       }
-      const float sum0 = sum.x, sum1 = sum.y, rsum0 = rsum.x, rsum1 = rsum.y;
+      const float2 sa = add2(add2(sum[0], sum[1]), add2(sum[2], sum[3]));
+      const float2 ra = add2(add2(rsum[0], rsum[1]), add2(rsum[2], rsum[3]));
+      const float sum0 = sa.x, sum1 = sa.y, rsum0 = ra.x, rsum1 = ra.y;
       l = l * alpha + (sum0 + sum1);
       lr = lr * alpha + (rsum0 + rsum1);
       if (j > 0 && __any_sync(0xffffffffu, need)) {
