@@ -83,13 +83,13 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&qdo_empty[s], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, 256);
+    mbar_init(p_full, 8);  // one arrival per softmax warp
     mbar_init(dp_full, 1);
-    mbar_init(ds_full, 256);
+    mbar_init(ds_full, 8);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
-    mbar_init(&stats_ready[0], 256);
-    mbar_init(&stats_ready[1], 256);
+    mbar_init(&stats_ready[0], 8);
+    mbar_init(&stats_ready[1], 8);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -147,13 +147,13 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t sv = smem_u32(smem + C::kOffV);
       const uint32_t sq = smem_u32(smem + C::kOffQ);
       const uint32_t sdo = smem_u32(smem + C::kOffDO);
-      bool ok = mbar_wait(kv_full, 0, limit, abort_flag, kWaitDkvKV) &&
-                mbar_wait(&q_full[0], 0, limit, abort_flag, kWaitDkvQ);
+      bool ok = mbar_poll(kv_full, 0, limit, abort_flag, kWaitDkvKV) &&
+                mbar_poll(&q_full[0], 0, limit, abort_flag, kWaitDkvQ);
       if (ok) {
         tc_fence_after();
         issue_rowdot<D>(tmem + C::kColS, sk, sq, idesc_st);
         mma_commit(s_full);
-        ok = mbar_wait(&do_full[0], 0, limit, abort_flag, kWaitDkvDO);
+        ok = mbar_poll(&do_full[0], 0, limit, abort_flag, kWaitDkvDO);
       }
       if (ok) {
         tc_fence_after();
@@ -164,24 +164,24 @@ __global__ void __launch_bounds__(320, 1)
         const int s = it % NS;
         const int in = it + 1;
         const int sn = in % NS;
-        if (!(ok = mbar_wait(p_full, it & 1, limit, abort_flag, kWaitDkvP))) break;
+        if (!(ok = mbar_poll(p_full, it & 1, limit, abort_flag, kWaitDkvP))) break;
         tc_fence_after();
         // dV_j += P^T dO_i
         issue_tmem_a_split(tmem + C::kColAcc0, tmem + C::kColS, sdo + s * C::kTileBytes,
                            idesc_acc, it > 0);
         if (in < n) {
-          if (!(ok = mbar_wait(&q_full[sn], (in / NS) & 1, limit, abort_flag, kWaitDkvQ))) break;
+          if (!(ok = mbar_poll(&q_full[sn], (in / NS) & 1, limit, abort_flag, kWaitDkvQ))) break;
           tc_fence_after();
           issue_rowdot<D>(tmem + C::kColS, sk, sq + sn * C::kTileBytes, idesc_st);
           mma_commit(s_full);
         }
-        if (!(ok = mbar_wait(ds_full, it & 1, limit, abort_flag, kWaitDkvDS))) break;
+        if (!(ok = mbar_poll(ds_full, it & 1, limit, abort_flag, kWaitDkvDS))) break;
         tc_fence_after();
         // dK_j += dS^T Q_i
         issue_tmem_a_split(tmem + C::kColAcc1, tmem + C::kColDP, sq + s * C::kTileBytes,
                            idesc_acc, it > 0);
         if (in < n) {
-          if (!(ok = mbar_wait(&do_full[sn], (in / NS) & 1, limit, abort_flag, kWaitDkvDO)))
+          if (!(ok = mbar_poll(&do_full[sn], (in / NS) & 1, limit, abort_flag, kWaitDkvDO)))
             break;
           tc_fence_after();
           issue_rowdot<D>(tmem + C::kColDP, sv, sdo + sn * C::kTileBytes, idesc_st);
@@ -217,11 +217,11 @@ __global__ void __launch_bounds__(320, 1)
     for (int it = 0; it < n; ++it) {
       const int i = i_first + it;
       // Double-buffered statistics: buffer it&1 was last read in iteration it-2, and
-      // every thread has passed iteration it-1's stats_ready wait, which needs all 256
-      // arrivals, so nobody still reads it.
+      // every thread has passed iteration it-1's stats_ready wait, which needs all eight
+      // warps' arrivals, so nobody still reads it.
       float* st = stats + (it & 1) * 256;
       st[g * 128 + row] = stat_next;
-      mbar_arrive(&stats_ready[it & 1]);
+      warp_arrive(&stats_ready[it & 1]);
       if (it + 1 < n) stat_next = load_stat(i + 1);
       if (!(ok = warp_wait(&stats_ready[it & 1], (it >> 1) & 1, limit, abort_flag,
                            kWaitDkvStats)))
@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(p_full);
+      warp_arrive(p_full);
 
       // ---- dS^T = P^T * (dP^T - D), 16-bit pairs over dP^T
       if (!(ok = warp_wait(dp_full, it & 1, limit, abort_flag, kWaitDkvDP))) break;
@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(ds_full);
+      warp_arrive(ds_full);
     }
     if (ok && warp_wait(acc_done, 0, limit, abort_flag, kWaitDkvDone)) {
       tc_fence_after();

@@ -7,11 +7,15 @@
 // Gradient for the recomputation and the gradient). D_i comes from the preprocess
 // kernel. The factor scale on dQ follows from S = scale Q K^T.
 //
+// Q_i and dO_i stay on chip as the A operands of S = Q_i K_j^T and dP = dO_i V_j^T, in
+// tensor memory (copied there once from the TMA-loaded tiles), so all three products
+// read only their B operand (K_j or V_j) from shared memory.
 // GB300 design: warps 0-3 and 4-7 are two softmax warpgroups that share each query row
 // (thread = row = TMEM lane), group g taking keys [64g, 64g + 64) of a block; they turn
 // S and dP (fp32 in tensor memory) into dS. Warp 8 is the TMA producer (Q_i and dO_i
 // once, then a ring of K_j / V_j blocks), warp 9 issues the tcgen05 MMAs. Tensor memory:
-// S (128 cols), dP (128 cols), dQ accumulator (d cols). Group g writes its dS pairs over
+// S (128 cols), dP (128 cols), dQ accumulator (d cols), Q_i and dO_i (d/2 cols each).
+// Group g writes its dS pairs over
 // dP columns [64g, 64g + 32), which feed dS K_j from tensor memory; S of the next block
 // is computed while the softmax warps work on dP of this one.
 #pragma once
@@ -55,8 +59,11 @@ struct DqCfg : BwdCfg<D> {
   static constexpr int kOffV = kOffK + B::kStages * B::kTileBytes;
   static constexpr int kOffBar = kOffV + B::kStages * B::kTileBytes;
   // qdo_full, k_full[S], v_full[S], kv_empty[S], s_full, s_free, dp_full, ds_full,
-  // acc_done, drain
-  static constexpr int kNumBars = 1 + 3 * B::kStages + 6;
+  // acc_done, drain, qdo_tmem
+  static constexpr int kNumBars = 1 + 3 * B::kStages + 7;
+  // Q_i and dO_i as 16-bit pairs in tensor memory (the A operands of S and dP):
+  // d/2 columns each, after S, dP and the dQ accumulator (512 columns in all at d=128).
+  static constexpr uint32_t kColQ = 256 + D, kColDO = 256 + D + D / 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes =
       (kOffMisc + 16 + 1024) > B::kMinSmem ? (kOffMisc + 16 + 1024) : B::kMinSmem;
@@ -72,6 +79,41 @@ __device__ __forceinline__ void store_row32(uint8_t* dst, const uint32_t (&r)[32
   uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+}
+
+// Copies row `row` of a [128 x D] 16-bit tile, stored as D/64 TMA boxes with 128-byte
+// swizzle, into tensor-memory columns [t_col, t_col + D/2) of this thread's lane as
+// packed pairs (the layout of an A operand read from tensor memory). Every lane of the
+// warp calls it (the TMEM store is warp-collective).
+template <int D>
+__device__ __forceinline__ void copy_row_to_tmem(const uint8_t* tile, int row, uint32_t t_col) {
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    const uint8_t* base = tile + c * kBoxBytes + row * 128;
+    uint32_t r[32];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {  // 16-byte chunk k of the row sits at slot k ^ (row % 8)
+      const uint4 v = *reinterpret_cast<const uint4*>(base + ((k ^ (row & 7)) << 4));
+      r[4 * k] = v.x;
+      r[4 * k + 1] = v.y;
+      r[4 * k + 2] = v.z;
+      r[4 * k + 3] = v.w;
+    }
+    tmem_st32(t_col + c * 32, r);
+  }
+}
+
+// A operand [128 x d] in tensor memory (16-bit pairs from column a_tmem) times a K-major
+// B tile [128 x d] in shared memory: D[128 x 128] = A B^T.
+template <int D>
+__device__ __forceinline__ void issue_rowdot_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b0,
+                                                uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+    mma_ts(d_tmem, a_tmem + kk * 8, make_sdesc_sw128(b0 + off, 16, 1024), idesc,
+           kk > 0 ? 1u : 0u);
+  }
 }
 
 // K-major x K-major product over the head dimension: D[128 x 128] = A[128 x d] B[128 x d]^T.
@@ -130,6 +172,7 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* ds_full = dp_full + 1;
   uint64_t* acc_done = ds_full + 1;
   uint64_t* drain = acc_done + 1;
+  uint64_t* qdo_tmem = drain + 1;  // Q_i and dO_i copied into tensor memory
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -149,11 +192,12 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&kv_empty[s], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(s_free, 256);
+    mbar_init(s_free, 8);  // one arrival per softmax warp
     mbar_init(dp_full, 1);
-    mbar_init(ds_full, 256);
+    mbar_init(ds_full, 8);
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
+    mbar_init(qdo_tmem, 8);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -206,21 +250,21 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0) {
       const uint32_t idesc_sq = make_idesc(BF16, 128, kTileN, false, false);
       const uint32_t idesc_acc = make_idesc(BF16, 128, D, false, true);
-      const uint32_t sq = smem_u32(smem + C::kOffQ);
-      const uint32_t sdo = smem_u32(smem + C::kOffDO);
       const uint32_t sk = smem_u32(smem + C::kOffK);
       const uint32_t sv = smem_u32(smem + C::kOffV);
-      bool ok = mbar_wait(qdo_full, 0, limit, abort_flag, kWaitDqQ) &&
-                mbar_wait(&k_full[0], 0, limit, abort_flag, kWaitDqK);
+      const uint32_t tq = tmem + C::kColQ;
+      const uint32_t tdo = tmem + C::kColDO;
+      bool ok = mbar_poll(qdo_tmem, 0, limit, abort_flag, kWaitDqQ) &&
+                mbar_poll(&k_full[0], 0, limit, abort_flag, kWaitDqK);
       if (ok) {
         tc_fence_after();
-        issue_rowdot<D>(tmem + C::kColS, sq, sk, idesc_sq);
+        issue_rowdot_ts<D>(tmem + C::kColS, tq, sk, idesc_sq);
         mma_commit(s_full);
-        ok = mbar_wait(&v_full[0], 0, limit, abort_flag, kWaitDqV);
+        ok = mbar_poll(&v_full[0], 0, limit, abort_flag, kWaitDqV);
       }
       if (ok) {
         tc_fence_after();
-        issue_rowdot<D>(tmem + C::kColDP, sdo, sv, idesc_sq);
+        issue_rowdot_ts<D>(tmem + C::kColDP, tdo, sv, idesc_sq);
         mma_commit(dp_full);
       }
       for (int j = 0; ok && j < n; ++j) {
@@ -229,22 +273,22 @@ __global__ void __launch_bounds__(320, 1)
         const int sn = jn % NS;
         if (jn < n) {
           // S of the next block overwrites S once the softmax warps have read it.
-          if (!(ok = mbar_wait(&k_full[sn], (jn / NS) & 1, limit, abort_flag, kWaitDqK) &&
-                     mbar_wait(s_free, j & 1, limit, abort_flag, kWaitDqSC)))
+          if (!(ok = mbar_poll(&k_full[sn], (jn / NS) & 1, limit, abort_flag, kWaitDqK) &&
+                     mbar_poll(s_free, j & 1, limit, abort_flag, kWaitDqSC)))
             break;
           tc_fence_after();
-          issue_rowdot<D>(tmem + C::kColS, sq, sk + sn * C::kTileBytes, idesc_sq);
+          issue_rowdot_ts<D>(tmem + C::kColS, tq, sk + sn * C::kTileBytes, idesc_sq);
           mma_commit(s_full);
         }
-        if (!(ok = mbar_wait(ds_full, j & 1, limit, abort_flag, kWaitDqDS))) break;
+        if (!(ok = mbar_poll(ds_full, j & 1, limit, abort_flag, kWaitDqDS))) break;
         tc_fence_after();
         // dQ_i += dS K_j (dS read from tensor memory, over dP)
         issue_tmem_a_split(tmem + C::kColAcc0, tmem + C::kColDP, sk + s * C::kTileBytes,
                            idesc_acc, j > 0);
         if (jn < n) {
-          if (!(ok = mbar_wait(&v_full[sn], (jn / NS) & 1, limit, abort_flag, kWaitDqV))) break;
+          if (!(ok = mbar_poll(&v_full[sn], (jn / NS) & 1, limit, abort_flag, kWaitDqV))) break;
           tc_fence_after();
-          issue_rowdot<D>(tmem + C::kColDP, sdo, sv + sn * C::kTileBytes, idesc_sq);
+          issue_rowdot_ts<D>(tmem + C::kColDP, tdo, sv + sn * C::kTileBytes, idesc_sq);
           mma_commit(dp_full);
         }
         mma_commit(&kv_empty[s]);
@@ -271,15 +315,23 @@ __global__ void __launch_bounds__(320, 1)
     }
     const float2 nl2x2 = make_float2(neg_l2, neg_l2);
     const float2 ndl2 = make_float2(-dlt, -dlt);
-    bool ok = true;
-    for (int j = 0; j < n; ++j) {
+    // Group 0 copies this row of Q_i, group 1 the row of dO_i, into tensor memory.
+    bool ok = warp_wait(qdo_full, 0, limit, abort_flag, kWaitDqQ);
+    if (ok) {
+      copy_row_to_tmem<D>(smem + (g == 0 ? C::kOffQ : C::kOffDO), wq * 32 + lane,
+                          tmem + lane_base + (g == 0 ? C::kColQ : C::kColDO));
+      tmem_st_wait();
+      tc_fence_before();
+      warp_arrive(qdo_tmem);
+    }
+    for (int j = 0; ok && j < n; ++j) {
       // ---- P = exp2(S * scale * log2(e) - L * log2(e)) for keys [c0, c0 + 64)
       if (!(ok = warp_wait(s_full, j & 1, limit, abort_flag, kWaitDqS))) break;
       tc_fence_after();
       uint32_t sr[64];
       tmem_ld64(t_s, sr);
       tc_fence_before();
-      mbar_arrive(s_free);
+      warp_arrive(s_free);
       float* pr = reinterpret_cast<float*>(sr);
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
@@ -316,7 +368,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(ds_full);
+      warp_arrive(ds_full);
     }
     if (ok && warp_wait(acc_done, 0, limit, abort_flag, kWaitDqDone)) {
       tc_fence_after();

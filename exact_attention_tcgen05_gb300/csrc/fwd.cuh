@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(320, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], 128);
+      mbar_init(&p_full[t], 4);  // one arrival per softmax warp
       mbar_init(&o_done[t], 1);
     }
     mbar_init(drain, 1);
@@ -198,8 +198,8 @@ __global__ void __launch_bounds__(320, 1)
         }
       };
 
-      bool ok = mbar_wait(q_full, 0, limit, abort_flag, kWaitFwdQ);
-      if (ok) ok = mbar_wait(&k_full[0], 0, limit, abort_flag, kWaitFwdK);
+      bool ok = mbar_poll(q_full, 0, limit, abort_flag, kWaitFwdQ);
+      if (ok) ok = mbar_poll(&k_full[0], 0, limit, abort_flag, kWaitFwdK);
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       for (int j = 0; ok && j < n_kv; ++j) {
         const int s = j % C::kStages;
-        if (!(ok = mbar_wait(&v_full[s], (j / C::kStages) & 1, limit, abort_flag,
+        if (!(ok = mbar_poll(&v_full[s], (j / C::kStages) & 1, limit, abort_flag,
                              kWaitFwdV)))
           break;
         tc_fence_after();
@@ -219,13 +219,13 @@ __global__ void __launch_bounds__(320, 1)
         bool next_k_ready = false;
         for (int t = 0; t < 2 && ok; ++t) {
           if (j >= nkv[t]) continue;
-          if (!(ok = mbar_wait(&p_full[t], j & 1, limit, abort_flag, kWaitFwdP))) break;
+          if (!(ok = mbar_poll(&p_full[t], j & 1, limit, abort_flag, kWaitFwdP))) break;
           tc_fence_after();
           issue_pv(t, s, j > 0);
           mma_commit(&o_done[t]);
           if (jn < nkv[t]) {
             if (!next_k_ready) {
-              if (!(ok = mbar_wait(&k_full[sn], (jn / C::kStages) & 1, limit, abort_flag,
+              if (!(ok = mbar_poll(&k_full[sn], (jn / C::kStages) & 1, limit, abort_flag,
                                    kWaitFwdK)))
                 break;
               tc_fence_after();
@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&p_full[t]);
+      warp_arrive(&p_full[t]);
     }
     if (ok && nkv[t] > 0 &&
         warp_wait(&o_done[t], (nkv[t] - 1) & 1, limit, abort_flag, kWaitFwdO)) {

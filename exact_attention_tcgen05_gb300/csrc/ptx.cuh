@@ -48,6 +48,14 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
       : "memory");
 }
 
+// One arrival per warp: every lane's prior writes (and, after
+// tcgen05.fence::before_thread_sync, its tensor-memory stores) are ordered before lane 0's
+// arrive by the warp barrier. Barriers signalled this way count warps, not threads.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile(
       "{\n\t.reg .b64 st;\n\t"
@@ -66,6 +74,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Like mbar_wait below, but polls with the non-suspending test_wait: for the single
+// thread that issues the MMAs, where the wake-up delay of a suspended try_wait would
+// leave the tensor core idle.
+__device__ __forceinline__ bool mbar_poll(uint64_t* bar, uint32_t parity, uint64_t limit,
+                                          volatile int* abort, int where) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = clock64();
+  while (true) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if (abort != nullptr && *abort) return false;
+    if (clock64() - t0 > limit) {
+      record_timeout(where);
+      if (abort != nullptr) *abort = 1;
+      return false;
+    }
+  }
 }
 
 // Waits for the phase of `bar` with parity `parity` to complete. Gives up (returns
