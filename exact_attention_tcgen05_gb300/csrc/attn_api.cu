@@ -217,7 +217,7 @@ attn_status attn_bwd_dkv(const void* q, const void* k, const void* v, const floa
   Maps m;
   if ((st = encode_bwd_maps(&m, q, k, v, dO, s)) != ATTN_OK) return st;
   return from_cuda(
-      attn::launch_dkv(m, s, lse, delta, dk, dv, static_cast<cudaStream_t>(cuda_stream)));
+      attn::launch_dkv(m, s, q, dO, lse, delta, dk, dv, static_cast<cudaStream_t>(cuda_stream)));
 }
 
 attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const float* lse,
@@ -236,7 +236,7 @@ attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const float
   Maps m;
   if ((st = encode_bwd_maps(&m, q, k, v, dO, s)) != ATTN_OK) return st;
   return from_cuda(
-      attn::launch_dq(m, s, lse, delta, dq, static_cast<cudaStream_t>(cuda_stream)));
+      attn::launch_dq(m, s, q, dO, lse, delta, dq, static_cast<cudaStream_t>(cuda_stream)));
 }
 
 attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -260,8 +260,8 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   cudaStream_t cs = static_cast<cudaStream_t>(cuda_stream);
   float* delta = static_cast<float*>(workspace);
   cudaError_t e = attn::launch_delta(s, o, dO, delta, cs);
-  if (e == cudaSuccess) e = attn::launch_dkv(m, s, lse, delta, dk, dv, cs);
-  if (e == cudaSuccess) e = attn::launch_dq(m, s, lse, delta, dq, cs);
+  if (e == cudaSuccess) e = attn::launch_dkv(m, s, q, dO, lse, delta, dk, dv, cs);
+  if (e == cudaSuccess) e = attn::launch_dq(m, s, q, dO, lse, delta, dq, cs);
   return from_cuda(e);
 }
 

@@ -8,8 +8,9 @@
 // kernel. The factor scale on dQ follows from S = scale Q K^T.
 //
 // Q_i and dO_i stay on chip as the A operands of S = Q_i K_j^T and dP = dO_i V_j^T, in
-// tensor memory (copied there once from the TMA-loaded tiles), so all three products
-// read only their B operand (K_j or V_j) from shared memory.
+// tensor memory (each thread copies its own row there once, from global memory), so all
+// three products read only their B operand (K_j or V_j) from shared memory, and shared
+// memory holds just a three-block K/V ring.
 // GB300 design: warps 0-3 and 4-7 are two softmax warpgroups that share each query row
 // (thread = row = TMEM lane), group g taking keys [64g, 64g + 64) of a block; they turn
 // S and dP (fp32 in tensor memory) into dS. Warp 8 is the TMA producer (Q_i and dO_i
@@ -25,6 +26,8 @@
 namespace attn {
 
 struct BwdParams {
+  const void* in_q;    // [BH, N, d] Q (read directly by the dQ kernel)
+  const void* in_do;   // [BH, N, d] dO (read directly by the dQ kernel)
   const float* lse;    // [BH, N] natural-log L
   const float* delta;  // [BH, N] D
   void* out0;          // dQ (dQ kernel) or dK (dKV kernel)
@@ -53,14 +56,16 @@ struct BwdCfg {
 template <int D>
 struct DqCfg : BwdCfg<D> {
   using B = BwdCfg<D>;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffDO = kOffQ + B::kTileBytes;
-  static constexpr int kOffK = kOffDO + B::kTileBytes;
-  static constexpr int kOffV = kOffK + B::kStages * B::kTileBytes;
-  static constexpr int kOffBar = kOffV + B::kStages * B::kTileBytes;
-  // qdo_full, k_full[S], v_full[S], kv_empty[S], s_full, s_free, dp_full, ds_full,
-  // acc_done, drain, qdo_tmem
-  static constexpr int kNumBars = 1 + 3 * B::kStages + 7;
+  // Q_i and dO_i go straight from global memory to tensor memory, so shared memory holds
+  // only the K/V ring, three blocks deep: block j + 3 can be fetched as soon as dQ of
+  // block j (the last reader of its K) has been issued and has finished.
+  static constexpr int kStages = 3;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kStages * B::kTileBytes;
+  static constexpr int kOffBar = kOffV + kStages * B::kTileBytes;
+  // k_full[S], v_full[S], kv_empty[S], s_full, s_free, dp_full, ds_full, acc_done, drain,
+  // qdo_tmem
+  static constexpr int kNumBars = 3 * kStages + 7;
   // Q_i and dO_i as 16-bit pairs in tensor memory (the A operands of S and dP):
   // d/2 columns each, after S, dP and the dQ accumulator (512 columns in all at d=128).
   static constexpr uint32_t kColQ = 256 + D, kColDO = 256 + D + D / 2;
@@ -81,19 +86,19 @@ __device__ __forceinline__ void store_row32(uint8_t* dst, const uint32_t (&r)[32
   for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
 }
 
-// Copies row `row` of a [128 x D] 16-bit tile, stored as D/64 TMA boxes with 128-byte
-// swizzle, into tensor-memory columns [t_col, t_col + D/2) of this thread's lane as
-// packed pairs (the layout of an A operand read from tensor memory). Every lane of the
-// warp calls it (the TMEM store is warp-collective).
+// Copies one D-element 16-bit row from global memory (zeros when src is null) into
+// tensor-memory columns [t_col, t_col + D/2) of this thread's lane as packed pairs (the
+// layout of an A operand read from tensor memory). Every lane of the warp calls it (the
+// TMEM store is warp-collective).
 template <int D>
-__device__ __forceinline__ void copy_row_to_tmem(const uint8_t* tile, int row, uint32_t t_col) {
+__device__ __forceinline__ void copy_row_to_tmem(const uint8_t* src, uint32_t t_col) {
 #pragma unroll
   for (int c = 0; c < D / 64; ++c) {
-    const uint8_t* base = tile + c * kBoxBytes + row * 128;
     uint32_t r[32];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {  // 16-byte chunk k of the row sits at slot k ^ (row % 8)
-      const uint4 v = *reinterpret_cast<const uint4*>(base + ((k ^ (row & 7)) << 4));
+    for (int k = 0; k < 8; ++k) {
+      const uint4 v = src ? *reinterpret_cast<const uint4*>(src + c * 128 + k * 16)
+                          : make_uint4(0, 0, 0, 0);
       r[4 * k] = v.x;
       r[4 * k + 1] = v.y;
       r[4 * k + 2] = v.z;
@@ -162,8 +167,7 @@ __global__ void __launch_bounds__(320, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint64_t* qdo_full = bars;
-  uint64_t* k_full = bars + 1;
+  uint64_t* k_full = bars;
   uint64_t* v_full = k_full + NS;
   uint64_t* kv_empty = v_full + NS;
   uint64_t* s_full = kv_empty + NS;
@@ -185,7 +189,6 @@ __global__ void __launch_bounds__(320, 1)
   const int n = p.causal ? ib + 1 : p.nb;  // key blocks 0 .. n-1
 
   if (threadIdx.x == 0) {
-    mbar_init(qdo_full, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
@@ -213,15 +216,8 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 8) {
     if (lane == 0) {
-      tma_prefetch_map(&map_q);
       tma_prefetch_map(&map_k);
       tma_prefetch_map(&map_v);
-      tma_prefetch_map(&map_do);
-      mbar_arrive_expect_tx(qdo_full, 2 * C::kTileBytes);
-      for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_3d(smem + C::kOffQ + c * kBoxBytes, &map_q, qdo_full, c * kBoxCols, i0, bh);
-        tma_load_3d(smem + C::kOffDO + c * kBoxBytes, &map_do, qdo_full, c * kBoxCols, i0, bh);
-      }
       int issued = 0;
       for (int j = 0; j < n; ++j) {
         const int s = j % NS;
@@ -239,7 +235,6 @@ __global__ void __launch_bounds__(320, 1)
         issued = j + 1;
       }
       if (*abort_flag) {
-        mbar_wait(qdo_full, 0, limit, nullptr, kWaitDqDrain);
         for (int j = max(0, issued - NS); j < issued; ++j) {
           mbar_wait(&k_full[j % NS], (j / NS) & 1, limit, nullptr, kWaitDqDrain);
           mbar_wait(&v_full[j % NS], (j / NS) & 1, limit, nullptr, kWaitDqDrain);
@@ -315,10 +310,12 @@ __global__ void __launch_bounds__(320, 1)
     }
     const float2 nl2x2 = make_float2(neg_l2, neg_l2);
     const float2 ndl2 = make_float2(-dlt, -dlt);
-    // Group 0 copies this row of Q_i, group 1 the row of dO_i, into tensor memory.
-    bool ok = warp_wait(qdo_full, 0, limit, abort_flag, kWaitDqQ);
-    if (ok) {
-      copy_row_to_tmem<D>(smem + (g == 0 ? C::kOffQ : C::kOffDO), wq * 32 + lane,
+    // Group 0 copies this row of Q_i, group 1 the row of dO_i, into tensor memory
+    // (rows past N as zeros).
+    bool ok = true;
+    {
+      const uint8_t* gsrc = reinterpret_cast<const uint8_t*>(g == 0 ? p.in_q : p.in_do);
+      copy_row_to_tmem<D>(row < N ? gsrc + ((size_t)bh * N + row) * (size_t)(D * 2) : nullptr,
                           tmem + lane_base + (g == 0 ? C::kColQ : C::kColDO));
       tmem_st_wait();
       tc_fence_before();

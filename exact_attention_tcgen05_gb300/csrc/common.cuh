@@ -22,7 +22,8 @@ enum WaitSite : int {
   kWaitDqQ = 0x21, kWaitDqK, kWaitDqV, kWaitDqEmpty, kWaitDqS, kWaitDqDP, kWaitDqDS,
   kWaitDqDone, kWaitDqDrain, kWaitDqSC,
   kWaitDkvKV = 0x31, kWaitDkvQ, kWaitDkvDO, kWaitDkvEmpty, kWaitDkvS, kWaitDkvDP,
-  kWaitDkvP, kWaitDkvDS, kWaitDkvDone, kWaitDkvDrain, kWaitDkvStats
+  kWaitDkvP, kWaitDkvDS, kWaitDkvDone, kWaitDkvDrain, kWaitDkvStats,
+  kErrSmemAlign = 0x7F  // dynamic shared memory not 1024-byte aligned (kernel skipped)
 };
 
 // Rounds a shared-memory pointer up to 1024 bytes (the swizzle-atom alignment).

@@ -5,7 +5,8 @@
 namespace attn {
 
 template <int D, bool BF16>
-static cudaError_t launch_dkv_t(const Maps& m, const Shape& s, const float* lse,
+static cudaError_t launch_dkv_t(const Maps& m, const Shape& s, const void* q,
+                               const void* d_o, const float* lse,
                                 const float* delta, void* dk, void* dv, cudaStream_t st) {
   using C = DkvCfg<D>;
   auto kern = attn_bwd_dkv_kernel<D, BF16>;
@@ -13,6 +14,8 @@ static cudaError_t launch_dkv_t(const Maps& m, const Shape& s, const float* lse,
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   BwdParams p;
+  p.in_q = q;
+  p.in_do = d_o;
   p.lse = lse;
   p.delta = delta;
   p.out0 = dk;
@@ -28,12 +31,13 @@ static cudaError_t launch_dkv_t(const Maps& m, const Shape& s, const float* lse,
   return cudaGetLastError();
 }
 
-cudaError_t launch_dkv(const Maps& m, const Shape& s, const float* lse, const float* delta,
+cudaError_t launch_dkv(const Maps& m, const Shape& s, const void* q, const void* d_o,
+                       const float* lse, const float* delta,
                        void* dk, void* dv, cudaStream_t st) {
-  if (s.d == 128) return s.bf16 ? launch_dkv_t<128, true>(m, s, lse, delta, dk, dv, st)
-                                : launch_dkv_t<128, false>(m, s, lse, delta, dk, dv, st);
-  return s.bf16 ? launch_dkv_t<64, true>(m, s, lse, delta, dk, dv, st)
-                : launch_dkv_t<64, false>(m, s, lse, delta, dk, dv, st);
+  if (s.d == 128) return s.bf16 ? launch_dkv_t<128, true>(m, s, q, d_o, lse, delta, dk, dv, st)
+                                : launch_dkv_t<128, false>(m, s, q, d_o, lse, delta, dk, dv, st);
+  return s.bf16 ? launch_dkv_t<64, true>(m, s, q, d_o, lse, delta, dk, dv, st)
+                : launch_dkv_t<64, false>(m, s, q, d_o, lse, delta, dk, dv, st);
 }
 
 ATTN_DEFINE_STATUS_READER(status_dkv)

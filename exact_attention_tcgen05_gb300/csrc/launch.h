@@ -22,10 +22,13 @@ struct Shape {
 cudaError_t launch_fwd(const Maps& m, const Shape& s, void* o, float* lse, cudaStream_t st);
 cudaError_t launch_delta(const Shape& s, const void* o, const void* dO, float* delta,
                          cudaStream_t st);
-cudaError_t launch_dq(const Maps& m, const Shape& s, const float* lse, const float* delta,
-                      void* dq, cudaStream_t st);
-cudaError_t launch_dkv(const Maps& m, const Shape& s, const float* lse, const float* delta,
-                       void* dk, void* dv, cudaStream_t st);
+// q and dO are the raw [B*H, N, d] tensors the maps describe (the dQ kernel reads its
+// query rows of both directly).
+cudaError_t launch_dq(const Maps& m, const Shape& s, const void* q, const void* dO,
+                      const float* lse, const float* delta, void* dq, cudaStream_t st);
+cudaError_t launch_dkv(const Maps& m, const Shape& s, const void* q, const void* dO,
+                       const float* lse, const float* delta, void* dk, void* dv,
+                       cudaStream_t st);
 
 // Each kernel translation unit has its own device status word; these read (after the
 // work queued on `st`, blocking) and clear it. Return the word (0 = no timeout).
