@@ -39,4 +39,17 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
   return __all_sync(0xffffffffu, ok);
 }
 
+// A operand in tensor memory whose 16-bit pairs sit in two halves: columns [0, 64) of A in
+// [base, base + 32) and columns [64, 128) in [base + 64, base + 96). B is an MN-major
+// [128 x d] tile in shared memory. D[128 x d] (+)= A B.
+__device__ __forceinline__ void issue_tmem_a_split(uint32_t d_tmem, uint32_t a_tmem,
+                                                   uint32_t b0, uint32_t idesc, bool acc) {
+#pragma unroll
+  for (int kk = 0; kk < 128 / 16; ++kk) {
+    const uint32_t a_col = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
+    mma_ts(d_tmem, a_tmem + a_col, make_sdesc_sw128(b0 + kk * 2048, kBoxBytes, 1024), idesc,
+           (acc || kk > 0) ? 1u : 0u);
+  }
+}
+
 }  // namespace attn
