@@ -54,7 +54,7 @@ def load_peaks() -> dict:
 # clocks during the timed region
 # ------------------------------------------------------------------------------------
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -68,12 +68,14 @@ class ClockSampler:
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def stop(self) -> dict | None:
+    def stop(self, t0: float | None = None, t1: float | None = None) -> dict | None:
+        """Median SM clock of the samples taken between host times t0 and t1 (the timed
+        region); throttle reasons seen in that window."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -82,27 +84,32 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.out.close()
+        import datetime
         sm, mx, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         with open(self.path) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 8:
+                if len(parts) < 9:
                     continue
                 try:
-                    sm.append(float(parts[0]))
-                    mx.append(float(parts[1]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    clk, clk_max = float(parts[1]), float(parts[2])
                 except ValueError:
                     continue
-                for name, val in zip(names, parts[4:8]):
+                if t0 is not None and not (t0 <= ts <= t1):
+                    continue
+                sm.append(clk)
+                mx.append(clk_max)
+                for name, val in zip(names, parts[5:9]):
                     if val.lower() == "active":
                         reasons.add(name)
         os.unlink(self.path)
         if not sm:
             return None
-        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),
-                "samples": len(sm), "reasons": sorted(reasons)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "samples": len(sm), "reasons": sorted(reasons),
+                "window": "samples taken inside the timed region, every 50 ms"}
 
 
 # ------------------------------------------------------------------------------------
@@ -215,6 +222,7 @@ def run_ours(args) -> None:
     clocks.start()
     time.sleep(0.3)
     torch.cuda.synchronize()
+    t_host0 = time.time()
     for i in range(args.steps):
         e = ev[i]
         e[0].record(stream)
@@ -228,7 +236,9 @@ def run_ours(args) -> None:
         binding.attn_bwd_dq(q, k, v, lse, delta, do, causal=w.causal, scale=w.scale, dq=dq)
         e[4].record(stream)
     torch.cuda.synchronize()
-    clock_info = clocks.stop()
+    t_host1 = time.time()
+    time.sleep(0.1)
+    clock_info = clocks.stop(t_host0, t_host1)
     barrier(world)
     total_ms = ev[0][0].elapsed_time(ev[-1][4])
     per_kernel = {n: [ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)]
@@ -374,7 +384,7 @@ def run_reference(args) -> None:
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
