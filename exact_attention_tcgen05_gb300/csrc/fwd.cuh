@@ -292,9 +292,10 @@ __global__ void __launch_bounds__(320, 1)
       // l sums the fp32 values (it defines L); lr sums the 16-bit values that enter
       // P V, so that O = acc / lr divides by exactly the weights it accumulated.
       // Two sums, each in four independent packed accumulators.
-      float2 sum[4], rsum[4];
+      float2 sum[4];
+      float rsum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int u = 0; u < 4; ++u) sum[u] = rsum[u] = make_float2(0.f, 0.f);
+      for (int u = 0; u < 4; ++u) sum[u] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int c4 = 0; c4 < kTileN / 32; ++c4) {
         uint32_t pk[16];
@@ -305,13 +306,12 @@ __global__ void __launch_bounds__(320, 1)
           const float2 pp = make_float2(ex2(x.x), ex2(x.y));
           sum[i & 3] = add2(sum[i & 3], pp);
           pk[i] = pack2<BF16>(pp.x, pp.y);
-          rsum[i & 3] = add2(rsum[i & 3], unpack2<BF16>(pk[i]));
+          add_pair16<BF16>(rsum[(i & 1) * 2], rsum[(i & 1) * 2 + 1], pk[i]);
         }
         tmem_st16(t_s + c4 * 16, pk);
       }
       const float2 sa = add2(add2(sum[0], sum[1]), add2(sum[2], sum[3]));
-      const float2 ra = add2(add2(rsum[0], rsum[1]), add2(rsum[2], rsum[3]));
-      const float sum0 = sa.x, sum1 = sa.y, rsum0 = ra.x, rsum1 = ra.y;
+      const float sum0 = sa.x, sum1 = sa.y, rsum0 = rsum[0] + rsum[1], rsum1 = rsum[2] + rsum[3];
       l = l * alpha + (sum0 + sum1);
       lr = lr * alpha + (rsum0 + rsum1);
       if (j > 0 && __any_sync(0xffffffffu, need)) {

@@ -364,6 +364,23 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+// acc + lo(v) + hi(v) for a packed pair of 16-bit values, adding each half straight into
+// the fp32 accumulators with the mixed-precision add (no separate unpack).
+template <bool BF16>
+__device__ __forceinline__ void add_pair16(float& acc0, float& acc1, uint32_t v) {
+  if constexpr (BF16) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+        : "+f"(acc0), "+f"(acc1)
+        : "r"(v));
+  } else {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+        : "+f"(acc0), "+f"(acc1)
+        : "r"(v));
+  }
+}
+
 // Named barrier over `count` threads (a multiple of 32), id 1..15.
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
