@@ -94,6 +94,23 @@ attn_status encode_map(CUtensorMap* m, const void* base, int BH, int N, int d, b
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// Map for whole-tile copies (tma_load_tile): dims {64, N, d / 64, BH} with strides
+// {2 d, 128, 2 N d} bytes, box {64, 128, d / 64, 1}.
+attn_status encode_tile_map(CUtensorMap* m, const void* base, int BH, int N, int d, bool bf16) {
+  EncodeFn enc = get_encode();
+  if (enc == nullptr) return ATTN_ERR_CUDA;
+  const cuuint64_t dims[4] = {64, (cuuint64_t)N, (cuuint64_t)(d / 64), (cuuint64_t)BH};
+  const cuuint64_t strides[3] = {(cuuint64_t)d * 2, 128, (cuuint64_t)N * (cuuint64_t)d * 2};
+  const cuuint32_t box[4] = {64, 128, (cuuint32_t)(d / 64), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r =
+      enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 Shape make_shape(int B, int H, int N, int d, attn_dtype dtype, int causal, float scale) {
   Shape s;
   s.BH = B * H;
@@ -147,12 +164,12 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   if (overlap(ro, rl)) return ATTN_ERR_INVALID_ARG;
 
   const Shape s = make_shape(B, H, N, d, dtype, causal, scale);
-  Maps m;
-  if ((st = encode_map(&m.q, q, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
-  if ((st = encode_map(&m.k, k, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
-  if ((st = encode_map(&m.v, v, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
+  Maps m;  // the forward reads Q with plain loads (into tensor memory): no Q map
+  if ((st = encode_tile_map(&m.k, k, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
+  if ((st = encode_tile_map(&m.v, v, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
+  m.q = m.k;
   m.d_o = m.v;
-  return from_cuda(attn::launch_fwd(m, s, o, lse, static_cast<cudaStream_t>(cuda_stream)));
+  return from_cuda(attn::launch_fwd(m, s, q, o, lse, static_cast<cudaStream_t>(cuda_stream)));
 }
 
 attn_status attn_bwd_preprocess(const void* o, const void* dO, float* delta, int B, int H,

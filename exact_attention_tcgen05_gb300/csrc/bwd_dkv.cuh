@@ -104,7 +104,8 @@ __global__ void __launch_bounds__(320, 1)
   const uint64_t limit = p.wait_limit;
 
   if (warp == 8) {
-    if (lane == 0) {
+    // TMA producer. The warp runs converged (waits in every lane); the elected lane issues.
+    if (elect_one()) {
       tma_prefetch_map(&map_q);
       tma_prefetch_map(&map_k);
       tma_prefetch_map(&map_v);
@@ -114,13 +115,16 @@ __global__ void __launch_bounds__(320, 1)
         tma_load_3d(smem + C::kOffK + c * kBoxBytes, &map_k, kv_full, c * kBoxCols, j0, bh);
         tma_load_3d(smem + C::kOffV + c * kBoxBytes, &map_v, kv_full, c * kBoxCols, j0, bh);
       }
-      int issued = 0;
-      for (int it = 0; it < n; ++it) {
-        const int s = it % NS;
-        const int i = i_first + it;
-        if (it >= NS &&
-            !mbar_wait(&qdo_empty[s], ((it / NS) - 1) & 1, limit, abort_flag, kWaitDkvEmpty))
-          break;
+    }
+    __syncwarp();
+    int issued = 0;
+    for (int it = 0; it < n; ++it) {
+      const int s = it % NS;
+      const int i = i_first + it;
+      if (it >= NS &&
+          !warp_wait(&qdo_empty[s], ((it / NS) - 1) & 1, limit, abort_flag, kWaitDkvEmpty))
+        break;
+      if (elect_one()) {
         mbar_arrive_expect_tx(&q_full[s], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(smem + C::kOffQ + s * C::kTileBytes + c * kBoxBytes, &map_q, &q_full[s],
@@ -129,70 +133,93 @@ __global__ void __launch_bounds__(320, 1)
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(smem + C::kOffDO + s * C::kTileBytes + c * kBoxBytes, &map_do,
                       &do_full[s], c * kBoxCols, i * kTileM, bh);
-        issued = it + 1;
       }
-      if (*abort_flag) {
-        mbar_wait(kv_full, 0, limit, nullptr, kWaitDkvDrain);
-        for (int it = max(0, issued - NS); it < issued; ++it) {
-          mbar_wait(&q_full[it % NS], (it / NS) & 1, limit, nullptr, kWaitDkvDrain);
-          mbar_wait(&do_full[it % NS], (it / NS) & 1, limit, nullptr, kWaitDkvDrain);
-        }
+      __syncwarp();
+      issued = it + 1;
+    }
+    if (*abort_flag) {
+      mbar_wait(kv_full, 0, limit, nullptr, kWaitDkvDrain);
+      for (int it = max(0, issued - NS); it < issued; ++it) {
+        mbar_wait(&q_full[it % NS], (it / NS) & 1, limit, nullptr, kWaitDkvDrain);
+        mbar_wait(&do_full[it % NS], (it / NS) & 1, limit, nullptr, kWaitDkvDrain);
       }
     }
   } else if (warp == 9) {
-    if (lane == 0) {
-      const uint32_t idesc_st = make_idesc(BF16, 128, kTileM, false, false);
-      const uint32_t idesc_acc = make_idesc(BF16, 128, D, false, true);
-      const uint32_t sk = smem_u32(smem + C::kOffK);
-      const uint32_t sv = smem_u32(smem + C::kOffV);
-      const uint32_t sq = smem_u32(smem + C::kOffQ);
-      const uint32_t sdo = smem_u32(smem + C::kOffDO);
-      bool ok = mbar_poll(kv_full, 0, limit, abort_flag, kWaitDkvKV) &&
-                mbar_poll(&q_full[0], 0, limit, abort_flag, kWaitDkvQ);
-      if (ok) {
-        tc_fence_after();
-        issue_rowdot<D>(tmem + C::kColS, sk, sq, idesc_st);
+    // MMA issuer: converged warp, elected lane issues (see the dQ kernel).
+    const uint32_t idesc_st = make_idesc(BF16, 128, kTileM, false, false);
+    const uint32_t idesc_acc = make_idesc(BF16, 128, D, false, true);
+    const uint64_t dk = make_sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
+    const uint64_t dv = make_sdesc_sw128(smem_u32(smem + C::kOffV), 16, 1024);
+    const uint64_t dq = make_sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
+    const uint64_t ddo = make_sdesc_sw128(smem_u32(smem + C::kOffDO), 16, 1024);
+    const uint64_t dq_mn = make_sdesc_sw128(smem_u32(smem + C::kOffQ), kBoxBytes, 1024);
+    const uint64_t ddo_mn = make_sdesc_sw128(smem_u32(smem + C::kOffDO), kBoxBytes, 1024);
+    constexpr uint32_t kStageStep = C::kTileBytes >> 4;
+    bool ok = warp_poll(kv_full, 0, limit, abort_flag, kWaitDkvKV) &&
+              warp_poll(&q_full[0], 0, limit, abort_flag, kWaitDkvQ);
+    if (ok) {
+      tc_fence_after();
+      if (elect_one()) {
+        issue_rowdot_d<D>(tmem + C::kColS, dk, dq, idesc_st);
         mma_commit(s_full);
-        ok = mbar_poll(&do_full[0], 0, limit, abort_flag, kWaitDkvDO);
       }
-      if (ok) {
-        tc_fence_after();
-        issue_rowdot<D>(tmem + C::kColDP, sv, sdo, idesc_st);
+      __syncwarp();
+      ok = warp_poll(&do_full[0], 0, limit, abort_flag, kWaitDkvDO);
+    }
+    if (ok) {
+      tc_fence_after();
+      if (elect_one()) {
+        issue_rowdot_d<D>(tmem + C::kColDP, dv, ddo, idesc_st);
         mma_commit(dp_full);
       }
-      for (int it = 0; ok && it < n; ++it) {
-        const int s = it % NS;
-        const int in = it + 1;
-        const int sn = in % NS;
-        if (!(ok = mbar_poll(p_full, it & 1, limit, abort_flag, kWaitDkvP))) break;
+      __syncwarp();
+    }
+    for (int it = 0; ok && it < n; ++it) {
+      const int s = it % NS;
+      const int in = it + 1;
+      const int sn = in % NS;
+      if (!(ok = warp_poll(p_full, it & 1, limit, abort_flag, kWaitDkvP))) break;
+      tc_fence_after();
+      // dV_j += P^T dO_i
+      if (elect_one())
+        issue_tmem_a_split_d(tmem + C::kColAcc0, tmem + C::kColS, ddo_mn + s * kStageStep,
+                             idesc_acc, it > 0);
+      __syncwarp();
+      if (in < n) {
+        if (!(ok = warp_poll(&q_full[sn], (in / NS) & 1, limit, abort_flag, kWaitDkvQ))) break;
         tc_fence_after();
-        // dV_j += P^T dO_i
-        issue_tmem_a_split(tmem + C::kColAcc0, tmem + C::kColS, sdo + s * C::kTileBytes,
-                           idesc_acc, it > 0);
-        if (in < n) {
-          if (!(ok = mbar_poll(&q_full[sn], (in / NS) & 1, limit, abort_flag, kWaitDkvQ))) break;
-          tc_fence_after();
-          issue_rowdot<D>(tmem + C::kColS, sk, sq + sn * C::kTileBytes, idesc_st);
+        if (elect_one()) {
+          issue_rowdot_d<D>(tmem + C::kColS, dk, dq + sn * kStageStep, idesc_st);
           mma_commit(s_full);
         }
-        if (!(ok = mbar_poll(ds_full, it & 1, limit, abort_flag, kWaitDkvDS))) break;
+        __syncwarp();
+      }
+      if (!(ok = warp_poll(ds_full, it & 1, limit, abort_flag, kWaitDkvDS))) break;
+      tc_fence_after();
+      // dK_j += dS^T Q_i
+      if (elect_one())
+        issue_tmem_a_split_d(tmem + C::kColAcc1, tmem + C::kColDP, dq_mn + s * kStageStep,
+                             idesc_acc, it > 0);
+      __syncwarp();
+      if (in < n) {
+        if (!(ok = warp_poll(&do_full[sn], (in / NS) & 1, limit, abort_flag, kWaitDkvDO)))
+          break;
         tc_fence_after();
-        // dK_j += dS^T Q_i
-        issue_tmem_a_split(tmem + C::kColAcc1, tmem + C::kColDP, sq + s * C::kTileBytes,
-                           idesc_acc, it > 0);
-        if (in < n) {
-          if (!(ok = mbar_poll(&do_full[sn], (in / NS) & 1, limit, abort_flag, kWaitDkvDO)))
-            break;
-          tc_fence_after();
-          issue_rowdot<D>(tmem + C::kColDP, sv, sdo + sn * C::kTileBytes, idesc_st);
+        if (elect_one()) {
+          issue_rowdot_d<D>(tmem + C::kColDP, dv, ddo + sn * kStageStep, idesc_st);
           mma_commit(dp_full);
         }
-        mma_commit(&qdo_empty[s]);
+        __syncwarp();
       }
+      if (elect_one()) mma_commit(&qdo_empty[s]);
+      __syncwarp();
+    }
+    if (elect_one()) {
       if (ok) mma_commit(acc_done);
       mma_commit(drain);
-      mbar_wait(drain, 0, limit, nullptr, kWaitDkvDrain);
     }
+    __syncwarp();
+    mbar_wait(drain, 0, limit, nullptr, kWaitDkvDrain);
   } else {
     // warps 0-7: thread = key row (TMEM lane); group g covers queries [64g, 64g + 64)
     const int g = warp >> 2;

@@ -108,19 +108,6 @@ __device__ __forceinline__ void copy_row_to_tmem(const uint8_t* src, uint32_t t_
   }
 }
 
-// A operand [128 x d] in tensor memory (16-bit pairs from column a_tmem) times a K-major
-// B tile [128 x d] in shared memory: D[128 x 128] = A B^T.
-template <int D>
-__device__ __forceinline__ void issue_rowdot_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b0,
-                                                uint32_t idesc) {
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-    mma_ts(d_tmem, a_tmem + kk * 8, make_sdesc_sw128(b0 + off, 16, 1024), idesc,
-           kk > 0 ? 1u : 0u);
-  }
-}
-
 // K-major x K-major product over the head dimension: D[128 x 128] = A[128 x d] B[128 x d]^T.
 template <int D>
 __device__ __forceinline__ void issue_rowdot(uint32_t d_tmem, uint32_t a0, uint32_t b0,
@@ -130,6 +117,17 @@ __device__ __forceinline__ void issue_rowdot(uint32_t d_tmem, uint32_t a0, uint3
     const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
     mma_ss(d_tmem, make_sdesc_sw128(a0 + off, 16, 1024), make_sdesc_sw128(b0 + off, 16, 1024),
            idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// The same with both descriptors built once by the caller (see issue_rowdot_ts_d).
+template <int D>
+__device__ __forceinline__ void issue_rowdot_d(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+    mma_ss(d_tmem, a_desc + off, b_desc + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -202,15 +200,18 @@ __global__ void __launch_bounds__(320, 1)
   const uint64_t limit = p.wait_limit;
 
   if (warp == 8) {
-    if (lane == 0) {
+    // TMA producer. The warp runs converged (waits in every lane); the elected lane issues.
+    if (elect_one()) {
       tma_prefetch_map(&map_k);
       tma_prefetch_map(&map_v);
-      int issued = 0;
-      for (int j = 0; j < n; ++j) {
-        const int s = j % NS;
-        if (j >= NS &&
-            !mbar_wait(&kv_empty[s], ((j / NS) - 1) & 1, limit, abort_flag, kWaitDqEmpty))
-          break;
+    }
+    int issued = 0;
+    for (int j = 0; j < n; ++j) {
+      const int s = j % NS;
+      if (j >= NS &&
+          !warp_wait(&kv_empty[s], ((j / NS) - 1) & 1, limit, abort_flag, kWaitDqEmpty))
+        break;
+      if (elect_one()) {
         mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(smem + C::kOffK + s * C::kTileBytes + c * kBoxBytes, &map_k, &k_full[s],
@@ -219,66 +220,89 @@ __global__ void __launch_bounds__(320, 1)
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(smem + C::kOffV + s * C::kTileBytes + c * kBoxBytes, &map_v, &v_full[s],
                       c * kBoxCols, j * kTileN, bh);
-        issued = j + 1;
       }
-      if (*abort_flag) {
-        for (int j = max(0, issued - NS); j < issued; ++j) {
-          mbar_wait(&k_full[j % NS], (j / NS) & 1, limit, nullptr, kWaitDqDrain);
-          mbar_wait(&v_full[j % NS], (j / NS) & 1, limit, nullptr, kWaitDqDrain);
-        }
+      __syncwarp();
+      issued = j + 1;
+    }
+    if (*abort_flag) {
+      for (int j = max(0, issued - NS); j < issued; ++j) {
+        mbar_wait(&k_full[j % NS], (j / NS) & 1, limit, nullptr, kWaitDqDrain);
+        mbar_wait(&v_full[j % NS], (j / NS) & 1, limit, nullptr, kWaitDqDrain);
       }
     }
   } else if (warp == 9) {
-    if (lane == 0) {
-      const uint32_t idesc_sq = make_idesc(BF16, 128, kTileN, false, false);
-      const uint32_t idesc_acc = make_idesc(BF16, 128, D, false, true);
-      const uint32_t sk = smem_u32(smem + C::kOffK);
-      const uint32_t sv = smem_u32(smem + C::kOffV);
-      const uint32_t tq = tmem + C::kColQ;
-      const uint32_t tdo = tmem + C::kColDO;
-      bool ok = mbar_poll(qdo_tmem, 0, limit, abort_flag, kWaitDqQ) &&
-                mbar_poll(&k_full[0], 0, limit, abort_flag, kWaitDqK);
-      if (ok) {
-        tc_fence_after();
-        issue_rowdot_ts<D>(tmem + C::kColS, tq, sk, idesc_sq);
+    // MMA issuer: the warp runs the loop converged and waits in every lane; one elected
+    // lane issues the MMAs and commits (a loop run by one lane alone loses issue slots to
+    // the arithmetic warps of its SM sub-partition and starves the tensor core).
+    const uint32_t idesc_sq = make_idesc(BF16, 128, kTileN, false, false);
+    const uint32_t idesc_acc = make_idesc(BF16, 128, D, false, true);
+    // Stage-0 descriptors: K (K-major, for S = Q K^T), K (MN-major, for dQ = dS K), V.
+    const uint64_t dk = make_sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
+    const uint64_t dk_mn = make_sdesc_sw128(smem_u32(smem + C::kOffK), kBoxBytes, 1024);
+    const uint64_t dv = make_sdesc_sw128(smem_u32(smem + C::kOffV), 16, 1024);
+    constexpr uint32_t kStageStep = C::kTileBytes >> 4;
+    const uint32_t tq = tmem + C::kColQ;
+    const uint32_t tdo = tmem + C::kColDO;
+    bool ok = warp_poll(qdo_tmem, 0, limit, abort_flag, kWaitDqQ) &&
+              warp_poll(&k_full[0], 0, limit, abort_flag, kWaitDqK);
+    if (ok) {
+      tc_fence_after();
+      if (elect_one()) {
+        issue_rowdot_ts_d<D>(tmem + C::kColS, tq, dk, idesc_sq);
         mma_commit(s_full);
-        ok = mbar_poll(&v_full[0], 0, limit, abort_flag, kWaitDqV);
       }
-      if (ok) {
-        tc_fence_after();
-        issue_rowdot_ts<D>(tmem + C::kColDP, tdo, sv, idesc_sq);
+      __syncwarp();
+      ok = warp_poll(&v_full[0], 0, limit, abort_flag, kWaitDqV);
+    }
+    if (ok) {
+      tc_fence_after();
+      if (elect_one()) {
+        issue_rowdot_ts_d<D>(tmem + C::kColDP, tdo, dv, idesc_sq);
         mma_commit(dp_full);
       }
-      for (int j = 0; ok && j < n; ++j) {
-        const int s = j % NS;
-        const int jn = j + 1;
-        const int sn = jn % NS;
-        if (jn < n) {
-          // S of the next block overwrites S once the softmax warps have read it.
-          if (!(ok = mbar_poll(&k_full[sn], (jn / NS) & 1, limit, abort_flag, kWaitDqK) &&
-                     mbar_poll(s_free, j & 1, limit, abort_flag, kWaitDqSC)))
-            break;
-          tc_fence_after();
-          issue_rowdot_ts<D>(tmem + C::kColS, tq, sk + sn * C::kTileBytes, idesc_sq);
+      __syncwarp();
+    }
+    for (int j = 0; ok && j < n; ++j) {
+      const int s = j % NS;
+      const int jn = j + 1;
+      const int sn = jn % NS;
+      if (jn < n) {
+        // S of the next block overwrites S once the softmax warps have read it.
+        if (!(ok = warp_poll(&k_full[sn], (jn / NS) & 1, limit, abort_flag, kWaitDqK) &&
+                   warp_poll(s_free, j & 1, limit, abort_flag, kWaitDqSC)))
+          break;
+        tc_fence_after();
+        if (elect_one()) {
+          issue_rowdot_ts_d<D>(tmem + C::kColS, tq, dk + sn * kStageStep, idesc_sq);
           mma_commit(s_full);
         }
-        if (!(ok = mbar_poll(ds_full, j & 1, limit, abort_flag, kWaitDqDS))) break;
+        __syncwarp();
+      }
+      if (!(ok = warp_poll(ds_full, j & 1, limit, abort_flag, kWaitDqDS))) break;
+      tc_fence_after();
+      // dQ_i += dS K_j (dS read from tensor memory, over dP)
+      if (elect_one())
+        issue_tmem_a_split_d(tmem + C::kColAcc0, tmem + C::kColDP, dk_mn + s * kStageStep,
+                             idesc_acc, j > 0);
+      __syncwarp();
+      if (jn < n) {
+        if (!(ok = warp_poll(&v_full[sn], (jn / NS) & 1, limit, abort_flag, kWaitDqV))) break;
         tc_fence_after();
-        // dQ_i += dS K_j (dS read from tensor memory, over dP)
-        issue_tmem_a_split(tmem + C::kColAcc0, tmem + C::kColDP, sk + s * C::kTileBytes,
-                           idesc_acc, j > 0);
-        if (jn < n) {
-          if (!(ok = mbar_poll(&v_full[sn], (jn / NS) & 1, limit, abort_flag, kWaitDqV))) break;
-          tc_fence_after();
-          issue_rowdot_ts<D>(tmem + C::kColDP, tdo, sv + sn * C::kTileBytes, idesc_sq);
+        if (elect_one()) {
+          issue_rowdot_ts_d<D>(tmem + C::kColDP, tdo, dv + sn * kStageStep, idesc_sq);
           mma_commit(dp_full);
         }
-        mma_commit(&kv_empty[s]);
+        __syncwarp();
       }
+      if (elect_one()) mma_commit(&kv_empty[s]);
+      __syncwarp();
+    }
+    if (elect_one()) {
       if (ok) mma_commit(acc_done);
       mma_commit(drain);
-      mbar_wait(drain, 0, limit, nullptr, kWaitDqDrain);
     }
+    __syncwarp();
+    mbar_wait(drain, 0, limit, nullptr, kWaitDqDrain);
   } else {
     // warps 0-7: thread = query row (TMEM lane); group g covers keys [64g, 64g + 64)
     const int g = warp >> 2;

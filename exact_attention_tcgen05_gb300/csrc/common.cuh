@@ -18,7 +18,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Codes recorded in the status word when a bounded wait gives up (kernel * 16 + site).
 enum WaitSite : int {
   kWaitFwdQ = 0x11, kWaitFwdK, kWaitFwdV, kWaitFwdEmpty, kWaitFwdS, kWaitFwdP, kWaitFwdO,
-  kWaitFwdDrain,
+  kWaitFwdDrain, kWaitFwdX,
   kWaitDqQ = 0x21, kWaitDqK, kWaitDqV, kWaitDqEmpty, kWaitDqS, kWaitDqDP, kWaitDqDS,
   kWaitDqDone, kWaitDqDrain, kWaitDqSC,
   kWaitDkvKV = 0x31, kWaitDkvQ, kWaitDkvDO, kWaitDkvEmpty, kWaitDkvS, kWaitDkvDP,
@@ -39,6 +39,14 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
   return __all_sync(0xffffffffu, ok);
 }
 
+// Warp-uniform bounded poll (non-suspending test_wait in every lane): for the converged
+// MMA-issuing warps.
+__device__ __forceinline__ bool warp_poll(uint64_t* bar, uint32_t parity, uint64_t limit,
+                                          volatile int* abort, int where) {
+  const bool ok = mbar_poll(bar, parity, limit, abort, where);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // A operand in tensor memory whose 16-bit pairs sit in two halves: columns [0, 64) of A in
 // [base, base + 32) and columns [64, 128) in [base + 64, base + 96). B is an MN-major
 // [128 x d] tile in shared memory. D[128 x d] (+)= A B.
@@ -48,6 +56,45 @@ __device__ __forceinline__ void issue_tmem_a_split(uint32_t d_tmem, uint32_t a_t
   for (int kk = 0; kk < 128 / 16; ++kk) {
     const uint32_t a_col = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
     mma_ts(d_tmem, a_tmem + a_col, make_sdesc_sw128(b0 + kk * 2048, kBoxBytes, 1024), idesc,
+           (acc || kk > 0) ? 1u : 0u);
+  }
+}
+
+// A operand [128 x d] in tensor memory (16-bit pairs from column a_tmem) times a K-major
+// B tile [128 x d] in shared memory: D[128 x 128] = A B^T.
+template <int D>
+__device__ __forceinline__ void issue_rowdot_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b0,
+                                                uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+    mma_ts(d_tmem, a_tmem + kk * 8, make_sdesc_sw128(b0 + off, 16, 1024), idesc,
+           kk > 0 ? 1u : 0u);
+  }
+}
+
+// The two products above with the shared-memory descriptor of the B tile built once by
+// the caller (make_sdesc_sw128 of the tile's first byte). The start-address field (bits
+// 0-13, in 16-byte units) is advanced by adding byte offset / 16, which cannot carry out
+// of the field for shared addresses below 256 KiB. Saves the single MMA-issuing thread
+// the descriptor arithmetic of every k-step.
+template <int D>
+__device__ __forceinline__ void issue_rowdot_ts_d(uint32_t d_tmem, uint32_t a_tmem,
+                                                  uint64_t b_desc, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+    mma_ts(d_tmem, a_tmem + kk * 8, b_desc + (off >> 4), idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+__device__ __forceinline__ void issue_tmem_a_split_d(uint32_t d_tmem, uint32_t a_tmem,
+                                                     uint64_t b_desc, uint32_t idesc,
+                                                     bool acc) {
+#pragma unroll
+  for (int kk = 0; kk < 128 / 16; ++kk) {
+    const uint32_t a_col = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;
+    mma_ts(d_tmem, a_tmem + a_col, b_desc + ((kk * 2048) >> 4), idesc,
            (acc || kk > 0) ? 1u : 0u);
   }
 }

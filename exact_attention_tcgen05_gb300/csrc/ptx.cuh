@@ -140,6 +140,20 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// A whole [128 rows x d] tile in one copy: the map views each row as d / 64 halves of 64
+// 16-bit values (dims {64, rows, d / 64, slices}); the box {64, 128, d / 64, 1} lands as
+// d / 64 consecutive 128B-swizzled [128 x 64] boxes. One copy per tile instead of one per
+// 64-column box halves the issue round trips of the producer thread.
+__device__ __forceinline__ void tma_load_tile(void* smem_dst, const CUtensorMap* map,
+                                              uint64_t* bar, int row, int slice) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(0), "r"(row), "r"(0),
+      "r"(slice)
+      : "memory");
+}
+
 // ------------------------------------------------------------------------------------
 // tcgen05: tensor memory and MMA
 // ------------------------------------------------------------------------------------
@@ -384,6 +398,18 @@ __device__ __forceinline__ void add_pair16(float& acc0, float& acc1, uint32_t v)
 // Named barrier over `count` threads (a multiple of 32), id 1..15.
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// True in exactly one lane of the (fully active) warp: the lowest one, the same lane on
+// every call. The MMA-issuing warps run their loops converged and issue from the elected
+// lane; a warp that runs a long loop in one lane (if (lane == 0) ...) loses issue slots to
+// arithmetic-heavy warps on its SM sub-partition, which measurably stalls the tensor core.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
 }
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31; }
