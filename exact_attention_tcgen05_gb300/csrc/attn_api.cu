@@ -164,12 +164,12 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   if (overlap(ro, rl)) return ATTN_ERR_INVALID_ARG;
 
   const Shape s = make_shape(B, H, N, d, dtype, causal, scale);
-  Maps m;  // the forward reads Q with plain loads (into tensor memory): no Q map
-  if ((st = encode_tile_map(&m.k, k, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
-  if ((st = encode_tile_map(&m.v, v, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
-  m.q = m.k;
+  Maps m;
+  if ((st = encode_map(&m.q, q, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
+  if ((st = encode_map(&m.k, k, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
+  if ((st = encode_map(&m.v, v, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
   m.d_o = m.v;
-  return from_cuda(attn::launch_fwd(m, s, q, o, lse, static_cast<cudaStream_t>(cuda_stream)));
+  return from_cuda(attn::launch_fwd(m, s, o, lse, static_cast<cudaStream_t>(cuda_stream)));
 }
 
 attn_status attn_bwd_preprocess(const void* o, const void* dO, float* delta, int B, int H,

@@ -120,16 +120,6 @@ __device__ __forceinline__ void issue_rowdot(uint32_t d_tmem, uint32_t a0, uint3
   }
 }
 
-// The same with both descriptors built once by the caller (see issue_rowdot_ts_d).
-template <int D>
-__device__ __forceinline__ void issue_rowdot_d(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                               uint32_t idesc) {
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-    mma_ss(d_tmem, a_desc + off, b_desc + off, idesc, kk > 0 ? 1u : 0u);
-  }
-}
 
 // Tensor-memory A [128 x 128] (16-bit pairs) times an MN-major [128 x d] tile in shared
 // memory: D[128 x d] (+)= A B.

@@ -8,26 +8,16 @@
 // the last block O / l once, and L = m + ln l. The scores never leave the chip.
 //
 // GB300 design (the pages' kernels were written for A100 / Ada / B200: prior art):
-//  * One CTA = one (b, h) slice x one 128-row query tile. Q_i is copied once from global
-//    memory into tensor memory, so S = Q_i K_j^T is a TS product (A from tensor memory,
-//    K_j from shared memory). On this part an MMA with both operands in shared memory
-//    and N = 128 runs at about half the tensor rate (the tensor core's shared-memory
-//    reads limit it); the TS form runs at the full rate.
-//  * S is double buffered in tensor memory: the tensor core computes S_{j+1} (and P_j V_j)
-//    while the softmax warps work on block j, in place of the two-tile ping-pong
-//    described for Blackwell on "FlashAttention·FA4·FP4", section HBM을 아낀 뒤에는
-//    무엇이 기다리는가. Tensor memory: S0, S1 (128 columns each), O (d), Q (d / 2).
-//  * Warp roles: warps 0-7 softmax (warp w: rows 32 (w % 4) .. + 31 of the tile, score
-//    columns 64 (w / 4) .. + 63 of each block), warp 8 TMA producer of the K ring, warp
-//    10 of the V ring, warp 9 MMA issuer (one thread) and TMEM owner. The two warps that
-//    share rows agree on the running max through shared memory and a two-arrival mbarrier
-//    each block.
-//  * Each K or V tile is one TMA copy (a 4-D view of the rows, see tma_load_tile), and K
-//    and V have a producer thread each: what limits how fast one SM takes in tiles is the
-//    round trip of the producer thread (wait for a free stage, issue), not the copy
-//    engine, so fewer and larger copies from two threads keep the tensor core fed.
-//  * P is written back over its own half of S as 16-bit pairs (columns [0, 32) and
-//    [64, 96)) and fed to the P V product straight from tensor memory.
+//  * One CTA = one (b, h) slice x 256 query rows, split into two 128-row tiles that
+//    ping-pong: while one tile's softmax runs on the CUDA cores, the tensor core works
+//    on the other tile (the two-tile schedule described for Blackwell on
+//    "FlashAttention·FA4·FP4", section HBM을 아낀 뒤에는 무엇이 기다리는가).
+//  * Warp roles: warps 0-3 softmax of tile 0, warps 4-7 softmax of tile 1, warp 8 TMA
+//    producer, warp 9 MMA issuer (one thread) and TMEM owner.
+//  * Q tiles, and a ring of K/V blocks, are TMA-copied into 128B-swizzled shared
+//    memory; S = Q K^T and O += P V run on tcgen05 with fp32 accumulators in tensor
+//    memory (S_t: 128 columns, O_t: d columns per tile). P is written back over S_t as
+//    16-bit pairs and fed to the P V product straight from tensor memory.
 //  * exp is exp2 with scale*log2(e) folded into one FFMA per score ("Triton 05",
 //    section 2. exp -> exp2 트릭); L is exported in the natural log.
 //  * P is rounded to the input type for P V (the Triton code's p.to(v.dtype)). O is
@@ -48,12 +38,11 @@
 namespace attn {
 
 struct FwdParams {
-  const void* q;
   void* o;
   float* lse;
   int N;
   int nkb;          // number of 128-key blocks
-  int nqt;          // number of 128-row query tiles
+  int nqb;          // number of 256-row query blocks
   int causal;
   float scale_log2; // scale * log2(e)
   unsigned long long wait_limit;
@@ -63,95 +52,69 @@ template <int D>
 struct FwdCfg {
   static constexpr int kChunks = D / kBoxCols;            // 64-column boxes per row
   static constexpr int kTileBytes = kChunks * kBoxBytes;  // one 128 x D tile
-  static constexpr int kStages = (D == 128) ? 3 : 4;      // depth of the K and V rings
-  static constexpr int kOffK = 0;
+  static constexpr int kStages = (D == 128) ? 2 : 4;      // K/V ring depth
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  // Exchange area: running-max halves [2 slots][2 halves][128 rows], then l and the
-  // rounded sum [2][2 halves][128 rows] for the epilogue.
-  static constexpr int kOffX = kOffV + kStages * kTileBytes;
-  static constexpr int kXFloats = 2 * 2 * 128 + 2 * 2 * 128;
-  static constexpr int kOffBar = kOffX + kXFloats * 4;
-  // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2],
-  // o_done, o_last, pair[4], drain
-  static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 2 + 4 + 1;
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  // barriers: q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2],
+  // o_done[2], drain
+  static constexpr int kNumBars = 1 + 3 * kStages + 6 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
   // All 512 tensor-memory columns per CTA: one CTA per SM, which the shared memory
   // footprint (> 114 KiB for both head dims) already guarantees.
   static_assert(kSmemBytes > 114 * 1024, "two CTAs could share an SM");
-  static constexpr int kThreads = 352;
+  static constexpr int kThreads = 320;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColQ = 256 + D;
-  static_assert(kColQ + D / 2 <= kTmemCols, "tensor memory overflow");
+  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
 };
 
-// Copies this thread's half row of Q (D / 2 16-bit values, D bytes) into tensor memory
-// as 16-bit pairs; a null source (a row past the end) writes zeros.
-template <int D>
-__device__ __forceinline__ void copy_half_row_to_tmem(const uint8_t* src, uint32_t t_col) {
-  constexpr int kWords = D / 4;  // 32-bit words in D bytes
-  uint32_t r[kWords];
-#pragma unroll
-  for (int k = 0; k < kWords / 4; ++k) {
-    const uint4 v = src ? *reinterpret_cast<const uint4*>(src + k * 16) : make_uint4(0, 0, 0, 0);
-    r[4 * k] = v.x;
-    r[4 * k + 1] = v.y;
-    r[4 * k + 2] = v.z;
-    r[4 * k + 3] = v.w;
-  }
-  if constexpr (kWords == 32) {
-    tmem_st32(t_col, r);
-  } else {
-    tmem_st16(t_col, r);
-  }
-}
-
 template <int D, bool BF16>
-__global__ void __launch_bounds__(352, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap map_k,
+__global__ void __launch_bounds__(320, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
+                    const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const FwdParams p) {
   using C = FwdCfg<D>;
-  constexpr int NS = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
-  uint64_t* k_empty = k_full + NS;
-  uint64_t* v_full = k_empty + NS;
-  uint64_t* v_empty = v_full + NS;
-  uint64_t* s_full = v_empty + NS;
+  uint64_t* v_full = k_full + C::kStages;
+  uint64_t* kv_empty = v_full + C::kStages;
+  uint64_t* s_full = kv_empty + C::kStages;
   uint64_t* p_full = s_full + 2;
-  uint64_t* o_done = p_full + 2;  // each P_j V_j done (phase j)
-  uint64_t* o_last = o_done + 1;  // all of them done (one phase)
-  uint64_t* pair = o_last + 1;
-  uint64_t* drain = pair + 4;
+  uint64_t* o_done = p_full + 2;
+  uint64_t* drain = o_done + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
   const int warp = warp_id();
   const int lane = lane_id();
   const int bh = blockIdx.y;
-  const int qt = p.nqt - 1 - blockIdx.x;  // within a head, longest (most key blocks) first
-  const int q0 = qt * kTileM;
+  const int qb = p.nqb - 1 - blockIdx.x;  // within a head, longest (most key blocks) first
+  const int q0 = qb * 256;
   const int N = p.N;
-  const int n = p.causal ? min(p.nkb, qt + 1) : p.nkb;  // key blocks this tile needs
+  const int ntiles = (q0 + kTileM < N) ? 2 : 1;
+  int nkv[2];
+  for (int t = 0; t < 2; ++t) {
+    nkv[t] = (t < ntiles) ? (p.causal ? min(p.nkb, q0 / kTileN + t + 1) : p.nkb) : 0;
+  }
+  const int n_kv = max(nkv[0], nkv[1]);
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 8);  // one arrival per softmax warp (its half rows of Q stored)
-    for (int s = 0; s < NS; ++s) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
+      mbar_init(&kv_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], 8);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 4);  // one arrival per softmax warp
+      mbar_init(&o_done[t], 1);
     }
-    mbar_init(o_done, 1);
-    mbar_init(o_last, 1);
-    for (int g = 0; g < 4; ++g) mbar_init(&pair[g], 2);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -166,153 +129,164 @@ __global__ void __launch_bounds__(352, 1)
   const uint32_t tmem = *tmem_holder;
   const uint64_t limit = p.wait_limit;
 
-  if (warp == 8 || warp == 10) {
-    // ------------------------------ TMA producers -----------------------------
-    // Warp 8 fills the K ring, warp 10 the V ring, one whole-tile copy per block. The
-    // warp runs converged (waits in every lane); the elected lane issues the copies.
-    const bool is_k = warp == 8;
-    const CUtensorMap* map = is_k ? &map_k : &map_v;
-    uint64_t* full = is_k ? k_full : v_full;
-    uint64_t* empty = is_k ? k_empty : v_empty;
-    uint8_t* ring = smem + (is_k ? C::kOffK : C::kOffV);
-    if (elect_one()) tma_prefetch_map(map);
+  if (warp == 8) {
+    // ------------------------------ TMA producer ------------------------------
+    // Converged warp (waits in every lane); the elected lane issues the copies.
+    if (elect_one()) {
+      tma_prefetch_map(&map_q);
+      tma_prefetch_map(&map_k);
+      tma_prefetch_map(&map_v);
+      mbar_arrive_expect_tx(q_full, ntiles * C::kTileBytes);
+      for (int t = 0; t < ntiles; ++t)
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(smem + C::kOffQ + t * C::kTileBytes + c * kBoxBytes, &map_q, q_full,
+                      c * kBoxCols, q0 + t * kTileM, bh);
+    }
+    __syncwarp();
     int issued = 0;
-    for (int i = 0; i < n; ++i) {
-      const int s = i % NS;
-      if (i >= NS &&
-          !warp_wait(&empty[s], ((i / NS) - 1) & 1, limit, abort_flag, kWaitFwdEmpty))
+    for (int j = 0; j < n_kv; ++j) {
+      const int s = j % C::kStages;
+      if (j >= C::kStages &&
+          !warp_wait(&kv_empty[s], ((j / C::kStages) - 1) & 1, limit, abort_flag,
+                     kWaitFwdEmpty))
         break;
       if (elect_one()) {
-        mbar_arrive_expect_tx(&full[s], C::kTileBytes);
-        tma_load_tile(ring + s * C::kTileBytes, map, &full[s], i * kTileN, bh);
+        mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(smem + C::kOffK + s * C::kTileBytes + c * kBoxBytes, &map_k,
+                      &k_full[s], c * kBoxCols, j * kTileN, bh);
+        mbar_arrive_expect_tx(&v_full[s], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(smem + C::kOffV + s * C::kTileBytes + c * kBoxBytes, &map_v,
+                      &v_full[s], c * kBoxCols, j * kTileN, bh);
       }
       __syncwarp();
-      issued = i + 1;
+      issued = j + 1;
     }
     if (*abort_flag) {
-      // Let every copy this warp started land before its shared memory is released.
-      for (int g = max(0, issued - NS); g < issued; ++g)
-        mbar_wait(&full[g % NS], (g / NS) & 1, limit, nullptr, kWaitFwdDrain);
+      // Let every copy this CTA started land before its shared memory is released.
+      mbar_wait(q_full, 0, limit, nullptr, kWaitFwdDrain);
+      for (int j = max(0, issued - C::kStages); j < issued; ++j) {
+        const int s = j % C::kStages;
+        mbar_wait(&k_full[s], (j / C::kStages) & 1, limit, nullptr, kWaitFwdDrain);
+        mbar_wait(&v_full[s], (j / C::kStages) & 1, limit, nullptr, kWaitFwdDrain);
+      }
     }
   } else if (warp == 9) {
     // ------------------------------ MMA issuer --------------------------------
-    // The whole warp runs the loop and waits; one elected lane issues the MMAs and the
-    // commits. Per block j: P_j V_j into O, then S_{j+2} into the buffer P_j came from (the
-    // tensor core runs one thread's MMAs in issue order, so P_j is read first).
+    // Converged warp; the elected lane issues the MMAs and commits.
     const uint32_t idesc_s = make_idesc(BF16, 128, kTileN, false, false);
     const uint32_t idesc_o = make_idesc(BF16, 128, D, false, true);
-    // Descriptors of stage 0 of each ring; stage s adds s * kTileBytes / 16.
-    const uint64_t dk = make_sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
-    const uint64_t dv = make_sdesc_sw128(smem_u32(smem + C::kOffV), kBoxBytes, 1024);
-    constexpr uint32_t kStageStep = C::kTileBytes >> 4;
-    const uint32_t tq = tmem + C::kColQ;
+    const uint64_t dq0 = make_sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
+    const uint64_t dk0 = make_sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
+    const uint64_t dv0 = make_sdesc_sw128(smem_u32(smem + C::kOffV), kBoxBytes, 1024);
+    constexpr uint32_t kStep = C::kTileBytes >> 4;
     const uint32_t col_s[2] = {C::kColS0, C::kColS1};
+    const uint32_t col_o[2] = {C::kColO0, C::kColO1};
+    auto issue_s = [&](int t, int stage) {
+      issue_rowdot_d<D>(tmem + col_s[t], dq0 + t * kStep, dk0 + stage * kStep, idesc_s);
+    };
+    auto issue_pv = [&](int t, int stage, bool acc) {
+#pragma unroll
+      for (int kk = 0; kk < kTileN / 16; ++kk)
+        mma_ts(tmem + col_o[t], tmem + col_s[t] + kk * 8,
+               dv0 + stage * kStep + ((kk * 2048) >> 4), idesc_o, (acc || kk > 0) ? 1u : 0u);
+    };
+
     bool ok = warp_poll(q_full, 0, limit, abort_flag, kWaitFwdQ);
-    for (int j = 0; ok && j < min(2, n); ++j) {
-      const int s = j % NS;
-      if (!(ok = warp_poll(&k_full[s], (j / NS) & 1, limit, abort_flag, kWaitFwdK))) break;
+    if (ok) ok = warp_poll(&k_full[0], 0, limit, abort_flag, kWaitFwdK);
+    if (ok) {
       tc_fence_after();
       if (elect_one()) {
-        issue_rowdot_ts_d<D>(tmem + col_s[j], tq, dk + s * kStageStep, idesc_s);
-        mma_commit(&s_full[j]);
-        mma_commit(&k_empty[s]);
+        for (int t = 0; t < 2; ++t)
+          if (nkv[t] > 0) {
+            issue_s(t, 0);
+            mma_commit(&s_full[t]);
+          }
       }
       __syncwarp();
     }
-    for (int j = 0; ok && j < n; ++j) {
-      const int b = j & 1;
-      const int s = j % NS;
-      if (!(ok = warp_poll(&v_full[s], (j / NS) & 1, limit, abort_flag, kWaitFwdV))) break;
-      if (!(ok = warp_poll(&p_full[b], (j >> 1) & 1, limit, abort_flag, kWaitFwdP))) break;
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const int s = j % C::kStages;
+      if (!(ok = warp_poll(&v_full[s], (j / C::kStages) & 1, limit, abort_flag, kWaitFwdV)))
+        break;
       tc_fence_after();
-      if (elect_one()) {
-        issue_tmem_a_split_d(tmem + C::kColO, tmem + col_s[b], dv + s * kStageStep, idesc_o,
-                             j > 0);
-        mma_commit(o_done);
-        mma_commit(&v_empty[s]);
-      }
-      __syncwarp();
-      const int jn = j + 2;
-      if (jn < n) {
-        const int sn = jn % NS;
-        if (!(ok = warp_poll(&k_full[sn], (jn / NS) & 1, limit, abort_flag, kWaitFwdK))) break;
+      const int jn = j + 1;
+      const int sn = jn % C::kStages;
+      bool next_k_ready = false;
+      for (int t = 0; t < 2 && ok; ++t) {
+        if (j >= nkv[t]) continue;
+        if (!(ok = warp_poll(&p_full[t], j & 1, limit, abort_flag, kWaitFwdP))) break;
         tc_fence_after();
         if (elect_one()) {
-          issue_rowdot_ts_d<D>(tmem + col_s[b], tq, dk + sn * kStageStep, idesc_s);
-          mma_commit(&s_full[b]);
-          mma_commit(&k_empty[sn]);
+          issue_pv(t, s, j > 0);
+          mma_commit(&o_done[t]);
         }
+        __syncwarp();
+        if (jn < nkv[t]) {
+          if (!next_k_ready) {
+            if (!(ok = warp_poll(&k_full[sn], (jn / C::kStages) & 1, limit, abort_flag,
+                                 kWaitFwdK)))
+              break;
+            tc_fence_after();
+            next_k_ready = true;
+          }
+          if (elect_one()) {
+            issue_s(t, sn);
+            mma_commit(&s_full[t]);
+          }
+          __syncwarp();
+        }
+      }
+      if (ok) {
+        if (elect_one()) mma_commit(&kv_empty[s]);
         __syncwarp();
       }
     }
-    // The epilogue waits on its own barrier: when the softmax leaves its last block two
-    // P V products can still be in flight, and a parity wait on o_done would then see the
-    // phase before them as the one it waits for. Every MMA issued must finish before tensor
-    // memory is released (drain).
-    if (elect_one()) {
-      if (ok) mma_commit(o_last);
-      mma_commit(drain);
-    }
+    // Every MMA issued must finish before tensor memory is released.
+    if (elect_one()) mma_commit(drain);
     __syncwarp();
     mbar_wait(drain, 0, limit, nullptr, kWaitFwdDrain);
   } else {
-    // ------------------------------ softmax -----------------------------------
-    const int g = warp & 3;   // row group: tile rows [32 g, 32 g + 32)
-    const int h = warp >> 2;  // column half: score columns [64 h, 64 h + 64)
-    const uint32_t lane_base = (uint32_t)(g * 32) << 16;
-    const int r = g * 32 + lane;  // row within the tile
-    const int row = q0 + r;       // query index of this thread
-    float* xm = reinterpret_cast<float*>(smem + C::kOffX);  // [2 slots][2 halves][128]
-    float* xl = xm + 2 * 2 * 128;                            // [l, lr][2 halves][128]
+    // ------------------------------ softmax (tile t) --------------------------
+    const int t = warp >> 2;
+    const int wq = warp & 3;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + (t == 0 ? C::kColS0 : C::kColS1);
+    const uint32_t t_o = tmem + lane_base + (t == 0 ? C::kColO0 : C::kColO1);
+    const int row = q0 + t * kTileM + wq * 32 + lane;  // query index of this thread
+    const int tile_row0 = q0 + t * kTileM;
     const float sl2 = p.scale_log2;
-
-    // Q half row -> tensor memory (A operand of S = Q K^T).
-    {
-      const uint8_t* src =
-          row < N ? reinterpret_cast<const uint8_t*>(p.q) +
-                        ((size_t)bh * N + (size_t)row) * (size_t)(D * 2) + h * D
-                  : nullptr;
-      copy_half_row_to_tmem<D>(src, tmem + lane_base + C::kColQ + h * (D / 4));
-      tmem_st_wait();
-      tc_fence_before();
-      warp_arrive(q_full);
-    }
-
     float m = -INFINITY;  // running max of scale*log2(e)*S (possibly stale by <= 8)
-    float l = 0.f;        // sum of exp2 values over this warp's columns (fp32)
+    float l = 0.f;        // sum of exp2 values (fp32)
     float lr = 0.f;       // sum of the same values after rounding to 16 bits
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      const int b = j & 1;
-      const uint32_t t_s = tmem + lane_base + (b == 0 ? C::kColS0 : C::kColS1) + 64 * h;
-      if (!(ok = warp_wait(&s_full[b], (j >> 1) & 1, limit, abort_flag, kWaitFwdS))) break;
+    for (int j = 0; j < nkv[t]; ++j) {
+      if (!(ok = warp_wait(&s_full[t], j & 1, limit, abort_flag, kWaitFwdS))) break;
       tc_fence_after();
-      uint32_t sr[64];
-      tmem_ld64(t_s, sr);
+      // One wide load of the whole score row, then a single wait.
+      uint32_t sr[kTileN];
+      tmem_ld128(t_s, sr);
       float* s = reinterpret_cast<float*>(sr);
-      const int kbase = j * kTileN + 64 * h;  // key index of this warp's column 0
-      if ((p.causal && kbase + 63 > q0) || kbase + 64 > N) {
-        int lim = N - 1 - kbase;                    // last key in range
-        if (p.causal) lim = min(lim, row - kbase);  // last key visible to this row
+      const int kbase = j * kTileN;
+      const bool diag = p.causal && (kbase + kTileN - 1 > tile_row0);
+      if (diag || kbase + kTileN > N) {
+        int lim = N - 1 - kbase;                       // last key in range
+        if (p.causal) lim = min(lim, row - kbase);     // last key visible to this row
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+        for (int c = 0; c < kTileN; ++c)
           if (c > lim) s[c] = -INFINITY;
       }
-      // Max over this warp's 64 columns in four independent chains of 3-input max.
+      // Row max in four independent chains of 3-input max (short dependency chains).
       float mx[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) mx[u] = fmaxf(s[2 * u], s[2 * u + 1]);
+      for (int u = 0; u < 4; ++u) mx[u] = fmaxf(s[2 * u], s[2 * u + 1]);  // columns 0..7
 #pragma unroll
-      for (int c = 8; c < 64; c += 8) {
+      for (int c = 8; c < kTileN; c += 8) {  // columns 8..127
 #pragma unroll
         for (int u = 0; u < 4; ++u) mx[u] = fmax3(mx[u], s[c + 2 * u], s[c + 2 * u + 1]);
       }
-      const float m_half = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      // The row max over both halves: both warps compute the same value bit for bit.
-      xm[(b * 2 + h) * 128 + r] = m_half;
-      warp_arrive(&pair[g]);
-      if (!(ok = warp_wait(&pair[g], j & 1, limit, abort_flag, kWaitFwdX))) break;
-      const float m_cand = fmaxf(m_half, xm[(b * 2 + (h ^ 1)) * 128 + r]) * sl2;
+      const float m_cand = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
       const bool need = m_cand > m + 8.0f;
       float alpha = 1.f;
       if (need) {
@@ -323,17 +297,18 @@ __global__ void __launch_bounds__(352, 1)
       const float2 neg_m2 = make_float2(-m, -m);
       // l sums the fp32 values (it defines L); lr sums the 16-bit values that enter
       // P V, so that O = acc / lr divides by exactly the weights it accumulated.
+      // Two sums, each in four independent packed accumulators.
       float2 sum[4];
       float rsum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int u = 0; u < 4; ++u) sum[u] = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int c4 = 0; c4 < 2; ++c4) {
+      for (int c4 = 0; c4 < kTileN / 32; ++c4) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float2 x =
-              fma2(make_float2(s[c4 * 32 + 2 * i], s[c4 * 32 + 2 * i + 1]), sl2x2, neg_m2);
+          const float2 x = fma2(make_float2(s[c4 * 32 + 2 * i], s[c4 * 32 + 2 * i + 1]), sl2x2,
+                                neg_m2);
           const float2 pp = make_float2(ex2(x.x), ex2(x.y));
           sum[i & 3] = add2(sum[i & 3], pp);
           pk[i] = pack2<BF16>(pp.x, pp.y);
@@ -342,72 +317,52 @@ __global__ void __launch_bounds__(352, 1)
         tmem_st16(t_s + c4 * 16, pk);
       }
       const float2 sa = add2(add2(sum[0], sum[1]), add2(sum[2], sum[3]));
-      l = l * alpha + (sa.x + sa.y);
-      lr = lr * alpha + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
+      const float sum0 = sa.x, sum1 = sa.y, rsum0 = rsum[0] + rsum[1], rsum1 = rsum[2] + rsum[3];
+      l = l * alpha + (sum0 + sum1);
+      lr = lr * alpha + (rsum0 + rsum1);
       if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // Bring this warp's half of O to the new max once P_{j-1} V_{j-1} has landed
-        // (P_{j-2} V_{j-2} has: S_j, already waited for, was issued after it).
-        if (!(ok = warp_wait(o_done, (j - 1) & 1, limit, abort_flag, kWaitFwdO))) break;
+        // Bring O to the new max: wait until the previous P V product has landed.
+        if (!(ok = warp_wait(&o_done[t], (j - 1) & 1, limit, abort_flag, kWaitFwdO))) break;
         tc_fence_after();
-        const uint32_t t_o = tmem + lane_base + C::kColO + h * (D / 2);
-        if constexpr (D == 128) {
-          uint32_t o[64];
-          tmem_ld64(t_o, o);
 #pragma unroll
-          for (int i = 0; i < 64; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&o[0]);
-          uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&o[32]);
-          tmem_st32(t_o, lo);
-          tmem_st32(t_o + 32, hi);
-        } else {
-          uint32_t o[32];
-          tmem_ld32(t_o, o);
+        for (int cc = 0; cc < D / 64; ++cc) {
+          uint32_t r[64];
+          tmem_ld64(t_o + cc * 64, r);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(t_o, o);
+          for (int i = 0; i < 64; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
+          uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[32]);
+          tmem_st32(t_o + cc * 64, lo);
+          tmem_st32(t_o + cc * 64 + 32, hi);
         }
       }
       tmem_st_wait();
       tc_fence_before();
-      warp_arrive(&p_full[b]);
+      warp_arrive(&p_full[t]);
     }
-    if (ok) {
-      // Both halves' sums, then this warp's half of the O row.
-      xl[h * 128 + r] = l;
-      xl[(2 + h) * 128 + r] = lr;
-      warp_arrive(&pair[g]);
-      ok = warp_wait(&pair[g], n & 1, limit, abort_flag, kWaitFwdX);
-    }
-    if (ok) {
-      const float l_row = l + xl[(h ^ 1) * 128 + r];
-      const float lr_row = lr + xl[(2 + (h ^ 1)) * 128 + r];
-      ok = warp_wait(o_last, 0, limit, abort_flag, kWaitFwdO);
-      if (ok) {
-        tc_fence_after();
-        const float inv_l = 1.f / lr_row;
-        const uint32_t t_o = tmem + lane_base + C::kColO + h * (D / 2);
-        uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
-                        ((size_t)bh * N + (size_t)row) * (size_t)(D * 2) + h * D;
-        constexpr int kCols = D / 2;  // fp32 columns of this half
-        uint32_t o[kCols];
-        if constexpr (kCols == 64) {
-          tmem_ld64(t_o, o);
-        } else {
-          tmem_ld32(t_o, o);
-        }
-        uint32_t pk[kCols / 2];
+    if (ok && nkv[t] > 0 &&
+        warp_wait(&o_done[t], (nkv[t] - 1) & 1, limit, abort_flag, kWaitFwdO)) {
+      tc_fence_after();
+      const float inv_l = 1.f / lr;
+      uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
+                      ((size_t)bh * N + (size_t)row) * (size_t)(D * 2);
 #pragma unroll
-        for (int i = 0; i < kCols / 2; ++i)
-          pk[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l,
-                              __uint_as_float(o[2 * i + 1]) * inv_l);
+      for (int cc = 0; cc < D / 64; ++cc) {
+        uint32_t r[64];
+        tmem_ld64(t_o + cc * 64, r);
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          pk[i] = pack2<BF16>(__uint_as_float(r[2 * i]) * inv_l,
+                              __uint_as_float(r[2 * i + 1]) * inv_l);
         if (row < N) {
-          uint4* dst = reinterpret_cast<uint4*>(orow);
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 128);
 #pragma unroll
-          for (int v = 0; v < kCols / 8; ++v)
+          for (int v = 0; v < 8; ++v)
             dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-          if (h == 0) p.lse[(size_t)bh * N + row] = (m + log2f(l_row)) * kLn2;
         }
       }
+      if (row < N) p.lse[(size_t)bh * N + row] = (m + log2f(l)) * kLn2;
     }
     tc_fence_before();
   }

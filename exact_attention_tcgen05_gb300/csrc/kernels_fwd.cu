@@ -5,34 +5,32 @@
 namespace attn {
 
 template <int D, bool BF16>
-static cudaError_t launch_fwd_t(const Maps& m, const Shape& s, const void* q, void* o,
-                                float* lse, cudaStream_t st) {
+static cudaError_t launch_fwd_t(const Maps& m, const Shape& s, void* o, float* lse,
+                                cudaStream_t st) {
   using C = FwdCfg<D>;
   auto kern = attn_fwd_kernel<D, BF16>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   FwdParams p;
-  p.q = q;
   p.o = o;
   p.lse = lse;
   p.N = s.N;
   p.nkb = (s.N + kTileN - 1) / kTileN;
-  p.nqt = (s.N + kTileM - 1) / kTileM;
+  p.nqb = (s.N + 2 * kTileM - 1) / (2 * kTileM);
   p.causal = s.causal ? 1 : 0;
   p.scale_log2 = s.scale * kLog2e;
   p.wait_limit = s.wait_limit;
-  dim3 grid(p.nqt, s.BH);
-  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(m.k, m.v, p);
+  dim3 grid(p.nqb, s.BH);
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(m.q, m.k, m.v, p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd(const Maps& m, const Shape& s, const void* q, void* o, float* lse,
-                       cudaStream_t st) {
-  if (s.d == 128) return s.bf16 ? launch_fwd_t<128, true>(m, s, q, o, lse, st)
-                                : launch_fwd_t<128, false>(m, s, q, o, lse, st);
-  return s.bf16 ? launch_fwd_t<64, true>(m, s, q, o, lse, st)
-                : launch_fwd_t<64, false>(m, s, q, o, lse, st);
+cudaError_t launch_fwd(const Maps& m, const Shape& s, void* o, float* lse, cudaStream_t st) {
+  if (s.d == 128) return s.bf16 ? launch_fwd_t<128, true>(m, s, o, lse, st)
+                                : launch_fwd_t<128, false>(m, s, o, lse, st);
+  return s.bf16 ? launch_fwd_t<64, true>(m, s, o, lse, st)
+                : launch_fwd_t<64, false>(m, s, o, lse, st);
 }
 
 ATTN_DEFINE_STATUS_READER(status_fwd)

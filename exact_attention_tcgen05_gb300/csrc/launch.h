@@ -19,8 +19,7 @@ struct Shape {
   unsigned long long wait_limit;  // SM cycles one pipeline wait may take
 };
 
-cudaError_t launch_fwd(const Maps& m, const Shape& s, const void* q, void* o, float* lse,
-                       cudaStream_t st);
+cudaError_t launch_fwd(const Maps& m, const Shape& s, void* o, float* lse, cudaStream_t st);
 cudaError_t launch_delta(const Shape& s, const void* o, const void* dO, float* delta,
                          cudaStream_t st);
 // q and dO are the raw [B*H, N, d] tensors the maps describe (the dQ kernel reads its

@@ -154,6 +154,29 @@ __device__ __forceinline__ void tma_load_tile(void* smem_dst, const CUtensorMap*
       : "memory");
 }
 
+// Prefetch of a whole tile (same coordinates as tma_load_tile) into L2, no completion.
+__device__ __forceinline__ void tma_prefetch_tile(const CUtensorMap* map, int row, int slice) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(0), "r"(row), "r"(0), "r"(slice)
+      : "memory");
+}
+
+// Asynchronous 16-byte global -> shared copy (no registers held while it is in flight);
+// src_bytes = 0 writes 16 zero bytes and reads nothing.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)),
+               "l"(gsrc), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------------------
 // tcgen05: tensor memory and MMA
 // ------------------------------------------------------------------------------------
