@@ -328,16 +328,27 @@ def load_traffic(kernel: str, workload: str):
     with open(path) as f:
         t = json.load(f)
     entry = t.get(kernel, {})
-    if entry.get("workload") == workload and entry.get("source_hash") == source_hash():
+    if entry.get("workload") == workload and entry.get("source_hash") == source_hash(kernel):
         return entry.get("dram_bytes_per_launch")
     return None
 
 
-def source_hash() -> str:
+# The source files each kernel is compiled from (a traffic record is valid only while
+# their contents match the hash stored with it).
+KERNEL_SOURCES = {
+    "fwd": ["fwd.cuh", "kernels_fwd.cu"],
+    "delta": ["bwd_delta.cuh", "kernels_delta.cu"],
+    "dkv": ["bwd_dkv.cuh", "bwd_dq.cuh", "kernels_dkv.cu"],
+    "dq": ["bwd_dq.cuh", "kernels_dq.cu"],
+}
+COMMON_SOURCES = ["common.cuh", "ptx.cuh", "launch.h"]
+
+
+def source_hash(kernel: str) -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_tcgen05_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in COMMON_SOURCES + KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
