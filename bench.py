@@ -314,9 +314,68 @@ def run_ours(args) -> None:
                      "algorithmic_tflop_per_launch": dom_flops / 1e12, "traffic": traffic},
         "e2e": e2e, "clocks": clock_info, "gpu_launches": 4 * args.steps,
     }
+    if not args.no_decode:
+        line["decode"] = measure_decode(args, peaks)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w)
     print(json.dumps(line), flush=True)
+
+
+# Split-KV decoding, measured after the step (outside its timed region): one query row per
+# (b, h) against a K/V cache larger than L2, inputs resident, partial + merge per call.
+DECODE_WORKLOAD = dict(name="decode_B8_H32_Nk32768_d128_bf16", B=8, H=32, Nk=32768, d=128,
+                       dtype="bf16", seed=2024)
+
+
+def measure_decode(args, peaks: dict) -> dict:
+    import torch
+    from exact_attention_tcgen05_gb300 import binding
+    from exact_attention_tcgen05_gb300 import inputs as I
+
+    c = DECODE_WORKLOAD
+    B, H, Nk, d = c["B"], c["H"], c["Nk"], c["d"]
+    wq = I.custom(B, H, 1, d, c["dtype"], False, seed=c["seed"])
+    wk = I.custom(B, H, Nk, d, c["dtype"], False, seed=c["seed"] + 1)
+    q, k, v = I.make_tensor_cuda(wq, "q"), I.make_tensor_cuda(wk, "k"), I.make_tensor_cuda(wk, "v")
+    splits = binding.attn_decode_splits(B, H, Nk)
+    parts = torch.empty((B, H, splits, d + 4), dtype=torch.float32, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        binding.attn_decode(q, k, v, num_splits=splits, o=o, lse=lse, partials=parts)
+    torch.cuda.synchronize()
+    n = max(10, min(args.steps, 100))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    for i in range(n):
+        ev[i][0].record(stream)
+        binding.attn_decode_partial(q, k, v, num_splits=splits, partials=parts)
+        ev[i][1].record(stream)
+        binding.attn_decode_merge(parts, q.dtype, o=o, lse=lse)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    code, where = binding.attn_last_kernel_status()
+    if code != binding.ATTN_OK:
+        raise RuntimeError(f"a bounded wait ran out inside a decode kernel (site {where:#x})")
+    part_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / n
+    merge_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / n
+    kv_bytes = 2 * B * H * Nk * d * 2
+    rec_bytes = B * H * splits * (d + 4) * 4
+    total_bytes = kv_bytes + 2 * B * H * d * 2 + 2 * rec_bytes + B * H * 4
+    total_ms = part_ms + merge_ms
+    gbs = total_bytes / (total_ms * 1e-3) / 1e9
+    part_gbs = (kv_bytes + B * H * d * 2 + rec_bytes) / (part_ms * 1e-3) / 1e9
+    out = {"workload": c["name"], "splits": splits, "calls": n, "ms_per_call": total_ms,
+           "partial_ms": part_ms, "merge_ms": merge_ms, "bytes_per_call": total_bytes,
+           "l2": "K and V are 2 GiB each, far larger than L2",
+           "roofline": {"kernel": "decode partial", "bound": "hbm", "achieved": part_gbs,
+                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": part_gbs / peaks["hbm_gbs"],
+                        "peak_kind": f"HBM copy ({peaks['source']})"},
+           "achieved_gbs_call": gbs}
+    del q, k, v, parts, o, lse
+    torch.cuda.empty_cache()
+    return out
 
 
 def load_traffic(kernel: str, workload: str):
@@ -401,6 +460,7 @@ def main() -> None:
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

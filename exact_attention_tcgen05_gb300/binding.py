@@ -35,6 +35,11 @@ SIGNATURES = {
     "attn_bwd_dq": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F,
                               _P]),
+    "attn_decode_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "attn_decode_splits": (_I, [_I, _I, _I]),
+    "attn_decode_partial": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "attn_decode_merge": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "attn_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
     "attn_status_str": (ctypes.c_char_p, [_I]),
     "attn_last_kernel_status": (_I, [_P, ctypes.POINTER(_I)]),
 }
@@ -251,6 +256,103 @@ def attn_bwd_dq(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, lse: torch.Te
                                   _stream_handle(stream))
     _check("attn_bwd_dq", code)
     return dq
+
+
+# ---------------------------------------------------------------- split-KV decode
+def attn_decode_splits(B: int, H: int, Nk: int) -> int:
+    return int(load().attn_decode_splits(B, H, Nk))
+
+
+def attn_decode_workspace_bytes(B: int, H: int, d: int, num_splits: int) -> int:
+    return int(load().attn_decode_workspace_bytes(B, H, d, num_splits))
+
+
+def _decode_args(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
+    B, H, Nq, d = _shape_of(q, "q")
+    if Nq != 1:
+        raise ValueError("q must hold one query row per (b, h): [B, H, 1, d]")
+    Bk, Hk, Nk, dk = _shape_of(k, "k")
+    if (Bk, Hk, dk) != (B, H, d) or k.dtype != q.dtype or k.device != q.device:
+        raise ValueError("k must be [B, H, Nk, d] with q's dtype and device")
+    if v.shape != k.shape or v.dtype != k.dtype or v.device != k.device or not v.is_contiguous():
+        raise ValueError("v must match k")
+    return B, H, Nk, d
+
+
+def _partials_like(q, B, H, d, splits, partials):
+    n = attn_decode_workspace_bytes(B, H, d, splits) // 4
+    if partials is None:
+        return torch.empty((B, H, splits, d + 4), dtype=torch.float32, device=q.device)
+    if partials.dtype != torch.float32 or not partials.is_contiguous() \
+            or partials.numel() < n or partials.device != q.device:
+        raise ValueError("partials must be a contiguous float32 tensor of "
+                         "attn_decode_workspace_bytes / 4 elements on q's device")
+    return partials
+
+
+def attn_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                scale: Optional[float] = None, num_splits: Optional[int] = None,
+                o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                partials: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None
+                ) -> tuple[torch.Tensor, torch.Tensor]:
+    """Split-KV decode: o = softmax(scale q k^T) v for q [B, H, 1, d], k, v [B, H, Nk, d];
+    lse [B, H] float32. Returns (o, lse)."""
+    B, H, Nk, d = _decode_args(q, k, v)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    splits = attn_decode_splits(B, H, Nk) if num_splits is None else int(num_splits)
+    o = torch.empty_like(q) if o is None else o
+    _same(q, o, "o")
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    if lse.shape != (B, H) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H] tensor")
+    partials = _partials_like(q, B, H, d, splits, partials)
+    with torch.cuda.device(q.device):
+        code = load().attn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  lse.data_ptr(), partials.data_ptr(), B, H, Nk, d,
+                                  _DTYPE_CODES[q.dtype], scale, splits, _stream_handle(stream))
+    _check("attn_decode", code)
+    return o, lse
+
+
+def attn_decode_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                        scale: Optional[float] = None, num_splits: int = 1,
+                        partials: Optional[torch.Tensor] = None,
+                        stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """The per-split records [B, H, num_splits, d + 4]: O~ [d], m, l, 2 unused."""
+    B, H, Nk, d = _decode_args(q, k, v)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    partials = _partials_like(q, B, H, d, num_splits, partials)
+    with torch.cuda.device(q.device):
+        code = load().attn_decode_partial(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                          partials.data_ptr(), B, H, Nk, d,
+                                          _DTYPE_CODES[q.dtype], scale, int(num_splits),
+                                          _stream_handle(stream))
+    _check("attn_decode_partial", code)
+    return partials
+
+
+def attn_decode_merge(partials: torch.Tensor, dtype: torch.dtype,
+                      o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                      stream: Optional[torch.cuda.Stream] = None
+                      ) -> tuple[torch.Tensor, torch.Tensor]:
+    """Joins [B, H, S, d + 4] records into o [B, H, 1, d] (dtype) and lse [B, H]."""
+    if partials.dim() != 4 or partials.dtype != torch.float32 or not partials.is_contiguous() \
+            or not partials.is_cuda:
+        raise ValueError("partials must be a contiguous CUDA float32 [B, H, S, d + 4] tensor")
+    B, H, S, d4 = partials.shape
+    d = d4 - 4
+    if o is None:
+        o = torch.empty((B, H, 1, d), dtype=dtype, device=partials.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=partials.device)
+    _shape_of(o, "o")
+    with torch.cuda.device(partials.device):
+        code = load().attn_decode_merge(partials.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H,
+                                        d, _DTYPE_CODES[o.dtype], S, _stream_handle(stream))
+    _check("attn_decode_merge", code)
+    return o, lse
 
 
 def attn_last_kernel_status(stream: Optional[torch.cuda.Stream] = None) -> tuple[int, int]:

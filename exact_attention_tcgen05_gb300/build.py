@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libattn.so")
 
 SOURCES = ["kernels_fwd.cu", "kernels_dq.cu", "kernels_dkv.cu", "kernels_delta.cu",
-           "attn_api.cu", "kernels_noalloc.cu"]
+           "kernels_decode.cu", "attn_api.cu", "kernels_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "--expt-relaxed-constexpr", "-I" + INCLUDE, "-I" + CSRC]

@@ -1,6 +1,7 @@
 // attn_api.cu - the C ABI declared in include/attn.h: argument validation (host only,
 // before any CUDA call), TMA descriptor encoding and kernel launches on the caller's
 // stream. The library allocates no device memory and keeps no per-call state.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -88,23 +89,6 @@ attn_status encode_map(CUtensorMap* m, const void* base, int BH, int N, int d, b
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r =
       enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
-}
-
-// Map for whole-tile copies (tma_load_tile): dims {64, N, d / 64, BH} with strides
-// {2 d, 128, 2 N d} bytes, box {64, 128, d / 64, 1}.
-attn_status encode_tile_map(CUtensorMap* m, const void* base, int BH, int N, int d, bool bf16) {
-  EncodeFn enc = get_encode();
-  if (enc == nullptr) return ATTN_ERR_CUDA;
-  const cuuint64_t dims[4] = {64, (cuuint64_t)N, (cuuint64_t)(d / 64), (cuuint64_t)BH};
-  const cuuint64_t strides[3] = {(cuuint64_t)d * 2, 128, (cuuint64_t)N * (cuuint64_t)d * 2};
-  const cuuint32_t box[4] = {64, 128, (cuuint32_t)(d / 64), 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUresult r =
-      enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -282,12 +266,121 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   return from_cuda(e);
 }
 
+// ---------------------------------------------------------------- split-KV decode
+namespace {
+constexpr int kMaxSplits = 65535;  // grid.x of the partial kernel
+
+attn_status check_decode(int B, int H, int Nk, int d, attn_dtype dtype, int splits) {
+  attn_status st = check_shape(B, H, Nk, d, dtype);
+  if (st != ATTN_OK) return st;
+  if (splits < 1 || splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+attn::DecodeShape make_decode_shape(int B, int H, int Nk, int d, attn_dtype dtype, int splits,
+                                    float scale) {
+  attn::DecodeShape s;
+  s.BH = B * H;
+  s.Nk = Nk;
+  s.d = d;
+  s.splits = splits;
+  s.bf16 = dtype == ATTN_BF16;
+  s.scale = scale;
+  s.wait_limit = wait_limit_cycles();
+  return s;
+}
+}  // namespace
+
+size_t attn_decode_workspace_bytes(int B, int H, int d, int num_splits) {
+  if (B <= 0 || H <= 0 || num_splits <= 0 || (d != 64 && d != 128)) return 0;
+  return (size_t)4 * (size_t)B * (size_t)H * (size_t)num_splits * (size_t)(d + 4);
+}
+
+int attn_decode_splits(int B, int H, int Nk) {
+  if (B <= 0 || H <= 0 || Nk <= 0) return 0;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms <= 0)
+    sms = 152;
+  // At least eight waves of resident CTAs, no split shorter than 256 keys, and among the
+  // counts up to twice that the one whose last wave is fullest.
+  const long long bh = (long long)B * H;
+  const long long resident = (long long)sms * attn::kDecodeCtasPerSmPublic;
+  const long long most = std::min(std::max(1LL, ((long long)Nk + 255) / 256),
+                                  (long long)kMaxSplits);
+  const long long lo = std::min(most, std::max(1LL, (8 * resident + bh - 1) / bh));
+  long long best = lo;
+  double best_fill = 0.0;
+  for (long long s = lo; s <= std::min(most, 2 * lo); ++s) {
+    const long long ctas = bh * s;
+    const long long waves = (ctas + resident - 1) / resident;
+    const double fill = (double)ctas / (double)(waves * resident);
+    if (fill > best_fill + 1e-9) {
+      best_fill = fill;
+      best = s;
+    }
+  }
+  return (int)best;
+}
+
+attn_status attn_decode_partial(const void* q, const void* k, const void* v, float* partials,
+                                int B, int H, int Nk, int d, attn_dtype dtype, float scale,
+                                int num_splits, void* cuda_stream) {
+  attn_status st = check_decode(B, H, Nk, d, dtype, num_splits);
+  if (st != ATTN_OK) return st;
+  if ((st = check_scale(scale)) != ATTN_OK) return st;
+  const void* ptrs[4] = {q, k, v, partials};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return ATTN_ERR_INVALID_ARG;
+  const size_t qb = (size_t)B * H * d * 2, kb = (size_t)B * H * Nk * d * 2;
+  const Range rp = range_of(partials, attn_decode_workspace_bytes(B, H, d, num_splits));
+  for (Range in : {range_of(q, qb), range_of(k, kb), range_of(v, kb)})
+    if (overlap(rp, in)) return ATTN_ERR_INVALID_ARG;
+  const attn::DecodeShape s = make_decode_shape(B, H, Nk, d, dtype, num_splits, scale);
+  return from_cuda(
+      attn::launch_decode_partial(s, q, k, v, partials, static_cast<cudaStream_t>(cuda_stream)));
+}
+
+attn_status attn_decode_merge(const float* partials, void* o, float* lse, int B, int H, int d,
+                              attn_dtype dtype, int num_splits, void* cuda_stream) {
+  attn_status st = check_decode(B, H, 1, d, dtype, num_splits);
+  if (st != ATTN_OK) return st;
+  const void* ptrs[3] = {partials, o, lse};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return ATTN_ERR_INVALID_ARG;
+  const Range rp = range_of(partials, attn_decode_workspace_bytes(B, H, d, num_splits));
+  const Range ro = range_of(o, (size_t)B * H * d * 2), rl = range_of(lse, (size_t)B * H * 4);
+  if (overlap(rp, ro) || overlap(rp, rl) || overlap(ro, rl)) return ATTN_ERR_INVALID_ARG;
+  const attn::DecodeShape s = make_decode_shape(B, H, 1, d, dtype, num_splits, 1.f);
+  return from_cuda(
+      attn::launch_decode_merge(s, partials, o, lse, static_cast<cudaStream_t>(cuda_stream)));
+}
+
+attn_status attn_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                        float* partials, int B, int H, int Nk, int d, attn_dtype dtype,
+                        float scale, int num_splits, void* cuda_stream) {
+  attn_status st = check_decode(B, H, Nk, d, dtype, num_splits);
+  if (st != ATTN_OK) return st;
+  if (o == nullptr || lse == nullptr || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_INVALID_ARG;
+  const size_t qb = (size_t)B * H * d * 2, kb = (size_t)B * H * Nk * d * 2;
+  const Range ro = range_of(o, qb), rl = range_of(lse, (size_t)B * H * 4);
+  for (Range out : {ro, rl})
+    for (Range in : {range_of(q, qb), range_of(k, kb), range_of(v, kb)})
+      if (overlap(out, in)) return ATTN_ERR_INVALID_ARG;
+  if ((st = attn_decode_partial(q, k, v, partials, B, H, Nk, d, dtype, scale, num_splits,
+                                cuda_stream)) != ATTN_OK)
+    return st;
+  return attn_decode_merge(partials, o, lse, B, H, d, dtype, num_splits, cuda_stream);
+}
+
 attn_status attn_last_kernel_status(void* cuda_stream, int* where) {
   cudaStream_t cs = static_cast<cudaStream_t>(cuda_stream);
   int first = 0;
   using Reader = int (*)(cudaStream_t, cudaError_t*);
-  const Reader readers[4] = {attn::status_fwd, attn::status_delta, attn::status_dq,
-                             attn::status_dkv};
+  const Reader readers[5] = {attn::status_fwd, attn::status_delta, attn::status_dq,
+                             attn::status_dkv, attn::status_decode};
   for (Reader r : readers) {
     cudaError_t e = cudaSuccess;
     const int w = r(cs, &e);

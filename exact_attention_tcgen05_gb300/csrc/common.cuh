@@ -23,6 +23,7 @@ enum WaitSite : int {
   kWaitDqDone, kWaitDqDrain, kWaitDqSC,
   kWaitDkvKV = 0x31, kWaitDkvQ, kWaitDkvDO, kWaitDkvEmpty, kWaitDkvS, kWaitDkvDP,
   kWaitDkvP, kWaitDkvDS, kWaitDkvDone, kWaitDkvDrain, kWaitDkvStats,
+  kWaitDecFull = 0x41, kWaitDecDrain,
   kErrSmemAlign = 0x7F  // dynamic shared memory not 1024-byte aligned (kernel skipped)
 };
 

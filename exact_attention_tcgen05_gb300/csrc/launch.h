@@ -30,12 +30,29 @@ cudaError_t launch_dkv(const Maps& m, const Shape& s, const void* q, const void*
                        const float* lse, const float* delta, void* dk, void* dv,
                        cudaStream_t st);
 
+// Split-KV decode: one query row per (b, h) against Nk keys, in `splits` key ranges.
+struct DecodeShape {
+  int BH, Nk, d, splits;
+  bool bf16;
+  float scale;
+  unsigned long long wait_limit;
+};
+// Resident CTAs of the decode partial kernel per SM (its shared-memory footprint).
+constexpr int kDecodeCtasPerSmPublic = 3;
+// Keys per split: ceil(Nk / splits) rounded up to a multiple of 64.
+int decode_chunk(int Nk, int splits);
+cudaError_t launch_decode_partial(const DecodeShape& s, const void* q, const void* k,
+                                  const void* v, float* partials, cudaStream_t st);
+cudaError_t launch_decode_merge(const DecodeShape& s, const float* partials, void* o,
+                                float* lse, cudaStream_t st);
+
 // Each kernel translation unit has its own device status word; these read (after the
 // work queued on `st`, blocking) and clear it. Return the word (0 = no timeout).
 int status_fwd(cudaStream_t st, cudaError_t* err);
 int status_delta(cudaStream_t st, cudaError_t* err);
 int status_dq(cudaStream_t st, cudaError_t* err);
 int status_dkv(cudaStream_t st, cudaError_t* err);
+int status_decode(cudaStream_t st, cudaError_t* err);
 
 }  // namespace attn
 

@@ -140,43 +140,6 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-// A whole [128 rows x d] tile in one copy: the map views each row as d / 64 halves of 64
-// 16-bit values (dims {64, rows, d / 64, slices}); the box {64, 128, d / 64, 1} lands as
-// d / 64 consecutive 128B-swizzled [128 x 64] boxes. One copy per tile instead of one per
-// 64-column box halves the issue round trips of the producer thread.
-__device__ __forceinline__ void tma_load_tile(void* smem_dst, const CUtensorMap* map,
-                                              uint64_t* bar, int row, int slice) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(0), "r"(row), "r"(0),
-      "r"(slice)
-      : "memory");
-}
-
-// Prefetch of a whole tile (same coordinates as tma_load_tile) into L2, no completion.
-__device__ __forceinline__ void tma_prefetch_tile(const CUtensorMap* map, int row, int slice) {
-  asm volatile(
-      "cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(0), "r"(row), "r"(0), "r"(slice)
-      : "memory");
-}
-
-// Asynchronous 16-byte global -> shared copy (no registers held while it is in flight);
-// src_bytes = 0 writes 16 zero bytes and reads nothing.
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)),
-               "l"(gsrc), "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
 // ------------------------------------------------------------------------------------
 // tcgen05: tensor memory and MMA
 // ------------------------------------------------------------------------------------

@@ -118,6 +118,19 @@ def make_tensor(w: Workload, tensor: str) -> torch.Tensor:
     return out
 
 
+def make_tensor_cuda(w: Workload, tensor: str) -> torch.Tensor:
+    """The full [B, H, N, d] tensor drawn directly on the current CUDA device, for
+    workloads too large to draw on the host (gigabytes of K/V): one CUDA generator per
+    tensor, seeded from the workload seed and the tensor name, fp32 N(0, 1) values times
+    qk_gain for q and k, then one rounding to the 16-bit type. Spikes are not applied.
+    The oracle reads the same rounded values back with to_f64."""
+    g = torch.Generator(device="cuda").manual_seed(slice_seed(w.seed, 0, 0, 1, tensor))
+    x = torch.randn(w.B, w.H, w.N, w.d, generator=g, device="cuda", dtype=torch.float32)
+    if tensor in ("q", "k") and w.qk_gain != 1.0:
+        x.mul_(w.qk_gain)
+    return x.to(w.torch_dtype)
+
+
 def sampled_slices(w: Workload, count: Optional[int] = None) -> list[tuple[int, int]]:
     """Seeded choice of (b, h) slices without replacement; always holds the first and
     the last slice."""

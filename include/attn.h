@@ -161,6 +161,47 @@ attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const 
                              int B, int H, int N, int d, attn_dtype dtype, int causal,
                              float scale, void* cuda_stream);
 
+/*
+ * Split-KV decoding: one query row per (b, h) attending to all Nk keys of a K/V cache
+ * (no mask), the keys split into ranges whose partial results are computed in parallel
+ * and then joined. "FlashAttentionを1から — 計算を増やして速くする逆説", section
+ * その後の版と、推論での事情: with a single query token the K/V side is split and the
+ * partial results are combined with the online-softmax update equations (same page,
+ * section オンラインsoftmax: 途中経過を、後から縮める), which gives the same answer as no
+ * split.
+ *
+ *   q        [B, H, 1, d] 16-bit (fp16 or bf16, like k and v)
+ *   k, v     [B, H, Nk, d] 16-bit, 1 <= Nk <= 1048576
+ *   o        [B, H, 1, d] 16-bit: softmax(scale q K^T) V
+ *   lse      [B, H] float32: L = m + ln l (natural log of the scaled scores)
+ *   partials [B, H, num_splits, d + 4] float32 scratch owned by the caller
+ *            (attn_decode_workspace_bytes); record s of a slice holds O~_s (d values,
+ *            the unnormalised weighted sum of the split's value rows), m_s (its largest
+ *            scaled score, natural-log units; -inf for an empty split), l_s (the sum of
+ *            exp(scale s_j - m_s)) and two unused floats.
+ *   num_splits 1 .. 65535. Split s covers keys [s C, min((s + 1) C, Nk)) with
+ *            C = 64 * ceil(ceil(Nk / num_splits) / 64); splits past the end are empty.
+ * Sizes, dtypes, alignment (16 bytes), scale, overlap rules and errors as for attn_fwd;
+ * B * H <= 65535. Nothing is allocated; the calls only enqueue work on cuda_stream.
+ */
+size_t attn_decode_workspace_bytes(int B, int H, int d, int num_splits); /* 0 if invalid */
+/* A split count that gives the GPU of the current device about eight CTAs per SM with
+ * splits of at least 256 keys (0 for invalid sizes). */
+int attn_decode_splits(int B, int H, int Nk);
+/* The partial record of every split (writes partials). */
+attn_status attn_decode_partial(const void* q, const void* k, const void* v, float* partials,
+                                int B, int H, int Nk, int d, attn_dtype dtype, float scale,
+                                int num_splits, void* cuda_stream);
+/* Joins the records of each slice (reads partials, writes o and lse). Also the merge step
+ * for partial results computed elsewhere, e.g. over key ranges held by different
+ * processes, as long as they use this record layout. */
+attn_status attn_decode_merge(const float* partials, void* o, float* lse, int B, int H, int d,
+                              attn_dtype dtype, int num_splits, void* cuda_stream);
+/* attn_decode_partial followed by attn_decode_merge on the same stream. */
+attn_status attn_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                        float* partials, int B, int H, int Nk, int d, attn_dtype dtype,
+                        float scale, int num_splits, void* cuda_stream);
+
 /* attn_status_str - static, NUL-terminated name of a status code. */
 const char* attn_status_str(attn_status s);
 

@@ -113,6 +113,33 @@ def test_stage_entry_points_reject_bad_arguments(lib):
     assert dq(scale=-2.0) == INVALID
 
 
+def decode(lib, q=Q, k=K, v=V, o=O, lse=L, part=WS, B=1, H=1, N=256, d=128, dt=1, scale=0.1,
+           splits=4):
+    return lib.attn_decode(q, k, v, o, lse, part, B, H, N, d, dt, scale, splits, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), INVALID), (dict(part=0), INVALID), (dict(part=WS + 8), INVALID),
+    (dict(splits=0), INVALID), (dict(splits=65536), INVALID), (dict(N=0), INVALID),
+    (dict(d=96), UNSUPPORTED), (dict(dt=3), INVALID), (dict(scale=0.0), INVALID),
+    (dict(o=K), INVALID), (dict(lse=V + 16), INVALID), (dict(part=Q), INVALID),
+    (dict(B=300, H=300), INVALID),
+])
+def test_decode_rejects_bad_arguments(lib, kw, code):
+    assert decode(lib, **kw) == code
+
+
+def test_decode_sizes(lib):
+    assert lib.attn_decode_workspace_bytes(2, 3, 128, 5) == 4 * 2 * 3 * 5 * 132
+    assert lib.attn_decode_workspace_bytes(2, 3, 96, 5) == 0
+    assert lib.attn_decode_workspace_bytes(0, 3, 64, 5) == 0
+    assert lib.attn_decode_splits(0, 1, 100) == 0
+    # merge validation happens before any CUDA call too
+    assert lib.attn_decode_merge(0, O, L, 1, 1, 128, 1, 4, None) == INVALID
+    assert lib.attn_decode_merge(WS, O, L, 1, 1, 128, 1, 0, None) == INVALID
+    assert lib.attn_decode_merge(WS, WS, L, 1, 1, 128, 1, 4, None) == INVALID
+
+
 def test_preprocess_rejects_bad_arguments(lib):
     assert lib.attn_bwd_preprocess(O, DO, 0, 1, 1, 16, 64, 0, None) == INVALID
     assert lib.attn_bwd_preprocess(O, DO, O, 1, 1, 16, 64, 0, None) == INVALID
