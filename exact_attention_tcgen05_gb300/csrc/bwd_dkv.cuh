@@ -138,10 +138,10 @@ __global__ void __launch_bounds__(320, 1)
       issued = it + 1;
     }
     if (*abort_flag) {
-      mbar_wait(kv_full, 0, limit, nullptr, kWaitDkvDrain);
+      mbar_wait(kv_full, 0, kDrainLimit, nullptr, kWaitDkvDrain);
       for (int it = max(0, issued - NS); it < issued; ++it) {
-        mbar_wait(&q_full[it % NS], (it / NS) & 1, limit, nullptr, kWaitDkvDrain);
-        mbar_wait(&do_full[it % NS], (it / NS) & 1, limit, nullptr, kWaitDkvDrain);
+        mbar_wait(&q_full[it % NS], (it / NS) & 1, kDrainLimit, nullptr, kWaitDkvDrain);
+        mbar_wait(&do_full[it % NS], (it / NS) & 1, kDrainLimit, nullptr, kWaitDkvDrain);
       }
     }
   } else if (warp == 9) {
@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(320, 1)
       mma_commit(drain);
     }
     __syncwarp();
-    mbar_wait(drain, 0, limit, nullptr, kWaitDkvDrain);
+    mbar_wait(drain, 0, kDrainLimit, nullptr, kWaitDkvDrain);
   } else {
     // warps 0-7: thread = key row (TMEM lane); group g covers queries [64g, 64g + 64)
     const int g = warp >> 2;
@@ -340,6 +340,7 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_before();
   }
 
+  tmem_st_wait();  // no tensor-memory store in flight when memory is released
   __syncthreads();
   if (warp == 9) {
     tc_fence_after();

@@ -216,8 +216,8 @@ __global__ void __launch_bounds__(320, 1)
     }
     if (*abort_flag) {
       for (int j = max(0, issued - NS); j < issued; ++j) {
-        mbar_wait(&k_full[j % NS], (j / NS) & 1, limit, nullptr, kWaitDqDrain);
-        mbar_wait(&v_full[j % NS], (j / NS) & 1, limit, nullptr, kWaitDqDrain);
+        mbar_wait(&k_full[j % NS], (j / NS) & 1, kDrainLimit, nullptr, kWaitDqDrain);
+        mbar_wait(&v_full[j % NS], (j / NS) & 1, kDrainLimit, nullptr, kWaitDqDrain);
       }
     }
   } else if (warp == 9) {
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(320, 1)
       mma_commit(drain);
     }
     __syncwarp();
-    mbar_wait(drain, 0, limit, nullptr, kWaitDqDrain);
+    mbar_wait(drain, 0, kDrainLimit, nullptr, kWaitDqDrain);
   } else {
     // warps 0-7: thread = query row (TMEM lane); group g covers keys [64g, 64g + 64)
     const int g = warp >> 2;
@@ -384,6 +384,7 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_before();
   }
 
+  tmem_st_wait();  // no tensor-memory store in flight when memory is released
   __syncthreads();
   if (warp == 9) {
     tc_fence_after();

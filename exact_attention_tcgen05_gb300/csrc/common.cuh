@@ -27,6 +27,12 @@ enum WaitSite : int {
   kErrSmemAlign = 0x7F  // dynamic shared memory not 1024-byte aligned (kernel skipped)
 };
 
+// Bound of the waits that let a CTA's own in-flight work finish before it releases shared
+// or tensor memory (copies it started, MMAs it issued). Deliberately independent of the
+// configurable pipeline limit: after a pipeline wait gives up, these must still see that
+// work complete (microseconds), or memory could be released under it.
+constexpr unsigned long long kDrainLimit = 1ull << 31;
+
 // Rounds a shared-memory pointer up to 1024 bytes (the swizzle-atom alignment).
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   const uint32_t a = smem_u32(p);

@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
   if (*abort_flag && threadIdx.x == 0) {
     // Copies this CTA started must land before its shared memory is released.
     for (int i = max(0, issued - NS); i < issued; ++i)
-      mbar_wait(&full[i % NS], (i / NS) & 1, limit, nullptr, kWaitDecDrain);
+      mbar_wait(&full[i % NS], (i / NS) & 1, kDrainLimit, nullptr, kWaitDecDrain);
   }
 }
 

@@ -165,11 +165,11 @@ __global__ void __launch_bounds__(320, 1)
     }
     if (*abort_flag) {
       // Let every copy this CTA started land before its shared memory is released.
-      mbar_wait(q_full, 0, limit, nullptr, kWaitFwdDrain);
+      mbar_wait(q_full, 0, kDrainLimit, nullptr, kWaitFwdDrain);
       for (int j = max(0, issued - C::kStages); j < issued; ++j) {
         const int s = j % C::kStages;
-        mbar_wait(&k_full[s], (j / C::kStages) & 1, limit, nullptr, kWaitFwdDrain);
-        mbar_wait(&v_full[s], (j / C::kStages) & 1, limit, nullptr, kWaitFwdDrain);
+        mbar_wait(&k_full[s], (j / C::kStages) & 1, kDrainLimit, nullptr, kWaitFwdDrain);
+        mbar_wait(&v_full[s], (j / C::kStages) & 1, kDrainLimit, nullptr, kWaitFwdDrain);
       }
     }
   } else if (warp == 9) {
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(320, 1)
     // Every MMA issued must finish before tensor memory is released.
     if (elect_one()) mma_commit(drain);
     __syncwarp();
-    mbar_wait(drain, 0, limit, nullptr, kWaitFwdDrain);
+    mbar_wait(drain, 0, kDrainLimit, nullptr, kWaitFwdDrain);
   } else {
     // ------------------------------ softmax (tile t) --------------------------
     const int t = warp >> 2;
@@ -367,6 +367,7 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_before();
   }
 
+  tmem_st_wait();  // no tensor-memory store in flight when memory is released
   __syncthreads();
   if (warp == 9) {
     tc_fence_after();
