@@ -35,6 +35,9 @@ SIGNATURES = {
     "attn_bwd_dq": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F,
                               _P]),
+    "attn_step_host_scratch_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),
+    "attn_step_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _I, _I, _I,
+                            _I, _I, _I, _F, _I, _P]),
     "attn_decode_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "attn_decode_splits": (_I, [_I, _I, _I]),
     "attn_decode_partial": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
@@ -256,6 +259,43 @@ def attn_bwd_dq(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, lse: torch.Te
                                   _stream_handle(stream))
     _check("attn_bwd_dq", code)
     return dq
+
+
+# ---------------------------------------------------------------- host-buffer step
+def attn_step_host_scratch_bytes(B: int, H: int, N: int, d: int, chunks: int) -> int:
+    return int(load().attn_step_host_scratch_bytes(B, H, N, d, chunks))
+
+
+def attn_step_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, do: torch.Tensor,
+                   o: torch.Tensor, lse: torch.Tensor, dq: torch.Tensor, dk: torch.Tensor,
+                   dv: torch.Tensor, scratch: torch.Tensor, causal: bool = False,
+                   scale: Optional[float] = None, chunks: int = 4,
+                   stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Forward + backward of host (CPU, ideally pinned) tensors through the library,
+    copies overlapped with the kernels. Writes o, lse, dq, dk, dv (host tensors); they are
+    valid after the stream is synchronised. scratch: a CUDA uint8 tensor of
+    attn_step_host_scratch_bytes(B, H, N, d, chunks) bytes."""
+    B, H, N, d = q.shape
+    for name, x in (("q", q), ("k", k), ("v", v), ("do", do), ("o", o), ("dq", dq), ("dk", dk),
+                    ("dv", dv)):
+        if x.is_cuda or not x.is_contiguous() or x.shape != q.shape or x.dtype != q.dtype:
+            raise ValueError(f"{name} must be a contiguous host tensor shaped and typed like q")
+    if q.dtype not in _DTYPE_CODES:
+        raise ValueError("q must be float16 or bfloat16")
+    if lse.is_cuda or lse.shape != (B, H, N) or lse.dtype != torch.float32 \
+            or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 host tensor [B, H, N]")
+    if not scratch.is_cuda or not scratch.is_contiguous():
+        raise ValueError("scratch must be a contiguous CUDA tensor")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    nbytes = scratch.numel() * scratch.element_size()
+    with torch.cuda.device(scratch.device):
+        code = load().attn_step_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(),
+                                     o.data_ptr(), lse.data_ptr(), dq.data_ptr(),
+                                     dk.data_ptr(), dv.data_ptr(), scratch.data_ptr(), nbytes,
+                                     B, H, N, d, _DTYPE_CODES[q.dtype], int(causal), scale,
+                                     int(chunks), _stream_handle(stream))
+    _check("attn_step_host", code)
 
 
 # ---------------------------------------------------------------- split-KV decode

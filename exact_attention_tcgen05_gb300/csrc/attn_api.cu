@@ -7,6 +7,7 @@
 #include <cstdlib>
 #include <initializer_list>
 #include <mutex>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -263,6 +264,119 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   cudaError_t e = attn::launch_delta(s, o, dO, delta, cs);
   if (e == cudaSuccess) e = attn::launch_dkv(m, s, q, dO, lse, delta, dk, dv, cs);
   if (e == cudaSuccess) e = attn::launch_dq(m, s, q, dO, lse, delta, dq, cs);
+  return from_cuda(e);
+}
+
+// ---------------------------------------------------------------- host-buffer step
+namespace {
+// Slices per chunk and the bytes of one chunk's device buffers (q k v dO o dq dk dv, lse, D).
+long long step_chunk_slices(long long bh, int chunks) { return (bh + chunks - 1) / chunks; }
+size_t step_set_bytes(long long slices, int N, int d) {
+  const size_t t = (size_t)slices * N * d * 2, r = (size_t)slices * N * 4;
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  return 8 * up(t) + 2 * up(r);
+}
+}  // namespace
+
+size_t attn_step_host_scratch_bytes(int B, int H, int N, int d, int chunks) {
+  if (B <= 0 || H <= 0 || N <= 0 || chunks <= 0 || (d != 64 && d != 128)) return 0;
+  const long long bh = (long long)B * H;
+  const int c = (int)std::min<long long>(chunks, bh);
+  return 2 * step_set_bytes(step_chunk_slices(bh, c), N, d);
+}
+
+attn_status attn_step_host(const void* q, const void* k, const void* v, const void* dO,
+                           void* o, float* lse, void* dq, void* dk, void* dv, void* scratch,
+                           size_t scratch_bytes, int B, int H, int N, int d, attn_dtype dtype,
+                           int causal, float scale, int chunks, void* cuda_stream) {
+  attn_status st = check_shape(B, H, N, d, dtype);
+  if (st != ATTN_OK) return st;
+  if ((st = check_scale(scale)) != ATTN_OK) return st;
+  if (chunks < 1) return ATTN_ERR_INVALID_ARG;
+  const void* ptrs[10] = {q, k, v, dO, o, lse, dq, dk, dv, scratch};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return ATTN_ERR_INVALID_ARG;
+  const long long bh = (long long)B * H;
+  chunks = (int)std::min<long long>(chunks, bh);
+  if (scratch_bytes < attn_step_host_scratch_bytes(B, H, N, d, chunks))
+    return ATTN_ERR_INVALID_ARG;
+  const long long per = step_chunk_slices(bh, chunks);
+  chunks = (int)((bh + per - 1) / per);
+  const size_t row_t = (size_t)N * d * 2, row_r = (size_t)N * 4;  // bytes per slice
+  const size_t set_bytes = step_set_bytes(per, N, d);
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+
+  cudaStream_t cs = static_cast<cudaStream_t>(cuda_stream);
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  cudaEvent_t start = nullptr;
+  std::vector<cudaEvent_t> ev_in(chunks, nullptr), ev_comp(chunks, nullptr),
+      ev_out(chunks, nullptr);
+  cudaError_t e = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&start, cudaEventDisableTiming);
+  for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
+    e = cudaEventCreateWithFlags(&ev_in[c], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_comp[c], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_out[c], cudaEventDisableTiming);
+  }
+  // The side streams start after the work already queued on the caller's stream.
+  if (e == cudaSuccess) e = cudaEventRecord(start, cs);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s_in, start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, start, 0);
+
+  for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
+    const long long b0 = (long long)c * per;
+    const long long n = std::min(per, bh - b0);
+    uint8_t* set = static_cast<uint8_t*>(scratch) + (size_t)(c & 1) * set_bytes;
+    uint8_t* dev[8];
+    for (int i = 0; i < 8; ++i) dev[i] = set + (size_t)i * up((size_t)per * row_t);
+    float* d_lse = reinterpret_cast<float*>(set + 8 * up((size_t)per * row_t));
+    float* d_delta = reinterpret_cast<float*>(set + 8 * up((size_t)per * row_t) +
+                                              up((size_t)per * row_r));
+    const size_t tb = (size_t)n * row_t, rb = (size_t)n * row_r;
+    const size_t off_t = (size_t)b0 * row_t, off_r = (size_t)b0 * row_r;
+    // inputs of chunk c, once chunk c - 2 (same buffers) has been computed
+    if (c >= 2) e = cudaStreamWaitEvent(s_in, ev_comp[c - 2], 0);
+    const void* hin[4] = {q, k, v, dO};
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+      e = cudaMemcpyAsync(dev[i], static_cast<const uint8_t*>(hin[i]) + off_t, tb,
+                          cudaMemcpyHostToDevice, s_in);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_in[c], s_in);
+    // compute chunk c once its inputs are in and chunk c - 2's outputs have left
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev_in[c], 0);
+    if (e == cudaSuccess && c >= 2) e = cudaStreamWaitEvent(cs, ev_out[c - 2], 0);
+    if (e == cudaSuccess) {
+      st = attn_fwd(dev[0], dev[1], dev[2], dev[4], d_lse, 1, (int)n, N, d, dtype, causal,
+                    scale, cs);
+      if (st == ATTN_OK)
+        st = attn_bwd(dev[0], dev[1], dev[2], dev[4], d_lse, dev[3], dev[5], dev[6], dev[7],
+                      d_delta, 1, (int)n, N, d, dtype, causal, scale, cs);
+      if (st != ATTN_OK) break;
+      e = cudaEventRecord(ev_comp[c], cs);
+    }
+    // outputs of chunk c
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, ev_comp[c], 0);
+    void* hout[4] = {o, dq, dk, dv};
+    const int dsrc[4] = {4, 5, 6, 7};
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+      e = cudaMemcpyAsync(static_cast<uint8_t*>(hout[i]) + off_t, dev[dsrc[i]], tb,
+                          cudaMemcpyDeviceToHost, s_out);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse) + off_r, d_lse, rb,
+                          cudaMemcpyDeviceToHost, s_out);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_out[c], s_out);
+  }
+  // The caller's stream completes after the last copy out.
+  if (e == cudaSuccess && st == ATTN_OK) e = cudaStreamWaitEvent(cs, ev_out[chunks - 1], 0);
+  for (int c = 0; c < chunks; ++c) {
+    if (ev_in[c]) cudaEventDestroy(ev_in[c]);
+    if (ev_comp[c]) cudaEventDestroy(ev_comp[c]);
+    if (ev_out[c]) cudaEventDestroy(ev_out[c]);
+  }
+  if (start) cudaEventDestroy(start);
+  if (s_in) cudaStreamDestroy(s_in);  // released once their queued work completes
+  if (s_out) cudaStreamDestroy(s_out);
+  if (st != ATTN_OK) return st;
   return from_cuda(e);
 }
 

@@ -162,6 +162,30 @@ attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const 
                              float scale, void* cuda_stream);
 
 /*
+ * attn_step_host - one training step of attention (attn_fwd then attn_bwd) on data that
+ * lives in HOST memory: copies q, k, v, dO in, computes, and copies o, lse, dq, dk, dv out,
+ * overlapping the copies with the kernels. The B*H slices are cut into `chunks` runs of
+ * consecutive slices (the last one shorter); while chunk c is computed on cuda_stream, the
+ * inputs of chunk c + 1 are copied in and the outputs of chunk c - 1 copied out on two
+ * streams the call creates and releases. Results are identical to attn_fwd + attn_bwd on
+ * the whole tensors (every (b, h) slice is computed independently).
+ *   q, k, v, dO        HOST [B, H, N, d] 16-bit inputs; pinned (page-locked) memory is
+ *                      needed for the copies to overlap (pageable memory works, serially)
+ *   o, dq, dk, dv, lse HOST outputs, [B, H, N, d] 16-bit and [B, H, N] float32
+ *   scratch            DEVICE buffer of scratch_bytes >=
+ *                      attn_step_host_scratch_bytes(B, H, N, d, chunks): two sets of
+ *                      per-chunk device tensors, used in turn
+ *   chunks             >= 1 (values above B*H are clamped)
+ * Sizes, dtypes, scale and errors as for attn_fwd; every pointer 16-byte aligned. The
+ * call only enqueues work: the outputs are valid once cuda_stream has completed it.
+ */
+size_t attn_step_host_scratch_bytes(int B, int H, int N, int d, int chunks); /* 0: invalid */
+attn_status attn_step_host(const void* q, const void* k, const void* v, const void* dO,
+                           void* o, float* lse, void* dq, void* dk, void* dv, void* scratch,
+                           size_t scratch_bytes, int B, int H, int N, int d, attn_dtype dtype,
+                           int causal, float scale, int chunks, void* cuda_stream);
+
+/*
  * Split-KV decoding: one query row per (b, h) attending to all Nk keys of a K/V cache
  * (no mask), the keys split into ranges whose partial results are computed in parallel
  * and then joined. "FlashAttentionを1から — 計算を増やして速くする逆説", section

@@ -129,6 +129,21 @@ def test_decode_rejects_bad_arguments(lib, kw, code):
     assert decode(lib, **kw) == code
 
 
+def test_step_host_rejects_bad_arguments(lib):
+    need = lib.attn_step_host_scratch_bytes(1, 2, 256, 128, 2)
+    assert need > 0 and lib.attn_step_host_scratch_bytes(1, 2, 256, 96, 2) == 0
+
+    def call(scratch=WS, nbytes=need, chunks=2, d=128, scale=0.1, q=Q):
+        return lib.attn_step_host(q, K, V, DO, O, L, DQ, DK, DV, scratch, nbytes, 1, 2, 256, d,
+                                  1, 0, scale, chunks, None)
+    assert call(scratch=0) == INVALID
+    assert call(nbytes=need - 1) == INVALID
+    assert call(chunks=0) == INVALID
+    assert call(d=32) == UNSUPPORTED
+    assert call(scale=-1.0) == INVALID
+    assert call(q=Q + 8) == INVALID
+
+
 def test_decode_sizes(lib):
     assert lib.attn_decode_workspace_bytes(2, 3, 128, 5) == 4 * 2 * 3 * 5 * 132
     assert lib.attn_decode_workspace_bytes(2, 3, 96, 5) == 0
