@@ -26,8 +26,12 @@ gradient were lost from the extracted text):
   dV = P^T dO, dP = dO V^T, D_i = sum_j P_ij dP_ij, dS = P * (dP - D),
   dQ = scale * dS K, dK = scale * dS^T Q. D_i equals rowsum(dO_i * O_i) in exact
   arithmetic; both are computed and returned.
-* Causal masking is top-left aligned with N_q = N_k: key j is visible to query i iff
-  j <= i, so every row sees at least key 0 and no row is fully masked.
+* Causal masking is bottom-right aligned: with N_q query rows and N_k >= N_q keys, key j
+  is visible to query i iff j <= i + (N_k - N_q), i.e. the queries are the last N_q
+  positions of the sequence (for N_q = N_k: j <= i). Every row sees at least key 0 and no
+  row is fully masked. The pages only say that future tokens are blocked ("Triton 05",
+  Causal Masking); placing the queries last is the reading for a query chunk that
+  follows the keys already in the cache.
 
 Rows are processed in panels of whole rows only to bound memory (S and P of one
 N = 16384 head are 2 GiB each in fp64). Each row's softmax and output depend on that
@@ -50,13 +54,15 @@ def _panel_rows(n: int, panel_elems: int) -> int:
 
 def scores(q: np.ndarray, k: np.ndarray, scale: float, causal: bool,
            row0: int = 0, row1: int | None = None) -> np.ndarray:
-    """Scaled, masked scores S[row0:row1, :] = scale * Q K^T with -inf on j > i."""
+    """Scaled, masked scores S[row0:row1, :] = scale * Q K^T with -inf on
+    j > i + (N_k - N_q) (bottom-right aligned; j > i when N_q = N_k)."""
     row1 = q.shape[0] if row1 is None else row1
     s = scale * (q[row0:row1] @ k.T)
     if causal:
+        offset = k.shape[0] - q.shape[0]
         rows = np.arange(row0, row1)[:, None]
         cols = np.arange(k.shape[0])[None, :]
-        s = np.where(cols > rows, -np.inf, s)
+        s = np.where(cols > rows + offset, -np.inf, s)
     return s
 
 
@@ -74,7 +80,8 @@ def attention_forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: bool,
                       ) -> tuple[np.ndarray, np.ndarray]:
     """O = softmax(scale * Q K^T [masked]) V and L = m + ln l, for one (b, h) slice.
 
-    q, k, v: [N, d] float64. Returns O [N, d] and L [N] (natural log), float64.
+    q: [N_q, d], k, v: [N_k, d] float64 (N_k >= N_q when causal). Returns O [N_q, d]
+    and L [N_q] (natural log), float64.
     """
     q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
     n, dv = q.shape[0], v.shape[1]

@@ -213,6 +213,33 @@ def pin_causal_future_independence(oa):
     assert np.array_equal(g1["dq"][: i + 1], g2["dq"][: i + 1])
 
 
+def pin_rectangular_is_a_suffix(oa):
+    """N_q < N_k (queries last): the rectangular problem equals the last N_q rows of the
+    square problem over the same keys; its dK, dV equal the square problem's with dO zero
+    on the first N_k - N_q rows, and its dQ equals the square dQ's last rows."""
+    rng = np.random.default_rng(23)
+    for nk, nq, d, causal in [(9, 4, 3, True), (9, 4, 3, False), (7, 7, 2, True), (12, 1, 4, True)]:
+        q = rng.standard_normal((nk, d))
+        k = rng.standard_normal((nk, d))
+        v = rng.standard_normal((nk, d))
+        do = rng.standard_normal((nk, d))
+        do[: nk - nq] = 0.0
+        sq = oa.attention_backward(q, k, v, do, causal, 0.6)
+        rect = oa.attention_backward(q[nk - nq:], k, v, do[nk - nq:], causal, 0.6)
+        np.testing.assert_allclose(rect["o"], sq["o"][nk - nq:], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(rect["lse"], sq["lse"][nk - nq:], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(rect["dq"], sq["dq"][nk - nq:], rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(rect["dk"], sq["dk"], rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(rect["dv"], sq["dv"], rtol=1e-10, atol=1e-12)
+        o, lse = oa.attention_forward(q[nk - nq:], k, v, causal, 0.6)
+        np.testing.assert_allclose(o, sq["o"][nk - nq:], rtol=1e-12, atol=1e-12)
+    # the last query row sees every key: it is plain softmax over all of them
+    s_last = 0.6 * (k @ q[-1])
+    p = scipy.special.softmax(s_last)
+    o, lse = oa.attention_forward(q[-1:], k, v, True, 0.6)
+    np.testing.assert_allclose(o[0], p @ v, rtol=1e-12, atol=1e-12)
+
+
 def pin_panels(oa):
     """Whole-row panels change nothing but summation order: 1 row per panel versus
     all rows at once."""
@@ -230,7 +257,7 @@ ALL_PINS = [
     pin_worked_example_a, pin_worked_example_b, pin_causal_row0_and_n1,
     pin_uniform_attention, pin_one_hot, pin_library_softmax, pin_blocked_recurrence,
     pin_finite_differences, pin_delta_two_ways, pin_shift_invariance,
-    pin_causal_future_independence, pin_panels,
+    pin_causal_future_independence, pin_panels, pin_rectangular_is_a_suffix,
 ]
 
 
@@ -321,8 +348,12 @@ def test_merge_of_partials_is_exact():
 MUTANTS = {
     "dropped_scale_in_dk": ("dk += scale * (ds.T @ q[r0:r1])", "dk += (ds.T @ q[r0:r1])"),
     "dropped_scale_in_dq": ("dq[r0:r1] = scale * (ds @ k)", "dq[r0:r1] = (ds @ k)"),
-    "mask_wrong_direction": ("np.where(cols > rows, -np.inf, s)", "np.where(cols < rows, -np.inf, s)"),
-    "mask_drops_diagonal": ("np.where(cols > rows, -np.inf, s)", "np.where(cols >= rows, -np.inf, s)"),
+    "mask_wrong_direction": ("np.where(cols > rows + offset, -np.inf, s)",
+                             "np.where(cols < rows + offset, -np.inf, s)"),
+    "mask_drops_diagonal": ("np.where(cols > rows + offset, -np.inf, s)",
+                            "np.where(cols >= rows + offset, -np.inf, s)"),
+    "mask_top_left_aligned": ("offset = k.shape[0] - q.shape[0]", "offset = 0"),
+    "mask_offset_sign": ("offset = k.shape[0] - q.shape[0]", "offset = q.shape[0] - k.shape[0]"),
     "lse_in_base2": ("lse[r0:r1] = m + np.log(l)\n    return o, lse",
                      "lse[r0:r1] = m + np.log2(l)\n    return o, lse"),
     "lse_without_max": ("lse[r0:r1] = m + np.log(l)\n    return o, lse",
