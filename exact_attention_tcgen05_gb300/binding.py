@@ -28,6 +28,9 @@ _I = ctypes.c_int
 _F = ctypes.c_float
 SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_fwd_qk": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P]),
+    "attn_bwd_qk": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
+                         _P]),
     "attn_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_bwd_preprocess": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P]),
@@ -101,6 +104,16 @@ def _same(ref: torch.Tensor, x: torch.Tensor, name: str) -> None:
         raise ValueError(f"{name} must match q in shape, dtype and device")
 
 
+def _keys_like(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> int:
+    """N_k of k and v, which match q in B, H, d, dtype and device and each other."""
+    B, H, _, d = q.shape
+    Bk, Hk, Nk, dk = _shape_of(k, "k")
+    if (Bk, Hk, dk) != (B, H, d) or k.dtype != q.dtype or k.device != q.device:
+        raise ValueError("k must be [B, H, N_k, d] with q's dtype and device")
+    _same(k, v, "v")
+    return Nk
+
+
 def _lse_like(q: torch.Tensor, x: Optional[torch.Tensor], name: str) -> torch.Tensor:
     B, H, N, _ = q.shape
     if x is None:
@@ -115,10 +128,10 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
              scale: Optional[float] = None, o: Optional[torch.Tensor] = None,
              lse: Optional[torch.Tensor] = None,
              stream: Optional[torch.cuda.Stream] = None) -> tuple[torch.Tensor, torch.Tensor]:
-    """O = softmax(scale q k^T [causal]) v and the natural-log LSE, via libattn.so."""
+    """O = softmax(scale q k^T [causal]) v and the natural-log LSE, via libattn.so.
+    k and v may hold more rows than q (N_k >= N_q when causal; bottom-right aligned)."""
     B, H, N, d = _shape_of(q, "q")
-    _same(q, k, "k")
-    _same(q, v, "v")
+    Nk = _keys_like(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     if o is None:
         o = torch.empty_like(q)
@@ -126,10 +139,10 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
         _same(q, o, "o")
     lse = _lse_like(q, lse, "lse")
     with torch.cuda.device(q.device):
-        code = load().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                               lse.data_ptr(), B, H, N, d, _DTYPE_CODES[q.dtype], int(causal),
-                               scale, _stream_handle(stream))
-    _check("attn_fwd", code)
+        code = load().attn_fwd_qk(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  lse.data_ptr(), B, H, N, Nk, d, _DTYPE_CODES[q.dtype],
+                                  int(causal), scale, _stream_handle(stream))
+    _check("attn_fwd_qk", code)
     return o, lse
 
 
@@ -144,25 +157,28 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              workspace: Optional[torch.Tensor] = None,
              stream: Optional[torch.cuda.Stream] = None
              ) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
-    """dq, dk, dv of sum(do * o), recomputing P from lse, via libattn.so."""
+    """dq, dk, dv of sum(do * o), recomputing P from lse, via libattn.so. k and v may
+    hold more rows than q (as in attn_fwd)."""
     B, H, N, d = _shape_of(q, "q")
-    for name, x in (("k", k), ("v", v), ("o", o), ("do", do)):
+    Nk = _keys_like(q, k, v)
+    for name, x in (("o", o), ("do", do)):
         _same(q, x, name)
     lse = _lse_like(q, lse, "lse")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
-    for name, x in (("dq", dq), ("dk", dk), ("dv", dv)):
-        _same(q, x, name)
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(k) if dv is None else dv
+    _same(q, dq, "dq")
+    _same(k, dk, "dk")
+    _same(k, dv, "dv")
     workspace = _lse_like(q, workspace, "workspace")
     with torch.cuda.device(q.device):
-        code = load().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                               lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                               dv.data_ptr(), workspace.data_ptr(), B, H, N, d,
-                               _DTYPE_CODES[q.dtype], int(causal), scale,
-                               _stream_handle(stream))
-    _check("attn_bwd", code)
+        code = load().attn_bwd_qk(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                  dv.data_ptr(), workspace.data_ptr(), B, H, N, Nk, d,
+                                  _DTYPE_CODES[q.dtype], int(causal), scale,
+                                  _stream_handle(stream))
+    _check("attn_bwd_qk", code)
     return dq, dk, dv
 
 

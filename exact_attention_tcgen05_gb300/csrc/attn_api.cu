@@ -96,10 +96,12 @@ attn_status encode_map(CUtensorMap* m, const void* base, int BH, int N, int d, b
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-Shape make_shape(int B, int H, int N, int d, attn_dtype dtype, int causal, float scale) {
+Shape make_shape(int B, int H, int N, int d, attn_dtype dtype, int causal, float scale,
+                 int Nk = -1) {
   Shape s;
   s.BH = B * H;
   s.N = N;
+  s.Nk = Nk < 0 ? N : Nk;
   s.d = d;
   s.bf16 = dtype == ATTN_BF16;
   s.causal = causal != 0;
@@ -130,31 +132,39 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N) {
   return (size_t)4 * (size_t)B * (size_t)H * (size_t)N;
 }
 
-attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                     int H, int N, int d, attn_dtype dtype, int causal, float scale,
-                     void* cuda_stream) {
-  attn_status st = check_shape(B, H, N, d, dtype);
+attn_status attn_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse,
+                        int B, int H, int Nq, int Nk, int d, attn_dtype dtype, int causal,
+                        float scale, void* cuda_stream) {
+  attn_status st = check_shape(B, H, Nq, d, dtype);
   if (st != ATTN_OK) return st;
+  if ((st = check_shape(B, H, Nk, d, dtype)) != ATTN_OK) return st;
+  if (causal && Nk < Nq) return ATTN_ERR_INVALID_ARG;  // rows would see no key
   if ((st = check_scale(scale)) != ATTN_OK) return st;
   const void* ptrs[5] = {q, k, v, o, lse};
   for (const void* p : ptrs)
     if (p == nullptr || !aligned16(p)) return ATTN_ERR_INVALID_ARG;
-  const size_t tb = (size_t)B * H * N * d * 2;
-  const size_t lb = (size_t)B * H * N * 4;
-  const Range rq = range_of(q, tb), rk = range_of(k, tb), rv = range_of(v, tb);
-  const Range ro = range_of(o, tb), rl = range_of(lse, lb);
+  const size_t qb = (size_t)B * H * Nq * d * 2, kb = (size_t)B * H * Nk * d * 2;
+  const size_t lb = (size_t)B * H * Nq * 4;
+  const Range rq = range_of(q, qb), rk = range_of(k, kb), rv = range_of(v, kb);
+  const Range ro = range_of(o, qb), rl = range_of(lse, lb);
   for (Range out : {ro, rl})
     for (Range in : {rq, rk, rv})
       if (overlap(out, in)) return ATTN_ERR_INVALID_ARG;
   if (overlap(ro, rl)) return ATTN_ERR_INVALID_ARG;
 
-  const Shape s = make_shape(B, H, N, d, dtype, causal, scale);
+  const Shape s = make_shape(B, H, Nq, d, dtype, causal, scale, Nk);
   Maps m;
-  if ((st = encode_map(&m.q, q, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
-  if ((st = encode_map(&m.k, k, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
-  if ((st = encode_map(&m.v, v, s.BH, N, d, s.bf16)) != ATTN_OK) return st;
+  if ((st = encode_map(&m.q, q, s.BH, Nq, d, s.bf16)) != ATTN_OK) return st;
+  if ((st = encode_map(&m.k, k, s.BH, Nk, d, s.bf16)) != ATTN_OK) return st;
+  if ((st = encode_map(&m.v, v, s.BH, Nk, d, s.bf16)) != ATTN_OK) return st;
   m.d_o = m.v;
   return from_cuda(attn::launch_fwd(m, s, o, lse, static_cast<cudaStream_t>(cuda_stream)));
+}
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int N, int d, attn_dtype dtype, int causal, float scale,
+                     void* cuda_stream) {
+  return attn_fwd_qk(q, k, v, o, lse, B, H, N, N, d, dtype, causal, scale, cuda_stream);
 }
 
 attn_status attn_bwd_preprocess(const void* o, const void* dO, float* delta, int B, int H,
@@ -195,8 +205,8 @@ attn_status encode_bwd_maps(Maps* m, const void* q, const void* k, const void* v
                             const void* dO, const Shape& s) {
   attn_status st;
   if ((st = encode_map(&m->q, q, s.BH, s.N, s.d, s.bf16)) != ATTN_OK) return st;
-  if ((st = encode_map(&m->k, k, s.BH, s.N, s.d, s.bf16)) != ATTN_OK) return st;
-  if ((st = encode_map(&m->v, v, s.BH, s.N, s.d, s.bf16)) != ATTN_OK) return st;
+  if ((st = encode_map(&m->k, k, s.BH, s.Nk, s.d, s.bf16)) != ATTN_OK) return st;
+  if ((st = encode_map(&m->v, v, s.BH, s.Nk, s.d, s.bf16)) != ATTN_OK) return st;
   return encode_map(&m->d_o, dO, s.BH, s.N, s.d, s.bf16);
 }
 
@@ -241,22 +251,25 @@ attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const float
       attn::launch_dq(m, s, q, dO, lse, delta, dq, static_cast<cudaStream_t>(cuda_stream)));
 }
 
-attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
-                     const float* lse, const void* dO, void* dq, void* dk, void* dv,
-                     void* workspace, int B, int H, int N, int d, attn_dtype dtype, int causal,
-                     float scale, void* cuda_stream) {
-  attn_status st = check_shape(B, H, N, d, dtype);
+attn_status attn_bwd_qk(const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                        void* workspace, int B, int H, int Nq, int Nk, int d,
+                        attn_dtype dtype, int causal, float scale, void* cuda_stream) {
+  attn_status st = check_shape(B, H, Nq, d, dtype);
   if (st != ATTN_OK) return st;
+  if ((st = check_shape(B, H, Nk, d, dtype)) != ATTN_OK) return st;
+  if (causal && Nk < Nq) return ATTN_ERR_INVALID_ARG;
   if ((st = check_scale(scale)) != ATTN_OK) return st;
   if ((st = check_ptrs({q, k, v, o, lse, dO, dq, dk, dv, workspace})) != ATTN_OK) return st;
-  const size_t tb = (size_t)B * H * N * d * 2, lb = (size_t)B * H * N * 4;
-  const Range ins[6] = {range_of(q, tb), range_of(k, tb),   range_of(v, tb),
-                        range_of(o, tb), range_of(lse, lb), range_of(dO, tb)};
-  const Range outs[4] = {range_of(dq, tb), range_of(dk, tb), range_of(dv, tb),
+  const size_t qb = (size_t)B * H * Nq * d * 2, kb = (size_t)B * H * Nk * d * 2;
+  const size_t lb = (size_t)B * H * Nq * 4;
+  const Range ins[6] = {range_of(q, qb), range_of(k, kb),   range_of(v, kb),
+                        range_of(o, qb), range_of(lse, lb), range_of(dO, qb)};
+  const Range outs[4] = {range_of(dq, qb), range_of(dk, kb), range_of(dv, kb),
                          range_of(workspace, lb)};
   if ((st = check_ranges(ins, 6, outs, 4)) != ATTN_OK) return st;
 
-  const Shape s = make_shape(B, H, N, d, dtype, causal, scale);
+  const Shape s = make_shape(B, H, Nq, d, dtype, causal, scale, Nk);
   Maps m;
   if ((st = encode_bwd_maps(&m, q, k, v, dO, s)) != ATTN_OK) return st;
   cudaStream_t cs = static_cast<cudaStream_t>(cuda_stream);
@@ -265,6 +278,14 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   if (e == cudaSuccess) e = attn::launch_dkv(m, s, q, dO, lse, delta, dk, dv, cs);
   if (e == cudaSuccess) e = attn::launch_dq(m, s, q, dO, lse, delta, dq, cs);
   return from_cuda(e);
+}
+
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                     void* workspace, int B, int H, int N, int d, attn_dtype dtype, int causal,
+                     float scale, void* cuda_stream) {
+  return attn_bwd_qk(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, H, N, N, d, dtype, causal,
+                     scale, cuda_stream);
 }
 
 // ---------------------------------------------------------------- host-buffer step

@@ -72,7 +72,8 @@ __global__ void __launch_bounds__(320, 1)
   const int jb = blockIdx.x;  // causal: block 0 sees the most query blocks, so runs first
   const int j0 = jb * kTileN;
   const int N = p.N;
-  const int i_first = p.causal ? jb : 0;
+  // causal: the first query block with a row that sees key j0 (row + off >= j0)
+  const int i_first = (p.causal && j0 > p.off) ? (j0 - p.off) / kTileM : 0;
   const int n = p.nb - i_first;  // query blocks i_first .. nb-1
 
   if (threadIdx.x == 0) {
@@ -273,11 +274,13 @@ __global__ void __launch_bounds__(320, 1)
         pr[4 * c4 + 2] = ex2(b.x);
         pr[4 * c4 + 3] = ex2(b.y);
       }
-      if (p.causal && i == jb) {
-        // Diagonal block: query column c0 + c sees this key iff c0 + c >= row.
+      if (p.causal && i * kTileM + p.off < j0 + kTileN - 1) {
+        // A block on the diagonal: query i*128 + c0 + c sees this key iff
+        // i*128 + c0 + c + off >= key, i.e. c >= key - off - i*128 - c0.
+        const int first = key - p.off - i * kTileM - c0;
 #pragma unroll
         for (int c = 0; c < 64; ++c)
-          if (c0 + c < row) pr[c] = 0.f;
+          if (c < first) pr[c] = 0.f;
       }
       {
         uint32_t pk[32];
@@ -326,7 +329,7 @@ __global__ void __launch_bounds__(320, 1)
     if (ok && warp_wait(acc_done, 0, limit, abort_flag, kWaitDkvDone)) {
       tc_fence_after();
       // Group 0 writes dV, group 1 writes dK (scaled).
-      const size_t off = ((size_t)bh * N + key) * (size_t)(D * 2);
+      const size_t off = ((size_t)bh * p.Nk + key) * (size_t)(D * 2);
       uint8_t* dst = reinterpret_cast<uint8_t*>(g == 0 ? p.out1 : p.out0) + off;
       const uint32_t t_acc = tmem + lane_base + (g == 0 ? C::kColAcc0 : C::kColAcc1);
       const float mul = (g == 0) ? 1.f : p.scale;
@@ -334,7 +337,7 @@ __global__ void __launch_bounds__(320, 1)
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t a[32];
         tmem_ld32(t_acc + cc * 32, a);
-        if (key < N) store_row32<BF16>(dst + cc * 64, a, mul);
+        if (key < p.Nk) store_row32<BF16>(dst + cc * 64, a, mul);
       }
     }
     tc_fence_before();

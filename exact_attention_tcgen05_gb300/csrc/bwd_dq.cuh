@@ -32,8 +32,11 @@ struct BwdParams {
   const float* delta;  // [BH, N] D
   void* out0;          // dQ (dQ kernel) or dK (dKV kernel)
   void* out1;          // dV (dKV kernel)
-  int N;
-  int nb;              // number of 128-row blocks
+  int N;               // query rows per slice (N_q)
+  int nb;              // number of 128-row query blocks
+  int Nk;              // key rows per slice (N_k)
+  int nkb;             // number of 128-row key blocks
+  int off;             // causal offset N_k - N_q: key j is visible to query i iff j <= i + off
   int causal;
   float scale;
   float scale_log2;    // scale * log2(e)
@@ -161,7 +164,8 @@ __global__ void __launch_bounds__(320, 1)
   const int ib = p.causal ? (p.nb - 1 - blockIdx.x) : blockIdx.x;  // longest first
   const int i0 = ib * kTileM;
   const int N = p.N;
-  const int n = p.causal ? ib + 1 : p.nb;  // key blocks 0 .. n-1
+  // key blocks 0 .. n-1 (causal: up to the block of the last key the tile's last row sees)
+  const int n = p.causal ? min(p.nkb, (i0 + kTileM - 1 + p.off) / kTileN + 1) : p.nkb;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -338,9 +342,9 @@ __global__ void __launch_bounds__(320, 1)
         pr[c + 1] = ex2(x.y);
       }
       const int kbase = j * kTileN + c0;  // key index of column 0 of this group
-      if ((p.causal && kbase + 63 > i0) || kbase + 64 > N) {  // diagonal or ragged
-        int lim = N - 1 - kbase;                    // last key in range
-        if (p.causal) lim = min(lim, row - kbase);  // last key this row sees
+      if ((p.causal && kbase + 63 > i0 + p.off) || kbase + 64 > p.Nk) {  // diagonal or ragged
+        int lim = p.Nk - 1 - kbase;                         // last key in range
+        if (p.causal) lim = min(lim, row + p.off - kbase);  // last key this row sees
 #pragma unroll
         for (int c = 0; c < 64; ++c)
           if (c > lim) pr[c] = 0.f;

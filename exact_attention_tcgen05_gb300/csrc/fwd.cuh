@@ -40,7 +40,9 @@ namespace attn {
 struct FwdParams {
   void* o;
   float* lse;
-  int N;
+  int N;            // query rows per slice (N_q)
+  int Nk;           // key rows per slice (N_k)
+  int off;          // causal offset N_k - N_q: key j is visible to query i iff j <= i + off
   int nkb;          // number of 128-key blocks
   int nqb;          // number of 256-row query blocks
   int causal;
@@ -99,7 +101,10 @@ __global__ void __launch_bounds__(320, 1)
   const int ntiles = (q0 + kTileM < N) ? 2 : 1;
   int nkv[2];
   for (int t = 0; t < 2; ++t) {
-    nkv[t] = (t < ntiles) ? (p.causal ? min(p.nkb, q0 / kTileN + t + 1) : p.nkb) : 0;
+    // causal: up to the block of the last key the tile's last row sees
+    nkv[t] = (t < ntiles) ? (p.causal ? min(p.nkb, (q0 + t * kTileM + kTileM - 1 + p.off) / kTileN + 1)
+                                      : p.nkb)
+                          : 0;
   }
   const int n_kv = max(nkv[0], nkv[1]);
 
@@ -269,10 +274,10 @@ __global__ void __launch_bounds__(320, 1)
       tmem_ld128(t_s, sr);
       float* s = reinterpret_cast<float*>(sr);
       const int kbase = j * kTileN;
-      const bool diag = p.causal && (kbase + kTileN - 1 > tile_row0);
-      if (diag || kbase + kTileN > N) {
-        int lim = N - 1 - kbase;                       // last key in range
-        if (p.causal) lim = min(lim, row - kbase);     // last key visible to this row
+      const bool diag = p.causal && (kbase + kTileN - 1 > tile_row0 + p.off);
+      if (diag || kbase + kTileN > p.Nk) {
+        int lim = p.Nk - 1 - kbase;                       // last key in range
+        if (p.causal) lim = min(lim, row + p.off - kbase);  // last key visible to this row
 #pragma unroll
         for (int c = 0; c < kTileN; ++c)
           if (c > lim) s[c] = -INFINITY;

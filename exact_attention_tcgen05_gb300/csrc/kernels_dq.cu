@@ -22,6 +22,9 @@ static cudaError_t launch_dq_t(const Maps& m, const Shape& s, const void* q,
   p.out1 = nullptr;
   p.N = s.N;
   p.nb = (s.N + kTileM - 1) / kTileM;
+  p.Nk = s.Nk;
+  p.nkb = (s.Nk + kTileN - 1) / kTileN;
+  p.off = s.Nk - s.N;
   p.causal = s.causal ? 1 : 0;
   p.scale = s.scale;
   p.scale_log2 = s.scale * kLog2e;

@@ -16,7 +16,9 @@ static cudaError_t launch_fwd_t(const Maps& m, const Shape& s, void* o, float* l
   p.o = o;
   p.lse = lse;
   p.N = s.N;
-  p.nkb = (s.N + kTileN - 1) / kTileN;
+  p.Nk = s.Nk;
+  p.off = s.Nk - s.N;
+  p.nkb = (s.Nk + kTileN - 1) / kTileN;
   p.nqb = (s.N + 2 * kTileM - 1) / (2 * kTileM);
   p.causal = s.causal ? 1 : 0;
   p.scale_log2 = s.scale * kLog2e;

@@ -13,7 +13,8 @@ struct Maps {
 };
 
 struct Shape {
-  int BH, N, d;
+  int BH, N, d;  // N: query rows per slice (N_q)
+  int Nk;        // key rows per slice (N_k); causal masking is bottom-right aligned
   bool bf16, causal;
   float scale;
   unsigned long long wait_limit;  // SM cycles one pipeline wait may take

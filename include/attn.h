@@ -104,6 +104,25 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                      int causal, float scale, void* cuda_stream);
 
 /*
+ * attn_fwd_qk / attn_bwd_qk - attn_fwd and attn_bwd for N_q query rows against N_k keys
+ * (a query chunk attending to a longer key sequence, as in chunked prefill):
+ *   q, o, dO, dq  [B, H, Nq, d];  k, v, dk, dv  [B, H, Nk, d];  lse, workspace [B, H, Nq]
+ * Causal masking is bottom-right aligned: the queries are the last Nq positions of the
+ * sequence, key j is visible to query i iff j <= i + (Nk - Nq) (the pages' "future tokens
+ * are blocked", "Triton 05: Flash Attention", section Causal Masking, read for a query
+ * chunk that follows the keys already in the cache); causal requires Nk >= Nq
+ * (ATTN_ERR_INVALID_ARG otherwise), so no row is fully masked. With Nq = Nk these are
+ * exactly attn_fwd and attn_bwd. Everything else as for attn_fwd / attn_bwd.
+ */
+attn_status attn_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse,
+                        int B, int H, int Nq, int Nk, int d, attn_dtype dtype, int causal,
+                        float scale, void* cuda_stream);
+attn_status attn_bwd_qk(const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                        void* workspace, int B, int H, int Nq, int Nk, int d,
+                        attn_dtype dtype, int causal, float scale, void* cuda_stream);
+
+/*
  * attn_bwd_preprocess - step 1 of attn_bwd alone: delta[b,h,i] = sum_c dO[b,h,i,c] *
  * o[b,h,i,c] in float32 ("Triton 05: Flash Attention", section 3단계 커널 구조,
  * [1단계] Preprocess). o, dO: [B, H, N, d] 16-bit device; delta: [B, H, N] float32

@@ -99,6 +99,33 @@ def test_bwd_rejects_bad_arguments(lib, kw, code):
     assert bwd(lib, **kw) == code
 
 
+def fwd_qk(lib, Nq=256, Nk=1024, causal=1, o=O, d=128):
+    return lib.attn_fwd_qk(Q, K, V, o, L, 1, 2, Nq, Nk, d, 1, causal, 0.1, None)
+
+
+def bwd_qk(lib, Nq=256, Nk=1024, causal=1, dk=DK):
+    return lib.attn_bwd_qk(Q, K, V, O, L, DO, DQ, dk, DV, WS, 1, 2, Nq, Nk, 128, 1, causal,
+                           0.1, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Nq=1024, Nk=256), INVALID),            # causal needs N_k >= N_q
+    (dict(Nk=0), INVALID), (dict(Nq=0), INVALID), (dict(Nk=(1 << 20) + 1), INVALID),
+    (dict(d=64, o=K + 64 * 1024 * 2 * 2 - 16), INVALID),   # o overlaps the tail of k
+    (dict(d=80), UNSUPPORTED),
+])
+def test_fwd_qk_rejects_bad_arguments(lib, kw, code):
+    assert fwd_qk(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Nq=1024, Nk=256), INVALID), (dict(Nk=-3), INVALID),
+    (dict(dk=DV + 1024 * 128 * 2 * 2 - 32), INVALID),      # dk overlaps the tail of dv
+])
+def test_bwd_qk_rejects_bad_arguments(lib, kw, code):
+    assert bwd_qk(lib, **kw) == code
+
+
 def test_stage_entry_points_reject_bad_arguments(lib):
     dkv = lambda dk=DK, dv=DV, d=128, lse=L: lib.attn_bwd_dkv(Q, K, V, lse, WS, DO, dk, dv, 1, 1,
                                                               256, d, 1, 1, 0.1, None)
