@@ -32,6 +32,11 @@ SIGNATURES = {
     "attn_bwd_qk": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
                          _P]),
     "attn_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I]),
+    "attn_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F,
+                             _P]),
+    "attn_bwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                             _I, _I, _I, _I, _F, _P]),
+    "attn_bwd_varlen_workspace_bytes": (ctypes.c_size_t, [_I, _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_bwd_preprocess": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "attn_bwd_dkv": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
@@ -420,3 +425,113 @@ def attn_last_kernel_status(stream: Optional[torch.cuda.Stream] = None) -> tuple
 
 def status_str(code: int) -> str:
     return load().attn_status_str(code).decode()
+
+
+# ------------------------------------------------------------------ packed batches
+
+def _packed_of(x: torch.Tensor, name: str) -> tuple[int, int, int]:
+    if not isinstance(x, torch.Tensor) or x.dim() != 3:
+        raise ValueError(f"{name} must be a packed [total, H, d] tensor")
+    if not x.is_cuda or not x.is_contiguous() or x.dtype not in _DTYPE_CODES:
+        raise ValueError(f"{name} must be a contiguous float16/bfloat16 CUDA tensor")
+    return tuple(x.shape)  # type: ignore[return-value]
+
+
+def _cu_of(cu: torch.Tensor, name: str, device: torch.device) -> torch.Tensor:
+    if (not isinstance(cu, torch.Tensor) or cu.dim() != 1 or cu.numel() < 2
+            or cu.dtype != torch.int32 or cu.device != device or not cu.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous int32 [B + 1] tensor on q's device")
+    return cu
+
+
+def _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k):
+    Tq, H, d = _packed_of(q, "q")
+    Tk, Hk, dk = _packed_of(k, "k")
+    if (Hk, dk) != (H, d) or k.dtype != q.dtype or k.device != q.device:
+        raise ValueError("k must be [total_k, H, d] with q's H, d, dtype and device")
+    if v.shape != k.shape or v.dtype != k.dtype or v.device != k.device:
+        raise ValueError("v must match k")
+    _packed_of(v, "v")
+    cu_q = _cu_of(cu_seqlens_q, "cu_seqlens_q", q.device)
+    cu_k = _cu_of(cu_seqlens_k, "cu_seqlens_k", q.device)
+    if cu_k.numel() != cu_q.numel():
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must describe the same batch")
+    return Tq, Tk, H, d, cu_q, cu_k, cu_q.numel() - 1
+
+
+def attn_bwd_varlen_workspace_bytes(H: int, total_q: int) -> int:
+    return int(load().attn_bwd_varlen_workspace_bytes(H, total_q))
+
+
+def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                    cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor,
+                    max_seqlen_q: int, max_seqlen_k: int, causal: bool = False,
+                    scale: Optional[float] = None, o: Optional[torch.Tensor] = None,
+                    lse: Optional[torch.Tensor] = None,
+                    stream: Optional[torch.cuda.Stream] = None
+                    ) -> tuple[torch.Tensor, torch.Tensor]:
+    """Forward over sequences packed along the token axis, via libattn.so.
+
+    q [total_q, H, d], k and v [total_k, H, d]; sequence b owns query tokens
+    cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key tokens cu_seqlens_k[b] ..
+    cu_seqlens_k[b+1]-1 (int32 device tensors of B + 1 entries). max_seqlen_q/_k bound
+    every sequence (the caller knows them; reading cu_seqlens here would synchronise).
+    Returns o [total_q, H, d] and lse [H, total_q]. Malformed sequences are reported by
+    attn_last_kernel_status() as ATTN_ERR_INVALID_ARG."""
+    Tq, Tk, H, d, cu_q, cu_k, B = _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if o is None else o
+    if o.shape != q.shape or o.dtype != q.dtype or o.device != q.device:
+        raise ValueError("o must match q")
+    lse = torch.empty(H, Tq, dtype=torch.float32, device=q.device) if lse is None else lse
+    if lse.shape != (H, Tq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [H, total_q] tensor")
+    with torch.cuda.device(q.device):
+        code = load().attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                      lse.data_ptr(), cu_q.data_ptr(), cu_k.data_ptr(), B, H,
+                                      Tq, Tk, int(max_seqlen_q), int(max_seqlen_k), d,
+                                      _DTYPE_CODES[q.dtype], int(causal), scale,
+                                      _stream_handle(stream))
+    _check("attn_fwd_varlen", code)
+    return o, lse
+
+
+def attn_bwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                    lse: torch.Tensor, do: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                    cu_seqlens_k: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int,
+                    causal: bool = False, scale: Optional[float] = None,
+                    dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
+                    dv: Optional[torch.Tensor] = None,
+                    workspace: Optional[torch.Tensor] = None,
+                    stream: Optional[torch.cuda.Stream] = None
+                    ) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """dq, dk, dv of sum(do * o) for a packed batch (layouts as attn_fwd_varlen), via
+    libattn.so; workspace holds D [H, total_q] float32."""
+    Tq, Tk, H, d, cu_q, cu_k, B = _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k)
+    for name, x in (("o", o), ("do", do)):
+        if x.shape != q.shape or x.dtype != q.dtype or x.device != q.device:
+            raise ValueError(f"{name} must match q")
+        _packed_of(x, name)
+    if lse.shape != (H, Tq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [H, total_q] tensor")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(k) if dv is None else dv
+    for name, x, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, k)):
+        if x.shape != ref.shape or x.dtype != ref.dtype or x.device != ref.device:
+            raise ValueError(f"{name} must match {'q' if ref is q else 'k'}")
+        _packed_of(x, name)
+    if workspace is None:
+        workspace = torch.empty(H, Tq, dtype=torch.float32, device=q.device)
+    if workspace.numel() * workspace.element_size() < 4 * H * Tq or not workspace.is_contiguous():
+        raise ValueError("workspace must hold H * total_q float32 values")
+    with torch.cuda.device(q.device):
+        code = load().attn_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                      lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                      dv.data_ptr(), workspace.data_ptr(), cu_q.data_ptr(),
+                                      cu_k.data_ptr(), B, H, Tq, Tk, int(max_seqlen_q),
+                                      int(max_seqlen_k), d, _DTYPE_CODES[q.dtype], int(causal),
+                                      scale, _stream_handle(stream))
+    _check("attn_bwd_varlen", code)
+    return dq, dk, dv

@@ -96,6 +96,25 @@ attn_status encode_map(CUtensorMap* m, const void* base, int BH, int N, int d, b
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// [total, H, d] packed 16-bit tensor, read as [64-column x 1-head x 128-token] boxes with
+// 128-byte swizzle: the same shared-memory image as a [64 x 128] box of the dense map.
+// Tokens past `total` read as zero.
+attn_status encode_map_packed(CUtensorMap* m, const void* base, int H, int total, int d,
+                              bool bf16) {
+  EncodeFn enc = get_encode();
+  if (enc == nullptr) return ATTN_ERR_CUDA;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)total};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * (cuuint64_t)d * 2};
+  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r =
+      enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 Shape make_shape(int B, int H, int N, int d, attn_dtype dtype, int causal, float scale,
                  int Nk = -1) {
   Shape s;
@@ -107,6 +126,7 @@ Shape make_shape(int B, int H, int N, int d, attn_dtype dtype, int causal, float
   s.causal = causal != 0;
   s.scale = scale;
   s.wait_limit = wait_limit_cycles();
+  s.vl = attn::Varlen{};  // dense tensors
   return s;
 }
 
@@ -286,6 +306,110 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                      float scale, void* cuda_stream) {
   return attn_bwd_qk(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, H, N, N, d, dtype, causal,
                      scale, cuda_stream);
+}
+
+// ---------------------------------------------------------------- packed batches
+namespace {
+
+// Sizes of a packed variable-length call; the per-sequence bounds in cu_seqlens live in
+// device memory and are checked by the kernels.
+attn_status check_varlen(int B, int H, int total_q, int total_k, int max_q, int max_k, int d,
+                         attn_dtype dtype, const int* cu_q, const int* cu_k) {
+  if (B < 1 || H < 1 || (long long)B * H > kMaxBH) return ATTN_ERR_INVALID_ARG;
+  if (total_q < 1 || total_k < 1) return ATTN_ERR_INVALID_ARG;
+  if (max_q < 1 || max_q > kMaxN || max_q > total_q) return ATTN_ERR_INVALID_ARG;
+  if (max_k < 1 || max_k > kMaxN || max_k > total_k) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_FP16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (cu_q == nullptr || cu_k == nullptr) return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(cu_q) | reinterpret_cast<uintptr_t>(cu_k)) & 3u)
+    return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+Shape make_varlen_shape(int B, int H, int total_q, int total_k, int max_q, int max_k, int d,
+                        attn_dtype dtype, int causal, float scale, const int* cu_q,
+                        const int* cu_k) {
+  Shape s = make_shape(B, H, max_q, d, dtype, causal, scale, max_k);
+  s.vl.cu_q = cu_q;
+  s.vl.cu_k = cu_k;
+  s.vl.H = H;
+  s.vl.total_q = total_q;
+  s.vl.total_k = total_k;
+  s.vl.max_q = max_q;
+  s.vl.max_k = max_k;
+  return s;
+}
+
+}  // namespace
+
+size_t attn_bwd_varlen_workspace_bytes(int H, int total_q) {
+  if (H <= 0 || total_q <= 0) return 0;
+  return (size_t)4 * (size_t)H * (size_t)total_q;
+}
+
+attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
+                            int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                            int d, attn_dtype dtype, int causal, float scale,
+                            void* cuda_stream) {
+  attn_status st = check_varlen(B, H, total_q, total_k, max_seqlen_q, max_seqlen_k, d, dtype,
+                                cu_seqlens_q, cu_seqlens_k);
+  if (st != ATTN_OK) return st;
+  if ((st = check_scale(scale)) != ATTN_OK) return st;
+  if ((st = check_ptrs({q, k, v, o, lse})) != ATTN_OK) return st;
+  const size_t qb = (size_t)total_q * H * d * 2, kb = (size_t)total_k * H * d * 2;
+  const size_t lb = (size_t)H * total_q * 4;
+  const Range ins[5] = {range_of(q, qb), range_of(k, kb), range_of(v, kb),
+                        range_of(cu_seqlens_q, (size_t)(B + 1) * 4),
+                        range_of(cu_seqlens_k, (size_t)(B + 1) * 4)};
+  const Range outs[2] = {range_of(o, qb), range_of(lse, lb)};
+  if ((st = check_ranges(ins, 5, outs, 2)) != ATTN_OK) return st;
+
+  const Shape s = make_varlen_shape(B, H, total_q, total_k, max_seqlen_q, max_seqlen_k, d,
+                                    dtype, causal, scale, cu_seqlens_q, cu_seqlens_k);
+  Maps m;
+  if ((st = encode_map_packed(&m.q, q, H, total_q, d, s.bf16)) != ATTN_OK) return st;
+  if ((st = encode_map_packed(&m.k, k, H, total_k, d, s.bf16)) != ATTN_OK) return st;
+  if ((st = encode_map_packed(&m.v, v, H, total_k, d, s.bf16)) != ATTN_OK) return st;
+  m.d_o = m.v;
+  return from_cuda(attn::launch_fwd(m, s, o, lse, static_cast<cudaStream_t>(cuda_stream)));
+}
+
+attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                            void* workspace, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                            int B, int H, int total_q, int total_k, int max_seqlen_q,
+                            int max_seqlen_k, int d, attn_dtype dtype, int causal, float scale,
+                            void* cuda_stream) {
+  attn_status st = check_varlen(B, H, total_q, total_k, max_seqlen_q, max_seqlen_k, d, dtype,
+                                cu_seqlens_q, cu_seqlens_k);
+  if (st != ATTN_OK) return st;
+  if ((st = check_scale(scale)) != ATTN_OK) return st;
+  if ((st = check_ptrs({q, k, v, o, lse, dO, dq, dk, dv, workspace})) != ATTN_OK) return st;
+  const size_t qb = (size_t)total_q * H * d * 2, kb = (size_t)total_k * H * d * 2;
+  const size_t lb = (size_t)H * total_q * 4;
+  const Range ins[8] = {range_of(q, qb), range_of(k, kb),   range_of(v, kb),
+                        range_of(o, qb), range_of(lse, lb), range_of(dO, qb),
+                        range_of(cu_seqlens_q, (size_t)(B + 1) * 4),
+                        range_of(cu_seqlens_k, (size_t)(B + 1) * 4)};
+  const Range outs[4] = {range_of(dq, qb), range_of(dk, kb), range_of(dv, kb),
+                         range_of(workspace, lb)};
+  if ((st = check_ranges(ins, 8, outs, 4)) != ATTN_OK) return st;
+
+  const Shape s = make_varlen_shape(B, H, total_q, total_k, max_seqlen_q, max_seqlen_k, d,
+                                    dtype, causal, scale, cu_seqlens_q, cu_seqlens_k);
+  Maps m;
+  if ((st = encode_map_packed(&m.q, q, H, total_q, d, s.bf16)) != ATTN_OK) return st;
+  if ((st = encode_map_packed(&m.k, k, H, total_k, d, s.bf16)) != ATTN_OK) return st;
+  if ((st = encode_map_packed(&m.v, v, H, total_k, d, s.bf16)) != ATTN_OK) return st;
+  if ((st = encode_map_packed(&m.d_o, dO, H, total_q, d, s.bf16)) != ATTN_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(cuda_stream);
+  float* delta = static_cast<float*>(workspace);
+  cudaError_t e = attn::launch_delta(s, o, dO, delta, cs);
+  if (e == cudaSuccess) e = attn::launch_dkv(m, s, q, dO, lse, delta, dk, dv, cs);
+  if (e == cudaSuccess) e = attn::launch_dq(m, s, q, dO, lse, delta, dq, cs);
+  return from_cuda(e);
 }
 
 // ---------------------------------------------------------------- host-buffer step
@@ -523,6 +647,7 @@ attn_status attn_last_kernel_status(void* cuda_stream, int* where) {
     if (first == 0 && w != 0) first = w;
   }
   if (where != nullptr) *where = first;
+  if (first == attn::kStatusBadSeqlens) return ATTN_ERR_INVALID_ARG;
   return first == 0 ? ATTN_OK : ATTN_ERR_TIMEOUT;
 }
 

@@ -45,11 +45,14 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   return v;
 }
 
-// rows = B*H*N; o, dO: rows x D 16-bit; delta: rows f32.
+// rows = B*H*N; o, dO: rows x D 16-bit; delta: rows f32, row r at delta[r].
+// Packed batch (heads > 0): rows = total*H in [total, H] order, and the D of row
+// r = t*H + h goes to delta[h*total + t] (the [H, total] layout of lse).
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kDeltaThreads)
     attn_bwd_delta_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO,
-                          float* __restrict__ delta, long long rows) {
+                          float* __restrict__ delta, long long rows, int heads,
+                          long long total) {
   constexpr int kLanesPerRow = D / 8;              // 16-byte chunks per row
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;  // rows one warp covers per load
   const int lane = threadIdx.x & 31;
@@ -78,7 +81,8 @@ __global__ void __launch_bounds__(kDeltaThreads)
       for (int off = kLanesPerRow / 2; off > 0; off >>= 1)
         acc += __shfl_xor_sync(0xffffffffu, acc, off);
       const long long row = r0 + u * kRowsPerWarp + sub;
-      if (part == 0 && row < rows) delta[row] = acc;
+      if (part == 0 && row < rows)
+        delta[heads > 0 ? (row % heads) * total + row / heads : row] = acc;
     }
   }
 }

@@ -69,12 +69,29 @@ __global__ void __launch_bounds__(320, 1)
   const int warp = warp_id();
   const int lane = lane_id();
   const int bh = blockIdx.y;
+  SliceRows sl;
+  if (!slice_rows(p.vl, bh, p.N, p.Nk, D, p.causal != 0, sl)) return;
+  const int N = sl.nq, Nk = sl.nk, off = sl.off;
   const int jb = blockIdx.x;  // causal: block 0 sees the most query blocks, so runs first
+  if (jb * kTileN >= Nk) return;  // packed batch: past this sequence's keys
   const int j0 = jb * kTileN;
-  const int N = p.N;
+  if (N == 0) {
+    // A packed sequence with keys but no queries: no query sees these keys, so their
+    // gradients are zero.
+    const int rows = min(kTileN, Nk - j0);
+    constexpr int kVec = D / 8;  // 16-byte chunks per row
+    for (int idx = threadIdx.x; idx < 2 * rows * kVec; idx += blockDim.x) {
+      const int t = idx / (rows * kVec), r = (idx / kVec) % rows, c = idx % kVec;
+      uint8_t* base = reinterpret_cast<uint8_t*>(t == 0 ? p.out0 : p.out1);
+      reinterpret_cast<uint4*>(base + (sl.k_elem0 + (size_t)(j0 + r) * sl.row_elems) * 2)[c] =
+          make_uint4(0, 0, 0, 0);
+    }
+    return;
+  }
+  const int nb = (N + kTileM - 1) / kTileM;
   // causal: the first query block with a row that sees key j0 (row + off >= j0)
-  const int i_first = (p.causal && j0 > p.off) ? (j0 - p.off) / kTileM : 0;
-  const int n = p.nb - i_first;  // query blocks i_first .. nb-1
+  const int i_first = (p.causal && j0 > off) ? (j0 - off) / kTileM : 0;
+  const int n = nb - i_first;  // query blocks i_first .. nb-1
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -113,8 +130,10 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_map(&map_do);
       mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
       for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_3d(smem + C::kOffK + c * kBoxBytes, &map_k, kv_full, c * kBoxCols, j0, bh);
-        tma_load_3d(smem + C::kOffV + c * kBoxBytes, &map_v, kv_full, c * kBoxCols, j0, bh);
+        tma_load_rows(smem + C::kOffK + c * kBoxBytes, &map_k, kv_full, c * kBoxCols, j0, sl,
+                      true);
+        tma_load_rows(smem + C::kOffV + c * kBoxBytes, &map_v, kv_full, c * kBoxCols, j0, sl,
+                      true);
       }
     }
     __syncwarp();
@@ -128,12 +147,12 @@ __global__ void __launch_bounds__(320, 1)
       if (elect_one()) {
         mbar_arrive_expect_tx(&q_full[s], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(smem + C::kOffQ + s * C::kTileBytes + c * kBoxBytes, &map_q, &q_full[s],
-                      c * kBoxCols, i * kTileM, bh);
+          tma_load_rows(smem + C::kOffQ + s * C::kTileBytes + c * kBoxBytes, &map_q,
+                        &q_full[s], c * kBoxCols, i * kTileM, sl, false);
         mbar_arrive_expect_tx(&do_full[s], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(smem + C::kOffDO + s * C::kTileBytes + c * kBoxBytes, &map_do,
-                      &do_full[s], c * kBoxCols, i * kTileM, bh);
+          tma_load_rows(smem + C::kOffDO + s * C::kTileBytes + c * kBoxBytes, &map_do,
+                        &do_full[s], c * kBoxCols, i * kTileM, sl, false);
       }
       __syncwarp();
       issued = it + 1;
@@ -233,7 +252,7 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t t_dp = tmem + lane_base + C::kColDP + c0;
     const float2 sl2x2 = make_float2(p.scale_log2, p.scale_log2);
     // Group 0 stages -L*log2(e), group 1 stages D: one value per thread per query block.
-    const float* src = (g == 0 ? p.lse : p.delta) + (size_t)bh * N;
+    const float* src = (g == 0 ? p.lse : p.delta) + sl.stat0;
     auto load_stat = [&](int i) -> float {
       const int q = i * kTileM + row;
       if (q >= N) return g == 0 ? -INFINITY : 0.f;  // padding queries: P = 0, D = 0
@@ -274,10 +293,10 @@ __global__ void __launch_bounds__(320, 1)
         pr[4 * c4 + 2] = ex2(b.x);
         pr[4 * c4 + 3] = ex2(b.y);
       }
-      if (p.causal && i * kTileM + p.off < j0 + kTileN - 1) {
+      if (p.causal && i * kTileM + off < j0 + kTileN - 1) {
         // A block on the diagonal: query i*128 + c0 + c sees this key iff
         // i*128 + c0 + c + off >= key, i.e. c >= key - off - i*128 - c0.
-        const int first = key - p.off - i * kTileM - c0;
+        const int first = key - off - i * kTileM - c0;
 #pragma unroll
         for (int c = 0; c < 64; ++c)
           if (c < first) pr[c] = 0.f;
@@ -329,15 +348,15 @@ __global__ void __launch_bounds__(320, 1)
     if (ok && warp_wait(acc_done, 0, limit, abort_flag, kWaitDkvDone)) {
       tc_fence_after();
       // Group 0 writes dV, group 1 writes dK (scaled).
-      const size_t off = ((size_t)bh * p.Nk + key) * (size_t)(D * 2);
-      uint8_t* dst = reinterpret_cast<uint8_t*>(g == 0 ? p.out1 : p.out0) + off;
+      uint8_t* dst = reinterpret_cast<uint8_t*>(g == 0 ? p.out1 : p.out0) +
+                     (sl.k_elem0 + (size_t)key * sl.row_elems) * 2;
       const uint32_t t_acc = tmem + lane_base + (g == 0 ? C::kColAcc0 : C::kColAcc1);
       const float mul = (g == 0) ? 1.f : p.scale;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t a[32];
         tmem_ld32(t_acc + cc * 32, a);
-        if (key < p.Nk) store_row32<BF16>(dst + cc * 64, a, mul);
+        if (key < Nk) store_row32<BF16>(dst + cc * 64, a, mul);
       }
     }
     tc_fence_before();

@@ -32,15 +32,14 @@ struct BwdParams {
   const float* delta;  // [BH, N] D
   void* out0;          // dQ (dQ kernel) or dK (dKV kernel)
   void* out1;          // dV (dKV kernel)
-  int N;               // query rows per slice (N_q)
-  int nb;              // number of 128-row query blocks
-  int Nk;              // key rows per slice (N_k)
-  int nkb;             // number of 128-row key blocks
-  int off;             // causal offset N_k - N_q: key j is visible to query i iff j <= i + off
+  int N;               // query rows per slice (N_q; packed batches: per sequence, from vl)
+  int Nk;              // key rows per slice (N_k); causal key j is visible to query i
+                       // iff j <= i + (N_k - N_q)
   int causal;
   float scale;
   float scale_log2;    // scale * log2(e)
   unsigned long long wait_limit;
+  Varlen vl;           // packed variable-length batch (vl.cu_q == nullptr: dense)
 };
 
 template <int D>
@@ -161,11 +160,16 @@ __global__ void __launch_bounds__(320, 1)
   const int warp = warp_id();
   const int lane = lane_id();
   const int bh = blockIdx.y;
-  const int ib = p.causal ? (p.nb - 1 - blockIdx.x) : blockIdx.x;  // longest first
+  SliceRows sl;
+  if (!slice_rows(p.vl, bh, p.N, p.Nk, D, p.causal != 0, sl)) return;
+  const int N = sl.nq, Nk = sl.nk, off = sl.off;
+  const int nb = (N + kTileM - 1) / kTileM;
+  const int nkb = (Nk + kTileN - 1) / kTileN;
+  if ((int)blockIdx.x >= nb) return;  // packed batch: past this sequence's query blocks
+  const int ib = p.causal ? (nb - 1 - blockIdx.x) : blockIdx.x;  // longest first
   const int i0 = ib * kTileM;
-  const int N = p.N;
   // key blocks 0 .. n-1 (causal: up to the block of the last key the tile's last row sees)
-  const int n = p.causal ? min(p.nkb, (i0 + kTileM - 1 + p.off) / kTileN + 1) : p.nkb;
+  const int n = p.causal ? min(nkb, (i0 + kTileM - 1 + off) / kTileN + 1) : nkb;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -208,12 +212,12 @@ __global__ void __launch_bounds__(320, 1)
       if (elect_one()) {
         mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(smem + C::kOffK + s * C::kTileBytes + c * kBoxBytes, &map_k, &k_full[s],
-                      c * kBoxCols, j * kTileN, bh);
+          tma_load_rows(smem + C::kOffK + s * C::kTileBytes + c * kBoxBytes, &map_k,
+                        &k_full[s], c * kBoxCols, j * kTileN, sl, true);
         mbar_arrive_expect_tx(&v_full[s], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(smem + C::kOffV + s * C::kTileBytes + c * kBoxBytes, &map_v, &v_full[s],
-                      c * kBoxCols, j * kTileN, bh);
+          tma_load_rows(smem + C::kOffV + s * C::kTileBytes + c * kBoxBytes, &map_v,
+                        &v_full[s], c * kBoxCols, j * kTileN, sl, true);
       }
       __syncwarp();
       issued = j + 1;
@@ -310,8 +314,8 @@ __global__ void __launch_bounds__(320, 1)
     float neg_l2 = -INFINITY;  // -L * log2(e); rows past N get P = 0
     float dlt = 0.f;
     if (row < N) {
-      neg_l2 = -p.lse[(size_t)bh * N + row] * kLog2e;
-      dlt = p.delta[(size_t)bh * N + row];
+      neg_l2 = -p.lse[sl.stat0 + row] * kLog2e;
+      dlt = p.delta[sl.stat0 + row];
     }
     const float2 nl2x2 = make_float2(neg_l2, neg_l2);
     const float2 ndl2 = make_float2(-dlt, -dlt);
@@ -320,7 +324,8 @@ __global__ void __launch_bounds__(320, 1)
     bool ok = true;
     {
       const uint8_t* gsrc = reinterpret_cast<const uint8_t*>(g == 0 ? p.in_q : p.in_do);
-      copy_row_to_tmem<D>(row < N ? gsrc + ((size_t)bh * N + row) * (size_t)(D * 2) : nullptr,
+      copy_row_to_tmem<D>(row < N ? gsrc + (sl.q_elem0 + (size_t)row * sl.row_elems) * 2
+                                  : nullptr,
                           tmem + lane_base + (g == 0 ? C::kColQ : C::kColDO));
       tmem_st_wait();
       tc_fence_before();
@@ -342,9 +347,9 @@ __global__ void __launch_bounds__(320, 1)
         pr[c + 1] = ex2(x.y);
       }
       const int kbase = j * kTileN + c0;  // key index of column 0 of this group
-      if ((p.causal && kbase + 63 > i0 + p.off) || kbase + 64 > p.Nk) {  // diagonal or ragged
-        int lim = p.Nk - 1 - kbase;                         // last key in range
-        if (p.causal) lim = min(lim, row + p.off - kbase);  // last key this row sees
+      if ((p.causal && kbase + 63 > i0 + off) || kbase + 64 > Nk) {  // diagonal or ragged
+        int lim = Nk - 1 - kbase;                       // last key in range
+        if (p.causal) lim = min(lim, row + off - kbase);  // last key this row sees
 #pragma unroll
         for (int c = 0; c < 64; ++c)
           if (c > lim) pr[c] = 0.f;
@@ -376,7 +381,7 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       // Group g writes columns [g*d/2, (g+1)*d/2) of dQ, scaled.
       uint8_t* drow = reinterpret_cast<uint8_t*>(p.out0) +
-                      ((size_t)bh * N + row) * (size_t)(D * 2) + g * D;
+                      (sl.q_elem0 + (size_t)row * sl.row_elems) * 2 + g * D;
       const uint32_t t_acc = tmem + lane_base + C::kColAcc0 + g * (D / 2);
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {

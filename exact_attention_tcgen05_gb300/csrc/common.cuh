@@ -5,6 +5,7 @@
 #include <cuda.h>
 
 #include "ptx.cuh"
+#include "varlen.h"
 
 namespace attn {
 
@@ -24,6 +25,7 @@ enum WaitSite : int {
   kWaitDkvKV = 0x31, kWaitDkvQ, kWaitDkvDO, kWaitDkvEmpty, kWaitDkvS, kWaitDkvDP,
   kWaitDkvP, kWaitDkvDS, kWaitDkvDone, kWaitDkvDrain, kWaitDkvStats,
   kWaitDecFull = 0x41, kWaitDecDrain,
+  kErrSeqlens = kStatusBadSeqlens,  // a packed batch's cu_seqlens hold a bad sequence
   kErrSmemAlign = 0x7F  // dynamic shared memory not 1024-byte aligned (kernel skipped)
 };
 
@@ -32,6 +34,73 @@ enum WaitSite : int {
 // configurable pipeline limit: after a pipeline wait gives up, these must still see that
 // work complete (microseconds), or memory could be released under it.
 constexpr unsigned long long kDrainLimit = 1ull << 31;
+
+// Where the rows of one (sequence, head) slice live.
+//   dense:  TMA coordinates (col, row, bh) of a [B*H, N, d] map; element offset of row r
+//           = bh*N*d + r*d.
+//   packed: TMA coordinates (col, h, start + r) of a [total, H, d] map; element offset
+//           of row r = ((start + r)*H + h)*d.
+struct SliceRows {
+  int nq, nk;            // query and key rows of the slice
+  int off;               // nk - nq: causal key j is visible to query i iff j <= i + off
+  int q_start, k_start;  // first token of the sequence (packed) or 0
+  int tma_bh;            // bh (dense) or h (packed)
+  bool packed;
+  size_t q_elem0, k_elem0;  // element offset of row 0 of the q-like / k-like tensors
+  size_t row_elems;         // elements between consecutive rows
+  size_t stat0;             // index of row 0 in lse and D
+};
+
+// Fills `s` for slice bh. Dense: the whole-call sizes N, Nk. Packed: reads the slice's
+// sequence bounds and checks them (in range, not longer than the grid covers, and every
+// query row sees a key); a malformed sequence records kErrSeqlens and returns false.
+__device__ __forceinline__ bool slice_rows(const Varlen& vl, int bh, int N, int Nk, int D,
+                                           bool causal, SliceRows& s) {
+  if (vl.cu_q == nullptr) {
+    s.nq = N;
+    s.nk = Nk;
+    s.q_start = s.k_start = 0;
+    s.tma_bh = bh;
+    s.packed = false;
+    s.q_elem0 = (size_t)bh * N * D;
+    s.k_elem0 = (size_t)bh * Nk * D;
+    s.row_elems = (size_t)D;
+    s.stat0 = (size_t)bh * N;
+  } else {
+    const int b = bh / vl.H, h = bh % vl.H;
+    const int q0 = vl.cu_q[b], q1 = vl.cu_q[b + 1];
+    const int k0 = vl.cu_k[b], k1 = vl.cu_k[b + 1];
+    const bool bad = q0 < 0 || q1 < q0 || q1 > vl.total_q || k0 < 0 || k1 < k0 ||
+                     k1 > vl.total_k || q1 - q0 > vl.max_q || k1 - k0 > vl.max_k ||
+                     (q1 > q0 && (k1 == k0 || (causal && k1 - k0 < q1 - q0)));
+    if (bad) {
+      record_timeout(kErrSeqlens);
+      return false;
+    }
+    s.nq = q1 - q0;
+    s.nk = k1 - k0;
+    s.q_start = q0;
+    s.k_start = k0;
+    s.tma_bh = h;
+    s.packed = true;
+    s.q_elem0 = ((size_t)q0 * vl.H + h) * D;
+    s.k_elem0 = ((size_t)k0 * vl.H + h) * D;
+    s.row_elems = (size_t)vl.H * D;
+    s.stat0 = (size_t)h * vl.total_q + q0;
+  }
+  s.off = s.nk - s.nq;
+  return true;
+}
+
+// TMA copy of one [128 rows x 64 cols] box of a slice, starting at slice row `row`
+// (`keys`: a k-like tensor), in the slice's layout (see SliceRows).
+__device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                              int col, int row, const SliceRows& s, bool keys) {
+  if (s.packed)
+    tma_load_3d(dst, map, bar, col, s.tma_bh, (keys ? s.k_start : s.q_start) + row);
+  else
+    tma_load_3d(dst, map, bar, col, row, s.tma_bh);
+}
 
 // Rounds a shared-memory pointer up to 1024 bytes (the swizzle-atom alignment).
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {

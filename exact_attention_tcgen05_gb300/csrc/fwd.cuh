@@ -40,14 +40,12 @@ namespace attn {
 struct FwdParams {
   void* o;
   float* lse;
-  int N;            // query rows per slice (N_q)
+  int N;            // query rows per slice (N_q; packed batches: per sequence, from vl)
   int Nk;           // key rows per slice (N_k)
-  int off;          // causal offset N_k - N_q: key j is visible to query i iff j <= i + off
-  int nkb;          // number of 128-key blocks
-  int nqb;          // number of 256-row query blocks
   int causal;
   float scale_log2; // scale * log2(e)
   unsigned long long wait_limit;
+  Varlen vl;        // packed variable-length batch (vl.cu_q == nullptr: dense)
 };
 
 template <int D>
@@ -95,15 +93,20 @@ __global__ void __launch_bounds__(320, 1)
   const int warp = warp_id();
   const int lane = lane_id();
   const int bh = blockIdx.y;
-  const int qb = p.nqb - 1 - blockIdx.x;  // within a head, longest (most key blocks) first
+  SliceRows sl;
+  if (!slice_rows(p.vl, bh, p.N, p.Nk, D, p.causal != 0, sl)) return;
+  const int N = sl.nq, Nk = sl.nk, off = sl.off;
+  const int nqb = (N + 2 * kTileM - 1) / (2 * kTileM);
+  const int nkb = (Nk + kTileN - 1) / kTileN;
+  if ((int)blockIdx.x >= nqb) return;  // packed batch: past this sequence's query blocks
+  const int qb = nqb - 1 - blockIdx.x;  // within a head, longest (most key blocks) first
   const int q0 = qb * 256;
-  const int N = p.N;
   const int ntiles = (q0 + kTileM < N) ? 2 : 1;
   int nkv[2];
   for (int t = 0; t < 2; ++t) {
     // causal: up to the block of the last key the tile's last row sees
-    nkv[t] = (t < ntiles) ? (p.causal ? min(p.nkb, (q0 + t * kTileM + kTileM - 1 + p.off) / kTileN + 1)
-                                      : p.nkb)
+    nkv[t] = (t < ntiles) ? (p.causal ? min(nkb, (q0 + t * kTileM + kTileM - 1 + off) / kTileN + 1)
+                                      : nkb)
                           : 0;
   }
   const int n_kv = max(nkv[0], nkv[1]);
@@ -144,8 +147,8 @@ __global__ void __launch_bounds__(320, 1)
       mbar_arrive_expect_tx(q_full, ntiles * C::kTileBytes);
       for (int t = 0; t < ntiles; ++t)
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(smem + C::kOffQ + t * C::kTileBytes + c * kBoxBytes, &map_q, q_full,
-                      c * kBoxCols, q0 + t * kTileM, bh);
+          tma_load_rows(smem + C::kOffQ + t * C::kTileBytes + c * kBoxBytes, &map_q, q_full,
+                        c * kBoxCols, q0 + t * kTileM, sl, false);
     }
     __syncwarp();
     int issued = 0;
@@ -158,12 +161,12 @@ __global__ void __launch_bounds__(320, 1)
       if (elect_one()) {
         mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(smem + C::kOffK + s * C::kTileBytes + c * kBoxBytes, &map_k,
-                      &k_full[s], c * kBoxCols, j * kTileN, bh);
+          tma_load_rows(smem + C::kOffK + s * C::kTileBytes + c * kBoxBytes, &map_k,
+                        &k_full[s], c * kBoxCols, j * kTileN, sl, true);
         mbar_arrive_expect_tx(&v_full[s], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(smem + C::kOffV + s * C::kTileBytes + c * kBoxBytes, &map_v,
-                      &v_full[s], c * kBoxCols, j * kTileN, bh);
+          tma_load_rows(smem + C::kOffV + s * C::kTileBytes + c * kBoxBytes, &map_v,
+                        &v_full[s], c * kBoxCols, j * kTileN, sl, true);
       }
       __syncwarp();
       issued = j + 1;
@@ -274,10 +277,10 @@ __global__ void __launch_bounds__(320, 1)
       tmem_ld128(t_s, sr);
       float* s = reinterpret_cast<float*>(sr);
       const int kbase = j * kTileN;
-      const bool diag = p.causal && (kbase + kTileN - 1 > tile_row0 + p.off);
-      if (diag || kbase + kTileN > p.Nk) {
-        int lim = p.Nk - 1 - kbase;                       // last key in range
-        if (p.causal) lim = min(lim, row + p.off - kbase);  // last key visible to this row
+      const bool diag = p.causal && (kbase + kTileN - 1 > tile_row0 + off);
+      if (diag || kbase + kTileN > Nk) {
+        int lim = Nk - 1 - kbase;                       // last key in range
+        if (p.causal) lim = min(lim, row + off - kbase);  // last key visible to this row
 #pragma unroll
         for (int c = 0; c < kTileN; ++c)
           if (c > lim) s[c] = -INFINITY;
@@ -350,7 +353,7 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       const float inv_l = 1.f / lr;
       uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
-                      ((size_t)bh * N + (size_t)row) * (size_t)(D * 2);
+                      (sl.q_elem0 + (size_t)row * sl.row_elems) * 2;
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
         uint32_t r[64];
@@ -367,7 +370,7 @@ __global__ void __launch_bounds__(320, 1)
             dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
-      if (row < N) p.lse[(size_t)bh * N + row] = (m + log2f(l)) * kLn2;
+      if (row < N) p.lse[sl.stat0 + row] = (m + log2f(l)) * kLn2;
     }
     tc_fence_before();
   }

@@ -15,14 +15,16 @@ static int sm_count_current() {
 template <int D, bool BF16>
 static cudaError_t launch_delta_t(const Shape& s, const void* o, const void* dO, float* delta,
                                   cudaStream_t st) {
-  const long long rows = (long long)s.BH * s.N;
+  const bool packed = s.vl.cu_q != nullptr;
+  const long long rows = packed ? (long long)s.vl.total_q * s.vl.H : (long long)s.BH * s.N;
   constexpr int kRowsPerBlockStep = (kDeltaThreads / 32) * (32 / (D / 8)) * kDeltaUnroll;
   const long long want = (rows + kRowsPerBlockStep - 1) / kRowsPerBlockStep;
   const int resident = 2048 / kDeltaThreads;  // blocks per SM at full occupancy
   const long long cap = (long long)sm_count_current() * resident;
   const int blocks = (int)(want < cap ? want : cap);
   attn_bwd_delta_kernel<D, BF16><<<blocks, kDeltaThreads, 0, st>>>(
-      reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dO), delta, rows);
+      reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dO), delta, rows,
+      packed ? s.vl.H : 0, packed ? (long long)s.vl.total_q : 0);
   return cudaGetLastError();
 }
 

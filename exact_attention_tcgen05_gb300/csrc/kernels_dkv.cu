@@ -21,15 +21,14 @@ static cudaError_t launch_dkv_t(const Maps& m, const Shape& s, const void* q,
   p.out0 = dk;
   p.out1 = dv;
   p.N = s.N;
-  p.nb = (s.N + kTileM - 1) / kTileM;
   p.Nk = s.Nk;
-  p.nkb = (s.Nk + kTileN - 1) / kTileN;
-  p.off = s.Nk - s.N;
+  p.vl = s.vl;
   p.causal = s.causal ? 1 : 0;
   p.scale = s.scale;
   p.scale_log2 = s.scale * kLog2e;
   p.wait_limit = s.wait_limit;
-  dim3 grid(p.nkb, s.BH);  // one CTA per key block
+  // One CTA per 128-key block (packed batches: of the longest sequence).
+  dim3 grid((s.Nk + kTileN - 1) / kTileN, s.BH);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(m.q, m.k, m.v, m.d_o, p);
   return cudaGetLastError();
 }

@@ -21,15 +21,14 @@ static cudaError_t launch_dq_t(const Maps& m, const Shape& s, const void* q,
   p.out0 = dq;
   p.out1 = nullptr;
   p.N = s.N;
-  p.nb = (s.N + kTileM - 1) / kTileM;
   p.Nk = s.Nk;
-  p.nkb = (s.Nk + kTileN - 1) / kTileN;
-  p.off = s.Nk - s.N;
+  p.vl = s.vl;
   p.causal = s.causal ? 1 : 0;
   p.scale = s.scale;
   p.scale_log2 = s.scale * kLog2e;
   p.wait_limit = s.wait_limit;
-  dim3 grid(p.nb, s.BH);
+  // One CTA per 128-row query block (packed batches: of the longest sequence).
+  dim3 grid((s.N + kTileM - 1) / kTileM, s.BH);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(m.q, m.k, m.v, m.d_o, p);
   return cudaGetLastError();
 }

@@ -17,13 +17,12 @@ static cudaError_t launch_fwd_t(const Maps& m, const Shape& s, void* o, float* l
   p.lse = lse;
   p.N = s.N;
   p.Nk = s.Nk;
-  p.off = s.Nk - s.N;
-  p.nkb = (s.Nk + kTileN - 1) / kTileN;
-  p.nqb = (s.N + 2 * kTileM - 1) / (2 * kTileM);
   p.causal = s.causal ? 1 : 0;
   p.scale_log2 = s.scale * kLog2e;
   p.wait_limit = s.wait_limit;
-  dim3 grid(p.nqb, s.BH);
+  p.vl = s.vl;
+  // Packed batches: s.N is the longest query sequence; CTAs past a sequence's end exit.
+  dim3 grid((s.N + 2 * kTileM - 1) / (2 * kTileM), s.BH);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(m.q, m.k, m.v, p);
   return cudaGetLastError();
 }

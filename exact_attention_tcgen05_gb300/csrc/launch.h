@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "varlen.h"
+
 namespace attn {
 
 // TMA descriptors of the [B*H, N, d] 16-bit tensors a kernel reads.
@@ -13,11 +15,12 @@ struct Maps {
 };
 
 struct Shape {
-  int BH, N, d;  // N: query rows per slice (N_q)
+  int BH, N, d;  // N: query rows per slice (N_q); packed batches: the longest sequence
   int Nk;        // key rows per slice (N_k); causal masking is bottom-right aligned
   bool bf16, causal;
   float scale;
   unsigned long long wait_limit;  // SM cycles one pipeline wait may take
+  Varlen vl;     // packed variable-length batch; vl.cu_q == nullptr for dense tensors
 };
 
 cudaError_t launch_fwd(const Maps& m, const Shape& s, void* o, float* lse, cudaStream_t st);

@@ -150,3 +150,113 @@ def sampled_slices(w: Workload, count: Optional[int] = None) -> list[tuple[int, 
 def to_f64(x: torch.Tensor):
     """Exact upcast of rounded 16-bit values to a float64 numpy array."""
     return x.detach().to("cpu").to(torch.float64).numpy()
+
+
+# ------------------------------------------------------------------------------------
+# Packed variable-length batches: sequences one after another along the token axis,
+# q, k, v, dO as [total, H, d], boundaries as cu_seqlens (B + 1 cumulative lengths).
+# ------------------------------------------------------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class VarlenWorkload:
+    """A packed batch of sequences of different lengths (query and key lengths per
+    sequence), 16-bit type, mask and seed."""
+
+    name: str
+    H: int
+    d: int
+    dtype: str
+    causal: bool
+    seed: int
+    seqlens_q: tuple
+    seqlens_k: tuple
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return _DTYPES[self.dtype]
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def B(self) -> int:
+        return len(self.seqlens_q)
+
+    @staticmethod
+    def _cu(lengths) -> list[int]:
+        out = [0]
+        for n in lengths:
+            out.append(out[-1] + int(n))
+        return out
+
+    @property
+    def cu_q(self) -> list[int]:
+        return self._cu(self.seqlens_q)
+
+    @property
+    def cu_k(self) -> list[int]:
+        return self._cu(self.seqlens_k)
+
+    @property
+    def total_q(self) -> int:
+        return sum(self.seqlens_q)
+
+    @property
+    def total_k(self) -> int:
+        return sum(self.seqlens_k)
+
+    @property
+    def max_q(self) -> int:
+        return max(self.seqlens_q)
+
+    @property
+    def max_k(self) -> int:
+        return max(self.seqlens_k)
+
+
+def length_mix(total: int, lo: int, hi: int, seed: int) -> tuple:
+    """Seeded sequence lengths drawn uniformly from [lo, hi] until they add up to
+    `total` (the last one is cut to fit; a cut below 1 is dropped)."""
+    g = torch.Generator().manual_seed(seed * 7 + 5)
+    out = []
+    left = total
+    while left > 0:
+        n = int(torch.randint(lo, hi + 1, (1,), generator=g))
+        out.append(min(n, left))
+        left -= out[-1]
+    return tuple(out)
+
+
+def varlen(H: int, d: int, dtype: str, causal: bool, seed: int, seqlens_q, seqlens_k=None,
+           name: Optional[str] = None) -> VarlenWorkload:
+    """A packed workload with the given per-sequence lengths (keys = queries if absent)."""
+    seqlens_q = tuple(int(n) for n in seqlens_q)
+    seqlens_k = seqlens_q if seqlens_k is None else tuple(int(n) for n in seqlens_k)
+    if len(seqlens_k) != len(seqlens_q):
+        raise ValueError("one key length per sequence")
+    if name is None:
+        name = (f"varlen_B{len(seqlens_q)}_H{H}_T{sum(seqlens_q)}_d{d}_{dtype}_"
+                f"{'causal' if causal else 'full'}_s{seed}")
+    return VarlenWorkload(name, H, d, dtype, causal, seed, seqlens_q, seqlens_k)
+
+
+# The packed benchmark batch: 16384 tokens (the token count of B4 x N4096) in sequences
+# of 512 .. 4096 tokens, 32 heads, d = 128, bf16, causal.
+VARLEN_BENCH = varlen(32, 128, "bf16", True, 1010, length_mix(16384, 512, 4096, 1010),
+                      name="varlen_H32_T16384_len512-4096_d128_bf16_causal")
+
+
+def make_varlen_tensor(w: VarlenWorkload, tensor: str) -> torch.Tensor:
+    """The packed [total, H, d] tensor on the CPU: rows cu[b] .. cu[b+1] of head h come
+    from the generator of slice (b, h) of `tensor` (as for the dense workloads: fp32
+    N(0, 1), one rounding to the 16-bit type)."""
+    lengths = w.seqlens_q if tensor in ("q", "do") else w.seqlens_k
+    cu = VarlenWorkload._cu(lengths)
+    out = torch.empty(cu[-1], w.H, w.d, dtype=w.torch_dtype)
+    for b, n in enumerate(lengths):
+        for h in range(w.H):
+            g = torch.Generator().manual_seed(slice_seed(w.seed, b, h, w.H, tensor))
+            out[cu[b]:cu[b + 1], h] = torch.randn(n, w.d, generator=g,
+                                                  dtype=torch.float32).to(w.torch_dtype)
+    return out

@@ -123,6 +123,42 @@ attn_status attn_bwd_qk(const void* q, const void* k, const void* v, const void*
                         attn_dtype dtype, int causal, float scale, void* cuda_stream);
 
 /*
+ * attn_fwd_varlen / attn_bwd_varlen - attn_fwd and attn_bwd over a batch of sequences of
+ * different lengths packed along the token axis, with no padding ("FlashAttentionを1から
+ * — 計算を増やして速くする逆説", section 現場ではこう使う: padding sentences to the
+ * longest one pays for the padded positions; the variable-length interface takes the
+ * boundaries as cu_seqlens instead).
+ *   q, o, dO, dq        [total_q, H, d] 16-bit, token-major (d innermost);
+ *   k, v, dk, dv        [total_k, H, d];
+ *   lse, workspace      [H, total_q] float32 (attn_bwd_varlen_workspace_bytes);
+ *   cu_seqlens_q/_k     int32 [B + 1] in DEVICE memory, 4-byte aligned: sequence b owns
+ *                       query tokens cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key tokens
+ *                       cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1;
+ *   max_seqlen_q/_k     bounds on every sequence's query / key count (1 .. 1048576, at
+ *                       most the totals); the grids cover this many rows per sequence.
+ * Each (sequence, head) pair is its own attention problem; causal masking is bottom-right
+ * aligned within the sequence, as for attn_fwd_qk. Tokens outside every sequence are
+ * neither read as queries nor written. A sequence with keys and no queries gets zero dk,
+ * dv. The sizes are checked on the host (ATTN_ERR_INVALID_ARG / ATTN_ERR_UNSUPPORTED as
+ * for attn_fwd). cu_seqlens are read on the device, without synchronising: a sequence
+ * that leaves its tensor, exceeds max_seqlen, has queries but no key, or (causal) fewer
+ * keys than queries is skipped (its outputs are not written) and attn_last_kernel_status
+ * then returns ATTN_ERR_INVALID_ARG.
+ */
+size_t attn_bwd_varlen_workspace_bytes(int H, int total_q); /* 4 * H * total_q; 0 if invalid */
+attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
+                            int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                            int d, attn_dtype dtype, int causal, float scale,
+                            void* cuda_stream);
+attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                            void* workspace, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                            int B, int H, int total_q, int total_k, int max_seqlen_q,
+                            int max_seqlen_k, int d, attn_dtype dtype, int causal, float scale,
+                            void* cuda_stream);
+
+/*
  * attn_bwd_preprocess - step 1 of attn_bwd alone: delta[b,h,i] = sum_c dO[b,h,i,c] *
  * o[b,h,i,c] in float32 ("Triton 05: Flash Attention", section 3단계 커널 구조,
  * [1단계] Preprocess). o, dO: [B, H, N, d] 16-bit device; delta: [B, H, N] float32
@@ -251,9 +287,10 @@ const char* attn_status_str(attn_status s);
 /*
  * attn_last_kernel_status - reads (with a blocking device-to-host copy on
  * cuda_stream, after the work queued before it) and clears the status word the
- * kernels set when a bounded pipeline wait runs out. Returns ATTN_OK when no wait
- * ran out since the last call, ATTN_ERR_TIMEOUT otherwise, ATTN_ERR_CUDA if the
- * copy fails. *where (may be NULL) receives the code of the first wait that gave up.
+ * kernels set when a bounded pipeline wait runs out or a packed batch holds a
+ * malformed sequence. Returns ATTN_OK when nothing was recorded since the last call,
+ * ATTN_ERR_INVALID_ARG for a malformed sequence (code 0x7E), ATTN_ERR_TIMEOUT for a
+ * wait, ATTN_ERR_CUDA if the copy fails. *where (may be NULL) receives the first code.
  */
 attn_status attn_last_kernel_status(void* cuda_stream, int* where);
 

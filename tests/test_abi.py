@@ -126,6 +126,46 @@ def test_bwd_qk_rejects_bad_arguments(lib, kw, code):
     assert bwd_qk(lib, **kw) == code
 
 
+CUQ, CUK = 0x10000000 + 10 * 64 * MB, 0x10000000 + 10 * 64 * MB + 4096
+
+
+def fwd_varlen(lib, q=Q, o=O, cu_q=CUQ, cu_k=CUK, B=4, H=2, Tq=1000, Tk=1200, mq=400, mk=500,
+               d=128, dt=1, scale=0.1):
+    return lib.attn_fwd_varlen(q, K, V, o, L, cu_q, cu_k, B, H, Tq, Tk, mq, mk, d, dt, 1, scale,
+                               None)
+
+
+def bwd_varlen(lib, dk=DK, ws=WS, cu_q=CUQ, Tq=1000, mq=400):
+    return lib.attn_bwd_varlen(Q, K, V, O, L, DO, DQ, dk, DV, ws, cu_q, CUK, 4, 2, Tq, 1200, mq,
+                               500, 128, 1, 1, 0.1, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cu_q=0), INVALID), (dict(cu_k=0), INVALID), (dict(cu_q=CUQ + 2), INVALID),
+    (dict(B=0), INVALID), (dict(Tq=0), INVALID), (dict(mq=0), INVALID),
+    (dict(mq=1001), INVALID),                    # longer than the whole packed tensor
+    (dict(mk=(1 << 20) + 1, Tk=1 << 21), INVALID), (dict(d=80), UNSUPPORTED),
+    (dict(scale=0.0), INVALID), (dict(q=Q + 8), INVALID),
+    (dict(o=Q + 1000 * 2 * 128 * 2 - 16), INVALID),  # o overlaps the tail of q
+    (dict(o=CUQ - 16), INVALID),                    # o overlaps cu_seqlens_q
+])
+def test_fwd_varlen_rejects_bad_arguments(lib, kw, code):
+    assert fwd_varlen(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ws=0), INVALID), (dict(dk=DV + 16), INVALID), (dict(ws=CUK), INVALID),
+    (dict(mq=2000), INVALID),
+])
+def test_bwd_varlen_rejects_bad_arguments(lib, kw, code):
+    assert bwd_varlen(lib, **kw) == code
+
+
+def test_varlen_workspace_bytes(lib):
+    assert lib.attn_bwd_varlen_workspace_bytes(32, 16384) == 4 * 32 * 16384
+    assert lib.attn_bwd_varlen_workspace_bytes(0, 5) == 0
+
+
 def test_stage_entry_points_reject_bad_arguments(lib):
     dkv = lambda dk=DK, dv=DV, d=128, lse=L: lib.attn_bwd_dkv(Q, K, V, lse, WS, DO, dk, dv, 1, 1,
                                                               256, d, 1, 1, 0.1, None)
