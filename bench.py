@@ -327,6 +327,8 @@ def run_ours(args) -> None:
     }
     if not args.no_decode:
         line["decode"] = measure_decode(args, peaks)
+    if not args.no_varlen:
+        line["varlen"] = measure_varlen(args, peaks)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w)
     print(json.dumps(line), flush=True)
@@ -391,6 +393,80 @@ def measure_decode(args, peaks: dict) -> dict:
     return out
 
 
+def measure_varlen(args, peaks: dict) -> dict:
+    """The packed benchmark batch (sequences of different lengths, no padding) through
+    attn_fwd_varlen + attn_bwd_varlen, next to the same sequences padded to the longest
+    one as a dense [B, H, max, d] batch through attn_fwd + attn_bwd. Both are credited
+    with the same useful FLOPs (those of the real sequences)."""
+    import torch
+    from exact_attention_tcgen05_gb300 import binding
+    from exact_attention_tcgen05_gb300 import inputs as I
+
+    w = I.VARLEN_BENCH
+    q, k, v, do = (I.make_varlen_tensor(w, t).cuda() for t in ("q", "k", "v", "do"))
+    cu_q = torch.tensor(w.cu_q, dtype=torch.int32, device="cuda")
+    cu_k = torch.tensor(w.cu_k, dtype=torch.int32, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty(w.H, w.total_q, dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(k)
+    ws = torch.empty_like(lse)
+    # The padded batch: sequence b in rows [0, n_b) of slice b, zeros after it.
+    B, H, M, d = w.B, w.H, w.max_q, w.d
+    pq, pk, pv, pdo = (torch.zeros(B, H, M, d, dtype=q.dtype, device="cuda") for _ in range(4))
+    for b in range(B):
+        r0, r1 = w.cu_q[b], w.cu_q[b + 1]
+        for src, dst in ((q, pq), (k, pk), (v, pv), (do, pdo)):
+            dst[b, :, : r1 - r0] = src[r0:r1].transpose(0, 1)
+    po = torch.empty_like(pq)
+    plse = torch.empty(B, H, M, dtype=torch.float32, device="cuda")
+    pdq, pdk, pdv = torch.empty_like(pq), torch.empty_like(pq), torch.empty_like(pq)
+    pws = torch.empty_like(plse)
+    stream = torch.cuda.current_stream()
+
+    def packed():
+        binding.attn_fwd_varlen(q, k, v, cu_q, cu_k, w.max_q, w.max_k, causal=w.causal,
+                                scale=w.scale, o=o, lse=lse)
+        binding.attn_bwd_varlen(q, k, v, o, lse, do, cu_q, cu_k, w.max_q, w.max_k,
+                                causal=w.causal, scale=w.scale, dq=dq, dk=dk, dv=dv,
+                                workspace=ws)
+
+    def padded():
+        binding.attn_fwd(pq, pk, pv, causal=w.causal, scale=w.scale, o=po, lse=plse)
+        binding.attn_bwd(pq, pk, pv, po, plse, pdo, causal=w.causal, scale=w.scale, dq=pdq,
+                         dk=pdk, dv=pdv, workspace=pws)
+
+    n = max(10, min(args.steps, 50))
+    result = {}
+    for name, fn in (("packed", packed), ("padded", padded)):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        ev[0].record(stream)
+        for i in range(n):
+            fn()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        result[name] = ev[0].elapsed_time(ev[n]) / n
+    code, where = binding.attn_last_kernel_status()
+    if code != binding.ATTN_OK:
+        raise RuntimeError(f"a packed-batch kernel reported status {code} (site {where:#x})")
+    # useful FLOPs: forward 4*H*n^2*d per sequence (halved causal), backward 2.5x
+    f_fwd = sum(4.0 * H * n_b * n_b * d for n_b in w.seqlens_q) / (2 if w.causal else 1)
+    useful = 3.5 * f_fwd
+    out = {"workload": w.name, "sequences": B, "lengths": list(w.seqlens_q),
+           "tokens": w.total_q, "steps": n,
+           "packed": {"ms_per_step": result["packed"],
+                      "tflops": useful / (result["packed"] * 1e-3) / 1e12},
+           "padded": {"shape": f"B{B} H{H} N{M} d{d}", "ms_per_step": result["padded"],
+                      "tflops_useful": useful / (result["padded"] * 1e-3) / 1e12},
+           "speedup_vs_padded": result["padded"] / result["packed"],
+           "frac_of_peak": useful / (result["packed"] * 1e-3) / 1e12 / peaks["bf16_tflops"]}
+    del q, k, v, do, o, dq, dk, dv, pq, pk, pv, pdo, po, pdq, pdk, pdv
+    torch.cuda.empty_cache()
+    return out
+
+
 def load_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it matches this kernel
     and workload (profiles/traffic.json); else None."""
@@ -413,7 +489,7 @@ KERNEL_SOURCES = {
     "dkv": ["bwd_dkv.cuh", "bwd_dq.cuh", "kernels_dkv.cu"],
     "dq": ["bwd_dq.cuh", "kernels_dq.cu"],
 }
-COMMON_SOURCES = ["common.cuh", "ptx.cuh", "launch.h"]
+COMMON_SOURCES = ["common.cuh", "ptx.cuh", "launch.h", "varlen.h"]
 
 
 def source_hash(kernel: str) -> str:
@@ -474,6 +550,7 @@ def main() -> None:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-varlen", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -46,9 +46,9 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
 }
 
 // rows = B*H*N; o, dO: rows x D 16-bit; delta: rows f32, row r at delta[r].
-// Packed batch (heads > 0): rows = total*H in [total, H] order, and the D of row
+// Packed batch (PACKED): rows = total*H in [total, H] order, and the D of row
 // r = t*H + h goes to delta[h*total + t] (the [H, total] layout of lse).
-template <int D, bool BF16>
+template <int D, bool BF16, bool PACKED>
 __global__ void __launch_bounds__(kDeltaThreads)
     attn_bwd_delta_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO,
                           float* __restrict__ delta, long long rows, int heads,
@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(kDeltaThreads)
         acc += __shfl_xor_sync(0xffffffffu, acc, off);
       const long long row = r0 + u * kRowsPerWarp + sub;
       if (part == 0 && row < rows)
-        delta[heads > 0 ? (row % heads) * total + row / heads : row] = acc;
+        delta[PACKED ? (row % heads) * total + row / heads : row] = acc;
     }
   }
 }

@@ -40,7 +40,7 @@ struct DkvCfg : BwdCfg<D> {
       (kOffMisc + 16 + 1024) > B::kMinSmem ? (kOffMisc + 16 + 1024) : B::kMinSmem;
 };
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool PACKED>
 __global__ void __launch_bounds__(320, 1)
     attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k,
@@ -70,12 +70,12 @@ __global__ void __launch_bounds__(320, 1)
   const int lane = lane_id();
   const int bh = blockIdx.y;
   SliceRows sl;
-  if (!slice_rows(p.vl, bh, p.N, p.Nk, D, p.causal != 0, sl)) return;
+  if (!slice_rows<PACKED>(p.vl, bh, p.N, p.Nk, D, p.causal != 0, sl)) return;
   const int N = sl.nq, Nk = sl.nk, off = sl.off;
   const int jb = blockIdx.x;  // causal: block 0 sees the most query blocks, so runs first
-  if (jb * kTileN >= Nk) return;  // packed batch: past this sequence's keys
+  if (PACKED && jb * kTileN >= Nk) return;  // past this sequence's keys
   const int j0 = jb * kTileN;
-  if (N == 0) {
+  if (PACKED && N == 0) {
     // A packed sequence with keys but no queries: no query sees these keys, so their
     // gradients are zero.
     const int rows = min(kTileN, Nk - j0);
@@ -130,10 +130,10 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_map(&map_do);
       mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
       for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_rows(smem + C::kOffK + c * kBoxBytes, &map_k, kv_full, c * kBoxCols, j0, sl,
-                      true);
-        tma_load_rows(smem + C::kOffV + c * kBoxBytes, &map_v, kv_full, c * kBoxCols, j0, sl,
-                      true);
+        tma_load_rows<PACKED>(smem + C::kOffK + c * kBoxBytes, &map_k, kv_full, c * kBoxCols,
+                              j0, sl, true);
+        tma_load_rows<PACKED>(smem + C::kOffV + c * kBoxBytes, &map_v, kv_full, c * kBoxCols,
+                              j0, sl, true);
       }
     }
     __syncwarp();
@@ -147,12 +147,12 @@ __global__ void __launch_bounds__(320, 1)
       if (elect_one()) {
         mbar_arrive_expect_tx(&q_full[s], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_rows(smem + C::kOffQ + s * C::kTileBytes + c * kBoxBytes, &map_q,
-                        &q_full[s], c * kBoxCols, i * kTileM, sl, false);
+          tma_load_rows<PACKED>(smem + C::kOffQ + s * C::kTileBytes + c * kBoxBytes, &map_q,
+                                &q_full[s], c * kBoxCols, i * kTileM, sl, false);
         mbar_arrive_expect_tx(&do_full[s], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_rows(smem + C::kOffDO + s * C::kTileBytes + c * kBoxBytes, &map_do,
-                        &do_full[s], c * kBoxCols, i * kTileM, sl, false);
+          tma_load_rows<PACKED>(smem + C::kOffDO + s * C::kTileBytes + c * kBoxBytes, &map_do,
+                                &do_full[s], c * kBoxCols, i * kTileM, sl, false);
       }
       __syncwarp();
       issued = it + 1;

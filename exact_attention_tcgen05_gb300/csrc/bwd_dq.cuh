@@ -133,7 +133,7 @@ __device__ __forceinline__ void issue_tmem_a(uint32_t d_tmem, uint32_t a_tmem, u
            (acc || kk > 0) ? 1u : 0u);
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool PACKED>
 __global__ void __launch_bounds__(320, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q,
                        const __grid_constant__ CUtensorMap map_k,
@@ -161,11 +161,11 @@ __global__ void __launch_bounds__(320, 1)
   const int lane = lane_id();
   const int bh = blockIdx.y;
   SliceRows sl;
-  if (!slice_rows(p.vl, bh, p.N, p.Nk, D, p.causal != 0, sl)) return;
+  if (!slice_rows<PACKED>(p.vl, bh, p.N, p.Nk, D, p.causal != 0, sl)) return;
   const int N = sl.nq, Nk = sl.nk, off = sl.off;
   const int nb = (N + kTileM - 1) / kTileM;
   const int nkb = (Nk + kTileN - 1) / kTileN;
-  if ((int)blockIdx.x >= nb) return;  // packed batch: past this sequence's query blocks
+  if (PACKED && (int)blockIdx.x >= nb) return;  // past this sequence's query blocks
   const int ib = p.causal ? (nb - 1 - blockIdx.x) : blockIdx.x;  // longest first
   const int i0 = ib * kTileM;
   // key blocks 0 .. n-1 (causal: up to the block of the last key the tile's last row sees)
@@ -212,12 +212,12 @@ __global__ void __launch_bounds__(320, 1)
       if (elect_one()) {
         mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_rows(smem + C::kOffK + s * C::kTileBytes + c * kBoxBytes, &map_k,
-                        &k_full[s], c * kBoxCols, j * kTileN, sl, true);
+          tma_load_rows<PACKED>(smem + C::kOffK + s * C::kTileBytes + c * kBoxBytes, &map_k,
+                                &k_full[s], c * kBoxCols, j * kTileN, sl, true);
         mbar_arrive_expect_tx(&v_full[s], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_rows(smem + C::kOffV + s * C::kTileBytes + c * kBoxBytes, &map_v,
-                        &v_full[s], c * kBoxCols, j * kTileN, sl, true);
+          tma_load_rows<PACKED>(smem + C::kOffV + s * C::kTileBytes + c * kBoxBytes, &map_v,
+                                &v_full[s], c * kBoxCols, j * kTileN, sl, true);
       }
       __syncwarp();
       issued = j + 1;

@@ -51,12 +51,15 @@ struct SliceRows {
   size_t stat0;             // index of row 0 in lse and D
 };
 
-// Fills `s` for slice bh. Dense: the whole-call sizes N, Nk. Packed: reads the slice's
-// sequence bounds and checks them (in range, not longer than the grid covers, and every
-// query row sees a key); a malformed sequence records kErrSeqlens and returns false.
+// Fills `s` for slice bh. Dense (PACKED = false): the whole-call sizes N, Nk. Packed:
+// reads the slice's sequence bounds and checks them (in range, not longer than the grid
+// covers, and every query row sees a key); a malformed sequence records kErrSeqlens and
+// returns false. The layout is a template parameter so that the dense kernels carry no
+// trace of the packed addressing.
+template <bool PACKED>
 __device__ __forceinline__ bool slice_rows(const Varlen& vl, int bh, int N, int Nk, int D,
                                            bool causal, SliceRows& s) {
-  if (vl.cu_q == nullptr) {
+  if constexpr (!PACKED) {
     s.nq = N;
     s.nk = Nk;
     s.q_start = s.k_start = 0;
@@ -94,9 +97,10 @@ __device__ __forceinline__ bool slice_rows(const Varlen& vl, int bh, int N, int 
 
 // TMA copy of one [128 rows x 64 cols] box of a slice, starting at slice row `row`
 // (`keys`: a k-like tensor), in the slice's layout (see SliceRows).
+template <bool PACKED>
 __device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* map, uint64_t* bar,
                                               int col, int row, const SliceRows& s, bool keys) {
-  if (s.packed)
+  if constexpr (PACKED)
     tma_load_3d(dst, map, bar, col, s.tma_bh, (keys ? s.k_start : s.q_start) + row);
   else
     tma_load_3d(dst, map, bar, col, row, s.tma_bh);

@@ -70,7 +70,7 @@ struct FwdCfg {
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
 };
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool PACKED>
 __global__ void __launch_bounds__(320, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_k,
@@ -94,11 +94,11 @@ __global__ void __launch_bounds__(320, 1)
   const int lane = lane_id();
   const int bh = blockIdx.y;
   SliceRows sl;
-  if (!slice_rows(p.vl, bh, p.N, p.Nk, D, p.causal != 0, sl)) return;
+  if (!slice_rows<PACKED>(p.vl, bh, p.N, p.Nk, D, p.causal != 0, sl)) return;
   const int N = sl.nq, Nk = sl.nk, off = sl.off;
   const int nqb = (N + 2 * kTileM - 1) / (2 * kTileM);
   const int nkb = (Nk + kTileN - 1) / kTileN;
-  if ((int)blockIdx.x >= nqb) return;  // packed batch: past this sequence's query blocks
+  if (PACKED && (int)blockIdx.x >= nqb) return;  // past this sequence's query blocks
   const int qb = nqb - 1 - blockIdx.x;  // within a head, longest (most key blocks) first
   const int q0 = qb * 256;
   const int ntiles = (q0 + kTileM < N) ? 2 : 1;
@@ -147,8 +147,8 @@ __global__ void __launch_bounds__(320, 1)
       mbar_arrive_expect_tx(q_full, ntiles * C::kTileBytes);
       for (int t = 0; t < ntiles; ++t)
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_rows(smem + C::kOffQ + t * C::kTileBytes + c * kBoxBytes, &map_q, q_full,
-                        c * kBoxCols, q0 + t * kTileM, sl, false);
+          tma_load_rows<PACKED>(smem + C::kOffQ + t * C::kTileBytes + c * kBoxBytes, &map_q,
+                                q_full, c * kBoxCols, q0 + t * kTileM, sl, false);
     }
     __syncwarp();
     int issued = 0;
@@ -161,12 +161,12 @@ __global__ void __launch_bounds__(320, 1)
       if (elect_one()) {
         mbar_arrive_expect_tx(&k_full[s], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_rows(smem + C::kOffK + s * C::kTileBytes + c * kBoxBytes, &map_k,
-                        &k_full[s], c * kBoxCols, j * kTileN, sl, true);
+          tma_load_rows<PACKED>(smem + C::kOffK + s * C::kTileBytes + c * kBoxBytes, &map_k,
+                                &k_full[s], c * kBoxCols, j * kTileN, sl, true);
         mbar_arrive_expect_tx(&v_full[s], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_rows(smem + C::kOffV + s * C::kTileBytes + c * kBoxBytes, &map_v,
-                        &v_full[s], c * kBoxCols, j * kTileN, sl, true);
+          tma_load_rows<PACKED>(smem + C::kOffV + s * C::kTileBytes + c * kBoxBytes, &map_v,
+                                &v_full[s], c * kBoxCols, j * kTileN, sl, true);
       }
       __syncwarp();
       issued = j + 1;

@@ -22,9 +22,11 @@ static cudaError_t launch_delta_t(const Shape& s, const void* o, const void* dO,
   const int resident = 2048 / kDeltaThreads;  // blocks per SM at full occupancy
   const long long cap = (long long)sm_count_current() * resident;
   const int blocks = (int)(want < cap ? want : cap);
-  attn_bwd_delta_kernel<D, BF16><<<blocks, kDeltaThreads, 0, st>>>(
-      reinterpret_cast<const uint4*>(o), reinterpret_cast<const uint4*>(dO), delta, rows,
-      packed ? s.vl.H : 0, packed ? (long long)s.vl.total_q : 0);
+  auto kern = packed ? attn_bwd_delta_kernel<D, BF16, true> : attn_bwd_delta_kernel<D, BF16, false>;
+  kern<<<blocks, kDeltaThreads, 0, st>>>(reinterpret_cast<const uint4*>(o),
+                                         reinterpret_cast<const uint4*>(dO), delta, rows,
+                                         packed ? s.vl.H : 0,
+                                         packed ? (long long)s.vl.total_q : 0);
   return cudaGetLastError();
 }
 

@@ -9,7 +9,8 @@ static cudaError_t launch_dq_t(const Maps& m, const Shape& s, const void* q,
                                const void* d_o, const float* lse,
                                const float* delta, void* dq, cudaStream_t st) {
   using C = DqCfg<D>;
-  auto kern = attn_bwd_dq_kernel<D, BF16>;
+  auto kern = s.vl.cu_q != nullptr ? attn_bwd_dq_kernel<D, BF16, true>
+                                   : attn_bwd_dq_kernel<D, BF16, false>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;

@@ -8,7 +8,8 @@ template <int D, bool BF16>
 static cudaError_t launch_fwd_t(const Maps& m, const Shape& s, void* o, float* lse,
                                 cudaStream_t st) {
   using C = FwdCfg<D>;
-  auto kern = attn_fwd_kernel<D, BF16>;
+  auto kern = s.vl.cu_q != nullptr ? attn_fwd_kernel<D, BF16, true>
+                                   : attn_fwd_kernel<D, BF16, false>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
