@@ -58,8 +58,8 @@ struct FwdCfg {
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
   // barriers: q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2],
-  // o_done[2], drain
-  static constexpr int kNumBars = 1 + 3 * kStages + 6 + 1;
+  // o_done[2], drain, s_free[2]
+  static constexpr int kNumBars = 1 + 3 * kStages + 6 + 1 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
   // All 512 tensor-memory columns per CTA: one CTA per SM, which the shared memory
@@ -68,6 +68,12 @@ struct FwdCfg {
   static constexpr int kThreads = 320;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+  // d = 64: P gets tensor-memory columns of its own (S0 S1 O0 O1 P0 P1 fill the 512), so
+  // S of the next key block is computed while the softmax still works on this one: it
+  // waits only until the softmax warps have read S into registers (s_free), not for P V.
+  // At d = 128 S and O fill all 512 columns and P is written over S.
+  static constexpr bool kOwnP = (D == 64);
+  static constexpr uint32_t kColP0 = 256 + 2 * D, kColP1 = 256 + 2 * D + 64;
 };
 
 template <int D, bool BF16, bool PACKED>
@@ -87,6 +93,7 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* p_full = s_full + 2;
   uint64_t* o_done = p_full + 2;
   uint64_t* drain = o_done + 2;
+  uint64_t* s_free = drain + 1;  // [2]: the softmax warps have read S_t (own-P layout)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -122,6 +129,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], 4);  // one arrival per softmax warp
       mbar_init(&o_done[t], 1);
+      mbar_init(&s_free[t], 4);  // one arrival per softmax warp
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -191,13 +199,15 @@ __global__ void __launch_bounds__(320, 1)
     constexpr uint32_t kStep = C::kTileBytes >> 4;
     const uint32_t col_s[2] = {C::kColS0, C::kColS1};
     const uint32_t col_o[2] = {C::kColO0, C::kColO1};
+    const uint32_t col_p[2] = {C::kOwnP ? C::kColP0 : C::kColS0,
+                               C::kOwnP ? C::kColP1 : C::kColS1};  // P: own columns or over S
     auto issue_s = [&](int t, int stage) {
       issue_rowdot_d<D>(tmem + col_s[t], dq0 + t * kStep, dk0 + stage * kStep, idesc_s);
     };
     auto issue_pv = [&](int t, int stage, bool acc) {
 #pragma unroll
       for (int kk = 0; kk < kTileN / 16; ++kk)
-        mma_ts(tmem + col_o[t], tmem + col_s[t] + kk * 8,
+        mma_ts(tmem + col_o[t], tmem + col_p[t] + kk * 8,
                dv0 + stage * kStep + ((kk * 2048) >> 4), idesc_o, (acc || kk > 0) ? 1u : 0u);
     };
 
@@ -214,41 +224,85 @@ __global__ void __launch_bounds__(320, 1)
       }
       __syncwarp();
     }
-    for (int j = 0; ok && j < n_kv; ++j) {
-      const int s = j % C::kStages;
-      if (!(ok = warp_poll(&v_full[s], (j / C::kStages) & 1, limit, abort_flag, kWaitFwdV)))
-        break;
-      tc_fence_after();
-      const int jn = j + 1;
-      const int sn = jn % C::kStages;
-      bool next_k_ready = false;
-      for (int t = 0; t < 2 && ok; ++t) {
-        if (j >= nkv[t]) continue;
-        if (!(ok = warp_poll(&p_full[t], j & 1, limit, abort_flag, kWaitFwdP))) break;
-        tc_fence_after();
-        if (elect_one()) {
-          issue_pv(t, s, j > 0);
-          mma_commit(&o_done[t]);
-        }
-        __syncwarp();
-        if (jn < nkv[t]) {
+    if constexpr (C::kOwnP) {
+      // Per key block j: S(t, j+1) for both tiles as soon as each softmax has read S(t, j),
+      // then P(t, j) V_j as each P is ready.
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int s = j % C::kStages;
+        const int jn = j + 1;
+        const int sn = jn % C::kStages;
+        bool next_k_ready = false;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (jn >= nkv[t]) continue;
           if (!next_k_ready) {
             if (!(ok = warp_poll(&k_full[sn], (jn / C::kStages) & 1, limit, abort_flag,
                                  kWaitFwdK)))
               break;
-            tc_fence_after();
             next_k_ready = true;
           }
+          if (!(ok = warp_poll(&s_free[t], j & 1, limit, abort_flag, kWaitFwdX))) break;
+          tc_fence_after();
           if (elect_one()) {
             issue_s(t, sn);
             mma_commit(&s_full[t]);
           }
           __syncwarp();
         }
+        if (!ok) break;
+        if (!(ok = warp_poll(&v_full[s], (j / C::kStages) & 1, limit, abort_flag, kWaitFwdV)))
+          break;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= nkv[t]) continue;
+          if (!(ok = warp_poll(&p_full[t], j & 1, limit, abort_flag, kWaitFwdP))) break;
+          tc_fence_after();
+          if (elect_one()) {
+            issue_pv(t, s, j > 0);
+            mma_commit(&o_done[t]);
+          }
+          __syncwarp();
+        }
+        if (ok) {
+          if (elect_one()) mma_commit(&kv_empty[s]);
+          __syncwarp();
+        }
       }
-      if (ok) {
-        if (elect_one()) mma_commit(&kv_empty[s]);
-        __syncwarp();
+    } else {
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int s = j % C::kStages;
+        if (!(ok = warp_poll(&v_full[s], (j / C::kStages) & 1, limit, abort_flag, kWaitFwdV)))
+          break;
+        tc_fence_after();
+        const int jn = j + 1;
+        const int sn = jn % C::kStages;
+        bool next_k_ready = false;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= nkv[t]) continue;
+          if (!(ok = warp_poll(&p_full[t], j & 1, limit, abort_flag, kWaitFwdP))) break;
+          tc_fence_after();
+          if (elect_one()) {
+            issue_pv(t, s, j > 0);
+            mma_commit(&o_done[t]);
+          }
+          __syncwarp();
+          if (jn < nkv[t]) {
+            if (!next_k_ready) {
+              if (!(ok = warp_poll(&k_full[sn], (jn / C::kStages) & 1, limit, abort_flag,
+                                   kWaitFwdK)))
+                break;
+              tc_fence_after();
+              next_k_ready = true;
+            }
+            if (elect_one()) {
+              issue_s(t, sn);
+              mma_commit(&s_full[t]);
+            }
+            __syncwarp();
+          }
+        }
+        if (ok) {
+          if (elect_one()) mma_commit(&kv_empty[s]);
+          __syncwarp();
+        }
       }
     }
     // Every MMA issued must finish before tensor memory is released.
@@ -262,6 +316,7 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const uint32_t t_s = tmem + lane_base + (t == 0 ? C::kColS0 : C::kColS1);
     const uint32_t t_o = tmem + lane_base + (t == 0 ? C::kColO0 : C::kColO1);
+    const uint32_t t_p = C::kOwnP ? tmem + lane_base + (t == 0 ? C::kColP0 : C::kColP1) : t_s;
     const int row = q0 + t * kTileM + wq * 32 + lane;  // query index of this thread
     const int tile_row0 = q0 + t * kTileM;
     const float sl2 = p.scale_log2;
@@ -269,12 +324,30 @@ __global__ void __launch_bounds__(320, 1)
     float l = 0.f;        // sum of exp2 values (fp32)
     float lr = 0.f;       // sum of the same values after rounding to 16 bits
     bool ok = true;
+    // O *= alpha in tensor memory (the previous P V product must have landed).
+    auto rescale_o = [&](float alpha) {
+#pragma unroll
+      for (int cc = 0; cc < D / 64; ++cc) {
+        uint32_t r[64];
+        tmem_ld64(t_o + cc * 64, r);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
+        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[32]);
+        tmem_st32(t_o + cc * 64, lo);
+        tmem_st32(t_o + cc * 64 + 32, hi);
+      }
+    };
     for (int j = 0; j < nkv[t]; ++j) {
       if (!(ok = warp_wait(&s_full[t], j & 1, limit, abort_flag, kWaitFwdS))) break;
       tc_fence_after();
       // One wide load of the whole score row, then a single wait.
       uint32_t sr[kTileN];
       tmem_ld128(t_s, sr);
+      if constexpr (C::kOwnP) {
+        tc_fence_before();
+        warp_arrive(&s_free[t]);  // S(t, j) is in registers: S(t, j + 1) may overwrite it
+      }
       float* s = reinterpret_cast<float*>(sr);
       const int kbase = j * kTileN;
       const bool diag = p.causal && (kbase + kTileN - 1 > tile_row0 + off);
@@ -308,6 +381,7 @@ __global__ void __launch_bounds__(320, 1)
       // Two sums, each in four independent packed accumulators.
       float2 sum[4];
       float rsum[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pall[C::kOwnP ? kTileN / 2 : 1];  // own-P layout: all of P before the store
 #pragma unroll
       for (int u = 0; u < 4; ++u) sum[u] = make_float2(0.f, 0.f);
 #pragma unroll
@@ -322,27 +396,33 @@ __global__ void __launch_bounds__(320, 1)
           pk[i] = pack2<BF16>(pp.x, pp.y);
           add_pair16<BF16>(rsum[(i & 1) * 2], rsum[(i & 1) * 2 + 1], pk[i]);
         }
-        tmem_st16(t_s + c4 * 16, pk);
+        if constexpr (C::kOwnP) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pall[c4 * 16 + i] = pk[i];
+        } else {
+          tmem_st16(t_s + c4 * 16, pk);
+        }
       }
       const float2 sa = add2(add2(sum[0], sum[1]), add2(sum[2], sum[3]));
       const float sum0 = sa.x, sum1 = sa.y, rsum0 = rsum[0] + rsum[1], rsum1 = rsum[2] + rsum[3];
       l = l * alpha + (sum0 + sum1);
       lr = lr * alpha + (rsum0 + rsum1);
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
+      if constexpr (C::kOwnP) {
+        // P V of the previous block reads P_t and accumulates into O_t: it must have
+        // finished before P_t is overwritten or O_t rescaled.
+        if (j > 0) {
+          if (!(ok = warp_wait(&o_done[t], (j - 1) & 1, limit, abort_flag, kWaitFwdO))) break;
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, need)) rescale_o(alpha);
+        }
+#pragma unroll
+        for (int c4 = 0; c4 < kTileN / 32; ++c4)
+          tmem_st16(t_p + c4 * 16, *reinterpret_cast<const uint32_t(*)[16]>(&pall[c4 * 16]));
+      } else if (j > 0 && __any_sync(0xffffffffu, need)) {
         // Bring O to the new max: wait until the previous P V product has landed.
         if (!(ok = warp_wait(&o_done[t], (j - 1) & 1, limit, abort_flag, kWaitFwdO))) break;
         tc_fence_after();
-#pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc) {
-          uint32_t r[64];
-          tmem_ld64(t_o + cc * 64, r);
-#pragma unroll
-          for (int i = 0; i < 64; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-          uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
-          uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[32]);
-          tmem_st32(t_o + cc * 64, lo);
-          tmem_st32(t_o + cc * 64 + 32, hi);
-        }
+        rescale_o(alpha);
       }
       tmem_st_wait();
       tc_fence_before();
