@@ -248,8 +248,8 @@ attn_status attn_bwd_dkv(const void* q, const void* k, const void* v, const floa
   const Shape s = make_shape(B, H, N, d, dtype, causal, scale);
   Maps m;
   if ((st = encode_bwd_maps(&m, q, k, v, dO, s)) != ATTN_OK) return st;
-  return from_cuda(
-      attn::launch_dkv(m, s, q, dO, lse, delta, dk, dv, static_cast<cudaStream_t>(cuda_stream)));
+  return from_cuda(attn::launch_dkv(m, s, q, k, v, dO, lse, delta, dk, dv,
+                                    static_cast<cudaStream_t>(cuda_stream)));
 }
 
 attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const float* lse,
@@ -295,7 +295,7 @@ attn_status attn_bwd_qk(const void* q, const void* k, const void* v, const void*
   cudaStream_t cs = static_cast<cudaStream_t>(cuda_stream);
   float* delta = static_cast<float*>(workspace);
   cudaError_t e = attn::launch_delta(s, o, dO, delta, cs);
-  if (e == cudaSuccess) e = attn::launch_dkv(m, s, q, dO, lse, delta, dk, dv, cs);
+  if (e == cudaSuccess) e = attn::launch_dkv(m, s, q, k, v, dO, lse, delta, dk, dv, cs);
   if (e == cudaSuccess) e = attn::launch_dq(m, s, q, dO, lse, delta, dq, cs);
   return from_cuda(e);
 }
@@ -407,7 +407,7 @@ attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const v
   cudaStream_t cs = static_cast<cudaStream_t>(cuda_stream);
   float* delta = static_cast<float*>(workspace);
   cudaError_t e = attn::launch_delta(s, o, dO, delta, cs);
-  if (e == cudaSuccess) e = attn::launch_dkv(m, s, q, dO, lse, delta, dk, dv, cs);
+  if (e == cudaSuccess) e = attn::launch_dkv(m, s, q, k, v, dO, lse, delta, dk, dv, cs);
   if (e == cudaSuccess) e = attn::launch_dq(m, s, q, dO, lse, delta, dq, cs);
   return from_cuda(e);
 }

@@ -38,15 +38,24 @@ struct DkvCfg : BwdCfg<D> {
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes =
       (kOffMisc + 16 + 1024) > B::kMinSmem ? (kOffMisc + 16 + 1024) : B::kMinSmem;
+  // d = 64 (KV_TMEM): K_j and V_j also fit in tensor memory (d/2 columns of 16-bit pairs
+  // each, after S^T, dP^T, dV and dK: 448 of 512), so S^T = K_j Q_i^T and dP^T = V_j dO_i^T
+  // run as TS products (A from tensor memory) at the full MMA rate instead of as SS
+  // products with M = N = 128, which take about twice as long. Each elementwise thread
+  // copies its own key row there once, which costs start-up latency; the launcher picks
+  // this form only when a key block meets enough query blocks. At d = 128 the four
+  // accumulators fill all 512 columns.
+  static constexpr uint32_t kColK = 256 + 2 * D, kColV = 256 + 2 * D + D / 2;
 };
 
-template <int D, bool BF16, bool PACKED>
+template <int D, bool BF16, bool PACKED, bool KV_TMEM>
 __global__ void __launch_bounds__(320, 1)
     attn_bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k,
                         const __grid_constant__ CUtensorMap map_v,
                         const __grid_constant__ CUtensorMap map_do, const BwdParams p) {
   using C = DkvCfg<D>;
+  static_assert(!KV_TMEM || D == 64, "K and V fit in tensor memory only at d = 64");
   constexpr int NS = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -94,7 +103,7 @@ __global__ void __launch_bounds__(320, 1)
   const int n = nb - i_first;  // query blocks i_first .. nb-1
 
   if (threadIdx.x == 0) {
-    mbar_init(kv_full, 1);
+    mbar_init(kv_full, KV_TMEM ? 8 : 1);  // elementwise warps (8) or TMA (1)
     for (int s = 0; s < NS; ++s) {
       mbar_init(&q_full[s], 1);
       mbar_init(&do_full[s], 1);
@@ -128,12 +137,14 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_map(&map_k);
       tma_prefetch_map(&map_v);
       tma_prefetch_map(&map_do);
-      mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
-      for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_rows<PACKED>(smem + C::kOffK + c * kBoxBytes, &map_k, kv_full, c * kBoxCols,
-                              j0, sl, true);
-        tma_load_rows<PACKED>(smem + C::kOffV + c * kBoxBytes, &map_v, kv_full, c * kBoxCols,
-                              j0, sl, true);
+      if constexpr (!KV_TMEM) {
+        mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_rows<PACKED>(smem + C::kOffK + c * kBoxBytes, &map_k, kv_full,
+                                c * kBoxCols, j0, sl, true);
+          tma_load_rows<PACKED>(smem + C::kOffV + c * kBoxBytes, &map_v, kv_full,
+                                c * kBoxCols, j0, sl, true);
+        }
       }
     }
     __syncwarp();
@@ -158,7 +169,7 @@ __global__ void __launch_bounds__(320, 1)
       issued = it + 1;
     }
     if (*abort_flag) {
-      mbar_wait(kv_full, 0, kDrainLimit, nullptr, kWaitDkvDrain);
+      if constexpr (!KV_TMEM) mbar_wait(kv_full, 0, kDrainLimit, nullptr, kWaitDkvDrain);
       for (int it = max(0, issued - NS); it < issued; ++it) {
         mbar_wait(&q_full[it % NS], (it / NS) & 1, kDrainLimit, nullptr, kWaitDkvDrain);
         mbar_wait(&do_full[it % NS], (it / NS) & 1, kDrainLimit, nullptr, kWaitDkvDrain);
@@ -175,12 +186,27 @@ __global__ void __launch_bounds__(320, 1)
     const uint64_t dq_mn = make_sdesc_sw128(smem_u32(smem + C::kOffQ), kBoxBytes, 1024);
     const uint64_t ddo_mn = make_sdesc_sw128(smem_u32(smem + C::kOffDO), kBoxBytes, 1024);
     constexpr uint32_t kStageStep = C::kTileBytes >> 4;
+    // S^T = K_j Q_i^T and dP^T = V_j dO_i^T, with K_j / V_j from shared or tensor memory.
+    auto issue_st = [&](int stage) {
+      if constexpr (KV_TMEM)
+        issue_rowdot_ts_d<D>(tmem + C::kColS, tmem + C::kColK, dq + stage * kStageStep,
+                             idesc_st);
+      else
+        issue_rowdot_d<D>(tmem + C::kColS, dk, dq + stage * kStageStep, idesc_st);
+    };
+    auto issue_dpt = [&](int stage) {
+      if constexpr (KV_TMEM)
+        issue_rowdot_ts_d<D>(tmem + C::kColDP, tmem + C::kColV, ddo + stage * kStageStep,
+                             idesc_st);
+      else
+        issue_rowdot_d<D>(tmem + C::kColDP, dv, ddo + stage * kStageStep, idesc_st);
+    };
     bool ok = warp_poll(kv_full, 0, limit, abort_flag, kWaitDkvKV) &&
               warp_poll(&q_full[0], 0, limit, abort_flag, kWaitDkvQ);
     if (ok) {
       tc_fence_after();
       if (elect_one()) {
-        issue_rowdot_d<D>(tmem + C::kColS, dk, dq, idesc_st);
+        issue_st(0);
         mma_commit(s_full);
       }
       __syncwarp();
@@ -189,7 +215,7 @@ __global__ void __launch_bounds__(320, 1)
     if (ok) {
       tc_fence_after();
       if (elect_one()) {
-        issue_rowdot_d<D>(tmem + C::kColDP, dv, ddo, idesc_st);
+        issue_dpt(0);
         mma_commit(dp_full);
       }
       __syncwarp();
@@ -209,7 +235,7 @@ __global__ void __launch_bounds__(320, 1)
         if (!(ok = warp_poll(&q_full[sn], (in / NS) & 1, limit, abort_flag, kWaitDkvQ))) break;
         tc_fence_after();
         if (elect_one()) {
-          issue_rowdot_d<D>(tmem + C::kColS, dk, dq + sn * kStageStep, idesc_st);
+          issue_st(sn);
           mma_commit(s_full);
         }
         __syncwarp();
@@ -226,7 +252,7 @@ __global__ void __launch_bounds__(320, 1)
           break;
         tc_fence_after();
         if (elect_one()) {
-          issue_rowdot_d<D>(tmem + C::kColDP, dv, ddo + sn * kStageStep, idesc_st);
+          issue_dpt(sn);
           mma_commit(dp_full);
         }
         __syncwarp();
@@ -259,7 +285,18 @@ __global__ void __launch_bounds__(320, 1)
       const float x = src[q];
       return g == 0 ? -x * kLog2e : x;
     };
-    float stat_next = load_stat(i_first);
+    float stat_next = load_stat(i_first);  // issued first: its latency overlaps the copy
+    if constexpr (KV_TMEM) {
+      // Group 0 copies this key's row of K_j, group 1 its row of V_j, into tensor memory
+      // (keys past the slice's end as zeros); the MMA warp waits for all eight warps.
+      const uint8_t* gsrc = reinterpret_cast<const uint8_t*>(g == 0 ? p.in_k : p.in_v);
+      copy_row_to_tmem<D>(key < Nk ? gsrc + (sl.k_elem0 + (size_t)key * sl.row_elems) * 2
+                                   : nullptr,
+                          tmem + lane_base + (g == 0 ? C::kColK : C::kColV));
+      tmem_st_wait();
+      tc_fence_before();
+      warp_arrive(kv_full);
+    }
     bool ok = true;
     for (int it = 0; it < n; ++it) {
       const int i = i_first + it;

@@ -27,6 +27,8 @@ namespace attn {
 
 struct BwdParams {
   const void* in_q;    // [BH, N, d] Q (read directly by the dQ kernel)
+  const void* in_k;    // [BH, N_k, d] K and V (read directly by the dK/dV kernel at d = 64)
+  const void* in_v;
   const void* in_do;   // [BH, N, d] dO (read directly by the dQ kernel)
   const float* lse;    // [BH, N] natural-log L
   const float* delta;  // [BH, N] D

@@ -5,17 +5,25 @@
 namespace attn {
 
 template <int D, bool BF16>
-static cudaError_t launch_dkv_t(const Maps& m, const Shape& s, const void* q,
-                               const void* d_o, const float* lse,
+static cudaError_t launch_dkv_t(const Maps& m, const Shape& s, const void* q, const void* k,
+                                const void* v, const void* d_o, const float* lse,
                                 const float* delta, void* dk, void* dv, cudaStream_t st) {
   using C = DkvCfg<D>;
-  auto kern = s.vl.cu_q != nullptr ? attn_bwd_dkv_kernel<D, BF16, true>
-                                   : attn_bwd_dkv_kernel<D, BF16, false>;
+  // d = 64: K_j, V_j in tensor memory when a key block meets about eight or more query
+  // blocks (the one-time row copy costs more than it saves on shorter work).
+  const bool kv_tmem = D == 64 && (s.causal ? s.N >= 2048 : s.N >= 1024);
+  auto kern = s.vl.cu_q != nullptr
+                  ? (kv_tmem ? attn_bwd_dkv_kernel<D, BF16, true, D == 64>
+                             : attn_bwd_dkv_kernel<D, BF16, true, false>)
+                  : (kv_tmem ? attn_bwd_dkv_kernel<D, BF16, false, D == 64>
+                             : attn_bwd_dkv_kernel<D, BF16, false, false>);
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   BwdParams p;
   p.in_q = q;
+  p.in_k = k;
+  p.in_v = v;
   p.in_do = d_o;
   p.lse = lse;
   p.delta = delta;
@@ -34,13 +42,14 @@ static cudaError_t launch_dkv_t(const Maps& m, const Shape& s, const void* q,
   return cudaGetLastError();
 }
 
-cudaError_t launch_dkv(const Maps& m, const Shape& s, const void* q, const void* d_o,
-                       const float* lse, const float* delta,
+cudaError_t launch_dkv(const Maps& m, const Shape& s, const void* q, const void* k,
+                       const void* v, const void* d_o, const float* lse, const float* delta,
                        void* dk, void* dv, cudaStream_t st) {
-  if (s.d == 128) return s.bf16 ? launch_dkv_t<128, true>(m, s, q, d_o, lse, delta, dk, dv, st)
-                                : launch_dkv_t<128, false>(m, s, q, d_o, lse, delta, dk, dv, st);
-  return s.bf16 ? launch_dkv_t<64, true>(m, s, q, d_o, lse, delta, dk, dv, st)
-                : launch_dkv_t<64, false>(m, s, q, d_o, lse, delta, dk, dv, st);
+  if (s.d == 128)
+    return s.bf16 ? launch_dkv_t<128, true>(m, s, q, k, v, d_o, lse, delta, dk, dv, st)
+                  : launch_dkv_t<128, false>(m, s, q, k, v, d_o, lse, delta, dk, dv, st);
+  return s.bf16 ? launch_dkv_t<64, true>(m, s, q, k, v, d_o, lse, delta, dk, dv, st)
+                : launch_dkv_t<64, false>(m, s, q, k, v, d_o, lse, delta, dk, dv, st);
 }
 
 ATTN_DEFINE_STATUS_READER(status_dkv)

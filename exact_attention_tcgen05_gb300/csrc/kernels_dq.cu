@@ -16,6 +16,8 @@ static cudaError_t launch_dq_t(const Maps& m, const Shape& s, const void* q,
   if (e != cudaSuccess) return e;
   BwdParams p;
   p.in_q = q;
+  p.in_k = nullptr;
+  p.in_v = nullptr;
   p.in_do = d_o;
   p.lse = lse;
   p.delta = delta;

@@ -30,7 +30,10 @@ cudaError_t launch_delta(const Shape& s, const void* o, const void* dO, float* d
 // query rows of both directly).
 cudaError_t launch_dq(const Maps& m, const Shape& s, const void* q, const void* dO,
                       const float* lse, const float* delta, void* dq, cudaStream_t st);
-cudaError_t launch_dkv(const Maps& m, const Shape& s, const void* q, const void* dO,
+// k and v are the raw tensors map.k / map.v describe (the d = 64 kernel reads its key rows
+// directly into tensor memory).
+cudaError_t launch_dkv(const Maps& m, const Shape& s, const void* q, const void* k,
+                       const void* v, const void* dO,
                        const float* lse, const float* delta, void* dk, void* dv,
                        cudaStream_t st);
 

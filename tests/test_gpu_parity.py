@@ -25,6 +25,9 @@ SMALL = [
     (2, 1, 513, 128, "bf16", True),
     (1, 2, 700, 64, "fp16", False),
     (1, 1, 1000, 128, "bf16", True),
+    # d = 64 with enough query blocks per key block for dK/dV to keep K, V in tensor memory
+    (1, 2, 1100, 64, "fp16", False),
+    (1, 1, 2100, 64, "bf16", True),
 ]
 
 

@@ -25,6 +25,7 @@ CASES = [
     (2, 64, "bf16", False, (200, 64, 1), (90, 300, 5)),           # fewer keys, no mask
     (2, 128, "bf16", True, (0, 77, 0, 256), (0, 77, 40, 300)),    # empty query sequences
     (3, 64, "bf16", True, (1000,), None),                         # one sequence
+    (2, 64, "bf16", False, (1100, 40, 700), None),  # long enough for K, V in tensor memory
 ]
 
 
