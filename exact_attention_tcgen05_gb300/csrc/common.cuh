@@ -19,7 +19,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Codes recorded in the status word when a bounded wait gives up (kernel * 16 + site).
 enum WaitSite : int {
   kWaitFwdQ = 0x11, kWaitFwdK, kWaitFwdV, kWaitFwdEmpty, kWaitFwdS, kWaitFwdP, kWaitFwdO,
-  kWaitFwdDrain, kWaitFwdX,
+  kWaitFwdDrain, kWaitFwdX, kWaitFwdQEmpty, kWaitFwdOFree,
   kWaitDqQ = 0x21, kWaitDqK, kWaitDqV, kWaitDqEmpty, kWaitDqS, kWaitDqDP, kWaitDqDS,
   kWaitDqDone, kWaitDqDrain, kWaitDqSC,
   kWaitDkvKV = 0x31, kWaitDkvQ, kWaitDkvDO, kWaitDkvEmpty, kWaitDkvS, kWaitDkvDP,

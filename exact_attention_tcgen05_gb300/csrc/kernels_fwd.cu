@@ -1,8 +1,35 @@
 // kernels_fwd.cu - instantiation and launch of the forward kernel.
+#include <algorithm>
+#include <cstdlib>
+
 #include "fwd.cuh"
+#include "fwd_persistent.cuh"
 #include "launch.h"
 
 namespace attn {
+
+static int sm_count_fwd() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 152;
+  return n;
+}
+
+// Which forward: the persistent kernel (fwd_persistent.cuh) except at d = 64 with long
+// items (24 or more key blocks per item on average), where the one-item kernel's loop
+// measured about 5% faster and the fixed cost per item matters little. ATTN_FWD_PERSISTENT
+// = 0 / 1 forces one or the other (both give the same bits).
+static bool use_persistent_fwd(const Shape& s) {
+  static const int forced = [] {
+    const char* e = std::getenv("ATTN_FWD_PERSISTENT");
+    return e == nullptr ? -1 : (e[0] == '0' ? 0 : 1);
+  }();
+  if (forced >= 0) return forced == 1;
+  const int nkb = (s.Nk + kTileN - 1) / kTileN;
+  const int blocks_per_item = s.causal ? (nkb + 1) / 2 : nkb;
+  return !(s.d == 64 && blocks_per_item >= 24);
+}
 
 template <int D, bool BF16>
 static cudaError_t launch_fwd_t(const Maps& m, const Shape& s, void* o, float* lse,
@@ -22,8 +49,21 @@ static cudaError_t launch_fwd_t(const Maps& m, const Shape& s, void* o, float* l
   p.scale_log2 = s.scale * kLog2e;
   p.wait_limit = s.wait_limit;
   p.vl = s.vl;
-  // Packed batches: s.N is the longest query sequence; CTAs past a sequence's end exit.
-  dim3 grid((s.N + 2 * kTileM - 1) / (2 * kTileM), s.BH);
+  // Packed batches: s.N is the longest query sequence; blocks past a sequence's end are
+  // skipped.
+  const int nqb_max = (s.N + 2 * kTileM - 1) / (2 * kTileM);
+  if (use_persistent_fwd(s)) {
+    using CP = FwdPCfg<D>;
+    auto kp = s.vl.cu_q != nullptr ? attn_fwd_persistent_kernel<D, BF16, true>
+                                   : attn_fwd_persistent_kernel<D, BF16, false>;
+    e = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, CP::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const long long n_items = (long long)nqb_max * s.BH;
+    const int grid = (int)std::min<long long>(n_items, sm_count_fwd());
+    kp<<<grid, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, p, (int)n_items, nqb_max);
+    return cudaGetLastError();
+  }
+  dim3 grid(nqb_max, s.BH);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(m.q, m.k, m.v, p);
   return cudaGetLastError();
 }
