@@ -21,7 +21,7 @@ enum WaitSite : int {
   kWaitFwdQ = 0x11, kWaitFwdK, kWaitFwdV, kWaitFwdEmpty, kWaitFwdS, kWaitFwdP, kWaitFwdO,
   kWaitFwdDrain, kWaitFwdX, kWaitFwdQEmpty, kWaitFwdOFree,
   kWaitDqQ = 0x21, kWaitDqK, kWaitDqV, kWaitDqEmpty, kWaitDqS, kWaitDqDP, kWaitDqDS,
-  kWaitDqDone, kWaitDqDrain, kWaitDqSC,
+  kWaitDqDone, kWaitDqDrain, kWaitDqSC, kWaitDqQFree, kWaitDqAccFree,
   kWaitDkvKV = 0x31, kWaitDkvQ, kWaitDkvDO, kWaitDkvEmpty, kWaitDkvS, kWaitDkvDP,
   kWaitDkvP, kWaitDkvDS, kWaitDkvDone, kWaitDkvDrain, kWaitDkvStats,
   kWaitDecFull = 0x41, kWaitDecDrain,

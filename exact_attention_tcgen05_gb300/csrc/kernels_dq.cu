@@ -1,8 +1,36 @@
 // kernels_dq.cu - instantiation and launch of the backward dQ kernel.
-#include "bwd_dq.cuh"
+#include <algorithm>
+#include <cstdlib>
+
+#include "bwd_dq_persistent.cuh"
 #include "launch.h"
 
 namespace attn {
+
+static int sm_count_dq() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 152;
+  return n;
+}
+
+// Which dQ kernel: the persistent one (bwd_dq_persistent.cuh) when the average item is short
+// (fewer than 8 key blocks), where the one-item kernel's fixed cost per CTA (about 7 us on
+// GB300, as much as 8 blocks of work) dominates; otherwise one CTA per item, whose dynamic
+// hardware scheduling balances the causal work better than the persistent kernel's static
+// pairs (about 13.5 rounds of pairs per SM on a B4 H32 N4096 step leave a 4% tail).
+// ATTN_BWD_PERSISTENT = 0 / 1 forces either (both give the same bits).
+static bool use_persistent_dq(const Shape& s) {
+  static const int forced = [] {
+    const char* e = std::getenv("ATTN_BWD_PERSISTENT");
+    return e == nullptr ? -1 : (e[0] == '0' ? 0 : 1);
+  }();
+  if (forced >= 0) return forced == 1;
+  const int nkb = (s.Nk + kTileN - 1) / kTileN;
+  const int blocks_per_item = s.causal ? (nkb + 1) / 2 : nkb;
+  return blocks_per_item < 8;
+}
 
 template <int D, bool BF16>
 static cudaError_t launch_dq_t(const Maps& m, const Shape& s, const void* q,
@@ -30,8 +58,22 @@ static cudaError_t launch_dq_t(const Maps& m, const Shape& s, const void* q,
   p.scale = s.scale;
   p.scale_log2 = s.scale * kLog2e;
   p.wait_limit = s.wait_limit;
-  // One CTA per 128-row query block (packed batches: of the longest sequence).
-  dim3 grid((s.N + kTileM - 1) / kTileM, s.BH);
+  const int nb_max = (s.N + kTileM - 1) / kTileM;  // packed batches: the longest sequence
+  if (use_persistent_dq(s)) {
+    using CP = DqPCfg<D>;
+    auto kp = s.vl.cu_q != nullptr ? attn_bwd_dq_persistent_kernel<D, BF16, true>
+                                   : attn_bwd_dq_persistent_kernel<D, BF16, false>;
+    e = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, CP::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int npairs = (nb_max + 1) / 2;
+    const long long n_pairs = (long long)npairs * s.BH;
+    const int grid = (int)std::min<long long>(n_pairs, sm_count_dq());
+    kp<<<grid, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, m.d_o, p, (int)n_pairs,
+                                                   npairs, nb_max);
+    return cudaGetLastError();
+  }
+  // One CTA per 128-row query block.
+  dim3 grid(nb_max, s.BH);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(m.q, m.k, m.v, m.d_o, p);
   return cudaGetLastError();
 }

@@ -1,0 +1,63 @@
+"""The persistent and the one-item kernels give the same bits.
+
+The forward and the dQ kernel each exist as a persistent kernel (one CTA per SM walking
+many work items) and as one CTA per item; which forward runs depends on the shape, and
+ATTN_FWD_PERSISTENT / ATTN_BWD_PERSISTENT = 0 / 1 force either. Both compute every tile in
+the same order with the same rounding, so O, LSE, dQ, dK and dV must agree bit for bit.
+Each setting runs in a child process of its own (the variables are read once per process)
+on the same seeded inputs.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+CHILD = r"""
+import sys, torch
+sys.path.insert(0, sys.argv[1])
+from exact_attention_tcgen05_gb300 import binding
+from exact_attention_tcgen05_gb300 import inputs as I
+out = {}
+for (B, H, N, d, dt, causal) in [(2, 3, 1000, 128, "bf16", True), (1, 4, 777, 64, "fp16", False),
+                                 (3, 2, 2100, 64, "bf16", True), (1, 2, 4096, 64, "bf16", False),
+                                 (1, 1, 300, 128, "fp16", False)]:
+    w = I.custom(B, H, N, d, dt, causal, seed=N + d)
+    q, k, v, do = (I.make_tensor(w, t).cuda() for t in ("q", "k", "v", "do"))
+    o, lse = binding.attn_fwd(q, k, v, causal=causal, scale=w.scale)
+    dq, dk, dv = binding.attn_bwd(q, k, v, o, lse, do, causal=causal, scale=w.scale)
+    out[w.name] = tuple(x.cpu() for x in (o, lse, dq, dk, dv))
+wv = I.varlen(2, 128, "bf16", True, seed=3, seqlens_q=(700, 64, 1500, 1))
+q, k, v, do = (I.make_varlen_tensor(wv, t).cuda() for t in ("q", "k", "v", "do"))
+cq = torch.tensor(wv.cu_q, dtype=torch.int32, device="cuda")
+o, lse = binding.attn_fwd_varlen(q, k, v, cq, cq, wv.max_q, wv.max_k, causal=True)
+dq, dk, dv = binding.attn_bwd_varlen(q, k, v, o, lse, do, cq, cq, wv.max_q, wv.max_k,
+                                     causal=True)
+out["packed"] = tuple(x.cpu() for x in (o, lse, dq, dk, dv))
+torch.cuda.synchronize()
+assert binding.attn_last_kernel_status() == (0, 0)
+torch.save(out, sys.argv[2])
+"""
+
+
+def _run(tmp_path, persistent):
+    path = str(tmp_path / f"run_{persistent}.pt")
+    env = dict(os.environ, ATTN_FWD_PERSISTENT=str(persistent),
+               ATTN_BWD_PERSISTENT=str(persistent))
+    subprocess.run([sys.executable, "-c", CHILD, ROOT, path], env=env, check=True,
+                   timeout=600)
+    return torch.load(path)
+
+
+def test_persistent_and_one_item_kernels_agree_bit_for_bit(tmp_path):
+    a = _run(tmp_path, 1)
+    b = _run(tmp_path, 0)
+    assert a.keys() == b.keys()
+    for name in a:
+        for what, x, y in zip(("O", "LSE", "dQ", "dK", "dV"), a[name], b[name]):
+            assert torch.equal(x, y), f"{name}: {what} differs"
