@@ -414,8 +414,33 @@ attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const v
 
 // ---------------------------------------------------------------- host-buffer step
 namespace {
-// Slices per chunk and the bytes of one chunk's device buffers (q k v dO o dq dk dv, lse, D).
-long long step_chunk_slices(long long bh, int chunks) { return (bh + chunks - 1) / chunks; }
+// Chunk boundaries of the host-buffer step: `chunks` chunks of B*H slices whose sizes ramp up
+// and down (weights 1, 2, 3, 3, ..., 3, 2, 1), so that the first upload, which nothing
+// overlaps, and the last chunk's compute and download, which nothing overlaps either, are
+// short. bounds[c] .. bounds[c+1] are the slices of chunk c. Returns the largest chunk.
+long long step_schedule(long long bh, int chunks, std::vector<long long>& bounds) {
+  std::vector<long long> w(chunks);
+  long long wsum = 0;
+  for (int c = 0; c < chunks; ++c) {
+    w[c] = std::min<long long>({(long long)c + 1, (long long)chunks - c, 3});
+    wsum += w[c];
+  }
+  bounds.assign(chunks + 1, 0);
+  long long acc = 0, largest = 0;
+  for (int c = 0; c < chunks; ++c) {
+    acc += w[c];
+    // at least one slice per chunk, and room for one per remaining chunk
+    long long b = std::max<long long>(bounds[c] + 1, (bh * acc + wsum / 2) / wsum);
+    b = std::min<long long>(b, bh - (chunks - 1 - c));
+    bounds[c + 1] = b;
+    largest = std::max(largest, b - bounds[c]);
+  }
+  return largest;
+}
+// Device buffer sets used in turn: chunk c's inputs go into set c % kStepSets once chunk
+// c - kStepSets has been computed, and its outputs once chunk c - kStepSets's outputs have
+// been copied out. (A third set measured no faster on GB300: the host link bounds the step.)
+constexpr int kStepSets = 2;
 size_t step_set_bytes(long long slices, int N, int d) {
   const size_t t = (size_t)slices * N * d * 2, r = (size_t)slices * N * 4;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
@@ -427,7 +452,8 @@ size_t attn_step_host_scratch_bytes(int B, int H, int N, int d, int chunks) {
   if (B <= 0 || H <= 0 || N <= 0 || chunks <= 0 || (d != 64 && d != 128)) return 0;
   const long long bh = (long long)B * H;
   const int c = (int)std::min<long long>(chunks, bh);
-  return 2 * step_set_bytes(step_chunk_slices(bh, c), N, d);
+  std::vector<long long> bounds;
+  return kStepSets * step_set_bytes(step_schedule(bh, c, bounds), N, d);
 }
 
 attn_status attn_step_host(const void* q, const void* k, const void* v, const void* dO,
@@ -445,8 +471,8 @@ attn_status attn_step_host(const void* q, const void* k, const void* v, const vo
   chunks = (int)std::min<long long>(chunks, bh);
   if (scratch_bytes < attn_step_host_scratch_bytes(B, H, N, d, chunks))
     return ATTN_ERR_INVALID_ARG;
-  const long long per = step_chunk_slices(bh, chunks);
-  chunks = (int)((bh + per - 1) / per);
+  std::vector<long long> bounds;
+  const long long per = step_schedule(bh, chunks, bounds);  // the largest chunk
   const size_t row_t = (size_t)N * d * 2, row_r = (size_t)N * 4;  // bytes per slice
   const size_t set_bytes = step_set_bytes(per, N, d);
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
@@ -470,9 +496,9 @@ attn_status attn_step_host(const void* q, const void* k, const void* v, const vo
   if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, start, 0);
 
   for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
-    const long long b0 = (long long)c * per;
-    const long long n = std::min(per, bh - b0);
-    uint8_t* set = static_cast<uint8_t*>(scratch) + (size_t)(c & 1) * set_bytes;
+    const long long b0 = bounds[c];
+    const long long n = bounds[c + 1] - b0;
+    uint8_t* set = static_cast<uint8_t*>(scratch) + (size_t)(c % kStepSets) * set_bytes;
     uint8_t* dev[8];
     for (int i = 0; i < 8; ++i) dev[i] = set + (size_t)i * up((size_t)per * row_t);
     float* d_lse = reinterpret_cast<float*>(set + 8 * up((size_t)per * row_t));
@@ -480,16 +506,17 @@ attn_status attn_step_host(const void* q, const void* k, const void* v, const vo
                                               up((size_t)per * row_r));
     const size_t tb = (size_t)n * row_t, rb = (size_t)n * row_r;
     const size_t off_t = (size_t)b0 * row_t, off_r = (size_t)b0 * row_r;
-    // inputs of chunk c, once chunk c - 2 (same buffers) has been computed
-    if (c >= 2) e = cudaStreamWaitEvent(s_in, ev_comp[c - 2], 0);
+    // inputs of chunk c, once chunk c - kStepSets (same buffers) has been computed
+    if (c >= kStepSets) e = cudaStreamWaitEvent(s_in, ev_comp[c - kStepSets], 0);
     const void* hin[4] = {q, k, v, dO};
     for (int i = 0; i < 4 && e == cudaSuccess; ++i)
       e = cudaMemcpyAsync(dev[i], static_cast<const uint8_t*>(hin[i]) + off_t, tb,
                           cudaMemcpyHostToDevice, s_in);
     if (e == cudaSuccess) e = cudaEventRecord(ev_in[c], s_in);
-    // compute chunk c once its inputs are in and chunk c - 2's outputs have left
+    // compute chunk c once its inputs are in and chunk c - kStepSets's outputs have left
     if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev_in[c], 0);
-    if (e == cudaSuccess && c >= 2) e = cudaStreamWaitEvent(cs, ev_out[c - 2], 0);
+    if (e == cudaSuccess && c >= kStepSets)
+      e = cudaStreamWaitEvent(cs, ev_out[c - kStepSets], 0);
     if (e == cudaSuccess) {
       st = attn_fwd(dev[0], dev[1], dev[2], dev[4], d_lse, 1, (int)n, N, d, dtype, causal,
                     scale, cs);

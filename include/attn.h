@@ -220,16 +220,18 @@ attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const 
  * attn_step_host - one training step of attention (attn_fwd then attn_bwd) on data that
  * lives in HOST memory: copies q, k, v, dO in, computes, and copies o, lse, dq, dk, dv out,
  * overlapping the copies with the kernels. The B*H slices are cut into `chunks` runs of
- * consecutive slices (the last one shorter); while chunk c is computed on cuda_stream, the
- * inputs of chunk c + 1 are copied in and the outputs of chunk c - 1 copied out on two
- * streams the call creates and releases. Results are identical to attn_fwd + attn_bwd on
+ * consecutive slices whose sizes ramp up and down (weights 1, 2, 3, 3, ..., 3, 2, 1): the
+ * first upload and the last chunk's compute and download overlap nothing, so those chunks
+ * are short. While chunk c is computed on cuda_stream, the inputs of chunk c + 1 are
+ * copied in and the outputs of chunk c - 1 copied out on two streams the call creates and
+ * releases. Results are identical to attn_fwd + attn_bwd on
  * the whole tensors (every (b, h) slice is computed independently).
  *   q, k, v, dO        HOST [B, H, N, d] 16-bit inputs; pinned (page-locked) memory is
  *                      needed for the copies to overlap (pageable memory works, serially)
  *   o, dq, dk, dv, lse HOST outputs, [B, H, N, d] 16-bit and [B, H, N] float32
  *   scratch            DEVICE buffer of scratch_bytes >=
  *                      attn_step_host_scratch_bytes(B, H, N, d, chunks): two sets of
- *                      per-chunk device tensors, used in turn
+ *                      per-chunk device tensors (of the largest chunk), used in turn
  *   chunks             >= 1 (values above B*H are clamped)
  * Sizes, dtypes, scale and errors as for attn_fwd; every pointer 16-byte aligned. The
  * call only enqueues work: the outputs are valid once cuda_stream has completed it.
