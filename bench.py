@@ -116,27 +116,49 @@ class ClockSampler:
 # our arm
 # ------------------------------------------------------------------------------------
 def dist_setup():
+    """Rank, world size and local rank from the torchrun environment; for N > 1 joins the
+    process group: NCCL, or gloo without CUDA or with BENCH_DIST_BACKEND=gloo (the
+    host-side logic is tested that way on the CPU)."""
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    use_cuda = torch.cuda.is_available() and os.environ.get("BENCH_DIST_BACKEND") != "gloo"
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
+        if use_cuda:
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if use_cuda else "gloo")
+    elif use_cuda:
         torch.cuda.set_device(0)
     return rank, world, local
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The largest x over all ranks (the job's time is its slowest rank's)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_workload(w, rank: int):
+    """Rank r's replica of workload w (weak scaling: every rank runs the whole workload on
+    its own GPU, with inputs of its own seed)."""
+    from exact_attention_tcgen05_gb300 import inputs as I
+    if rank == 0:
+        return w
+    return I.Workload(w.name, w.B, w.H, w.N, w.d, w.dtype, w.causal, w.seed + 7919 * rank,
+                      w.qk_gain, w.spike, w.spike_frac, w.oracle_slices)
+
+
+def job_tflops(tflop_per_step: float, steps: int, max_ms: float, world: int) -> float:
+    """Whole-job throughput: the work of every rank over the slowest rank's time."""
+    return world * tflop_per_step * steps / (max_ms * 1e-3)
 
 
 def barrier(world: int) -> None:
@@ -190,9 +212,7 @@ def run_ours(args) -> None:
 
     rank, world, local = dist_setup()
     w = I.BY_NAME[args.workload]
-    if world > 1:  # each rank: its own replica of the workload (weak scaling)
-        w = I.Workload(w.name, w.B, w.H, w.N, w.d, w.dtype, w.causal, w.seed + 7919 * rank,
-                       w.qk_gain, w.spike, w.spike_frac, w.oracle_slices)
+    w = replica_workload(w, rank)  # each rank: its own replica (weak scaling)
     binding.load()
     host = {t: I.make_tensor(w, t).pin_memory() for t in ("q", "k", "v", "do")}
     dev = {t: x.cuda(non_blocking=True) for t, x in host.items()}
@@ -249,7 +269,7 @@ def run_ours(args) -> None:
     total_ms = max_over_ranks(total_ms, world)
     ms_step = total_ms / args.steps
     f_fwd, f_bwd = flops(w, "fwd"), flops(w, "bwd")
-    value = world * (f_fwd + f_bwd) * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_tflops((f_fwd + f_bwd) / 1e12, args.steps, total_ms, world)
 
     # --- end to end through the C ABI with host buffers: attn_step_host copies the step's
     # inputs in from pinned host memory and its results out, overlapped with the kernels.
@@ -279,7 +299,7 @@ def run_ours(args) -> None:
         e_end.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), world)
-        e2e = {"value": world * (f_fwd + f_bwd) * args.steps / (e2e_ms * 1e-3) / 1e12,
+        e2e = {"value": job_tflops((f_fwd + f_bwd) / 1e12, args.steps, e2e_ms, world),
                "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / args.steps,
                "api": f"attn_step_host, {E2E_CHUNKS} chunks of (b, h) slices, copies "
