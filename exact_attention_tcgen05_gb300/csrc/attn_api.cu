@@ -34,11 +34,16 @@ Range range_of(const void* p, size_t bytes) {
 }
 bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
 
+// Head dimensions the attention kernels take: multiples of 8 (16-byte rows for TMA) up to
+// 128; d <= 64 runs on the 64-column kernels, d > 64 on the 128-column ones, with the
+// columns past d read as zero.
+bool head_dim_ok(int d) { return d >= 8 && d <= 128 && d % 8 == 0; }
+
 attn_status check_shape(int B, int H, int N, int d, attn_dtype dtype) {
   if (B < 1 || H < 1 || N < 1 || N > kMaxN) return ATTN_ERR_INVALID_ARG;
   if ((long long)B * H > kMaxBH) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_FP16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!head_dim_ok(d)) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
 }
 
@@ -323,7 +328,7 @@ attn_status check_varlen(int B, int H, int total_q, int total_k, int max_q, int 
   if (cu_q == nullptr || cu_k == nullptr) return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(cu_q) | reinterpret_cast<uintptr_t>(cu_k)) & 3u)
     return ATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!head_dim_ok(d)) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
 }
 
@@ -449,7 +454,7 @@ size_t step_set_bytes(long long slices, int N, int d) {
 }  // namespace
 
 size_t attn_step_host_scratch_bytes(int B, int H, int N, int d, int chunks) {
-  if (B <= 0 || H <= 0 || N <= 0 || chunks <= 0 || (d != 64 && d != 128)) return 0;
+  if (B <= 0 || H <= 0 || N <= 0 || chunks <= 0 || !head_dim_ok(d)) return 0;
   const long long bh = (long long)B * H;
   const int c = (int)std::min<long long>(chunks, bh);
   std::vector<long long> bounds;
@@ -559,6 +564,7 @@ constexpr int kMaxSplits = 65535;  // grid.x of the partial kernel
 attn_status check_decode(int B, int H, int Nk, int d, attn_dtype dtype, int splits) {
   attn_status st = check_shape(B, H, Nk, d, dtype);
   if (st != ATTN_OK) return st;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;  // the decode kernels' widths
   if (splits < 1 || splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }

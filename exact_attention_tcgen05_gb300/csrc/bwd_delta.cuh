@@ -52,7 +52,8 @@ template <int D, bool BF16, bool PACKED>
 __global__ void __launch_bounds__(kDeltaThreads)
     attn_bwd_delta_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO,
                           float* __restrict__ delta, long long rows, int heads,
-                          long long total) {
+                          long long total, int n16) {
+  // n16: 16-byte pieces per row (head dimension / 8, at most D / 8); lanes past it add 0.
   constexpr int kLanesPerRow = D / 8;              // 16-byte chunks per row
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;  // rows one warp covers per load
   const int lane = threadIdx.x & 31;
@@ -66,9 +67,9 @@ __global__ void __launch_bounds__(kDeltaThreads)
 #pragma unroll
     for (int u = 0; u < kDeltaUnroll; ++u) {
       const long long row = r0 + u * kRowsPerWarp + sub;
-      if (row < rows) {
-        a[u] = ld_stream(o + row * kLanesPerRow + part);
-        b[u] = ld_stream(dO + row * kLanesPerRow + part);
+      if (row < rows && part < n16) {
+        a[u] = ld_stream(o + row * n16 + part);
+        b[u] = ld_stream(dO + row * n16 + part);
       } else {
         a[u] = make_uint4(0, 0, 0, 0);
         b[u] = a[u];

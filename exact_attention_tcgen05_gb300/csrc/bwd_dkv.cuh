@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(320, 1)
   const int lane = lane_id();
   const int bh = blockIdx.y;
   SliceRows sl;
-  if (!slice_rows<PACKED>(p.vl, bh, p.N, p.Nk, D, p.causal != 0, sl)) return;
+  if (!slice_rows<PACKED>(p.vl, bh, p.N, p.Nk, p.dh, p.causal != 0, sl)) return;
   const int N = sl.nq, Nk = sl.nk, off = sl.off;
   const int jb = blockIdx.x;  // causal: block 0 sees the most query blocks, so runs first
   if (PACKED && jb * kTileN >= Nk) return;  // past this sequence's keys
@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(320, 1)
     // A packed sequence with keys but no queries: no query sees these keys, so their
     // gradients are zero.
     const int rows = min(kTileN, Nk - j0);
-    constexpr int kVec = D / 8;  // 16-byte chunks per row
+    const int kVec = p.dh / 8;  // 16-byte pieces per row
     for (int idx = threadIdx.x; idx < 2 * rows * kVec; idx += blockDim.x) {
       const int t = idx / (rows * kVec), r = (idx / kVec) % rows, c = idx % kVec;
       uint8_t* base = reinterpret_cast<uint8_t*>(t == 0 ? p.out0 : p.out1);
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(320, 1)
       const uint8_t* gsrc = reinterpret_cast<const uint8_t*>(g == 0 ? p.in_k : p.in_v);
       copy_row_to_tmem<D>(key < Nk ? gsrc + (sl.k_elem0 + (size_t)key * sl.row_elems) * 2
                                    : nullptr,
-                          tmem + lane_base + (g == 0 ? C::kColK : C::kColV));
+                          tmem + lane_base + (g == 0 ? C::kColK : C::kColV), p.dh / 8);
       tmem_st_wait();
       tc_fence_before();
       warp_arrive(kv_full);
@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(320, 1)
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t a[32];
         tmem_ld32(t_acc + cc * 32, a);
-        if (key < Nk) store_row32<BF16>(dst + cc * 64, a, mul);
+        if (key < Nk) store_row32<BF16>(dst + cc * 64, a, mul, valid16(p.dh, cc * 32, 4));
       }
     }
     tc_fence_before();

@@ -34,6 +34,7 @@ struct BwdParams {
   const float* delta;  // [BH, N] D
   void* out0;          // dQ (dQ kernel) or dK (dKV kernel)
   void* out1;          // dV (dKV kernel)
+  int dh;              // head dimension of the tensors (<= D; columns past it read as zero)
   int N;               // query rows per slice (N_q; packed batches: per sequence, from vl)
   int Nk;              // key rows per slice (N_k); causal key j is visible to query i
                        // iff j <= i + (N_k - N_q)
@@ -78,30 +79,35 @@ struct DqCfg : BwdCfg<D> {
       (kOffMisc + 16 + 1024) > B::kMinSmem ? (kOffMisc + 16 + 1024) : B::kMinSmem;
 };
 
-// Writes 32 fp32 accumulator values, multiplied by `mul`, as 16-bit to a global row.
+// Writes 32 fp32 accumulator values, multiplied by `mul`, as 16-bit to a global row: the
+// first n16 16-byte pieces (all four when the row is that wide).
 template <bool BF16>
-__device__ __forceinline__ void store_row32(uint8_t* dst, const uint32_t (&r)[32], float mul) {
+__device__ __forceinline__ void store_row32(uint8_t* dst, const uint32_t (&r)[32], float mul,
+                                            int n16 = 4) {
   uint32_t pk[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i)
     pk[i] = pack2<BF16>(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
   uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-  for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+  for (int v = 0; v < 4; ++v)
+    if (v < n16) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
 }
 
-// Copies one D-element 16-bit row from global memory (zeros when src is null) into
-// tensor-memory columns [t_col, t_col + D/2) of this thread's lane as packed pairs (the
-// layout of an A operand read from tensor memory). Every lane of the warp calls it (the
-// TMEM store is warp-collective).
+// Copies one 16-bit row of n16 16-byte pieces from global memory (zeros past them, and
+// everywhere when src is null) into tensor-memory columns [t_col, t_col + D/2) of this
+// thread's lane as packed pairs (the layout of an A operand read from tensor memory). Every
+// lane of the warp calls it (the TMEM store is warp-collective).
 template <int D>
-__device__ __forceinline__ void copy_row_to_tmem(const uint8_t* src, uint32_t t_col) {
+__device__ __forceinline__ void copy_row_to_tmem(const uint8_t* src, uint32_t t_col,
+                                                 int n16 = D / 8) {
   // Every load of the row is issued before the first tensor-memory store (the stores are
   // ordering points for the compiler), so the row costs one memory latency, not D / 64.
   uint32_t r[D / 2];
 #pragma unroll
   for (int k = 0; k < D / 8; ++k) {
-    const uint4 v = src ? *reinterpret_cast<const uint4*>(src + k * 16) : make_uint4(0, 0, 0, 0);
+    const uint4 v = (src && k < n16) ? *reinterpret_cast<const uint4*>(src + k * 16)
+                                     : make_uint4(0, 0, 0, 0);
     r[4 * k] = v.x;
     r[4 * k + 1] = v.y;
     r[4 * k + 2] = v.z;
@@ -163,7 +169,7 @@ __global__ void __launch_bounds__(320, 1)
   const int lane = lane_id();
   const int bh = blockIdx.y;
   SliceRows sl;
-  if (!slice_rows<PACKED>(p.vl, bh, p.N, p.Nk, D, p.causal != 0, sl)) return;
+  if (!slice_rows<PACKED>(p.vl, bh, p.N, p.Nk, p.dh, p.causal != 0, sl)) return;
   const int N = sl.nq, Nk = sl.nk, off = sl.off;
   const int nb = (N + kTileM - 1) / kTileM;
   const int nkb = (Nk + kTileN - 1) / kTileN;
@@ -328,7 +334,7 @@ __global__ void __launch_bounds__(320, 1)
       const uint8_t* gsrc = reinterpret_cast<const uint8_t*>(g == 0 ? p.in_q : p.in_do);
       copy_row_to_tmem<D>(row < N ? gsrc + (sl.q_elem0 + (size_t)row * sl.row_elems) * 2
                                   : nullptr,
-                          tmem + lane_base + (g == 0 ? C::kColQ : C::kColDO));
+                          tmem + lane_base + (g == 0 ? C::kColQ : C::kColDO), p.dh / 8);
       tmem_st_wait();
       tc_fence_before();
       warp_arrive(qdo_tmem);
@@ -389,7 +395,8 @@ __global__ void __launch_bounds__(320, 1)
       for (int cc = 0; cc < D / 64; ++cc) {
         uint32_t a[32];
         tmem_ld32(t_acc + cc * 32, a);
-        if (row < N) store_row32<BF16>(drow + cc * 64, a, p.scale);
+        if (row < N)
+          store_row32<BF16>(drow + cc * 64, a, p.scale, valid16(p.dh, g * (D / 2) + cc * 32, 4));
       }
     }
     tc_fence_before();

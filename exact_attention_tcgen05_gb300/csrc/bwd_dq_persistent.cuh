@@ -53,7 +53,7 @@ __device__ __forceinline__ bool dq_item_geom(const BwdParams& p, int item, int n
                                              DqItem& it) {
   const int bh = item / nb_max;
   const int x = item - bh * nb_max;
-  if (!slice_rows<PACKED>(p.vl, bh, p.N, p.Nk, D, p.causal != 0, it.sl)) return false;
+  if (!slice_rows<PACKED>(p.vl, bh, p.N, p.Nk, p.dh, p.causal != 0, it.sl)) return false;
   it.N = it.sl.nq;
   it.Nk = it.sl.nk;
   it.off = it.sl.off;
@@ -81,10 +81,11 @@ struct DqPCfg : DqCfg<D> {
 // this thread's lane: copy_row_to_tmem in two halves, so that the loads can be issued
 // well before the tensor memory they go to is free.
 template <int D>
-__device__ __forceinline__ void load_row(const uint8_t* src, uint32_t (&r)[D / 2]) {
+__device__ __forceinline__ void load_row(const uint8_t* src, uint32_t (&r)[D / 2], int n16) {
 #pragma unroll
   for (int k = 0; k < D / 8; ++k) {
-    const uint4 v = src ? *reinterpret_cast<const uint4*>(src + k * 16) : make_uint4(0, 0, 0, 0);
+    const uint4 v = (src && k < n16) ? *reinterpret_cast<const uint4*>(src + k * 16)
+                                     : make_uint4(0, 0, 0, 0);
     r[4 * k] = v.x;
     r[4 * k + 1] = v.y;
     r[4 * k + 2] = v.z;
@@ -329,7 +330,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       load_row<D>(row < it.N ? gsrc + (it.sl.q_elem0 + (size_t)row * it.sl.row_elems) * 2
                              : nullptr,
-                  rr);
+                  rr, p.dh / 8);
     };
     DqItem cur;
     bool have = next_item(cur);
@@ -429,7 +430,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int cc = 0; cc < D / 64; ++cc)
           store_row32<BF16>(drow + cc * 64, *reinterpret_cast<const uint32_t(*)[32]>(&a[cc * 32]),
-                            p.scale);
+                            p.scale, valid16(p.dh, g * (D / 2) + cc * 32, 4));
       }
       ++items;
       cur = nxt;

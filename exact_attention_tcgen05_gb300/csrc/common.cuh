@@ -51,7 +51,8 @@ struct SliceRows {
   size_t stat0;             // index of row 0 in lse and D
 };
 
-// Fills `s` for slice bh. Dense (PACKED = false): the whole-call sizes N, Nk. Packed:
+// Fills `s` for slice bh; D is the head dimension of the tensors (elements per row). Dense
+// (PACKED = false): the whole-call sizes N, Nk. Packed:
 // reads the slice's sequence bounds and checks them (in range, not longer than the grid
 // covers, and every query row sees a key); a malformed sequence records kErrSeqlens and
 // returns false. The layout is a template parameter so that the dense kernels carry no
@@ -104,6 +105,15 @@ __device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* map,
     tma_load_3d(dst, map, bar, col, s.tma_bh, (keys ? s.k_start : s.q_start) + row);
   else
     tma_load_3d(dst, map, bar, col, row, s.tma_bh);
+}
+
+// Head dimensions other than the kernels' own (64 or 128): a tensor row of dh elements is
+// loaded into a D-column tile whose columns past dh read as zero (TMA fills them, or the
+// row copies below do), so every product sees exact zeros there; only the first dh columns
+// are stored. These give the number of valid 16-byte pieces (8 columns each).
+__device__ __forceinline__ int valid16(int dh, int col0, int max16) {
+  const int v = (dh - col0) / 8;
+  return v < 0 ? 0 : (v > max16 ? max16 : v);
 }
 
 // Rounds a shared-memory pointer up to 1024 bytes (the swizzle-atom alignment).

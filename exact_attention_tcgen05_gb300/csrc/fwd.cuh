@@ -40,6 +40,7 @@ namespace attn {
 struct FwdParams {
   void* o;
   float* lse;
+  int dh;           // head dimension of the tensors (<= D; columns past it read as zero)
   int N;            // query rows per slice (N_q; packed batches: per sequence, from vl)
   int Nk;           // key rows per slice (N_k)
   int causal;
@@ -101,7 +102,7 @@ __global__ void __launch_bounds__(320, 1)
   const int lane = lane_id();
   const int bh = blockIdx.y;
   SliceRows sl;
-  if (!slice_rows<PACKED>(p.vl, bh, p.N, p.Nk, D, p.causal != 0, sl)) return;
+  if (!slice_rows<PACKED>(p.vl, bh, p.N, p.Nk, p.dh, p.causal != 0, sl)) return;
   const int N = sl.nq, Nk = sl.nk, off = sl.off;
   const int nqb = (N + 2 * kTileM - 1) / (2 * kTileM);
   const int nkb = (Nk + kTileN - 1) / kTileN;
@@ -445,9 +446,11 @@ __global__ void __launch_bounds__(320, 1)
                               __uint_as_float(r[2 * i + 1]) * inv_l);
         if (row < N) {
           uint4* dst = reinterpret_cast<uint4*>(orow + cc * 128);
+          const int n16 = valid16(p.dh, cc * 64, 8);  // columns past dh are not stored
 #pragma unroll
           for (int v = 0; v < 8; ++v)
-            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            if (v < n16)
+              dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
       if (row < N) p.lse[sl.stat0 + row] = (m + log2f(l)) * kLn2;

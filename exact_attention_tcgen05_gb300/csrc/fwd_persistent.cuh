@@ -52,7 +52,7 @@ __device__ __forceinline__ bool fwd_item_geom(const FwdParams& p, int item, int 
                                               FwdItem& it) {
   const int bh = item / nqb_max;
   const int x = item - bh * nqb_max;
-  if (!slice_rows<PACKED>(p.vl, bh, p.N, p.Nk, D, p.causal != 0, it.sl)) return false;
+  if (!slice_rows<PACKED>(p.vl, bh, p.N, p.Nk, p.dh, p.causal != 0, it.sl)) return false;
   it.N = it.sl.nq;
   it.Nk = it.sl.nk;
   it.off = it.sl.off;
@@ -498,9 +498,11 @@ __global__ void __launch_bounds__(320, 1)
             pk[i] = pack2<BF16>(__uint_as_float(r[cc * 64 + 2 * i]) * inv_l,
                                 __uint_as_float(r[cc * 64 + 2 * i + 1]) * inv_l);
           uint4* dst = reinterpret_cast<uint4*>(orow + cc * 128);
+          const int n16 = valid16(p.dh, cc * 64, 8);  // columns past dh are not stored
 #pragma unroll
           for (int v = 0; v < 8; ++v)
-            dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            if (v < n16)
+              dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
         p.lse[it.sl.stat0 + row] = (m + log2f(l)) * kLn2;
       }

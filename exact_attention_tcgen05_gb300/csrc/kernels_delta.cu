@@ -26,13 +26,13 @@ static cudaError_t launch_delta_t(const Shape& s, const void* o, const void* dO,
   kern<<<blocks, kDeltaThreads, 0, st>>>(reinterpret_cast<const uint4*>(o),
                                          reinterpret_cast<const uint4*>(dO), delta, rows,
                                          packed ? s.vl.H : 0,
-                                         packed ? (long long)s.vl.total_q : 0);
+                                         packed ? (long long)s.vl.total_q : 0, s.d / 8);
   return cudaGetLastError();
 }
 
 cudaError_t launch_delta(const Shape& s, const void* o, const void* dO, float* delta,
                          cudaStream_t st) {
-  if (s.d == 128) return s.bf16 ? launch_delta_t<128, true>(s, o, dO, delta, st)
+  if (s.d > 64) return s.bf16 ? launch_delta_t<128, true>(s, o, dO, delta, st)
                                 : launch_delta_t<128, false>(s, o, dO, delta, st);
   return s.bf16 ? launch_delta_t<64, true>(s, o, dO, delta, st)
                 : launch_delta_t<64, false>(s, o, dO, delta, st);

@@ -29,6 +29,7 @@ static cudaError_t launch_dkv_t(const Maps& m, const Shape& s, const void* q, co
   p.delta = delta;
   p.out0 = dk;
   p.out1 = dv;
+  p.dh = s.d;
   p.N = s.N;
   p.Nk = s.Nk;
   p.vl = s.vl;
@@ -45,7 +46,7 @@ static cudaError_t launch_dkv_t(const Maps& m, const Shape& s, const void* q, co
 cudaError_t launch_dkv(const Maps& m, const Shape& s, const void* q, const void* k,
                        const void* v, const void* d_o, const float* lse, const float* delta,
                        void* dk, void* dv, cudaStream_t st) {
-  if (s.d == 128)
+  if (s.d > 64)
     return s.bf16 ? launch_dkv_t<128, true>(m, s, q, k, v, d_o, lse, delta, dk, dv, st)
                   : launch_dkv_t<128, false>(m, s, q, k, v, d_o, lse, delta, dk, dv, st);
   return s.bf16 ? launch_dkv_t<64, true>(m, s, q, k, v, d_o, lse, delta, dk, dv, st)

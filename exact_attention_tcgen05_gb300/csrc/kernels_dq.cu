@@ -51,6 +51,7 @@ static cudaError_t launch_dq_t(const Maps& m, const Shape& s, const void* q,
   p.delta = delta;
   p.out0 = dq;
   p.out1 = nullptr;
+  p.dh = s.d;
   p.N = s.N;
   p.Nk = s.Nk;
   p.vl = s.vl;
@@ -81,7 +82,7 @@ static cudaError_t launch_dq_t(const Maps& m, const Shape& s, const void* q,
 cudaError_t launch_dq(const Maps& m, const Shape& s, const void* q, const void* d_o,
                        const float* lse, const float* delta,
                       void* dq, cudaStream_t st) {
-  if (s.d == 128) return s.bf16 ? launch_dq_t<128, true>(m, s, q, d_o, lse, delta, dq, st)
+  if (s.d > 64) return s.bf16 ? launch_dq_t<128, true>(m, s, q, d_o, lse, delta, dq, st)
                                 : launch_dq_t<128, false>(m, s, q, d_o, lse, delta, dq, st);
   return s.bf16 ? launch_dq_t<64, true>(m, s, q, d_o, lse, delta, dq, st)
                 : launch_dq_t<64, false>(m, s, q, d_o, lse, delta, dq, st);

@@ -28,7 +28,7 @@ static bool use_persistent_fwd(const Shape& s) {
   if (forced >= 0) return forced == 1;
   const int nkb = (s.Nk + kTileN - 1) / kTileN;
   const int blocks_per_item = s.causal ? (nkb + 1) / 2 : nkb;
-  return !(s.d == 64 && blocks_per_item >= 24);
+  return !(s.d <= 64 && blocks_per_item >= 24);
 }
 
 template <int D, bool BF16>
@@ -43,6 +43,7 @@ static cudaError_t launch_fwd_t(const Maps& m, const Shape& s, void* o, float* l
   FwdParams p;
   p.o = o;
   p.lse = lse;
+  p.dh = s.d;
   p.N = s.N;
   p.Nk = s.Nk;
   p.causal = s.causal ? 1 : 0;
@@ -69,7 +70,7 @@ static cudaError_t launch_fwd_t(const Maps& m, const Shape& s, void* o, float* l
 }
 
 cudaError_t launch_fwd(const Maps& m, const Shape& s, void* o, float* lse, cudaStream_t st) {
-  if (s.d == 128) return s.bf16 ? launch_fwd_t<128, true>(m, s, o, lse, st)
+  if (s.d > 64) return s.bf16 ? launch_fwd_t<128, true>(m, s, o, lse, st)
                                 : launch_fwd_t<128, false>(m, s, o, lse, st);
   return s.bf16 ? launch_fwd_t<64, true>(m, s, o, lse, st)
                 : launch_fwd_t<64, false>(m, s, o, lse, st);

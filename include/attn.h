@@ -18,7 +18,11 @@
  *            floats (fp16 or bf16, one type for all of them), row-major, d innermost.
  *            lse and the backward workspace are contiguous [B, H, N] float32.
  *            Every pointer is a DEVICE pointer, 16-byte aligned.
- *   Sizes    B >= 1, H >= 1, 1 <= N <= 1048576, d in {64, 128}; B*H <= 65535.
+ *   Sizes    B >= 1, H >= 1, 1 <= N <= 1048576, B*H <= 65535; d a multiple of 8 from 8
+ *            to 128 (split-KV decoding: d in {64, 128}). The kernels are 64 or 128 columns
+ *            wide: a smaller d runs on the next width with the missing columns read as
+ *            zero (exact: they add zeros to every product) and never written, so d = 96
+ *            costs what d = 128 costs.
  *   Mask     causal != 0 masks key j for query i when j > i (top-left aligned,
  *            N_q = N_k, diagonal kept), so no row is ever fully masked.
  *   scale    the factor applied to Q K^T; finite and > 0 (the usual value is

@@ -81,7 +81,8 @@ INVALID, UNSUPPORTED = 1, 2
     (dict(q=0), INVALID), (dict(o=0), INVALID), (dict(lse=L + 4), INVALID),
     (dict(k=K + 2), INVALID), (dict(B=0), INVALID), (dict(H=-1), INVALID),
     (dict(N=0), INVALID), (dict(N=(1 << 20) + 1), INVALID), (dict(B=300, H=300), INVALID),
-    (dict(d=96), UNSUPPORTED), (dict(d=256), UNSUPPORTED), (dict(dt=2), INVALID),
+    (dict(d=100), UNSUPPORTED), (dict(d=256), UNSUPPORTED), (dict(d=136), UNSUPPORTED),
+    (dict(d=4), UNSUPPORTED), (dict(dt=2), INVALID),
     (dict(scale=0.0), INVALID), (dict(scale=-1.0), INVALID), (dict(scale=float("nan")), INVALID),
     (dict(scale=float("inf")), INVALID), (dict(o=Q), INVALID), (dict(o=K + 16), INVALID),
     (dict(lse=O + 1024), INVALID),
@@ -92,7 +93,7 @@ def test_fwd_rejects_bad_arguments(lib, kw, code):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(dq=0), INVALID), (dict(ws=0), INVALID), (dict(dq=DK), INVALID), (dict(ws=Q), INVALID),
-    (dict(dq=O + 32), INVALID), (dict(d=32), UNSUPPORTED), (dict(scale=0.0), INVALID),
+    (dict(dq=O + 32), INVALID), (dict(d=132), UNSUPPORTED), (dict(scale=0.0), INVALID),
     (dict(ws=WS + 8), INVALID),
 ])
 def test_bwd_rejects_bad_arguments(lib, kw, code):
@@ -112,7 +113,7 @@ def bwd_qk(lib, Nq=256, Nk=1024, causal=1, dk=DK):
     (dict(Nq=1024, Nk=256), INVALID),            # causal needs N_k >= N_q
     (dict(Nk=0), INVALID), (dict(Nq=0), INVALID), (dict(Nk=(1 << 20) + 1), INVALID),
     (dict(d=64, o=K + 64 * 1024 * 2 * 2 - 16), INVALID),   # o overlaps the tail of k
-    (dict(d=80), UNSUPPORTED),
+    (dict(d=84), UNSUPPORTED),
 ])
 def test_fwd_qk_rejects_bad_arguments(lib, kw, code):
     assert fwd_qk(lib, **kw) == code
@@ -144,7 +145,7 @@ def bwd_varlen(lib, dk=DK, ws=WS, cu_q=CUQ, Tq=1000, mq=400):
     (dict(cu_q=0), INVALID), (dict(cu_k=0), INVALID), (dict(cu_q=CUQ + 2), INVALID),
     (dict(B=0), INVALID), (dict(Tq=0), INVALID), (dict(mq=0), INVALID),
     (dict(mq=1001), INVALID),                    # longer than the whole packed tensor
-    (dict(mk=(1 << 20) + 1, Tk=1 << 21), INVALID), (dict(d=80), UNSUPPORTED),
+    (dict(mk=(1 << 20) + 1, Tk=1 << 21), INVALID), (dict(d=84), UNSUPPORTED),
     (dict(scale=0.0), INVALID), (dict(q=Q + 8), INVALID),
     (dict(o=Q + 1000 * 2 * 128 * 2 - 16), INVALID),  # o overlaps the tail of q
     (dict(o=CUQ - 16), INVALID),                    # o overlaps cu_seqlens_q
@@ -172,7 +173,7 @@ def test_stage_entry_points_reject_bad_arguments(lib):
     assert dkv(dk=DV) == INVALID
     assert dkv(dk=Q) == INVALID
     assert dkv(lse=0) == INVALID
-    assert dkv(d=80) == UNSUPPORTED
+    assert dkv(d=84) == UNSUPPORTED
     dq = lambda out=DQ, scale=0.1: lib.attn_bwd_dq(Q, K, V, L, WS, DO, out, 1, 1, 256, 64, 0, 0,
                                                    scale, None)
     assert dq(out=WS) == INVALID
@@ -198,7 +199,8 @@ def test_decode_rejects_bad_arguments(lib, kw, code):
 
 def test_step_host_rejects_bad_arguments(lib):
     need = lib.attn_step_host_scratch_bytes(1, 2, 256, 128, 2)
-    assert need > 0 and lib.attn_step_host_scratch_bytes(1, 2, 256, 96, 2) == 0
+    assert need > 0 and lib.attn_step_host_scratch_bytes(1, 2, 256, 100, 2) == 0
+    assert lib.attn_step_host_scratch_bytes(1, 2, 256, 96, 2) > 0  # any multiple of 8 <= 128
 
     def call(scratch=WS, nbytes=need, chunks=2, d=128, scale=0.1, q=Q):
         return lib.attn_step_host(q, K, V, DO, O, L, DQ, DK, DV, scratch, nbytes, 1, 2, 256, d,
@@ -206,7 +208,7 @@ def test_step_host_rejects_bad_arguments(lib):
     assert call(scratch=0) == INVALID
     assert call(nbytes=need - 1) == INVALID
     assert call(chunks=0) == INVALID
-    assert call(d=32) == UNSUPPORTED
+    assert call(d=100) == UNSUPPORTED
     assert call(scale=-1.0) == INVALID
     assert call(q=Q + 8) == INVALID
 
@@ -225,7 +227,7 @@ def test_decode_sizes(lib):
 def test_preprocess_rejects_bad_arguments(lib):
     assert lib.attn_bwd_preprocess(O, DO, 0, 1, 1, 16, 64, 0, None) == INVALID
     assert lib.attn_bwd_preprocess(O, DO, O, 1, 1, 16, 64, 0, None) == INVALID
-    assert lib.attn_bwd_preprocess(O, DO, WS, 1, 1, 16, 48, 0, None) == UNSUPPORTED
+    assert lib.attn_bwd_preprocess(O, DO, WS, 1, 1, 16, 44, 0, None) == UNSUPPORTED
 
 
 def test_binding_refuses_cpu_tensors():

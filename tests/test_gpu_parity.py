@@ -28,6 +28,13 @@ SMALL = [
     # d = 64 with enough query blocks per key block for dK/dV to keep K, V in tensor memory
     (1, 2, 1100, 64, "fp16", False),
     (1, 1, 2100, 64, "bf16", True),
+    # other head dims (multiples of 8): run on the 64- or 128-column kernels, zero-padded
+    (1, 2, 300, 96, "bf16", True),
+    (1, 2, 257, 32, "fp16", False),
+    (2, 1, 200, 72, "bf16", False),
+    (1, 1, 130, 8, "bf16", True),
+    (1, 2, 400, 120, "fp16", True),
+    (1, 1, 1100, 40, "bf16", False),  # d <= 64 with K, V in tensor memory in dK/dV
 ]
 
 

@@ -28,6 +28,7 @@ CASES = [
     (1, 2, 200, 333, 128, "bf16", False),
     (2, 1, 1000, 130, 64, "fp16", False),    # more queries than keys, no mask
     (1, 1, 17, 17, 128, "bf16", True),       # N_q = N_k: attn_fwd's own alignment
+    (1, 2, 100, 333, 48, "fp16", True),      # a head dim of 48
 ]
 
 

@@ -26,6 +26,7 @@ CASES = [
     (2, 128, "bf16", True, (0, 77, 0, 256), (0, 77, 40, 300)),    # empty query sequences
     (3, 64, "bf16", True, (1000,), None),                         # one sequence
     (2, 64, "bf16", False, (1100, 40, 700), None),  # long enough for K, V in tensor memory
+    (2, 96, "bf16", True, (300, 129, 64), (310, 200, 64)),  # a head dim of 96
 ]
 
 
