@@ -344,6 +344,9 @@ def run_ours(args) -> None:
                      "peak_kind": f"bf16 sustained ({peaks['source']})",
                      "algorithmic_tflop_per_launch": dom_flops / 1e12, "traffic": traffic},
         "e2e": e2e, "clocks": clock_info, "gpu_launches": 4 * args.steps,
+        "env": {"gpu": torch.cuda.get_device_name(), "torch": torch.__version__,
+                "cuda": torch.version.cuda,
+                "sm_count": torch.cuda.get_device_properties(0).multi_processor_count},
     }
     if not args.no_decode:
         line["decode"] = measure_decode(args, peaks)
