@@ -509,7 +509,8 @@ def load_traffic(kernel: str, workload: str):
 KERNEL_SOURCES = {
     "fwd": ["fwd.cuh", "fwd_persistent.cuh", "kernels_fwd.cu"],
     "delta": ["bwd_delta.cuh", "kernels_delta.cu"],
-    "dkv": ["bwd_dkv.cuh", "bwd_dq.cuh", "kernels_dkv.cu"],
+    "dkv": ["bwd_dkv.cuh", "bwd_dkv_persistent.cuh", "bwd_dq.cuh", "bwd_dq_persistent.cuh",
+            "kernels_dkv.cu"],
     "dq": ["bwd_dq.cuh", "bwd_dq_persistent.cuh", "kernels_dq.cu"],
 }
 COMMON_SOURCES = ["common.cuh", "ptx.cuh", "launch.h", "varlen.h"]

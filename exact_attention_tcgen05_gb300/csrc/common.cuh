@@ -23,7 +23,8 @@ enum WaitSite : int {
   kWaitDqQ = 0x21, kWaitDqK, kWaitDqV, kWaitDqEmpty, kWaitDqS, kWaitDqDP, kWaitDqDS,
   kWaitDqDone, kWaitDqDrain, kWaitDqSC, kWaitDqQFree, kWaitDqAccFree,
   kWaitDkvKV = 0x31, kWaitDkvQ, kWaitDkvDO, kWaitDkvEmpty, kWaitDkvS, kWaitDkvDP,
-  kWaitDkvP, kWaitDkvDS, kWaitDkvDone, kWaitDkvDrain, kWaitDkvStats,
+  kWaitDkvP, kWaitDkvDS, kWaitDkvDone, kWaitDkvDrain, kWaitDkvStats, kWaitDkvKVFree,
+  kWaitDkvAccFree,
   kWaitDecFull = 0x41, kWaitDecDrain,
   kErrSeqlens = kStatusBadSeqlens,  // a packed batch's cu_seqlens hold a bad sequence
   kErrSmemAlign = 0x7F  // dynamic shared memory not 1024-byte aligned (kernel skipped)

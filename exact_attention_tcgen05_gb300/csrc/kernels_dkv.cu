@@ -1,8 +1,35 @@
 // kernels_dkv.cu - instantiation and launch of the backward dK/dV kernel.
-#include "bwd_dkv.cuh"
+#include <algorithm>
+#include <cstdlib>
+
+#include "bwd_dkv_persistent.cuh"
 #include "launch.h"
 
 namespace attn {
+
+static int sm_count_dkv() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 152;
+  return n;
+}
+
+// Which dK/dV kernel: the persistent one (bwd_dkv_persistent.cuh) when a key block meets
+// fewer than 8 query blocks on average (short work items, where the one-item kernel's fixed
+// cost per CTA dominates); otherwise one CTA per key block. ATTN_BWD_PERSISTENT = 0 / 1
+// forces either (both give the same bits; the persistent one keeps K_j, V_j in shared
+// memory).
+static bool use_persistent_dkv(const Shape& s, bool kv_tmem) {
+  static const int forced = [] {
+    const char* e = std::getenv("ATTN_BWD_PERSISTENT");
+    return e == nullptr ? -1 : (e[0] == '0' ? 0 : 1);
+  }();
+  if (forced >= 0) return forced == 1;
+  if (kv_tmem) return false;
+  const int nb = (s.N + kTileM - 1) / kTileM;
+  return (s.causal ? (nb + 1) / 2 : nb) < 8;
+}
 
 template <int D, bool BF16>
 static cudaError_t launch_dkv_t(const Maps& m, const Shape& s, const void* q, const void* k,
@@ -37,8 +64,22 @@ static cudaError_t launch_dkv_t(const Maps& m, const Shape& s, const void* q, co
   p.scale = s.scale;
   p.scale_log2 = s.scale * kLog2e;
   p.wait_limit = s.wait_limit;
-  // One CTA per 128-key block (packed batches: of the longest sequence).
-  dim3 grid((s.Nk + kTileN - 1) / kTileN, s.BH);
+  const int nkb_max = (s.Nk + kTileN - 1) / kTileN;  // packed batches: the longest sequence
+  if (use_persistent_dkv(s, kv_tmem)) {
+    using CP = DkvPCfg<D>;
+    auto kp = s.vl.cu_q != nullptr ? attn_bwd_dkv_persistent_kernel<D, BF16, true>
+                                   : attn_bwd_dkv_persistent_kernel<D, BF16, false>;
+    e = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, CP::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int npairs = (nkb_max + 1) / 2;
+    const long long n_pairs = (long long)npairs * s.BH;
+    const int grid = (int)std::min<long long>(n_pairs, sm_count_dkv());
+    kp<<<grid, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, m.d_o, p, (int)n_pairs,
+                                                   npairs, nkb_max);
+    return cudaGetLastError();
+  }
+  // One CTA per 128-key block.
+  dim3 grid(nkb_max, s.BH);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(m.q, m.k, m.v, m.d_o, p);
   return cudaGetLastError();
 }

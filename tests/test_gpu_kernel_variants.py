@@ -1,7 +1,7 @@
 """The persistent and the one-item kernels give the same bits.
 
-The forward and the dQ kernel each exist as a persistent kernel (one CTA per SM walking
-many work items) and as one CTA per item; which forward runs depends on the shape, and
+The forward, dK/dV and dQ kernels each exist as a persistent kernel (one CTA per SM walking
+many work items) and as one CTA per item; which one runs depends on the shape, and
 ATTN_FWD_PERSISTENT / ATTN_BWD_PERSISTENT = 0 / 1 force either. Both compute every tile in
 the same order with the same rounding, so O, LSE, dQ, dK and dV must agree bit for bit.
 Each setting runs in a child process of its own (the variables are read once per process)
