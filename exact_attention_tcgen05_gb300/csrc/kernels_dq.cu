@@ -15,11 +15,15 @@ static int sm_count_dq() {
   return n;
 }
 
-// Which dQ kernel: the persistent one (bwd_dq_persistent.cuh) when the average item is short
-// (fewer than 8 key blocks), where the one-item kernel's fixed cost per CTA (about 7 us on
-// GB300, as much as 8 blocks of work) dominates; otherwise one CTA per item, whose dynamic
-// hardware scheduling balances the causal work better than the persistent kernel's static
-// pairs (about 13.5 rounds of pairs per SM on a B4 H32 N4096 step leave a 4% tail).
+// Which dQ kernel: the persistent one (bwd_dq_persistent.cuh) or one CTA per item. The
+// one-item kernel pays a fixed cost per CTA (about 7 us on GB300, as much as 8 blocks of
+// work) but the hardware schedules its CTAs dynamically; the persistent kernel removes most
+// of that cost, but its static long/short pairs end when the busiest SM ends: after
+// ceil(pairs / SMs) rounds, against pairs / SMs rounds of work. Measured on GB300: the
+// persistent kernel wins for items shorter than 8 key blocks whatever the rounds, wins or
+// ties up to 16 blocks when the last round is at least 95% full (B4 H32 N4096 causal:
+// 13.5 rounds, 0.621 -> 0.599 ms), and ties or loses for longer items or emptier last
+// rounds (10.1 rounds at N3072 and N6144; B2 H32 N8192 d64 full: 1.375 -> 1.430 ms).
 // ATTN_BWD_PERSISTENT = 0 / 1 forces either (both give the same bits).
 static bool use_persistent_dq(const Shape& s) {
   static const int forced = [] {
@@ -29,7 +33,15 @@ static bool use_persistent_dq(const Shape& s) {
   if (forced >= 0) return forced == 1;
   const int nkb = (s.Nk + kTileN - 1) / kTileN;
   const int blocks_per_item = s.causal ? (nkb + 1) / 2 : nkb;
-  return blocks_per_item < 8;
+  if (blocks_per_item < 8) return true;
+  // Packed batches: pairs of sequences shorter than the longest are skipped, so the round
+  // count says little about the balance (an 8-sequence batch of 601-4008 tokens took
+  // 1.54 -> 1.57 ms per step with the persistent dQ).
+  if (blocks_per_item > 16 || s.vl.cu_q != nullptr) return false;
+  const long long n_pairs = (long long)(((s.N + kTileM - 1) / kTileM + 1) / 2) * s.BH;
+  const long long sms = sm_count_dq();
+  const long long rounds = (n_pairs + sms - 1) / sms;
+  return n_pairs * 20 >= rounds * sms * 19;
 }
 
 template <int D, bool BF16>
