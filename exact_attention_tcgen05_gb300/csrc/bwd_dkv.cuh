@@ -26,15 +26,17 @@ template <int D>
 struct DkvCfg : BwdCfg<D> {
   using B = BwdCfg<D>;
   static constexpr int kThreads = 320;
+  // Q/dO ring depth: three blocks at d = 64 (shared memory has room), two at d = 128.
+  static constexpr int kStages = D == 64 ? 3 : 2;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + B::kTileBytes;
   static constexpr int kOffQ = kOffV + B::kTileBytes;
-  static constexpr int kOffDO = kOffQ + B::kStages * B::kTileBytes;
-  static constexpr int kOffStats = kOffDO + B::kStages * B::kTileBytes;  // 2 x (128 + 128) f32
+  static constexpr int kOffDO = kOffQ + kStages * B::kTileBytes;
+  static constexpr int kOffStats = kOffDO + kStages * B::kTileBytes;  // 2 x (128 + 128) f32
   static constexpr int kOffBar = kOffStats + 2 * 256 * 4;
   // kv_full, q_full[S], do_full[S], qdo_empty[S], s_full, p_full, dp_full, ds_full,
   // acc_done, drain, stats_ready[2]
-  static constexpr int kNumBars = 1 + 3 * B::kStages + 8;
+  static constexpr int kNumBars = 1 + 3 * kStages + 8;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes =
       (kOffMisc + 16 + 1024) > B::kMinSmem ? (kOffMisc + 16 + 1024) : B::kMinSmem;

@@ -39,6 +39,13 @@ o, lse = binding.attn_fwd_varlen(q, k, v, cq, cq, wv.max_q, wv.max_k, causal=Tru
 dq, dk, dv = binding.attn_bwd_varlen(q, k, v, o, lse, do, cq, cq, wv.max_q, wv.max_k,
                                      causal=True)
 out["packed"] = tuple(x.cpu() for x in (o, lse, dq, dk, dv))
+wv = I.varlen(3, 64, "fp16", True, seed=4, seqlens_q=(300, 1, 900, 129, 40))
+q, k, v, do = (I.make_varlen_tensor(wv, t).cuda() for t in ("q", "k", "v", "do"))
+cq = torch.tensor(wv.cu_q, dtype=torch.int32, device="cuda")
+o, lse = binding.attn_fwd_varlen(q, k, v, cq, cq, wv.max_q, wv.max_k, causal=True)
+dq, dk, dv = binding.attn_bwd_varlen(q, k, v, o, lse, do, cq, cq, wv.max_q, wv.max_k,
+                                     causal=True)
+out["packed_d64"] = tuple(x.cpu() for x in (o, lse, dq, dk, dv))
 torch.cuda.synchronize()
 assert binding.attn_last_kernel_status() == (0, 0)
 torch.save(out, sys.argv[2])
