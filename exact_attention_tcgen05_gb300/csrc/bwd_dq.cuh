@@ -62,9 +62,10 @@ template <int D>
 struct DqCfg : BwdCfg<D> {
   using B = BwdCfg<D>;
   // Q_i and dO_i go straight from global memory to tensor memory, so shared memory holds
-  // only the K/V ring, three blocks deep: block j + 3 can be fetched as soon as dQ of
-  // block j (the last reader of its K) has been issued and has finished.
-  static constexpr int kStages = 3;
+  // only the K/V ring: block j + S can be fetched as soon as dQ of block j (the last reader
+  // of its K) has been issued and has finished. S = 3 at d = 128 (192 KiB), 4 at d = 64
+  // (B2 H32 N8192 d64 on GB300: 1.371 -> 1.358 ms against 3).
+  static constexpr int kStages = D == 64 ? 4 : 3;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kStages * B::kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * B::kTileBytes;
