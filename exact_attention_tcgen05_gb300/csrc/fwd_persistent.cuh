@@ -15,9 +15,12 @@
 // rounding): the outputs are bit-identical.
 //
 // Schedule: items are numbered head by head, longest (most key blocks) first within a
-// head, so the CTAs working at one time share the K/V of a few heads in L2. CTA c takes
-// items c, 2G - 1 - c, 2G + c, 4G - 1 - c, ... (G CTAs): a serpentine over the list,
-// which pairs a long causal item of one round with a short one of the next.
+// head, so the CTAs working at one time share the K/V of a few heads in L2. By default CTA
+// c takes items c, 2G - 1 - c, 2G + c, 4G - 1 - c, ... (G CTAs): a serpentine over the
+// list, which pairs a long causal item of one round with a short one of the next. With
+// few rounds of unequal causal items that leaves the busiest CTA well above the mean, so
+// for dense causal inputs the host computes a longest-first greedy assignment instead
+// (kernels_fwd.cu) and passes it as a table in the kernel's parameters.
 //
 // Barrier phases: every barrier completes once per event of a running count kept alike by
 // all roles (blocks per tile, items per tile, Q loads, ring fills), and a wait names the
@@ -43,6 +46,25 @@ struct FwdItem {
 __device__ __forceinline__ int fwd_item_index(int k, int G, int c, int n_items) {
   const int i = k * G + ((k & 1) ? (G - 1 - c) : c);
   return i < n_items ? i : -1;
+}
+
+// The schedule types the persistent kernel takes (by value, as a kernel parameter): the
+// serpentine above, or a table in which CTA c walks items[start[c]] .. items[start[c+1]-1]
+// (29 KiB: kernel parameters may take up to 32 KiB).
+struct FwdSerpentine {};
+constexpr int kFwdSchedMaxItems = 14336;
+constexpr int kFwdSchedMaxCtas = 255;
+struct FwdSched {
+  uint16_t start[kFwdSchedMaxCtas + 1];
+  uint16_t items[kFwdSchedMaxItems];
+};
+__device__ __forceinline__ int fwd_sched_item(const FwdSerpentine&, int k, int G, int c,
+                                              int n_items) {
+  return fwd_item_index(k, G, c, n_items);
+}
+__device__ __forceinline__ int fwd_sched_item(const FwdSched& t, int k, int, int c, int) {
+  const int i = t.start[c] + k;
+  return i < t.start[c + 1] ? t.items[i] : -1;
 }
 
 // Geometry of item `item` (nqb_max query blocks per slice). False: nothing to do (a packed
@@ -80,12 +102,12 @@ struct FwdPCfg : FwdCfg<D> {
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 };
 
-template <int D, bool BF16, bool PACKED>
+template <int D, bool BF16, bool PACKED, class Sched>
 __global__ void __launch_bounds__(320, 1)
     attn_fwd_persistent_kernel(const __grid_constant__ CUtensorMap map_q,
                                const __grid_constant__ CUtensorMap map_k,
                                const __grid_constant__ CUtensorMap map_v, const FwdParams p,
-                               int n_items, int nqb_max) {
+                               int n_items, int nqb_max, const __grid_constant__ Sched sched) {
   using C = FwdPCfg<D>;
   constexpr int NS = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -148,7 +170,7 @@ __global__ void __launch_bounds__(320, 1)
     __syncwarp();
     int q_loads = 0, kv_loads = 0;  // copies issued so far (running counts)
     for (int k = 0;; ++k) {
-      const int item = fwd_item_index(k, G, cta, n_items);
+      const int item = fwd_sched_item(sched, k, G, cta, n_items);
       if (item < 0) break;
       FwdItem it;
       if (!fwd_item_geom<D, PACKED>(p, item, nqb_max, it)) continue;
@@ -229,7 +251,7 @@ __global__ void __launch_bounds__(320, 1)
     int tb[2] = {0, 0}, ti[2] = {0, 0};
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const int item = fwd_item_index(k, G, cta, n_items);
+      const int item = fwd_sched_item(sched, k, G, cta, n_items);
       if (item < 0) break;
       FwdItem it;
       if (!fwd_item_geom<D, PACKED>(p, item, nqb_max, it)) continue;
@@ -377,7 +399,7 @@ __global__ void __launch_bounds__(320, 1)
     int tb = 0;  // blocks of this tile so far (running count, as the MMA warp keeps it)
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const int item = fwd_item_index(k, G, cta, n_items);
+      const int item = fwd_sched_item(sched, k, G, cta, n_items);
       if (item < 0) break;
       FwdItem it;
       if (!fwd_item_geom<D, PACKED>(p, item, nqb_max, it)) continue;

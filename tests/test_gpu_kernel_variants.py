@@ -26,7 +26,9 @@ from exact_attention_tcgen05_gb300 import inputs as I
 out = {}
 for (B, H, N, d, dt, causal) in [(2, 3, 1000, 128, "bf16", True), (1, 4, 777, 64, "fp16", False),
                                  (3, 2, 2100, 64, "bf16", True), (1, 2, 4096, 64, "bf16", False),
-                                 (1, 1, 300, 128, "fp16", False)]:
+                                 (1, 1, 300, 128, "fp16", False),
+                                 # more causal items than SMs: the forward's scheduled order
+                                 (4, 16, 1280, 128, "bf16", True), (8, 8, 1024, 64, "fp16", True)]:
     w = I.custom(B, H, N, d, dt, causal, seed=N + d)
     q, k, v, do = (I.make_tensor(w, t).cuda() for t in ("q", "k", "v", "do"))
     o, lse = binding.attn_fwd(q, k, v, causal=causal, scale=w.scale)
