@@ -59,13 +59,14 @@ struct DkvPCfg : DkvCfg<D> {
       (kOffMisc + 16 + 1024) > B::kMinSmem ? (kOffMisc + 16 + 1024) : B::kMinSmem;
 };
 
-template <int D, bool BF16, bool PACKED>
+template <int D, bool BF16, bool PACKED, class Sched>
 __global__ void __launch_bounds__(320, 1)
     attn_bwd_dkv_persistent_kernel(const __grid_constant__ CUtensorMap map_q,
                                    const __grid_constant__ CUtensorMap map_k,
                                    const __grid_constant__ CUtensorMap map_v,
                                    const __grid_constant__ CUtensorMap map_do,
-                                   const BwdParams p, int n_pairs, int npairs, int nkb_max) {
+                                   const BwdParams p, int n_pairs, int npairs, int nkb_max,
+                                   const __grid_constant__ Sched sched) {
   using C = DkvPCfg<D>;
   constexpr int NS = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(320, 1)
     int kv_loads = 0, loads = 0;  // K/V copies (items) and ring blocks issued so far
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const int item = bwd_pair_item(k, G, cta, n_pairs, npairs, nkb_max);
+      const int item = sched_item(sched, k, G, cta, n_pairs, npairs, nkb_max);
       if (item == -1) break;
       DkvItem it;
       if (item < 0 || !dkv_item_geom<D, PACKED>(p, item, nkb_max, it) || it.n == 0) continue;
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(320, 1)
     int items = 0, tb = 0;  // items and blocks so far
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const int item = bwd_pair_item(k, G, cta, n_pairs, npairs, nkb_max);
+      const int item = sched_item(sched, k, G, cta, n_pairs, npairs, nkb_max);
       if (item == -1) break;
       DkvItem it;
       if (item < 0 || !dkv_item_geom<D, PACKED>(p, item, nkb_max, it) || it.n == 0) continue;
@@ -297,7 +298,7 @@ __global__ void __launch_bounds__(320, 1)
     int items = 0, tb = 0;  // items and blocks so far
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const int item = bwd_pair_item(k, G, cta, n_pairs, npairs, nkb_max);
+      const int item = sched_item(sched, k, G, cta, n_pairs, npairs, nkb_max);
       if (item == -1) break;
       DkvItem it;
       if (item < 0 || !dkv_item_geom<D, PACKED>(p, item, nkb_max, it)) continue;

@@ -26,6 +26,7 @@
 #pragma once
 
 #include "bwd_dq.cuh"
+#include "schedule.h"
 
 namespace attn {
 
@@ -47,6 +48,18 @@ __device__ __forceinline__ int bwd_pair_item(int k, int G, int c, int n_pairs, i
   const int x = (k & 1) ? nb_max - 1 - pp : pp;
   if ((k & 1) && x == pp) return -2;
   return slice * nb_max + x;
+}
+
+// The schedule types the persistent backward kernels take (by value, as a kernel
+// parameter): the long/short pairs dealt round-robin above, or an ItemTable (schedule.h),
+// which the host builds for dense causal inputs.
+struct PairSchedule {};
+__device__ __forceinline__ int sched_item(const PairSchedule&, int k, int G, int c, int n_pairs,
+                                          int npairs, int nb_max) {
+  return bwd_pair_item(k, G, c, n_pairs, npairs, nb_max);
+}
+__device__ __forceinline__ int sched_item(const ItemTable& t, int k, int, int c, int, int, int) {
+  return table_item(t, k, c);
 }
 
 // Geometry of dQ item `item` (nb_max query blocks per slice). False: nothing to do.
@@ -107,13 +120,14 @@ __device__ __forceinline__ void store_row_tmem(const uint32_t (&r)[D / 2], uint3
     tmem_st32(t_col + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(&r[32 * c]));
 }
 
-template <int D, bool BF16, bool PACKED>
+template <int D, bool BF16, bool PACKED, class Sched>
 __global__ void __launch_bounds__(320, 1)
     attn_bwd_dq_persistent_kernel(const __grid_constant__ CUtensorMap map_q,
                                   const __grid_constant__ CUtensorMap map_k,
                                   const __grid_constant__ CUtensorMap map_v,
                                   const __grid_constant__ CUtensorMap map_do, const BwdParams p,
-                                  int n_pairs, int npairs, int nb_max) {
+                                  int n_pairs, int npairs, int nb_max,
+                                  const __grid_constant__ Sched sched) {
   using C = DqPCfg<D>;
   constexpr int NS = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -176,7 +190,7 @@ __global__ void __launch_bounds__(320, 1)
     int loads = 0;  // ring blocks issued so far
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const int item = bwd_pair_item(k, G, cta, n_pairs, npairs, nb_max);
+      const int item = sched_item(sched, k, G, cta, n_pairs, npairs, nb_max);
       if (item == -1) break;
       DqItem it;
       if (item < 0 || !dq_item_geom<D, PACKED>(p, item, nb_max, it)) continue;
@@ -225,7 +239,7 @@ __global__ void __launch_bounds__(320, 1)
     int items = 0, tb = 0;  // items and blocks so far
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const int item = bwd_pair_item(k, G, cta, n_pairs, npairs, nb_max);
+      const int item = sched_item(sched, k, G, cta, n_pairs, npairs, nb_max);
       if (item == -1) break;
       DqItem it;
       if (item < 0 || !dq_item_geom<D, PACKED>(p, item, nb_max, it)) continue;
@@ -318,7 +332,7 @@ __global__ void __launch_bounds__(320, 1)
     // The next item of this CTA (false past the end).
     auto next_item = [&](DqItem& it) -> bool {
       for (;; ++k) {
-        const int item = bwd_pair_item(k, G, cta, n_pairs, npairs, nb_max);
+        const int item = sched_item(sched, k, G, cta, n_pairs, npairs, nb_max);
         if (item == -1) return false;
         if (item >= 0 && dq_item_geom<D, PACKED>(p, item, nb_max, it)) {
           ++k;

@@ -30,6 +30,7 @@
 #pragma once
 
 #include "fwd.cuh"
+#include "schedule.h"
 
 namespace attn {
 
@@ -49,22 +50,14 @@ __device__ __forceinline__ int fwd_item_index(int k, int G, int c, int n_items) 
 }
 
 // The schedule types the persistent kernel takes (by value, as a kernel parameter): the
-// serpentine above, or a table in which CTA c walks items[start[c]] .. items[start[c+1]-1]
-// (29 KiB: kernel parameters may take up to 32 KiB).
+// serpentine above, or an ItemTable (schedule.h).
 struct FwdSerpentine {};
-constexpr int kFwdSchedMaxItems = 14336;
-constexpr int kFwdSchedMaxCtas = 255;
-struct FwdSched {
-  uint16_t start[kFwdSchedMaxCtas + 1];
-  uint16_t items[kFwdSchedMaxItems];
-};
 __device__ __forceinline__ int fwd_sched_item(const FwdSerpentine&, int k, int G, int c,
                                               int n_items) {
   return fwd_item_index(k, G, c, n_items);
 }
-__device__ __forceinline__ int fwd_sched_item(const FwdSched& t, int k, int, int c, int) {
-  const int i = t.start[c] + k;
-  return i < t.start[c + 1] ? t.items[i] : -1;
+__device__ __forceinline__ int fwd_sched_item(const ItemTable& t, int k, int, int c, int) {
+  return table_item(t, k, c);
 }
 
 // Geometry of item `item` (nqb_max query blocks per slice). False: nothing to do (a packed

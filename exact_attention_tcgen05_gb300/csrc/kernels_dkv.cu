@@ -1,6 +1,7 @@
 // kernels_dkv.cu - instantiation and launch of the backward dK/dV kernel.
 #include <algorithm>
 #include <cstdlib>
+#include <vector>
 
 #include "bwd_dkv_persistent.cuh"
 #include "launch.h"
@@ -19,17 +20,46 @@ static int sm_count_dkv() {
 // where the one-item kernel's fixed cost per CTA dominates: a key block meets fewer than 8
 // query blocks on average (causal), or at most 8 (non-causal: every item is equally long,
 // and B16 H32 N1024 d128 ran 0.521 -> 0.485 ms on GB300, while causal N2048 ran 1% slower);
-// otherwise one CTA per key block. ATTN_BWD_PERSISTENT = 0 / 1 forces either (both give the
-// same bits; the persistent one keeps K_j, V_j in shared memory).
+// otherwise one CTA per key block. Dense causal inputs with more items than CTAs get a
+// greedy table (schedule.h) instead of the pairs; with it the persistent kernel won or tied
+// on every causal shape measured (B4 H32 N4096: 0.786 -> 0.772 ms; at d = 64 also against
+// the one-item kernel's K_j, V_j in tensor memory: B8 H32 N2048 0.394 -> 0.349 ms), so it
+// always runs there. ATTN_BWD_PERSISTENT = 0 / 1 forces either (both give the same bits;
+// the persistent one keeps K_j, V_j in shared memory).
 static bool use_persistent_dkv(const Shape& s, bool kv_tmem) {
   static const int forced = [] {
     const char* e = std::getenv("ATTN_BWD_PERSISTENT");
     return e == nullptr ? -1 : (e[0] == '0' ? 0 : 1);
   }();
   if (forced >= 0) return forced == 1;
+  const long long n_items = (long long)((s.Nk + kTileN - 1) / kTileN) * s.BH;
+  if (item_table_applies(s.causal, s.vl.cu_q != nullptr, n_items,
+                         (int)std::min<long long>(n_items, sm_count_dkv())))
+    return true;
   if (kv_tmem) return false;
   const int nb = (s.N + kTileM - 1) / kTileM;
   return s.causal ? (nb + 1) / 2 < 8 : nb <= 8;
+}
+
+// The persistent dK/dV's table (schedule.h) for dense causal inputs with more items than
+// CTAs: item jb of a slice is key block jb, its cost the query blocks that see it + 1,
+// windows of heads by their Q/dO bytes. False: the long/short pairs run.
+static bool dkv_schedule(const Shape& s, int nkb, int G, ItemTable& out) {
+  const long long n_items = (long long)nkb * s.BH;
+  if (!item_table_applies(s.causal, s.vl.cu_q != nullptr, n_items, G)) return false;
+  static ItemTableCache cache;
+  const long long k[6] = {s.BH, s.N, s.Nk, s.d, G, nkb};
+  cache.get(k, G, n_items, out, [&](ItemTable& t) {
+    const int nb = (s.N + kTileM - 1) / kTileM, off = s.Nk - s.N;
+    std::vector<long long> cost(nkb);
+    for (int jb = 0; jb < nkb; ++jb) {
+      const int j0 = jb * kTileN;
+      const int i_first = j0 > off ? (j0 - off) / kTileM : 0;
+      cost[jb] = std::max(0, nb - i_first) + 1;
+    }
+    greedy_item_table(s.BH, nkb, cost, item_table_window(s.BH, 4LL * s.N * s.d), G, t);
+  });
+  return true;
 }
 
 template <int D, bool BF16>
@@ -68,15 +98,26 @@ static cudaError_t launch_dkv_t(const Maps& m, const Shape& s, const void* q, co
   const int nkb_max = (s.Nk + kTileN - 1) / kTileN;  // packed batches: the longest sequence
   if (use_persistent_dkv(s, kv_tmem)) {
     using CP = DkvPCfg<D>;
-    auto kp = s.vl.cu_q != nullptr ? attn_bwd_dkv_persistent_kernel<D, BF16, true>
-                                   : attn_bwd_dkv_persistent_kernel<D, BF16, false>;
-    e = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, CP::kSmemBytes);
-    if (e != cudaSuccess) return e;
     const int npairs = (nkb_max + 1) / 2;
     const long long n_pairs = (long long)npairs * s.BH;
+    const int gt = (int)std::min<long long>((long long)nkb_max * s.BH, sm_count_dkv());
+    static thread_local ItemTable table;  // 29 KiB: not on the stack
+    if (dkv_schedule(s, nkb_max, gt, table)) {
+      auto kt = attn_bwd_dkv_persistent_kernel<D, BF16, false, ItemTable>;
+      e = cudaFuncSetAttribute(kt, cudaFuncAttributeMaxDynamicSharedMemorySize, CP::kSmemBytes);
+      if (e != cudaSuccess) return e;
+      kt<<<gt, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, m.d_o, p, (int)n_pairs,
+                                                   npairs, nkb_max, table);
+      return cudaGetLastError();
+    }
+    auto kp = s.vl.cu_q != nullptr
+                  ? attn_bwd_dkv_persistent_kernel<D, BF16, true, PairSchedule>
+                  : attn_bwd_dkv_persistent_kernel<D, BF16, false, PairSchedule>;
+    e = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, CP::kSmemBytes);
+    if (e != cudaSuccess) return e;
     const int grid = (int)std::min<long long>(n_pairs, sm_count_dkv());
     kp<<<grid, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, m.d_o, p, (int)n_pairs,
-                                                   npairs, nkb_max);
+                                                   npairs, nkb_max, PairSchedule{});
     return cudaGetLastError();
   }
   // One CTA per 128-key block.

@@ -1,6 +1,7 @@
 // kernels_dq.cu - instantiation and launch of the backward dQ kernel.
 #include <algorithm>
 #include <cstdlib>
+#include <vector>
 
 #include "bwd_dq_persistent.cuh"
 #include "launch.h"
@@ -24,6 +25,10 @@ static int sm_count_dq() {
 // ties up to 16 blocks when the last round is at least 95% full (B4 H32 N4096 causal:
 // 13.5 rounds, 0.621 -> 0.599 ms), and ties or loses for longer items or emptier last
 // rounds (10.1 rounds at N3072 and N6144; B2 H32 N8192 d64 full: 1.375 -> 1.430 ms).
+// Dense causal inputs with more items than CTAs get a greedy table (schedule.h) instead of
+// the pairs, which balances any number of rounds; with it the persistent kernel won or tied
+// on every causal shape measured (N = 1024-16384, d = 64 and 128; B4 H32 N4096:
+// 0.602 -> 0.577 ms), so it always runs there.
 // ATTN_BWD_PERSISTENT = 0 / 1 forces either (both give the same bits).
 static bool use_persistent_dq(const Shape& s) {
   static const int forced = [] {
@@ -31,6 +36,10 @@ static bool use_persistent_dq(const Shape& s) {
     return e == nullptr ? -1 : (e[0] == '0' ? 0 : 1);
   }();
   if (forced >= 0) return forced == 1;
+  const long long n_items = (long long)((s.N + kTileM - 1) / kTileM) * s.BH;
+  if (item_table_applies(s.causal, s.vl.cu_q != nullptr, n_items,
+                         (int)std::min<long long>(n_items, sm_count_dq())))
+    return true;
   const int nkb = (s.Nk + kTileN - 1) / kTileN;
   const int blocks_per_item = s.causal ? (nkb + 1) / 2 : nkb;
   if (blocks_per_item < 8) return true;
@@ -42,6 +51,24 @@ static bool use_persistent_dq(const Shape& s) {
   const long long sms = sm_count_dq();
   const long long rounds = (n_pairs + sms - 1) / sms;
   return n_pairs * 20 >= rounds * sms * 19;
+}
+
+// The persistent dQ's table (schedule.h) for dense causal inputs with more items than
+// CTAs: item x of a slice is query block nb - 1 - x, its cost the key blocks it sees + 1,
+// windows of heads by their K/V bytes. False: the long/short pairs run.
+static bool dq_schedule(const Shape& s, int nb, int G, ItemTable& out) {
+  const long long n_items = (long long)nb * s.BH;
+  if (!item_table_applies(s.causal, s.vl.cu_q != nullptr, n_items, G)) return false;
+  static ItemTableCache cache;
+  const long long k[6] = {s.BH, s.N, s.Nk, s.d, G, nb};
+  cache.get(k, G, n_items, out, [&](ItemTable& t) {
+    const int nkb = (s.Nk + kTileN - 1) / kTileN, off = s.Nk - s.N;
+    std::vector<long long> cost(nb);
+    for (int x = 0; x < nb; ++x)
+      cost[x] = std::min(nkb, ((nb - 1 - x) * kTileM + kTileM - 1 + off) / kTileN + 1) + 1;
+    greedy_item_table(s.BH, nb, cost, item_table_window(s.BH, 4LL * s.Nk * s.d), G, t);
+  });
+  return true;
 }
 
 template <int D, bool BF16>
@@ -74,15 +101,25 @@ static cudaError_t launch_dq_t(const Maps& m, const Shape& s, const void* q,
   const int nb_max = (s.N + kTileM - 1) / kTileM;  // packed batches: the longest sequence
   if (use_persistent_dq(s)) {
     using CP = DqPCfg<D>;
-    auto kp = s.vl.cu_q != nullptr ? attn_bwd_dq_persistent_kernel<D, BF16, true>
-                                   : attn_bwd_dq_persistent_kernel<D, BF16, false>;
-    e = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, CP::kSmemBytes);
-    if (e != cudaSuccess) return e;
     const int npairs = (nb_max + 1) / 2;
     const long long n_pairs = (long long)npairs * s.BH;
+    const int gt = (int)std::min<long long>((long long)nb_max * s.BH, sm_count_dq());
+    static thread_local ItemTable table;  // 29 KiB: not on the stack
+    if (dq_schedule(s, nb_max, gt, table)) {
+      auto kt = attn_bwd_dq_persistent_kernel<D, BF16, false, ItemTable>;
+      e = cudaFuncSetAttribute(kt, cudaFuncAttributeMaxDynamicSharedMemorySize, CP::kSmemBytes);
+      if (e != cudaSuccess) return e;
+      kt<<<gt, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, m.d_o, p, (int)n_pairs,
+                                                   npairs, nb_max, table);
+      return cudaGetLastError();
+    }
+    auto kp = s.vl.cu_q != nullptr ? attn_bwd_dq_persistent_kernel<D, BF16, true, PairSchedule>
+                                   : attn_bwd_dq_persistent_kernel<D, BF16, false, PairSchedule>;
+    e = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, CP::kSmemBytes);
+    if (e != cudaSuccess) return e;
     const int grid = (int)std::min<long long>(n_pairs, sm_count_dq());
     kp<<<grid, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, m.d_o, p, (int)n_pairs,
-                                                   npairs, nb_max);
+                                                   npairs, nb_max, PairSchedule{});
     return cudaGetLastError();
   }
   // One CTA per 128-row query block.

@@ -1,11 +1,6 @@
 // kernels_fwd.cu - instantiation and launch of the forward kernel.
 #include <algorithm>
 #include <cstdlib>
-#include <cstring>
-#include <functional>
-#include <mutex>
-#include <queue>
-#include <utility>
 #include <vector>
 
 #include "fwd.cuh"
@@ -51,58 +46,19 @@ static int fwd_item_blocks(const Shape& s, int nqb, int x) {
   return n;
 }
 
-// A longest-first greedy assignment of the persistent forward's items to G CTAs, for
-// dense causal inputs: the items of a window of W heads, sorted by key blocks (longest
-// first, head order among equals), each go to the CTA that becomes free first, counting
-// one block more per item for its fixed cost. W keeps the K/V of the heads in flight (at
-// most two windows) within about 96 MiB of the 126 MiB L2. False: not worth it or too
-// large for the table (then the serpentine order runs). The last table is kept (one entry
-// keyed by the shape) and copied into `out` under the lock.
-static bool fwd_schedule(const Shape& s, int nqb, int G, FwdSched& out) {
+// The persistent forward's table (schedule.h) for dense causal inputs with more items than
+// CTAs: cost = key blocks + 1 for an item's fixed cost, windows of heads by their K/V
+// bytes. False: the serpentine runs.
+static bool fwd_schedule(const Shape& s, int nqb, int G, ItemTable& out) {
   const long long n_items = (long long)nqb * s.BH;
-  if (!s.causal || s.vl.cu_q != nullptr || n_items <= G || n_items > kFwdSchedMaxItems ||
-      G > kFwdSchedMaxCtas)
-    return false;
-  static std::mutex mu;
-  static FwdSched table;
-  static long long key[6] = {-1, -1, -1, -1, -1, -1};
+  if (!item_table_applies(s.causal, s.vl.cu_q != nullptr, n_items, G)) return false;
+  static ItemTableCache cache;
   const long long k[6] = {s.BH, s.N, s.Nk, s.d, G, nqb};
-  std::lock_guard<std::mutex> lock(mu);
-  if (std::memcmp(k, key, sizeof(k)) != 0) {
-    std::vector<int> len(nqb);
-    for (int x = 0; x < nqb; ++x) len[x] = fwd_item_blocks(s, nqb, x);
-    std::vector<int> by_len(nqb);  // x values, longest first (x ascending among equals)
-    for (int x = 0; x < nqb; ++x) by_len[x] = x;
-    std::stable_sort(by_len.begin(), by_len.end(), [&](int a, int b) { return len[a] > len[b]; });
-    const long long kv_bytes = 4LL * s.Nk * s.d;  // K and V of one head, 16-bit
-    const int W = (int)std::max(1LL, std::min<long long>(s.BH, (48LL << 20) / kv_bytes));
-    using Slot = std::pair<long long, int>;  // (busy until, CTA)
-    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
-    for (int c = 0; c < G; ++c) free_at.push({0, c});
-    std::vector<int> owner(n_items), order;
-    order.reserve(n_items);
-    for (int h0 = 0; h0 < s.BH; h0 += W) {
-      const int h1 = std::min(s.BH, h0 + W);
-      for (int x : by_len)
-        for (int h = h0; h < h1; ++h) {
-          const int item = h * nqb + x;
-          Slot sl = free_at.top();
-          free_at.pop();
-          owner[item] = sl.second;
-          order.push_back(item);
-          free_at.push({sl.first + len[x] + 1, sl.second});
-        }
-    }
-    // Items grouped by CTA, each CTA's in assignment order.
-    std::vector<int> count(G + 1, 0);
-    for (int item : order) ++count[owner[item] + 1];
-    for (int c = 0; c < G; ++c) count[c + 1] += count[c];
-    for (int c = 0; c <= G; ++c) table.start[c] = (uint16_t)count[c];
-    for (int item : order) table.items[count[owner[item]]++] = (uint16_t)item;
-    std::memcpy(key, k, sizeof(k));
-  }
-  std::memcpy(out.start, table.start, sizeof(uint16_t) * (G + 1));
-  std::memcpy(out.items, table.items, sizeof(uint16_t) * n_items);
+  cache.get(k, G, n_items, out, [&](ItemTable& t) {
+    std::vector<long long> cost(nqb);
+    for (int x = 0; x < nqb; ++x) cost[x] = fwd_item_blocks(s, nqb, x) + 1;
+    greedy_item_table(s.BH, nqb, cost, item_table_window(s.BH, 4LL * s.Nk * s.d), G, t);
+  });
   return true;
 }
 
@@ -132,9 +88,9 @@ static cudaError_t launch_fwd_t(const Maps& m, const Shape& s, void* o, float* l
     using CP = FwdPCfg<D>;
     const long long n_items = (long long)nqb_max * s.BH;
     const int grid = (int)std::min<long long>(n_items, sm_count_fwd());
-    static thread_local FwdSched table;  // 29 KiB: not on the stack
+    static thread_local ItemTable table;  // 29 KiB: not on the stack
     if (fwd_schedule(s, nqb_max, grid, table)) {
-      auto kt = attn_fwd_persistent_kernel<D, BF16, false, FwdSched>;
+      auto kt = attn_fwd_persistent_kernel<D, BF16, false, ItemTable>;
       e = cudaFuncSetAttribute(kt, cudaFuncAttributeMaxDynamicSharedMemorySize, CP::kSmemBytes);
       if (e != cudaSuccess) return e;
       kt<<<grid, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, p, (int)n_items, nqb_max,
