@@ -31,11 +31,13 @@ struct ItemTable {
   uint16_t items[kItemTableMaxItems];
 };
 
+#ifdef __CUDACC__
 // The k-th item of CTA c in the table; -1 past the end.
 __device__ __forceinline__ int table_item(const ItemTable& t, int k, int c) {
   const int i = t.start[c] + k;
   return i < t.start[c + 1] ? t.items[i] : -1;
 }
+#endif
 
 // Host: the greedy assignment of slices x per_slice items (item = slice * per_slice + x,
 // cost[x] in any unit, the same for every slice) to G CTAs, in windows of W slices.
