@@ -517,12 +517,18 @@ COMMON_SOURCES = ["common.cuh", "ptx.cuh", "launch.h", "varlen.h"]
 
 
 def source_hash(kernel: str) -> str:
+    """A hash of the code (comments and whitespace removed) of one kernel's sources: the
+    DRAM counters in profiles/traffic.json hold only while it matches."""
     import hashlib
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_tcgen05_gb300", "csrc")
     for fn in COMMON_SOURCES + KERNEL_SOURCES[kernel]:
-        with open(os.path.join(csrc, fn), "rb") as f:
-            h.update(fn.encode() + f.read())
+        with open(os.path.join(csrc, fn), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)  # block comments
+        text = re.sub(r"//[^\n]*", " ", text)                # line comments
+        h.update(fn.encode() + " ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

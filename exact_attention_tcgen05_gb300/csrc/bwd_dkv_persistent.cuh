@@ -12,8 +12,9 @@
 // The arithmetic of every item is exactly that of bwd_dkv.cuh (K_j, V_j in shared memory):
 // the outputs are bit-identical.
 //
-// Schedule: as for the persistent dQ kernel - key block p of a slice paired with block
-// nkb - 1 - p (a long and a short causal block), the pairs dealt round-robin.
+// Schedule: as for the persistent dQ kernel - a greedy table (schedule.h) for dense causal
+// inputs with more items than CTAs, otherwise key block p of a slice paired with block
+// nkb - 1 - p (a long and a short causal block) and the pairs dealt round-robin.
 #pragma once
 
 #include "bwd_dkv.cuh"

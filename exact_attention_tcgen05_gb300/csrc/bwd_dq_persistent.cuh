@@ -15,10 +15,12 @@
 // The arithmetic of every item is exactly that of bwd_dq.cuh: the outputs are
 // bit-identical.
 //
-// Schedule: the items of a slice are paired, query block p with block nb - 1 - p (a long
-// and a short causal block: every pair carries the same work), and the pairs, numbered
-// slice by slice, are dealt round-robin to the G CTAs: the CTAs working at one time share
-// the K/V of a few slices in L2.
+// Schedule (the kernel's Sched parameter): for dense causal inputs with more items than
+// CTAs, a longest-first greedy table built on the host (schedule.h); otherwise the items of
+// a slice are paired, query block p with block nb - 1 - p (a long and a short causal
+// block: every pair carries the same work), and the pairs, numbered slice by slice, are
+// dealt round-robin to the G CTAs. Either way the CTAs working at one time share the K/V
+// of a few slices in L2.
 //
 // Barrier phases follow running counts kept alike by all roles (blocks, items); each
 // barrier's next completion needs a step its waiter takes after the previous wait, so no
