@@ -48,6 +48,15 @@ o, lse = binding.attn_fwd_varlen(q, k, v, cq, cq, wv.max_q, wv.max_k, causal=Tru
 dq, dk, dv = binding.attn_bwd_varlen(q, k, v, o, lse, do, cq, cq, wv.max_q, wv.max_k,
                                      causal=True)
 out["packed_d64"] = tuple(x.cpu() for x in (o, lse, dq, dk, dv))
+# N_q = 640 against N_k = 1000 (bottom-right causal), more items than SMs in every kernel:
+# the scheduled orders with an offset
+wq = I.custom(4, 40, 640, 64, "bf16", True, seed=21)
+wk = I.custom(4, 40, 1000, 64, "bf16", True, seed=22)
+q, do = (I.make_tensor(wq, t).cuda() for t in ("q", "do"))
+k, v = (I.make_tensor(wk, t).cuda() for t in ("k", "v"))
+o, lse = binding.attn_fwd(q, k, v, causal=True, scale=wq.scale)
+dq, dk, dv = binding.attn_bwd(q, k, v, o, lse, do, causal=True, scale=wq.scale)
+out["rect"] = tuple(x.cpu() for x in (o, lse, dq, dk, dv))
 torch.cuda.synchronize()
 assert binding.attn_last_kernel_status() == (0, 0)
 torch.save(out, sys.argv[2])

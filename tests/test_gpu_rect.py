@@ -57,6 +57,17 @@ def test_rectangular_all_slices(case):
             assert_within(compare_slice(w, run, b, h), f"{case} slice {(b, h)}")
 
 
+def test_rectangular_many_items_sampled():
+    """B4 H40, N_q = 640 against N_k = 1000: more work items than SMs in all three kernels,
+    so they walk the host-computed greedy orders (item costs from the offset); sampled
+    slices against the oracle."""
+    case = (4, 40, 640, 1000, 64, "bf16", True)
+    w, run = _run(*case, seed=2000)
+    assert all_finite(run)
+    for b, h in [(0, 0), (1, 17), (2, 31), (3, 39)]:
+        assert_within(compare_slice(w, run, b, h), f"{case} slice {(b, h)}")
+
+
 @pytest.mark.parametrize("Nq,Nk,d", [(192, 700, 128), (100, 355, 64)])
 def test_keys_past_each_row_do_not_leak(Nq, Nk, d):
     """Changing keys j > i0 + (N_k - N_q) leaves rows i <= i0 of O and LSE bit-for-bit
