@@ -420,7 +420,9 @@ def measure_varlen(args, peaks: dict) -> dict:
     """The packed benchmark batch (sequences of different lengths, no padding) through
     attn_fwd_varlen + attn_bwd_varlen, next to the same sequences padded to the longest
     one as a dense [B, H, max, d] batch through attn_fwd + attn_bwd. Both are credited
-    with the same useful FLOPs (those of the real sequences)."""
+    with the same useful FLOPs (those of the real sequences). The packed calls get the host
+    copies of cu_seqlens (which order the kernels' work items); the same calls without them
+    are timed too."""
     import torch
     from exact_attention_tcgen05_gb300 import binding
     from exact_attention_tcgen05_gb300 import inputs as I
@@ -429,6 +431,8 @@ def measure_varlen(args, peaks: dict) -> dict:
     q, k, v, do = (I.make_varlen_tensor(w, t).cuda() for t in ("q", "k", "v", "do"))
     cu_q = torch.tensor(w.cu_q, dtype=torch.int32, device="cuda")
     cu_k = torch.tensor(w.cu_k, dtype=torch.int32, device="cuda")
+    cu_q_host = torch.tensor(w.cu_q, dtype=torch.int32)
+    cu_k_host = torch.tensor(w.cu_k, dtype=torch.int32)
     o = torch.empty_like(q)
     lse = torch.empty(w.H, w.total_q, dtype=torch.float32, device="cuda")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(k)
@@ -446,12 +450,16 @@ def measure_varlen(args, peaks: dict) -> dict:
     pws = torch.empty_like(plse)
     stream = torch.cuda.current_stream()
 
-    def packed():
+    def packed(hq=cu_q_host, hk=cu_k_host):
         binding.attn_fwd_varlen(q, k, v, cu_q, cu_k, w.max_q, w.max_k, causal=w.causal,
-                                scale=w.scale, o=o, lse=lse)
+                                scale=w.scale, o=o, lse=lse, cu_seqlens_q_host=hq,
+                                cu_seqlens_k_host=hk)
         binding.attn_bwd_varlen(q, k, v, o, lse, do, cu_q, cu_k, w.max_q, w.max_k,
                                 causal=w.causal, scale=w.scale, dq=dq, dk=dk, dv=dv,
-                                workspace=ws)
+                                workspace=ws, cu_seqlens_q_host=hq, cu_seqlens_k_host=hk)
+
+    def packed_device_lengths():
+        packed(None, None)
 
     def padded():
         binding.attn_fwd(pq, pk, pv, causal=w.causal, scale=w.scale, o=po, lse=plse)
@@ -460,7 +468,8 @@ def measure_varlen(args, peaks: dict) -> dict:
 
     n = max(10, min(args.steps, 50))
     result = {}
-    for name, fn in (("packed", packed), ("padded", padded)):
+    for name, fn in (("packed", packed), ("packed_device_lengths", packed_device_lengths),
+                     ("padded", padded)):
         for _ in range(max(3, args.warmup)):
             fn()
         torch.cuda.synchronize()
@@ -480,7 +489,11 @@ def measure_varlen(args, peaks: dict) -> dict:
     out = {"workload": w.name, "sequences": B, "lengths": list(w.seqlens_q),
            "tokens": w.total_q, "steps": n,
            "packed": {"ms_per_step": result["packed"],
-                      "tflops": useful / (result["packed"] * 1e-3) / 1e12},
+                      "tflops": useful / (result["packed"] * 1e-3) / 1e12,
+                      "host_cu_seqlens": True},
+           "packed_device_lengths_only": {
+               "ms_per_step": result["packed_device_lengths"],
+               "tflops": useful / (result["packed_device_lengths"] * 1e-3) / 1e12},
            "padded": {"shape": f"B{B} H{H} N{M} d{d}", "ms_per_step": result["padded"],
                       "tflops_useful": useful / (result["padded"] * 1e-3) / 1e12},
            "speedup_vs_padded": result["padded"] / result["packed"],

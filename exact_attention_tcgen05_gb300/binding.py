@@ -32,10 +32,10 @@ SIGNATURES = {
     "attn_bwd_qk": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
                          _P]),
     "attn_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I]),
-    "attn_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F,
-                             _P]),
-    "attn_bwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
-                             _I, _I, _I, _I, _F, _P]),
+    "attn_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                             _I, _F, _P]),
+    "attn_bwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I,
+                             _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_bwd_varlen_workspace_bytes": (ctypes.c_size_t, [_I, _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "attn_bwd_preprocess": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P]),
@@ -444,6 +444,18 @@ def _cu_of(cu: torch.Tensor, name: str, device: torch.device) -> torch.Tensor:
     return cu
 
 
+def _host_cu(cu_q_host, cu_k_host, B):
+    """Host pointers of the optional CPU copies of cu_seqlens (both or neither)."""
+    if cu_q_host is None and cu_k_host is None:
+        return None, None
+    for name, cu in (("cu_seqlens_q_host", cu_q_host), ("cu_seqlens_k_host", cu_k_host)):
+        if (not isinstance(cu, torch.Tensor) or cu.device.type != "cpu" or cu.dtype != torch.int32
+                or cu.dim() != 1 or cu.numel() != B + 1 or not cu.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous int32 CPU tensor of B + 1 entries "
+                             "(give both host copies or neither)")
+    return cu_q_host.data_ptr(), cu_k_host.data_ptr()
+
+
 def _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k):
     Tq, H, d = _packed_of(q, "q")
     Tk, Hk, dk = _packed_of(k, "k")
@@ -468,9 +480,15 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                     max_seqlen_q: int, max_seqlen_k: int, causal: bool = False,
                     scale: Optional[float] = None, o: Optional[torch.Tensor] = None,
                     lse: Optional[torch.Tensor] = None,
-                    stream: Optional[torch.cuda.Stream] = None
+                    stream: Optional[torch.cuda.Stream] = None,
+                    cu_seqlens_q_host: Optional[torch.Tensor] = None,
+                    cu_seqlens_k_host: Optional[torch.Tensor] = None
                     ) -> tuple[torch.Tensor, torch.Tensor]:
     """Forward over sequences packed along the token axis, via libattn.so.
+
+    cu_seqlens_q_host / _k_host: optional CPU int32 copies of the same offsets. They only
+    order the kernels' work items (longest first, balanced over the SMs); the results do not
+    depend on them.
 
     q [total_q, H, d], k and v [total_k, H, d]; sequence b owns query tokens
     cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key tokens cu_seqlens_k[b] ..
@@ -479,6 +497,7 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     Returns o [total_q, H, d] and lse [H, total_q]. Malformed sequences are reported by
     attn_last_kernel_status() as ATTN_ERR_INVALID_ARG."""
     Tq, Tk, H, d, cu_q, cu_k, B = _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k)
+    hq, hk = _host_cu(cu_seqlens_q_host, cu_seqlens_k_host, B)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty_like(q) if o is None else o
     if o.shape != q.shape or o.dtype != q.dtype or o.device != q.device:
@@ -488,8 +507,8 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
         raise ValueError("lse must be a contiguous float32 [H, total_q] tensor")
     with torch.cuda.device(q.device):
         code = load().attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                      lse.data_ptr(), cu_q.data_ptr(), cu_k.data_ptr(), B, H,
-                                      Tq, Tk, int(max_seqlen_q), int(max_seqlen_k), d,
+                                      lse.data_ptr(), cu_q.data_ptr(), cu_k.data_ptr(), hq, hk,
+                                      B, H, Tq, Tk, int(max_seqlen_q), int(max_seqlen_k), d,
                                       _DTYPE_CODES[q.dtype], int(causal), scale,
                                       _stream_handle(stream))
     _check("attn_fwd_varlen", code)
@@ -503,11 +522,15 @@ def attn_bwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.
                     dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
                     dv: Optional[torch.Tensor] = None,
                     workspace: Optional[torch.Tensor] = None,
-                    stream: Optional[torch.cuda.Stream] = None
+                    stream: Optional[torch.cuda.Stream] = None,
+                    cu_seqlens_q_host: Optional[torch.Tensor] = None,
+                    cu_seqlens_k_host: Optional[torch.Tensor] = None
                     ) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
-    """dq, dk, dv of sum(do * o) for a packed batch (layouts as attn_fwd_varlen), via
-    libattn.so; workspace holds D [H, total_q] float32."""
+    """dq, dk, dv of sum(do * o) for a packed batch (layouts and the optional host copies
+    of cu_seqlens as attn_fwd_varlen), via libattn.so; workspace holds D [H, total_q]
+    float32."""
     Tq, Tk, H, d, cu_q, cu_k, B = _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k)
+    hq, hk = _host_cu(cu_seqlens_q_host, cu_seqlens_k_host, B)
     for name, x in (("o", o), ("do", do)):
         if x.shape != q.shape or x.dtype != q.dtype or x.device != q.device:
             raise ValueError(f"{name} must match q")
@@ -530,7 +553,7 @@ def attn_bwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.
         code = load().attn_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                       lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(),
                                       dv.data_ptr(), workspace.data_ptr(), cu_q.data_ptr(),
-                                      cu_k.data_ptr(), B, H, Tq, Tk, int(max_seqlen_q),
+                                      cu_k.data_ptr(), hq, hk, B, H, Tq, Tk, int(max_seqlen_q),
                                       int(max_seqlen_k), d, _DTYPE_CODES[q.dtype], int(causal),
                                       scale, _stream_handle(stream))
     _check("attn_bwd_varlen", code)

@@ -84,21 +84,37 @@ EncodeFn get_encode() {
   return fn;
 }
 
+// A 3-D 16-bit tiled map with 128-byte swizzle and zero fill. cuTensorMapEncodeTiled is a
+// driver call and needs a current context in the calling thread; a thread that has made no
+// runtime call yet (an autograd worker thread, say) has none and gets
+// CUDA_ERROR_INVALID_CONTEXT. The thread is then bound to its current device's primary
+// context (what the runtime's own calls would do) and the encoding retried once.
+attn_status encode_3d(CUtensorMap* m, const void* base, bool bf16, const cuuint64_t (&dims)[3],
+                      const cuuint64_t (&strides)[2], const cuuint32_t (&box)[3]) {
+  EncodeFn enc = get_encode();
+  if (enc == nullptr) return ATTN_ERR_CUDA;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  auto encode = [&] {
+    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+               const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  };
+  CUresult r = encode();
+  if (r == CUDA_ERROR_INVALID_CONTEXT) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaSetDevice(dev) == cudaSuccess) r = encode();
+  }
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 // [BH, N, d] 16-bit tensor, read as [64-column x 128-row] boxes with 128-byte swizzle;
 // rows past N read as zero.
 attn_status encode_map(CUtensorMap* m, const void* base, int BH, int N, int d, bool bf16) {
-  EncodeFn enc = get_encode();
-  if (enc == nullptr) return ATTN_ERR_CUDA;
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * (cuuint64_t)d * 2};
   const cuuint32_t box[3] = {64, 128, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r =
-      enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+  return encode_3d(m, base, bf16, dims, strides, box);
 }
 
 // [total, H, d] packed 16-bit tensor, read as [64-column x 1-head x 128-token] boxes with
@@ -106,18 +122,10 @@ attn_status encode_map(CUtensorMap* m, const void* base, int BH, int N, int d, b
 // Tokens past `total` read as zero.
 attn_status encode_map_packed(CUtensorMap* m, const void* base, int H, int total, int d,
                               bool bf16) {
-  EncodeFn enc = get_encode();
-  if (enc == nullptr) return ATTN_ERR_CUDA;
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)total};
   const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * (cuuint64_t)d * 2};
   const cuuint32_t box[3] = {64, 1, 128};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r =
-      enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+  return encode_3d(m, base, bf16, dims, strides, box);
 }
 
 Shape make_shape(int B, int H, int N, int d, attn_dtype dtype, int causal, float scale,
@@ -334,8 +342,11 @@ attn_status check_varlen(int B, int H, int total_q, int total_k, int max_q, int 
 
 Shape make_varlen_shape(int B, int H, int total_q, int total_k, int max_q, int max_k, int d,
                         attn_dtype dtype, int causal, float scale, const int* cu_q,
-                        const int* cu_k) {
+                        const int* cu_k, const int* host_cu_q, const int* host_cu_k) {
   Shape s = make_shape(B, H, max_q, d, dtype, causal, scale, max_k);
+  s.host_cu_q = host_cu_q;
+  s.host_cu_k = host_cu_k;
+  s.vl_b = B;
   s.vl.cu_q = cu_q;
   s.vl.cu_k = cu_k;
   s.vl.H = H;
@@ -354,13 +365,16 @@ size_t attn_bwd_varlen_workspace_bytes(int H, int total_q) {
 }
 
 attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
-                            const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
-                            int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
-                            int d, attn_dtype dtype, int causal, float scale,
+                            const int* cu_seqlens_q, const int* cu_seqlens_k,
+                            const int* cu_seqlens_q_host, const int* cu_seqlens_k_host, int B,
+                            int H, int total_q, int total_k, int max_seqlen_q,
+                            int max_seqlen_k, int d, attn_dtype dtype, int causal, float scale,
                             void* cuda_stream) {
   attn_status st = check_varlen(B, H, total_q, total_k, max_seqlen_q, max_seqlen_k, d, dtype,
                                 cu_seqlens_q, cu_seqlens_k);
   if (st != ATTN_OK) return st;
+  if ((cu_seqlens_q_host == nullptr) != (cu_seqlens_k_host == nullptr))
+    return ATTN_ERR_INVALID_ARG;
   if ((st = check_scale(scale)) != ATTN_OK) return st;
   if ((st = check_ptrs({q, k, v, o, lse})) != ATTN_OK) return st;
   const size_t qb = (size_t)total_q * H * d * 2, kb = (size_t)total_k * H * d * 2;
@@ -372,7 +386,8 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
   if ((st = check_ranges(ins, 5, outs, 2)) != ATTN_OK) return st;
 
   const Shape s = make_varlen_shape(B, H, total_q, total_k, max_seqlen_q, max_seqlen_k, d,
-                                    dtype, causal, scale, cu_seqlens_q, cu_seqlens_k);
+                                    dtype, causal, scale, cu_seqlens_q, cu_seqlens_k,
+                                    cu_seqlens_q_host, cu_seqlens_k_host);
   Maps m;
   if ((st = encode_map_packed(&m.q, q, H, total_q, d, s.bf16)) != ATTN_OK) return st;
   if ((st = encode_map_packed(&m.k, k, H, total_k, d, s.bf16)) != ATTN_OK) return st;
@@ -384,11 +399,14 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
 attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
                             const float* lse, const void* dO, void* dq, void* dk, void* dv,
                             void* workspace, const int* cu_seqlens_q, const int* cu_seqlens_k,
-                            int B, int H, int total_q, int total_k, int max_seqlen_q,
+                            const int* cu_seqlens_q_host, const int* cu_seqlens_k_host, int B,
+                            int H, int total_q, int total_k, int max_seqlen_q,
                             int max_seqlen_k, int d, attn_dtype dtype, int causal, float scale,
                             void* cuda_stream) {
   attn_status st = check_varlen(B, H, total_q, total_k, max_seqlen_q, max_seqlen_k, d, dtype,
                                 cu_seqlens_q, cu_seqlens_k);
+  if (st == ATTN_OK && (cu_seqlens_q_host == nullptr) != (cu_seqlens_k_host == nullptr))
+    st = ATTN_ERR_INVALID_ARG;
   if (st != ATTN_OK) return st;
   if ((st = check_scale(scale)) != ATTN_OK) return st;
   if ((st = check_ptrs({q, k, v, o, lse, dO, dq, dk, dv, workspace})) != ATTN_OK) return st;
@@ -403,7 +421,8 @@ attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const v
   if ((st = check_ranges(ins, 8, outs, 4)) != ATTN_OK) return st;
 
   const Shape s = make_varlen_shape(B, H, total_q, total_k, max_seqlen_q, max_seqlen_k, d,
-                                    dtype, causal, scale, cu_seqlens_q, cu_seqlens_k);
+                                    dtype, causal, scale, cu_seqlens_q, cu_seqlens_k,
+                                    cu_seqlens_q_host, cu_seqlens_k_host);
   Maps m;
   if ((st = encode_map_packed(&m.q, q, H, total_q, d, s.bf16)) != ATTN_OK) return st;
   if ((st = encode_map_packed(&m.k, k, H, total_k, d, s.bf16)) != ATTN_OK) return st;

@@ -33,7 +33,7 @@ static bool use_persistent_dkv(const Shape& s, bool kv_tmem) {
   }();
   if (forced >= 0) return forced == 1;
   const long long n_items = (long long)((s.Nk + kTileN - 1) / kTileN) * s.BH;
-  if (item_table_applies(s.causal, s.vl.cu_q != nullptr, n_items,
+  if (item_table_applies(s.causal, s.vl.cu_q != nullptr, s.host_cu_q != nullptr, n_items,
                          (int)std::min<long long>(n_items, sm_count_dkv())))
     return true;
   if (kv_tmem) return false;
@@ -41,23 +41,31 @@ static bool use_persistent_dkv(const Shape& s, bool kv_tmem) {
   return s.causal ? (nb + 1) / 2 < 8 : nb <= 8;
 }
 
-// The persistent dK/dV's table (schedule.h) for dense causal inputs with more items than
-// CTAs: item jb of a slice is key block jb, its cost the query blocks that see it + 1,
-// windows of heads by their Q/dO bytes. False: the long/short pairs run.
-static bool dkv_schedule(const Shape& s, int nkb, int G, ItemTable& out) {
-  const long long n_items = (long long)nkb * s.BH;
-  if (!item_table_applies(s.causal, s.vl.cu_q != nullptr, n_items, G)) return false;
+// The persistent dK/dV's table (schedule.h) for causal dense inputs, or packed batches
+// whose host lengths are known, with more items than CTAs: item slot jb of a slice is key
+// block jb, its cost the query blocks that see it + 1 (the geometry of dkv_item_geom; a
+// key block of a sequence without queries costs 1: its gradients are zero-filled), windows
+// of heads by their Q/dO bytes. False: the long/short pairs run.
+static bool dkv_schedule(const Shape& s, int nkb_max, int G, ItemTable& out) {
+  const bool packed = s.vl.cu_q != nullptr;
+  const long long n_items = (long long)nkb_max * s.BH;
+  if (!item_table_applies(s.causal, packed, s.host_cu_q != nullptr, n_items, G)) return false;
   static ItemTableCache cache;
-  const long long k[6] = {s.BH, s.N, s.Nk, s.d, G, nkb};
+  const long long k[8] = {s.BH, s.N, s.Nk, s.d, G, nkb_max, s.causal ? 1 : 0,
+                          lengths_hash(s.host_cu_q, s.host_cu_k, s.vl_b)};
   cache.get(k, G, n_items, out, [&](ItemTable& t) {
-    const int nb = (s.N + kTileM - 1) / kTileM, off = s.Nk - s.N;
-    std::vector<long long> cost(nkb);
-    for (int jb = 0; jb < nkb; ++jb) {
+    const long long qdo_bytes =
+        packed ? 4LL * std::max(1, s.vl.total_q / std::max(1, s.vl_b)) * s.d : 4LL * s.N * s.d;
+    auto cost = [&](int bh, int jb) -> long long {
+      int nq, nk;
+      slice_lengths(s, bh, nq, nk);
       const int j0 = jb * kTileN;
-      const int i_first = j0 > off ? (j0 - off) / kTileM : 0;
-      cost[jb] = std::max(0, nb - i_first) + 1;
-    }
-    greedy_item_table(s.BH, nkb, cost, item_table_window(s.BH, 4LL * s.N * s.d), G, t);
+      if (j0 >= nk) return 0;
+      const int nb = (nq + kTileM - 1) / kTileM, off = nk - nq;
+      const int i_first = (s.causal && j0 > off) ? (j0 - off) / kTileM : 0;
+      return (nq == 0 ? 0 : std::max(0, nb - i_first)) + 1;
+    };
+    greedy_item_table(s.BH, nkb_max, cost, item_table_window(s.BH, qdo_bytes), G, t);
   });
   return true;
 }
@@ -103,7 +111,8 @@ static cudaError_t launch_dkv_t(const Maps& m, const Shape& s, const void* q, co
     const int gt = (int)std::min<long long>((long long)nkb_max * s.BH, sm_count_dkv());
     static thread_local ItemTable table;  // 29 KiB: not on the stack
     if (dkv_schedule(s, nkb_max, gt, table)) {
-      auto kt = attn_bwd_dkv_persistent_kernel<D, BF16, false, ItemTable>;
+      auto kt = s.vl.cu_q != nullptr ? attn_bwd_dkv_persistent_kernel<D, BF16, true, ItemTable>
+                                     : attn_bwd_dkv_persistent_kernel<D, BF16, false, ItemTable>;
       e = cudaFuncSetAttribute(kt, cudaFuncAttributeMaxDynamicSharedMemorySize, CP::kSmemBytes);
       if (e != cudaSuccess) return e;
       kt<<<gt, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, m.d_o, p, (int)n_pairs,

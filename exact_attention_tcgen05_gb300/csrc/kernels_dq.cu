@@ -37,7 +37,7 @@ static bool use_persistent_dq(const Shape& s) {
   }();
   if (forced >= 0) return forced == 1;
   const long long n_items = (long long)((s.N + kTileM - 1) / kTileM) * s.BH;
-  if (item_table_applies(s.causal, s.vl.cu_q != nullptr, n_items,
+  if (item_table_applies(s.causal, s.vl.cu_q != nullptr, s.host_cu_q != nullptr, n_items,
                          (int)std::min<long long>(n_items, sm_count_dq())))
     return true;
   const int nkb = (s.Nk + kTileN - 1) / kTileN;
@@ -53,20 +53,31 @@ static bool use_persistent_dq(const Shape& s) {
   return n_pairs * 20 >= rounds * sms * 19;
 }
 
-// The persistent dQ's table (schedule.h) for dense causal inputs with more items than
-// CTAs: item x of a slice is query block nb - 1 - x, its cost the key blocks it sees + 1,
-// windows of heads by their K/V bytes. False: the long/short pairs run.
-static bool dq_schedule(const Shape& s, int nb, int G, ItemTable& out) {
-  const long long n_items = (long long)nb * s.BH;
-  if (!item_table_applies(s.causal, s.vl.cu_q != nullptr, n_items, G)) return false;
+// The persistent dQ's table (schedule.h) for causal dense inputs, or packed batches whose
+// host lengths are known, with more items than CTAs: item slot x of a slice is query block
+// nb - 1 - x (causal) or x, its cost the key blocks it sees + 1 (the geometry of
+// dq_item_geom), windows of heads by their K/V bytes. False: the long/short pairs run.
+static bool dq_schedule(const Shape& s, int nb_max, int G, ItemTable& out) {
+  const bool packed = s.vl.cu_q != nullptr;
+  const long long n_items = (long long)nb_max * s.BH;
+  if (!item_table_applies(s.causal, packed, s.host_cu_q != nullptr, n_items, G)) return false;
   static ItemTableCache cache;
-  const long long k[6] = {s.BH, s.N, s.Nk, s.d, G, nb};
+  const long long k[8] = {s.BH, s.N, s.Nk, s.d, G, nb_max, s.causal ? 1 : 0,
+                          lengths_hash(s.host_cu_q, s.host_cu_k, s.vl_b)};
   cache.get(k, G, n_items, out, [&](ItemTable& t) {
-    const int nkb = (s.Nk + kTileN - 1) / kTileN, off = s.Nk - s.N;
-    std::vector<long long> cost(nb);
-    for (int x = 0; x < nb; ++x)
-      cost[x] = std::min(nkb, ((nb - 1 - x) * kTileM + kTileM - 1 + off) / kTileN + 1) + 1;
-    greedy_item_table(s.BH, nb, cost, item_table_window(s.BH, 4LL * s.Nk * s.d), G, t);
+    const long long kv_bytes =
+        packed ? 4LL * std::max(1, s.vl.total_k / std::max(1, s.vl_b)) * s.d : 4LL * s.Nk * s.d;
+    auto cost = [&](int bh, int x) -> long long {
+      int nq, nk;
+      slice_lengths(s, bh, nq, nk);
+      const int nb = (nq + kTileM - 1) / kTileM;
+      if (x >= nb) return 0;
+      const int nkb = (nk + kTileN - 1) / kTileN;
+      const int i0 = (s.causal ? nb - 1 - x : x) * kTileM;
+      const int n = s.causal ? std::min(nkb, (i0 + kTileM - 1 + nk - nq) / kTileN + 1) : nkb;
+      return n + 1;
+    };
+    greedy_item_table(s.BH, nb_max, cost, item_table_window(s.BH, kv_bytes), G, t);
   });
   return true;
 }
@@ -106,7 +117,8 @@ static cudaError_t launch_dq_t(const Maps& m, const Shape& s, const void* q,
     const int gt = (int)std::min<long long>((long long)nb_max * s.BH, sm_count_dq());
     static thread_local ItemTable table;  // 29 KiB: not on the stack
     if (dq_schedule(s, nb_max, gt, table)) {
-      auto kt = attn_bwd_dq_persistent_kernel<D, BF16, false, ItemTable>;
+      auto kt = s.vl.cu_q != nullptr ? attn_bwd_dq_persistent_kernel<D, BF16, true, ItemTable>
+                                     : attn_bwd_dq_persistent_kernel<D, BF16, false, ItemTable>;
       e = cudaFuncSetAttribute(kt, cudaFuncAttributeMaxDynamicSharedMemorySize, CP::kSmemBytes);
       if (e != cudaSuccess) return e;
       kt<<<gt, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, m.d_o, p, (int)n_pairs,

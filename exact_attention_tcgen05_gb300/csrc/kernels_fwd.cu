@@ -32,32 +32,42 @@ static bool use_persistent_fwd(const Shape& s) {
   return !(s.d <= 64 && blocks_per_item >= 24);
 }
 
-// Key blocks item `x` of a dense slice works through (the larger of its two tiles; the
-// same geometry as fwd_item_geom).
-static int fwd_item_blocks(const Shape& s, int nqb, int x) {
-  const int nkb = (s.Nk + kTileN - 1) / kTileN;
-  const int off = s.Nk - s.N;
+// Key blocks item slot `x` of a slice with nq queries and nk keys works through (the larger
+// of its two tiles; the same geometry as fwd_item_geom); 0 past the slice's end.
+static int fwd_item_blocks(int nq, int nk, bool causal, int x) {
+  const int nqb = (nq + 2 * kTileM - 1) / (2 * kTileM);
+  if (x >= nqb) return 0;
+  const int nkb = (nk + kTileN - 1) / kTileN;
+  const int off = nk - nq;
   const int q0 = (nqb - 1 - x) * 2 * kTileM;
-  const int ntiles = (q0 + kTileM < s.N) ? 2 : 1;
+  const int ntiles = (q0 + kTileM < nq) ? 2 : 1;
   int n = 0;
   for (int t = 0; t < ntiles; ++t)
-    n = std::max(n, s.causal ? std::min(nkb, (q0 + t * kTileM + kTileM - 1 + off) / kTileN + 1)
-                             : nkb);
+    n = std::max(n, causal ? std::min(nkb, (q0 + t * kTileM + kTileM - 1 + off) / kTileN + 1)
+                           : nkb);
   return n;
 }
 
-// The persistent forward's table (schedule.h) for dense causal inputs with more items than
-// CTAs: cost = key blocks + 1 for an item's fixed cost, windows of heads by their K/V
-// bytes. False: the serpentine runs.
+// The persistent forward's table (schedule.h) for causal dense inputs, or packed batches
+// whose host lengths are known, with more items than CTAs: cost = key blocks + 1 for an
+// item's fixed cost, windows of heads by their K/V bytes. False: the serpentine runs.
 static bool fwd_schedule(const Shape& s, int nqb, int G, ItemTable& out) {
+  const bool packed = s.vl.cu_q != nullptr;
   const long long n_items = (long long)nqb * s.BH;
-  if (!item_table_applies(s.causal, s.vl.cu_q != nullptr, n_items, G)) return false;
+  if (!item_table_applies(s.causal, packed, s.host_cu_q != nullptr, n_items, G)) return false;
   static ItemTableCache cache;
-  const long long k[6] = {s.BH, s.N, s.Nk, s.d, G, nqb};
+  const long long k[8] = {s.BH, s.N, s.Nk, s.d, G, nqb, s.causal ? 1 : 0,
+                          lengths_hash(s.host_cu_q, s.host_cu_k, s.vl_b)};
   cache.get(k, G, n_items, out, [&](ItemTable& t) {
-    std::vector<long long> cost(nqb);
-    for (int x = 0; x < nqb; ++x) cost[x] = fwd_item_blocks(s, nqb, x) + 1;
-    greedy_item_table(s.BH, nqb, cost, item_table_window(s.BH, 4LL * s.Nk * s.d), G, t);
+    const long long kv_bytes =
+        packed ? 4LL * std::max(1, s.vl.total_k / std::max(1, s.vl_b)) * s.d : 4LL * s.Nk * s.d;
+    auto cost = [&](int bh, int x) -> long long {
+      int nq, nk;
+      slice_lengths(s, bh, nq, nk);
+      const int n = fwd_item_blocks(nq, nk, s.causal, x);
+      return n > 0 ? n + 1 : 0;
+    };
+    greedy_item_table(s.BH, nqb, cost, item_table_window(s.BH, kv_bytes), G, t);
   });
   return true;
 }
@@ -90,7 +100,8 @@ static cudaError_t launch_fwd_t(const Maps& m, const Shape& s, void* o, float* l
     const int grid = (int)std::min<long long>(n_items, sm_count_fwd());
     static thread_local ItemTable table;  // 29 KiB: not on the stack
     if (fwd_schedule(s, nqb_max, grid, table)) {
-      auto kt = attn_fwd_persistent_kernel<D, BF16, false, ItemTable>;
+      auto kt = s.vl.cu_q != nullptr ? attn_fwd_persistent_kernel<D, BF16, true, ItemTable>
+                                     : attn_fwd_persistent_kernel<D, BF16, false, ItemTable>;
       e = cudaFuncSetAttribute(kt, cudaFuncAttributeMaxDynamicSharedMemorySize, CP::kSmemBytes);
       if (e != cudaSuccess) return e;
       kt<<<grid, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, p, (int)n_items, nqb_max,

@@ -21,7 +21,27 @@ struct Shape {
   float scale;
   unsigned long long wait_limit;  // SM cycles one pipeline wait may take
   Varlen vl;     // packed variable-length batch; vl.cu_q == nullptr for dense tensors
+  // Packed batches: HOST copies of vl.cu_q / vl.cu_k ([vl_b + 1] each), or null. Used only
+  // to order the persistent kernels' work items (schedule.h); the kernels read the device
+  // copies, and every item slot is processed whatever the host copies say.
+  const int* host_cu_q = nullptr;
+  const int* host_cu_k = nullptr;
+  int vl_b = 0;  // sequences in the packed batch
 };
+
+// Query and key rows of slice bh (packed: of its sequence, from the host copies; a
+// malformed entry counts as empty). Host only; for ordering work, never for addressing.
+inline void slice_lengths(const Shape& s, int bh, int& nq, int& nk) {
+  if (s.vl.cu_q == nullptr) {
+    nq = s.N;
+    nk = s.Nk;
+    return;
+  }
+  const int b = bh / s.vl.H;
+  nq = s.host_cu_q[b + 1] - s.host_cu_q[b];
+  nk = s.host_cu_k[b + 1] - s.host_cu_k[b];
+  if (nq < 0 || nq > s.vl.max_q || nk < 0 || nk > s.vl.max_k) nq = nk = 0;
+}
 
 cudaError_t launch_fwd(const Maps& m, const Shape& s, void* o, float* lse, cudaStream_t st);
 cudaError_t launch_delta(const Shape& s, const void* o, const void* dO, float* delta,

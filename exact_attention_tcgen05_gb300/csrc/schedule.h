@@ -39,31 +39,54 @@ __device__ __forceinline__ int table_item(const ItemTable& t, int k, int c) {
 }
 #endif
 
-// Host: the greedy assignment of slices x per_slice items (item = slice * per_slice + x,
-// cost[x] in any unit, the same for every slice) to G CTAs, in windows of W slices.
-inline void greedy_item_table(int slices, int per_slice, const std::vector<long long>& cost,
-                              int W, int G, ItemTable& t) {
-  std::vector<int> by_cost(per_slice);
-  for (int x = 0; x < per_slice; ++x) by_cost[x] = x;
-  std::stable_sort(by_cost.begin(), by_cost.end(),
-                   [&](int a, int b) { return cost[a] > cost[b]; });
+// Host: the greedy assignment of slices x per_slice items (item = slice * per_slice + x)
+// to G CTAs, in windows of W slices; cost(slice, x) in any unit, 0 for an empty slot (a
+// block past its sequence's end). Within a window the items go longest first (then by x,
+// then by slice); each to the CTA that becomes free first. Empty slots are still listed -
+// the kernels skip them after looking at their geometry - but dealt round-robin at the
+// ends of the CTAs' lists, so that no CTA collects them all.
+template <class Cost>
+inline void greedy_item_table(int slices, int per_slice, Cost cost, int W, int G,
+                              ItemTable& t) {
   using Slot = std::pair<long long, int>;  // (busy until, CTA)
   std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
   for (int c = 0; c < G; ++c) free_at.push({0, c});
   const long long n = (long long)slices * per_slice;
-  std::vector<int> owner(n), order;
+  std::vector<int> owner(n), order, empty;
   order.reserve(n);
+  struct Item {
+    long long cost;
+    int x, slice;
+  };
+  std::vector<Item> win;
   for (int s0 = 0; s0 < slices; s0 += W) {
     const int s1 = std::min(slices, s0 + W);
-    for (int x : by_cost)
-      for (int s = s0; s < s1; ++s) {
-        const int item = s * per_slice + x;
-        const Slot sl = free_at.top();
-        free_at.pop();
-        owner[item] = sl.second;
-        order.push_back(item);
-        free_at.push({sl.first + cost[x], sl.second});
+    win.clear();
+    for (int s = s0; s < s1; ++s)
+      for (int x = 0; x < per_slice; ++x) {
+        const long long c = cost(s, x);
+        if (c > 0)
+          win.push_back({c, x, s});
+        else
+          empty.push_back(s * per_slice + x);
       }
+    std::stable_sort(win.begin(), win.end(), [](const Item& a, const Item& b) {
+      if (a.cost != b.cost) return a.cost > b.cost;
+      if (a.x != b.x) return a.x < b.x;
+      return a.slice < b.slice;
+    });
+    for (const Item& it : win) {
+      const int item = it.slice * per_slice + it.x;
+      const Slot sl = free_at.top();
+      free_at.pop();
+      owner[item] = sl.second;
+      order.push_back(item);
+      free_at.push({sl.first + it.cost, sl.second});
+    }
+  }
+  for (size_t i = 0; i < empty.size(); ++i) {
+    owner[empty[i]] = (int)(i % G);
+    order.push_back(empty[i]);
   }
   // Items grouped by CTA, each CTA's in assignment order.
   std::vector<int> pos(G + 1, 0);
@@ -79,9 +102,9 @@ inline void greedy_item_table(int slices, int per_slice, const std::vector<long 
 struct ItemTableCache {
   std::mutex mu;
   ItemTable table;
-  long long key[6] = {-1, -1, -1, -1, -1, -1};
+  long long key[8] = {-1, -1, -1, -1, -1, -1, -1, -1};
   template <class Build>
-  void get(const long long (&k)[6], int G, long long n_items, ItemTable& out, Build build) {
+  void get(const long long (&k)[8], int G, long long n_items, ItemTable& out, Build build) {
     std::lock_guard<std::mutex> lock(mu);
     if (std::memcmp(k, key, sizeof(key)) != 0) {
       build(table);
@@ -92,14 +115,27 @@ struct ItemTableCache {
   }
 };
 
-// Host: whether a table applies (dense causal inputs with more items than CTAs, within the
-// table's size), and the window of slices whose K/V (or Q/dO) rows of `row_bytes` each
-// take about 32 MiB, so that two windows in flight take half of the 126 MiB L2 (measured on
-// GB300 against 48 MiB: B4 H32 N4096 forward 0.452 -> 0.433 ms, dK/dV -2%; B1 H16 N16384
-// forward 1-3% slower).
-inline bool item_table_applies(bool causal, bool packed, long long n_items, int G) {
-  return causal && !packed && n_items > G && n_items <= kItemTableMaxItems &&
-         G <= kItemTableMaxCtas;
+// Host: a hash of a packed batch's host lengths for the cache key (0 for dense inputs). A
+// collision only reuses another order of the same item slots.
+inline long long lengths_hash(const int* cu_q, const int* cu_k, int n) {
+  if (cu_q == nullptr) return 0;
+  unsigned long long h = 1469598103934665603ull;
+  for (int i = 0; i <= n; ++i) {
+    h = (h ^ (unsigned)cu_q[i]) * 1099511628211ull;
+    h = (h ^ (unsigned)cu_k[i]) * 1099511628211ull;
+  }
+  return (long long)(h >> 1);
+}
+
+// Host: whether a table applies - items of unequal cost (causal inputs, or packed
+// sequences whose lengths the host knows), more items than CTAs, within the table's size -
+// and the window of slices whose K/V (or Q/dO) rows take about 32 MiB, so that two windows
+// in flight take half of the 126 MiB L2 (measured on GB300 against 48 MiB: B4 H32 N4096
+// forward 0.452 -> 0.433 ms, dK/dV -2%; B1 H16 N16384 forward 1-3% slower).
+inline bool item_table_applies(bool causal, bool packed, bool packed_lengths_known,
+                               long long n_items, int G) {
+  if (packed ? !packed_lengths_known : !causal) return false;
+  return n_items > G && n_items <= kItemTableMaxItems && G <= kItemTableMaxCtas;
 }
 inline int item_table_window(int slices, long long bytes_per_slice) {
   return (int)std::max(1LL, std::min<long long>(slices, (32LL << 20) / bytes_per_slice));

@@ -138,6 +138,13 @@ attn_status attn_bwd_qk(const void* q, const void* k, const void* v, const void*
  *   cu_seqlens_q/_k     int32 [B + 1] in DEVICE memory, 4-byte aligned: sequence b owns
  *                       query tokens cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key tokens
  *                       cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1;
+ *   cu_seqlens_q_host/_k_host  optional (both NULL, or both set) HOST copies of the same
+ *                       B + 1 offsets, read during the call. They only order the work: the
+ *                       persistent kernels then walk their items longest first, balanced
+ *                       over the SMs, instead of in a fixed order (the sequences' lengths
+ *                       differ, so a fixed order leaves some SMs working long after the
+ *                       rest). Results do not depend on them: every item is computed,
+ *                       whatever they say, from the device copies.
  *   max_seqlen_q/_k     bounds on every sequence's query / key count (1 .. 1048576, at
  *                       most the totals); the grids cover this many rows per sequence.
  * Each (sequence, head) pair is its own attention problem; causal masking is bottom-right
@@ -151,14 +158,16 @@ attn_status attn_bwd_qk(const void* q, const void* k, const void* v, const void*
  */
 size_t attn_bwd_varlen_workspace_bytes(int H, int total_q); /* 4 * H * total_q; 0 if invalid */
 attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
-                            const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
-                            int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
-                            int d, attn_dtype dtype, int causal, float scale,
+                            const int* cu_seqlens_q, const int* cu_seqlens_k,
+                            const int* cu_seqlens_q_host, const int* cu_seqlens_k_host, int B,
+                            int H, int total_q, int total_k, int max_seqlen_q,
+                            int max_seqlen_k, int d, attn_dtype dtype, int causal, float scale,
                             void* cuda_stream);
 attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
                             const float* lse, const void* dO, void* dq, void* dk, void* dv,
                             void* workspace, const int* cu_seqlens_q, const int* cu_seqlens_k,
-                            int B, int H, int total_q, int total_k, int max_seqlen_q,
+                            const int* cu_seqlens_q_host, const int* cu_seqlens_k_host, int B,
+                            int H, int total_q, int total_k, int max_seqlen_q,
                             int max_seqlen_k, int d, attn_dtype dtype, int causal, float scale,
                             void* cuda_stream);
 

@@ -130,15 +130,20 @@ def test_bwd_qk_rejects_bad_arguments(lib, kw, code):
 CUQ, CUK = 0x10000000 + 10 * 64 * MB, 0x10000000 + 10 * 64 * MB + 4096
 
 
+# Host copies of cu_seqlens (read on the host only to order work): B = 4 sequences.
+HOST_CU = (ctypes.c_int * 5)(0, 250, 500, 750, 1000)
+HOST_CU_ADDR = ctypes.addressof(HOST_CU)
+
+
 def fwd_varlen(lib, q=Q, o=O, cu_q=CUQ, cu_k=CUK, B=4, H=2, Tq=1000, Tk=1200, mq=400, mk=500,
-               d=128, dt=1, scale=0.1):
-    return lib.attn_fwd_varlen(q, K, V, o, L, cu_q, cu_k, B, H, Tq, Tk, mq, mk, d, dt, 1, scale,
-                               None)
+               d=128, dt=1, scale=0.1, hq=None, hk=None):
+    return lib.attn_fwd_varlen(q, K, V, o, L, cu_q, cu_k, hq, hk, B, H, Tq, Tk, mq, mk, d, dt, 1,
+                               scale, None)
 
 
-def bwd_varlen(lib, dk=DK, ws=WS, cu_q=CUQ, Tq=1000, mq=400):
-    return lib.attn_bwd_varlen(Q, K, V, O, L, DO, DQ, dk, DV, ws, cu_q, CUK, 4, 2, Tq, 1200, mq,
-                               500, 128, 1, 1, 0.1, None)
+def bwd_varlen(lib, dk=DK, ws=WS, cu_q=CUQ, Tq=1000, mq=400, hq=None, hk=None):
+    return lib.attn_bwd_varlen(Q, K, V, O, L, DO, DQ, dk, DV, ws, cu_q, CUK, hq, hk, 4, 2, Tq,
+                               1200, mq, 500, 128, 1, 1, 0.1, None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -149,6 +154,7 @@ def bwd_varlen(lib, dk=DK, ws=WS, cu_q=CUQ, Tq=1000, mq=400):
     (dict(scale=0.0), INVALID), (dict(q=Q + 8), INVALID),
     (dict(o=Q + 1000 * 2 * 128 * 2 - 16), INVALID),  # o overlaps the tail of q
     (dict(o=CUQ - 16), INVALID),                    # o overlaps cu_seqlens_q
+    (dict(hq=HOST_CU_ADDR), INVALID), (dict(hk=HOST_CU_ADDR), INVALID),  # one host copy alone
 ])
 def test_fwd_varlen_rejects_bad_arguments(lib, kw, code):
     assert fwd_varlen(lib, **kw) == code
@@ -156,7 +162,7 @@ def test_fwd_varlen_rejects_bad_arguments(lib, kw, code):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(ws=0), INVALID), (dict(dk=DV + 16), INVALID), (dict(ws=CUK), INVALID),
-    (dict(mq=2000), INVALID),
+    (dict(mq=2000), INVALID), (dict(hq=HOST_CU_ADDR), INVALID),
 ])
 def test_bwd_varlen_rejects_bad_arguments(lib, kw, code):
     assert bwd_varlen(lib, **kw) == code

@@ -44,3 +44,31 @@ def test_packed_autograd_matches_binding():
     assert torch.equal(o, o_ref)
     for got, want in zip((qg.grad, kg.grad, vg.grad), ref):
         assert torch.equal(got, want)
+
+
+def test_calls_from_a_thread_without_cuda_context():
+    """A host thread that has made no CUDA call has no current context; the C ABI's own
+    driver call (tensor-map encoding) must still work there, as it must in the autograd
+    engine's worker threads. The results equal the main thread's bit for bit."""
+    import threading
+    w = I.custom(2, 2, 300, 128, "bf16", True, seed=5)
+    q, k, v, do = (I.make_tensor(w, t).cuda() for t in ("q", "k", "v", "do"))
+    o_ref, lse_ref = binding.attn_fwd(q, k, v, causal=True)
+    grads_ref = binding.attn_bwd(q, k, v, o_ref, lse_ref, do, causal=True)
+    torch.cuda.synchronize()
+    out, errors = {}, []
+
+    def worker():
+        try:
+            o, lse = binding.attn_fwd(q, k, v, causal=True)
+            out["r"] = (o, lse) + tuple(binding.attn_bwd(q, k, v, o, lse, do, causal=True))
+            torch.cuda.synchronize()
+        except Exception as e:  # reported below, on the test's thread
+            errors.append(e)
+
+    t = threading.Thread(target=worker)
+    t.start()
+    t.join(timeout=120)
+    assert not errors, errors
+    for a, b in zip(out["r"], (o_ref, lse_ref) + tuple(grads_ref)):
+        assert torch.equal(a, b)

@@ -183,3 +183,37 @@ def test_bench_batch_sampled_against_the_oracle():
             assert np.abs(lse[h, q0:q1].cpu().double().numpy() - ref["lse"]).max() <= LSE_TOL
             for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
                 assert rel_fro(_f64(got[q0:q1, h]), ref[name]) <= GRAD_TOL, (b, h, name)
+
+
+@pytest.mark.parametrize("causal,d,lq,lk", [
+    (True, 128, (700, 1, 1500, 129, 2048, 300, 999, 64), None),
+    (False, 64, (200, 1800, 64, 1, 900, 1300), (250, 1800, 100, 7, 1000, 1300)),
+])
+def test_host_lengths_only_order_the_work(causal, d, lq, lk):
+    """With host copies of cu_seqlens the persistent kernels walk their items in a greedy
+    longest-first order (more items than SMs here); the results are those of the call
+    without them, bit for bit - also when the host copies are wrong, since every item slot
+    is computed from the device copies whatever the host copies say."""
+    w = I.varlen(16, d, "bf16", causal, seed=90 + d, seqlens_q=lq, seqlens_k=lk)
+    q, k, v, do, cu_q, cu_k = _tensors(w)
+
+    def run(hq, hk):
+        o, lse = binding.attn_fwd_varlen(q, k, v, cu_q, cu_k, w.max_q, w.max_k, causal=causal,
+                                         scale=w.scale, cu_seqlens_q_host=hq,
+                                         cu_seqlens_k_host=hk)
+        dq, dk, dv = binding.attn_bwd_varlen(q, k, v, o, lse, do, cu_q, cu_k, w.max_q, w.max_k,
+                                             causal=causal, scale=w.scale,
+                                             cu_seqlens_q_host=hq, cu_seqlens_k_host=hk)
+        torch.cuda.synchronize()
+        assert binding.attn_last_kernel_status() == (0, 0)
+        return o, lse, dq, dk, dv
+
+    base = run(None, None)
+    right = run(torch.tensor(w.cu_q, dtype=torch.int32), torch.tensor(w.cu_k, dtype=torch.int32))
+    # wrong host lengths: the sequences' lengths in reverse order
+    rev_q = np.concatenate([[0], np.cumsum(list(reversed(w.seqlens_q)))]).astype(np.int32)
+    rev_k = np.concatenate([[0], np.cumsum(list(reversed(w.seqlens_k)))]).astype(np.int32)
+    wrong = run(torch.from_numpy(rev_q), torch.from_numpy(rev_k))
+    for name, a, b, c in zip(("O", "LSE", "dQ", "dK", "dV"), base, right, wrong):
+        assert torch.equal(a, b), f"{name}: host lengths changed the result"
+        assert torch.equal(a, c), f"{name}: wrong host lengths changed the result"

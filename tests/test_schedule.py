@@ -37,7 +37,7 @@ int main() {
     std::vector<long long> cost(per);
     for (int x = 0; x < per; ++x) cost[x] = (causal ? 2LL * (per - x) : 2LL * per) + 1;
     const int W = item_table_window(slices, 2LL << 20);
-    greedy_item_table(slices, per, cost, W, G, t);
+    greedy_item_table(slices, per, [&](int, int x) { return cost[x]; }, W, G, t);
     const long long n = (long long)slices * per;
     std::vector<int> seen(n, 0);
     int bad = 0;
