@@ -44,6 +44,15 @@ def test_packed_autograd_matches_binding():
     assert torch.equal(o, o_ref)
     for got, want in zip((qg.grad, kg.grad, vg.grad), ref):
         assert torch.equal(got, want)
+    # with the host copies of cu_seqlens (they only order the work): the same bits
+    qg2, kg2, vg2 = (x.clone().requires_grad_() for x in (q, k, v))
+    o2 = autograd.attention_varlen(qg2, kg2, vg2, cq, ck, w.max_q, w.max_k, causal=True,
+                                   cu_seqlens_q_host=cq.cpu(), cu_seqlens_k_host=ck.cpu())
+    o2.backward(do)
+    torch.cuda.synchronize()
+    assert torch.equal(o2, o_ref)
+    for got, want in zip((qg2.grad, kg2.grad, vg2.grad), ref):
+        assert torch.equal(got, want)
 
 
 def test_calls_from_a_thread_without_cuda_context():
