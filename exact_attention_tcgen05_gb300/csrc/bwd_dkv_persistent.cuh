@@ -53,11 +53,29 @@ __device__ __forceinline__ bool dkv_item_geom(const BwdParams& p, int item, int 
 template <int D>
 struct DkvPCfg : DkvCfg<D> {
   using B = DkvCfg<D>;
-  // The barriers of the one-item kernel, then kv_free and acc_free.
-  static constexpr int kNumBars = B::kNumBars + 2;
-  static constexpr int kOffMisc = B::kOffBar + kNumBars * 8;
+  // Q and dO in rings of their own depths. A Q block's last reader is dK += dS^T Q, a dO
+  // block's dV += P^T dO, which the tensor core runs earlier; so at d = 128, where the
+  // Q + dO copies of a block barely keep up with its work, Q gets three slots and dO two
+  // (with K_j, V_j: 224 KiB of tiles; measured on GB300 against two of each: B4 H32 N4096
+// dK/dV 0.781 -> 0.757 ms). d = 64: three of each.
+  static constexpr int kQStages = D == 128 ? 3 : B::kStages;
+  static constexpr int kDOStages = B::kStages;
+  static constexpr int kOffQ = B::kOffQ;  // after K_j, V_j
+  static constexpr int kOffDO = kOffQ + kQStages * B::kTileBytes;
+  static constexpr int kOffStats = kOffDO + kDOStages * B::kTileBytes;
+  static constexpr int kOffBar = kOffStats + 2 * 256 * 4;
+  // kv_full, q_full[QS], do_full[DS], q_empty[QS], do_empty[DS], s_full, p_full, dp_full,
+  // ds_full, acc_done, drain, stats_ready[2], kv_free, acc_free
+  static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDOStages + 8 + 2;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  // 1024 bytes of slack to align the dynamic shared memory's base, where they fit in the
+  // 227 KiB a CTA may take; otherwise none, and the kernel checks that the base is aligned
+  // (it is on GB300: no static shared memory comes before it).
+  static constexpr int kLimit = 227 * 1024;
+  static constexpr int kSlack = (kOffMisc + 16 + 1024 <= kLimit) ? 1024 : 0;
   static constexpr int kSmemBytes =
-      (kOffMisc + 16 + 1024) > B::kMinSmem ? (kOffMisc + 16 + 1024) : B::kMinSmem;
+      (kOffMisc + 16 + kSlack) > B::kMinSmem ? (kOffMisc + 16 + kSlack) : B::kMinSmem;
+  static_assert(kSmemBytes <= kLimit, "shared memory");
 };
 
 template <int D, bool BF16, bool PACKED, class Sched>
@@ -69,22 +87,33 @@ __global__ void __launch_bounds__(320, 1)
                                    const BwdParams p, int n_pairs, int npairs, int nkb_max,
                                    const __grid_constant__ Sched sched) {
   using C = DkvPCfg<D>;
-  constexpr int NS = C::kStages;
+  constexpr int QS = C::kQStages, DS = C::kDOStages;
+  // Rings of different depths release their slots separately (dO after the block's dV
+  // product, Q after its dK product); at equal depths one release per block covers both
+  // (q_empty, committed after the block's last product), which measured 1% faster at d = 64.
+  constexpr bool kSplit = QS != DS;
   extern __shared__ uint8_t smem_raw[];
+  if (C::kSlack == 0 && (smem_u32(smem_raw) & 1023u) != 0) {
+    // Without slack the layout needs an aligned base: report and do nothing (every thread
+    // takes this branch, before any barrier or tensor memory is set up).
+    if (threadIdx.x == 0) record_timeout(kErrSmemAlign);
+    return;
+  }
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* kv_full = bars;
-  uint64_t* q_full = bars + 1;
-  uint64_t* do_full = q_full + NS;
-  uint64_t* qdo_empty = do_full + NS;
-  uint64_t* s_full = qdo_empty + NS;
+  uint64_t* q_full = bars + 1;          // [QS]
+  uint64_t* do_full = q_full + QS;      // [DS]
+  uint64_t* q_empty = do_full + DS;     // [QS] the block's dK product has read Q_i
+  uint64_t* do_empty = q_empty + QS;    // [DS] the block's dV product has read dO_i
+  uint64_t* s_full = do_empty + DS;
   uint64_t* p_full = s_full + 1;
   uint64_t* dp_full = p_full + 1;
   uint64_t* ds_full = dp_full + 1;
   uint64_t* acc_done = ds_full + 1;
   uint64_t* drain = acc_done + 1;
   uint64_t* stats_ready = drain + 1;  // [2], one per statistics buffer
-  uint64_t* kv_free = bars + DkvCfg<D>::kNumBars;  // the item's S^T, dP^T have read K_j, V_j
+  uint64_t* kv_free = stats_ready + 2;  // the item's S^T, dP^T have read K_j, V_j
   uint64_t* acc_free = kv_free + 1;  // the epilogue has read dK, dV
   float* stats = reinterpret_cast<float*>(smem + C::kOffStats);  // [2][-L*log2e x128, D x128]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
@@ -96,10 +125,13 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < QS; ++s) {
       mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
+    for (int s = 0; s < DS; ++s) {
       mbar_init(&do_full[s], 1);
-      mbar_init(&qdo_empty[s], 1);
+      mbar_init(&do_empty[s], 1);
     }
     mbar_init(s_full, 1);
     mbar_init(p_full, 8);  // one arrival per elementwise warp
@@ -133,7 +165,7 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_map(&map_do);
     }
     __syncwarp();
-    int kv_loads = 0, loads = 0;  // K/V copies (items) and ring blocks issued so far
+    int kv_loads = 0, q_loads = 0, do_loads = 0;  // K/V (items), Q and dO copies so far
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int item = sched_item(sched, k, G, cta, n_pairs, npairs, nkb_max);
@@ -157,33 +189,81 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       ++kv_loads;
       for (int t = 0; t < it.n; ++t) {
-        const int s = loads % NS;
         const int i = it.i_first + t;
-        if (loads >= NS &&
-            !(ok = warp_wait(&qdo_empty[s], ((loads / NS) - 1) & 1, limit, abort_flag,
-                             kWaitDkvEmpty)))
-          break;
-        if (elect_one()) {
-          mbar_arrive_expect_tx(&q_full[s], C::kTileBytes);
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_rows<PACKED>(smem + C::kOffQ + s * C::kTileBytes + c * kBoxBytes, &map_q,
-                                  &q_full[s], c * kBoxCols, i * kTileM, it.sl, false);
-          mbar_arrive_expect_tx(&do_full[s], C::kTileBytes);
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_rows<PACKED>(smem + C::kOffDO + s * C::kTileBytes + c * kBoxBytes,
-                                  &map_do, &do_full[s], c * kBoxCols, i * kTileM, it.sl, false);
+        // Q_i into its slot once the block that held it has had its dK product (q_empty:
+        // one completion per block using the slot; the next needs this copy), dO_i once
+        // its slot's block has had its dV product. Waited in the order the slots free up:
+        // Q first when its ring is deeper (dK of block b - QS runs before dV of block
+        // b - DS), dO first at equal depths (dV runs before dK of the same block).
+        auto load_q = [&]() -> bool {
+          const int sq = q_loads % QS;
+          if (q_loads >= QS && !warp_wait(&q_empty[sq], ((q_loads / QS) - 1) & 1, limit,
+                                          abort_flag, kWaitDkvEmpty))
+            return false;
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&q_full[sq], C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_rows<PACKED>(smem + C::kOffQ + sq * C::kTileBytes + c * kBoxBytes,
+                                    &map_q, &q_full[sq], c * kBoxCols, i * kTileM, it.sl,
+                                    false);
+          }
+          __syncwarp();
+          ++q_loads;
+          return true;
+        };
+        auto load_do = [&]() -> bool {
+          const int sd = do_loads % DS;
+          if (do_loads >= DS && !warp_wait(&do_empty[sd], ((do_loads / DS) - 1) & 1, limit,
+                                           abort_flag, kWaitDkvEmpty))
+            return false;
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&do_full[sd], C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_rows<PACKED>(smem + C::kOffDO + sd * C::kTileBytes + c * kBoxBytes,
+                                    &map_do, &do_full[sd], c * kBoxCols, i * kTileM, it.sl,
+                                    false);
+          }
+          __syncwarp();
+          ++do_loads;
+          return true;
+        };
+        if constexpr (!kSplit) {
+          // one slot index for both rings: q_empty is the block's combined release
+          const int s = q_loads % QS;
+          if (q_loads >= QS && !(ok = warp_wait(&q_empty[s], ((q_loads / QS) - 1) & 1, limit,
+                                                abort_flag, kWaitDkvEmpty)))
+            break;
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&q_full[s], C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_rows<PACKED>(smem + C::kOffQ + s * C::kTileBytes + c * kBoxBytes,
+                                    &map_q, &q_full[s], c * kBoxCols, i * kTileM, it.sl,
+                                    false);
+            mbar_arrive_expect_tx(&do_full[s], C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_rows<PACKED>(smem + C::kOffDO + s * C::kTileBytes + c * kBoxBytes,
+                                    &map_do, &do_full[s], c * kBoxCols, i * kTileM, it.sl,
+                                    false);
+          }
+          __syncwarp();
+          ++q_loads;
+          ++do_loads;
+        } else {
+          if (QS > DS)
+            ok = load_q() && load_do();
+          else
+            ok = load_do() && load_q();
+          if (!ok) break;
         }
-        __syncwarp();
-        ++loads;
       }
     }
     if (*abort_flag) {
       if (kv_loads > 0)
         mbar_wait(kv_full, (kv_loads - 1) & 1, kDrainLimit, nullptr, kWaitDkvDrain);
-      for (int b = max(0, loads - NS); b < loads; ++b) {
-        mbar_wait(&q_full[b % NS], (b / NS) & 1, kDrainLimit, nullptr, kWaitDkvDrain);
-        mbar_wait(&do_full[b % NS], (b / NS) & 1, kDrainLimit, nullptr, kWaitDkvDrain);
-      }
+      for (int b = max(0, q_loads - QS); b < q_loads; ++b)
+        mbar_wait(&q_full[b % QS], (b / QS) & 1, kDrainLimit, nullptr, kWaitDkvDrain);
+      for (int b = max(0, do_loads - DS); b < do_loads; ++b)
+        mbar_wait(&do_full[b % DS], (b / DS) & 1, kDrainLimit, nullptr, kWaitDkvDrain);
     }
   }
   else if (warp == 9) {
@@ -213,28 +293,28 @@ __global__ void __launch_bounds__(320, 1)
       // K_j, V_j of this item (kv_full: one completion per item; the next copy needs the
       // kv_free committed below) and its first Q block.
       if (!(ok = warp_poll(kv_full, items & 1, limit, abort_flag, kWaitDkvKV) &&
-                 warp_poll(&q_full[tb % NS], (tb / NS) & 1, limit, abort_flag, kWaitDkvQ)))
+                 warp_poll(&q_full[tb % QS], (tb / QS) & 1, limit, abort_flag, kWaitDkvQ)))
         break;
       // S^T overwrites the previous item's last P^T, read by a dV product the tensor core
       // runs before this one; dP^T likewise the last dS^T, read by the last dK product.
       tc_fence_after();
       if (elect_one()) {
-        issue_rowdot_d<D>(tmem + C::kColS, dk, dq + (tb % NS) * kStageStep, idesc_st);
+        issue_rowdot_d<D>(tmem + C::kColS, dk, dq + (tb % QS) * kStageStep, idesc_st);
         mma_commit(s_full);
       }
       __syncwarp();
-      if (!(ok = warp_poll(&do_full[tb % NS], (tb / NS) & 1, limit, abort_flag, kWaitDkvDO)))
+      if (!(ok = warp_poll(&do_full[tb % DS], (tb / DS) & 1, limit, abort_flag, kWaitDkvDO)))
         break;
       tc_fence_after();
       if (elect_one()) {
-        issue_rowdot_d<D>(tmem + C::kColDP, dv, ddo + (tb % NS) * kStageStep, idesc_st);
+        issue_rowdot_d<D>(tmem + C::kColDP, dv, ddo + (tb % DS) * kStageStep, idesc_st);
         mma_commit(dp_full);
       }
       __syncwarp();
       if (n == 1) commit(kv_free);  // every S^T and dP^T of the item issued
       for (int t = 0; ok && t < n; ++t) {
         const int b = tb + t, bn = b + 1;
-        const int s = b % NS, sn = bn % NS;
+        const int sq = b % QS, sqn = bn % QS, sd = b % DS, sdn = bn % DS;
         if (!(ok = warp_poll(p_full, b & 1, limit, abort_flag, kWaitDkvP))) break;
         // The first accumulating products of an item overwrite dV and dK: the previous
         // item's epilogue must have read them (acc_free: one completion per item, each
@@ -243,40 +323,42 @@ __global__ void __launch_bounds__(320, 1)
             !(ok = warp_poll(acc_free, (items - 1) & 1, limit, abort_flag, kWaitDkvAccFree)))
           break;
         tc_fence_after();
-        // dV_j += P^T dO_i
+        // dV_j += P^T dO_i, the last reader of dO_i's slot
         if (elect_one())
-          issue_tmem_a_split_d(tmem + C::kColAcc0, tmem + C::kColS, ddo_mn + s * kStageStep,
+          issue_tmem_a_split_d(tmem + C::kColAcc0, tmem + C::kColS, ddo_mn + sd * kStageStep,
                                idesc_acc, t > 0);
         __syncwarp();
+        if constexpr (kSplit) commit(&do_empty[sd]);
         if (t + 1 < n) {
-          if (!(ok = warp_poll(&q_full[sn], (bn / NS) & 1, limit, abort_flag, kWaitDkvQ)))
+          if (!(ok = warp_poll(&q_full[sqn], (bn / QS) & 1, limit, abort_flag, kWaitDkvQ)))
             break;
           tc_fence_after();
           if (elect_one()) {
-            issue_rowdot_d<D>(tmem + C::kColS, dk, dq + sn * kStageStep, idesc_st);
+            issue_rowdot_d<D>(tmem + C::kColS, dk, dq + sqn * kStageStep, idesc_st);
             mma_commit(s_full);
           }
           __syncwarp();
         }
         if (!(ok = warp_poll(ds_full, b & 1, limit, abort_flag, kWaitDkvDS))) break;
         tc_fence_after();
-        // dK_j += dS^T Q_i
+        // dK_j += dS^T Q_i, the last reader of Q_i's slot
         if (elect_one())
-          issue_tmem_a_split_d(tmem + C::kColAcc1, tmem + C::kColDP, dq_mn + s * kStageStep,
+          issue_tmem_a_split_d(tmem + C::kColAcc1, tmem + C::kColDP, dq_mn + sq * kStageStep,
                                idesc_acc, t > 0);
         __syncwarp();
+        if constexpr (kSplit) commit(&q_empty[sq]);
         if (t + 1 < n) {
-          if (!(ok = warp_poll(&do_full[sn], (bn / NS) & 1, limit, abort_flag, kWaitDkvDO)))
+          if (!(ok = warp_poll(&do_full[sdn], (bn / DS) & 1, limit, abort_flag, kWaitDkvDO)))
             break;
           tc_fence_after();
           if (elect_one()) {
-            issue_rowdot_d<D>(tmem + C::kColDP, dv, ddo + sn * kStageStep, idesc_st);
+            issue_rowdot_d<D>(tmem + C::kColDP, dv, ddo + sdn * kStageStep, idesc_st);
             mma_commit(dp_full);
           }
           __syncwarp();
           if (t + 2 == n) commit(kv_free);
         }
-        commit(&qdo_empty[s]);
+        if constexpr (!kSplit) commit(&q_empty[sq]);  // both slots of block b
       }
       if (!ok) break;
       commit(acc_done);
