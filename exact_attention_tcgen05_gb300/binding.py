@@ -456,6 +456,18 @@ def _host_cu(cu_q_host, cu_k_host, B):
     return cu_q_host.data_ptr(), cu_k_host.data_ptr()
 
 
+def _upload_cpu_cu(q, cu_q, cu_k, cu_q_host, cu_k_host):
+    """cu_seqlens given as CPU int32 tensors (both): uploaded to q's device for the kernels,
+    and kept as the host copies that order the work unless host copies were given."""
+    if (isinstance(cu_q, torch.Tensor) and isinstance(cu_k, torch.Tensor)
+            and cu_q.device.type == "cpu" and cu_k.device.type == "cpu"
+            and q.device.type == "cuda"):
+        if cu_q_host is None and cu_k_host is None:
+            cu_q_host, cu_k_host = cu_q.contiguous(), cu_k.contiguous()
+        cu_q, cu_k = cu_q.contiguous().to(q.device), cu_k.contiguous().to(q.device)
+    return cu_q, cu_k, cu_q_host, cu_k_host
+
+
 def _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k):
     Tq, H, d = _packed_of(q, "q")
     Tk, Hk, dk = _packed_of(k, "k")
@@ -488,7 +500,8 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
 
     cu_seqlens_q_host / _k_host: optional CPU int32 copies of the same offsets. They only
     order the kernels' work items (longest first, balanced over the SMs); the results do not
-    depend on them.
+    depend on them. cu_seqlens_q / _k may also be given as CPU int32 tensors: they are then
+    uploaded for the kernels and serve as the host copies.
 
     q [total_q, H, d], k and v [total_k, H, d]; sequence b owns query tokens
     cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key tokens cu_seqlens_k[b] ..
@@ -496,6 +509,8 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     every sequence (the caller knows them; reading cu_seqlens here would synchronise).
     Returns o [total_q, H, d] and lse [H, total_q]. Malformed sequences are reported by
     attn_last_kernel_status() as ATTN_ERR_INVALID_ARG."""
+    cu_seqlens_q, cu_seqlens_k, cu_seqlens_q_host, cu_seqlens_k_host = _upload_cpu_cu(
+        q, cu_seqlens_q, cu_seqlens_k, cu_seqlens_q_host, cu_seqlens_k_host)
     Tq, Tk, H, d, cu_q, cu_k, B = _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k)
     hq, hk = _host_cu(cu_seqlens_q_host, cu_seqlens_k_host, B)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
@@ -529,6 +544,8 @@ def attn_bwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.
     """dq, dk, dv of sum(do * o) for a packed batch (layouts and the optional host copies
     of cu_seqlens as attn_fwd_varlen), via libattn.so; workspace holds D [H, total_q]
     float32."""
+    cu_seqlens_q, cu_seqlens_k, cu_seqlens_q_host, cu_seqlens_k_host = _upload_cpu_cu(
+        q, cu_seqlens_q, cu_seqlens_k, cu_seqlens_q_host, cu_seqlens_k_host)
     Tq, Tk, H, d, cu_q, cu_k, B = _varlen_args(q, k, v, cu_seqlens_q, cu_seqlens_k)
     hq, hk = _host_cu(cu_seqlens_q_host, cu_seqlens_k_host, B)
     for name, x in (("o", o), ("do", do)):

@@ -217,3 +217,14 @@ def test_host_lengths_only_order_the_work(causal, d, lq, lk):
     for name, a, b, c in zip(("O", "LSE", "dQ", "dK", "dV"), base, right, wrong):
         assert torch.equal(a, b), f"{name}: host lengths changed the result"
         assert torch.equal(a, c), f"{name}: wrong host lengths changed the result"
+
+
+def test_cpu_cu_seqlens_are_uploaded_and_order_the_work():
+    """cu_seqlens given as CPU tensors: the binding uploads them for the kernels and uses
+    them as the host copies; the results are those of device cu_seqlens, bit for bit."""
+    w = I.varlen(8, 128, "bf16", True, seed=123, seqlens_q=(900, 33, 1500, 257, 640))
+    q, k, v, do, cu_q, cu_k = _tensors(w)
+    ref = _run(w, q, k, v, do, cu_q, cu_k)
+    got = _run(w, q, k, v, do, cu_q.cpu(), cu_k.cpu())
+    for name, a, b in zip(("O", "LSE", "dQ", "dK", "dV"), ref, got):
+        assert torch.equal(a, b), name
