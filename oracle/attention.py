@@ -137,10 +137,3 @@ def delta_rowsum(o: np.ndarray, do: np.ndarray) -> np.ndarray:
     """D_i = sum_c dO_ic * O_ic (the backward's preprocess quantity)."""
     return (np.asarray(do, dtype=np.float64) * np.asarray(o, dtype=np.float64)).sum(axis=1)
 
-
-def forward_row(q_row: np.ndarray, k: np.ndarray, v: np.ndarray, i: int, causal: bool,
-                scale: float) -> tuple[np.ndarray, float]:
-    """O_i and L_i of a single query row i (used to spot-check huge slices)."""
-    o, lse = attention_forward(q_row[None, :], k[: i + 1] if causal else k,
-                               v[: i + 1] if causal else v, False, scale)
-    return o[0], float(lse[0])

@@ -16,9 +16,10 @@ from exact_attention_tcgen05_gb300 import binding
 from exact_attention_tcgen05_gb300 import inputs as I
 import oracle.decode as OD
 
+from parity import o_error
+
 pytestmark = pytest.mark.gpu
 
-O_TOL = 1e-2
 L_TOL = 1e-3
 REC_TOL = 1e-3
 
@@ -42,8 +43,8 @@ def _check_slice(q, k, v, o, lse, parts, b, h, scale, splits):
     qd, kd, vd = (I.to_f64(x[b, h].cpu()) for x in (q, k, v))
     ref_o, ref_l, ref_parts = OD.decode(qd[0], kd, vd, scale, splits)
     got_o = o[b, h, 0].float().cpu().double().numpy()
-    err = np.abs(got_o - ref_o)
-    assert np.all(err <= O_TOL + _half_ulp(ref_o, o.dtype)), f"O error {err.max():.3e}"
+    r = o_error(got_o, ref_o, o.dtype)
+    assert r["o_excess"] <= 0, f"O error {r['o_max']:.3e}"
     assert abs(float(lse[b, h]) - ref_l) <= L_TOL, f"L {float(lse[b, h])} vs {ref_l}"
     if parts is None:
         return

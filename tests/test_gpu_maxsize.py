@@ -40,8 +40,8 @@ def test_maximum_length_sampled_rows_and_identities():
     O, L, DQ, DK, DV = (_f64(x[0, 0]) for x in (o, lse, dq, dk, dv))
 
     def check_rows(rows, ref):
-        raw, excess = o_error(O[rows], ref["o"], w.torch_dtype)
-        assert excess <= 0, (rows, raw)
+        r = o_error(O[rows], ref["o"], w.torch_dtype)
+        assert r["o_excess"] <= 0, (rows, r["o_max"])
         assert np.abs(L[rows] - ref["lse"]).max() <= LSE_TOL, rows
         assert rel_fro(DQ[rows], ref["dq"]) <= GRAD_TOL, rows
 

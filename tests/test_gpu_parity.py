@@ -11,7 +11,7 @@ from exact_attention_tcgen05_gb300 import binding
 from exact_attention_tcgen05_gb300 import inputs as I
 import oracle.attention as OA
 
-from parity import all_finite, assert_within, compare_slice, run_gpu
+from parity import all_finite, assert_within, compare_slice, record, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -65,7 +65,9 @@ def test_workload_sampled_slices(w):
     run = run_gpu(w)
     assert all_finite(run)
     for b, h in I.sampled_slices(w):
-        assert_within(compare_slice(w, run, b, h), f"{w.name} slice {(b, h)}")
+        res = compare_slice(w, run, b, h)
+        record(w.name, res)
+        assert_within(res, f"{w.name} slice {(b, h)}")
 
 
 def test_preprocess_kernel_matches_rowsum():
