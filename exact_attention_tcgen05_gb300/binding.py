@@ -2,13 +2,18 @@
 
 Every function here checks that the tensors are what the C ABI expects (CUDA,
 contiguous, [B, H, N, d], one 16-bit dtype), allocates outputs with torch when the
-caller passes none, and calls the library on torch's current stream. All arithmetic
+caller passes none, and calls the library on `stream` (default: torch's current
+stream). With a stream given, everything the function allocates or copies (outputs,
+workspaces, cu_seqlens uploaded from the CPU) is made on that stream, so the caching
+allocator cannot hand that memory to other work while the kernels still use it. All arithmetic
 runs in the library's kernels; there is no fallback of any kind: if the library is
 missing or fails, these functions raise.
 """
 from __future__ import annotations
 
 import ctypes
+import functools
+import inspect
 import math
 import os
 from typing import Optional
@@ -81,6 +86,21 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     return _lib
 
 
+def _on_launch_stream(fn):
+    """Runs fn with its `stream` argument (if given) as torch's current stream, so that
+    the tensors fn allocates and the copies it makes are ordered with its launches."""
+    sig = inspect.signature(fn)
+
+    @functools.wraps(fn)
+    def wrapper(*args, **kwargs):
+        stream = sig.bind_partial(*args, **kwargs).arguments.get("stream")
+        if stream is None:
+            return fn(*args, **kwargs)
+        with torch.cuda.stream(stream):
+            return fn(*args, **kwargs)
+    return wrapper
+
+
 def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
     s = torch.cuda.current_stream() if stream is None else stream
     return s.cuda_stream
@@ -129,6 +149,7 @@ def _lse_like(q: torch.Tensor, x: Optional[torch.Tensor], name: str) -> torch.Te
     return x
 
 
+@_on_launch_stream
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
              scale: Optional[float] = None, o: Optional[torch.Tensor] = None,
              lse: Optional[torch.Tensor] = None,
@@ -155,6 +176,7 @@ def attn_bwd_workspace_bytes(B: int, H: int, N: int) -> int:
     return int(load().attn_bwd_workspace_bytes(B, H, N))
 
 
+@_on_launch_stream
 def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              lse: torch.Tensor, do: torch.Tensor, causal: bool = False,
              scale: Optional[float] = None, dq: Optional[torch.Tensor] = None,
@@ -190,6 +212,7 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
 NOALLOC_MAX_ROWS = 4194304  # ATTN_NOALLOC_MAX_ROWS in include/attn.h
 
 
+@_on_launch_stream
 def attn_bwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
                      lse: torch.Tensor, do: torch.Tensor, causal: bool = False,
                      scale: Optional[float] = None, dq: Optional[torch.Tensor] = None,
@@ -220,6 +243,7 @@ def attn_bwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch
     return dq, dk, dv
 
 
+@_on_launch_stream
 def attn_bwd_preprocess(o: torch.Tensor, do: torch.Tensor,
                         delta: Optional[torch.Tensor] = None,
                         stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
@@ -234,6 +258,7 @@ def attn_bwd_preprocess(o: torch.Tensor, do: torch.Tensor,
     return delta
 
 
+@_on_launch_stream
 def attn_bwd_dkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, lse: torch.Tensor,
                  delta: torch.Tensor, do: torch.Tensor, causal: bool = False,
                  scale: Optional[float] = None, dk: Optional[torch.Tensor] = None,
@@ -260,6 +285,7 @@ def attn_bwd_dkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, lse: torch.T
     return dk, dv
 
 
+@_on_launch_stream
 def attn_bwd_dq(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, lse: torch.Tensor,
                 delta: torch.Tensor, do: torch.Tensor, causal: bool = False,
                 scale: Optional[float] = None, dq: Optional[torch.Tensor] = None,
@@ -287,6 +313,7 @@ def attn_step_host_scratch_bytes(B: int, H: int, N: int, d: int, chunks: int) ->
     return int(load().attn_step_host_scratch_bytes(B, H, N, d, chunks))
 
 
+@_on_launch_stream
 def attn_step_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, do: torch.Tensor,
                    o: torch.Tensor, lse: torch.Tensor, dq: torch.Tensor, dk: torch.Tensor,
                    dv: torch.Tensor, scratch: torch.Tensor, causal: bool = False,
@@ -351,6 +378,7 @@ def _partials_like(q, B, H, d, splits, partials):
     return partials
 
 
+@_on_launch_stream
 def attn_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                 scale: Optional[float] = None, num_splits: Optional[int] = None,
                 o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
@@ -377,6 +405,7 @@ def attn_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     return o, lse
 
 
+@_on_launch_stream
 def attn_decode_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                         scale: Optional[float] = None, num_splits: int = 1,
                         partials: Optional[torch.Tensor] = None,
@@ -394,6 +423,7 @@ def attn_decode_partial(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     return partials
 
 
+@_on_launch_stream
 def attn_decode_merge(partials: torch.Tensor, dtype: torch.dtype,
                       o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                       stream: Optional[torch.cuda.Stream] = None
@@ -458,7 +488,9 @@ def _host_cu(cu_q_host, cu_k_host, B):
 
 def _upload_cpu_cu(q, cu_q, cu_k, cu_q_host, cu_k_host):
     """cu_seqlens given as CPU int32 tensors (both): uploaded to q's device for the kernels,
-    and kept as the host copies that order the work unless host copies were given."""
+    and kept as the host copies that order the work unless host copies were given. The
+    callers run on their launch stream (_on_launch_stream), so the upload is queued there,
+    before the kernels that read it, and its memory belongs to that stream."""
     if (isinstance(cu_q, torch.Tensor) and isinstance(cu_k, torch.Tensor)
             and cu_q.device.type == "cpu" and cu_k.device.type == "cpu"
             and q.device.type == "cuda"):
@@ -487,6 +519,7 @@ def attn_bwd_varlen_workspace_bytes(H: int, total_q: int) -> int:
     return int(load().attn_bwd_varlen_workspace_bytes(H, total_q))
 
 
+@_on_launch_stream
 def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                     cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor,
                     max_seqlen_q: int, max_seqlen_k: int, causal: bool = False,
@@ -530,6 +563,7 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     return o, lse
 
 
+@_on_launch_stream
 def attn_bwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
                     lse: torch.Tensor, do: torch.Tensor, cu_seqlens_q: torch.Tensor,
                     cu_seqlens_k: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int,

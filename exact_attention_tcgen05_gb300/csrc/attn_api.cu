@@ -472,6 +472,89 @@ size_t step_set_bytes(long long slices, int N, int d) {
 }
 }  // namespace
 
+namespace {
+// attn_step_host's two side streams and 3 x chunks events, per CUDA context (streams and
+// events belong to the context current when they are made), created on the first call in
+// that context and kept until the process exits: creating and destroying them on every
+// call costs time inside the step.
+struct StepResources {
+  CUcontext ctx = nullptr;
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  cudaEvent_t start = nullptr;
+  std::vector<cudaEvent_t> ev_in, ev_comp, ev_out;
+};
+std::mutex g_step_mu;
+std::vector<StepResources*> g_step_res;
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = []() -> CtxGetCurrentFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<CtxGetCurrentFn>(p);
+    return nullptr;
+  }();
+  return fn;
+}
+
+cudaError_t new_event(cudaEvent_t* ev) {
+  return cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+}
+
+// The resources of the calling thread's current context with at least `chunks` events of
+// each kind (call with g_step_mu held). A thread without a current context is bound to its
+// device's primary context by the first runtime call, as any runtime call would.
+cudaError_t step_resources(int chunks, StepResources** out) {
+  CtxGetCurrentFn get = ctx_get_current();
+  if (get == nullptr) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  if (ctx == nullptr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return e;
+    if (get(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorDeviceUninitialized;
+  }
+  StepResources* r = nullptr;
+  for (StepResources* x : g_step_res)
+    if (x->ctx == ctx) r = x;
+  if (r == nullptr) {
+    r = new StepResources;
+    r->ctx = ctx;
+    cudaError_t e = cudaStreamCreateWithFlags(&r->s_in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&r->s_out, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = new_event(&r->start);
+    if (e != cudaSuccess) {
+      if (r->s_in) cudaStreamDestroy(r->s_in);
+      if (r->s_out) cudaStreamDestroy(r->s_out);
+      delete r;
+      return e;
+    }
+    g_step_res.push_back(r);
+  }
+  while ((int)r->ev_in.size() < chunks) {
+    cudaEvent_t a = nullptr, b = nullptr, c = nullptr;
+    cudaError_t e = new_event(&a);
+    if (e == cudaSuccess) e = new_event(&b);
+    if (e == cudaSuccess) e = new_event(&c);
+    if (e != cudaSuccess) {
+      for (cudaEvent_t x : {a, b, c})
+        if (x) cudaEventDestroy(x);
+      return e;
+    }
+    r->ev_in.push_back(a);
+    r->ev_comp.push_back(b);
+    r->ev_out.push_back(c);
+  }
+  *out = r;
+  return cudaSuccess;
+}
+}  // namespace
+
 size_t attn_step_host_scratch_bytes(int B, int H, int N, int d, int chunks) {
   if (B <= 0 || H <= 0 || N <= 0 || chunks <= 0 || !head_dim_ok(d)) return 0;
   const long long bh = (long long)B * H;
@@ -502,20 +585,21 @@ attn_status attn_step_host(const void* q, const void* k, const void* v, const vo
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
 
   cudaStream_t cs = static_cast<cudaStream_t>(cuda_stream);
-  cudaStream_t s_in = nullptr, s_out = nullptr;
-  cudaEvent_t start = nullptr;
-  std::vector<cudaEvent_t> ev_in(chunks, nullptr), ev_comp(chunks, nullptr),
-      ev_out(chunks, nullptr);
-  cudaError_t e = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking);
-  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&start, cudaEventDisableTiming);
-  for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
-    e = cudaEventCreateWithFlags(&ev_in[c], cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_comp[c], cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_out[c], cudaEventDisableTiming);
-  }
+  // The side streams and events of this context, created on its first call and kept; the
+  // lock is held while this call enqueues its work, so concurrent calls never re-record
+  // an event another call is still queueing waits on (waits already queued keep the
+  // state the event had when they were queued).
+  std::lock_guard<std::mutex> lock(g_step_mu);
+  StepResources* res = nullptr;
+  cudaError_t e = step_resources(chunks, &res);
+  if (e != cudaSuccess) return from_cuda(e);
+  cudaStream_t s_in = res->s_in, s_out = res->s_out;
+  cudaEvent_t start = res->start;
+  const std::vector<cudaEvent_t>& ev_in = res->ev_in;
+  const std::vector<cudaEvent_t>& ev_comp = res->ev_comp;
+  const std::vector<cudaEvent_t>& ev_out = res->ev_out;
   // The side streams start after the work already queued on the caller's stream.
-  if (e == cudaSuccess) e = cudaEventRecord(start, cs);
+  e = cudaEventRecord(start, cs);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(s_in, start, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, start, 0);
 
@@ -564,14 +648,6 @@ attn_status attn_step_host(const void* q, const void* k, const void* v, const vo
   }
   // The caller's stream completes after the last copy out.
   if (e == cudaSuccess && st == ATTN_OK) e = cudaStreamWaitEvent(cs, ev_out[chunks - 1], 0);
-  for (int c = 0; c < chunks; ++c) {
-    if (ev_in[c]) cudaEventDestroy(ev_in[c]);
-    if (ev_comp[c]) cudaEventDestroy(ev_comp[c]);
-    if (ev_out[c]) cudaEventDestroy(ev_out[c]);
-  }
-  if (start) cudaEventDestroy(start);
-  if (s_in) cudaStreamDestroy(s_in);  // released once their queued work completes
-  if (s_out) cudaStreamDestroy(s_out);
   if (st != ATTN_OK) return st;
   return from_cuda(e);
 }

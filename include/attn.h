@@ -31,9 +31,17 @@
  *            is enqueued on it; the calls never synchronise the device and return
  *            as soon as the launches are queued.
  *   Ownership the caller allocates and owns every buffer and the stream. The library
- *            allocates no device memory and keeps no state between calls (tensor
- *            maps are encoded per call); its only device globals are the status
- *            words described under Errors. Safe to call from several host threads.
+ *            allocates no device memory and keeps no per-call state (tensor maps
+ *            are encoded per call). Its device globals, one copy per device and
+ *            shared by every call in the process, are the status words described
+ *            under Errors and the 16 MiB array g_bwd_scratch that attn_bwd_noalloc
+ *            keeps its D values in. Its host-side caches (the last schedule table
+ *            of each persistent kernel, attn_step_host's side streams and events,
+ *            attn_bwd_noalloc's array addresses) are guarded by locks. The calls
+ *            may be made from several host threads; but calls whose work can
+ *            overlap on the GPU share the status words, so attn_last_kernel_status
+ *            then reports the first timeout of any of them, and they race on
+ *            g_bwd_scratch if both are attn_bwd_noalloc.
  *   Errors   ATTN_ERR_INVALID_ARG for a bad size, pointer, alignment, scale or an
  *            output that overlaps an input (checked on the host before any CUDA
  *            call); ATTN_ERR_UNSUPPORTED for a head dimension or type the kernels do
@@ -216,9 +224,10 @@ attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const float
  * library, in device memory that every GPU which loads the library reserves until the
  * process exits. B * H * N above ATTN_NOALLOC_MAX_ROWS returns ATTN_ERR_INVALID_ARG.
  * Neither the library nor this call allocates anything.
- * The first call on a device looks up that device's address of the array (a
- * cudaGetSymbolAddress with the device current); make that first call before any stream
- * capture on the device. Every call shares the one array and it keeps the last call's
+ * The first call in a CUDA context (the device's primary context, or one a host engine
+ * created and made current) looks up the array's address in that context (a
+ * cudaGetSymbolAddress, with that context current) and remembers it for later calls in
+ * the same context; make that first call before any stream capture there. Every call shares the one array and it keeps the last call's
  * values: calls whose work can overlap on the GPU (other streams, or host threads with
  * no ordering between them) race on it and produce wrong gradients, so serialise them.
  * Nothing in it has to start at zero: each call writes every entry it reads.
@@ -236,8 +245,11 @@ attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const 
  * consecutive slices whose sizes ramp up and down (weights 1, 2, 3, 3, ..., 3, 2, 1): the
  * first upload and the last chunk's compute and download overlap nothing, so those chunks
  * are short. While chunk c is computed on cuda_stream, the inputs of chunk c + 1 are
- * copied in and the outputs of chunk c - 1 copied out on two streams the call creates and
- * releases. Results are identical to attn_fwd + attn_bwd on
+ * copied in and the outputs of chunk c - 1 copied out on two side streams. The side
+ * streams and the call's events are made on the first call in a CUDA context and kept for
+ * later calls there until the process exits; a lock orders the enqueueing of concurrent
+ * calls, whose copies then share the side streams. Results are identical to attn_fwd +
+ * attn_bwd on
  * the whole tensors (every (b, h) slice is computed independently).
  *   q, k, v, dO        HOST [B, H, N, d] 16-bit inputs; pinned (page-locked) memory is
  *                      needed for the copies to overlap (pageable memory works, serially)
@@ -306,6 +318,9 @@ const char* attn_status_str(attn_status s);
  * malformed sequence. Returns ATTN_OK when nothing was recorded since the last call,
  * ATTN_ERR_INVALID_ARG for a malformed sequence (code 0x7E), ATTN_ERR_TIMEOUT for a
  * wait, ATTN_ERR_CUDA if the copy fails. *where (may be NULL) receives the first code.
+ * The status words are process-wide (one per device, per kernel file), not per call or
+ * per stream: after calls on several streams or threads whose work overlapped, the word
+ * holds the first code any of them recorded, and reading it clears it for all of them.
  */
 attn_status attn_last_kernel_status(void* cuda_stream, int* where);
 
