@@ -53,6 +53,72 @@ def load_peaks() -> dict:
 # ------------------------------------------------------------------------------------
 # clocks during the timed region
 # ------------------------------------------------------------------------------------
+class NvmlClockSampler:
+    """SM clock and clock-event reasons of one GPU polled every ~2 ms through NVML (the
+    driver's management library, loaded with ctypes; reads only), so that even a timed
+    region of a few tens of milliseconds gets a few dozen samples. start()/stop() as for
+    ClockSampler; unavailable (None from create) where the library cannot be loaded."""
+
+    # clock-event reason bits of the public NVML API
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    @classmethod
+    def create(cls, index: int):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return None
+            handle = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(handle)) != 0:
+                return None
+            reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+            if reasons is None:
+                reasons = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        except (OSError, AttributeError):
+            return None
+        return cls(lib, handle, reasons)
+
+    def __init__(self, lib, handle, reasons_fn):
+        import ctypes
+        import threading
+        self.ct = ctypes
+        self.lib, self.handle, self.reasons_fn = lib, handle, reasons_fn
+        self.samples = []
+        self.stop_flag = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        mx = ctypes.c_uint(0)
+        lib.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx))  # NVML_CLOCK_SM = 1
+        self.max_mhz = float(mx.value)
+
+    def _run(self):
+        ct = self.ct
+        clk, rs = ct.c_uint(0), ct.c_ulonglong(0)
+        while not self.stop_flag.is_set():
+            t = time.time()
+            ok = self.lib.nvmlDeviceGetClockInfo(self.handle, 1, ct.byref(clk)) == 0
+            ok = ok and self.reasons_fn(self.handle, ct.byref(rs)) == 0
+            if ok:
+                self.samples.append((t, float(clk.value), int(rs.value)))
+            time.sleep(0.002)
+
+    def start(self):
+        self.thread.start()
+
+    def stop(self, t0: float | None = None, t1: float | None = None) -> dict | None:
+        self.stop_flag.set()
+        self.thread.join(timeout=5)
+        inside = [x for x in self.samples if t0 is None or t0 <= x[0] <= t1]
+        if not inside:
+            return None
+        reasons = sorted({name for _, _, r in inside for bit, name in self.REASONS.items()
+                          if r & bit})
+        return {"sm_mhz": statistics.median(c for _, c, _ in inside),
+                "sm_max_mhz": self.max_mhz, "samples": len(inside), "reasons": reasons,
+                "window": "NVML samples taken inside the timed region, every ~2 ms"}
+
+
 class ClockSampler:
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -205,6 +271,82 @@ print(json.dumps({{"slices": done, "seconds": t_total}}))
                       f"{r['seconds']:.1f} s"}
 
 
+def config_of(w, world: int) -> dict:
+    """The `config` object of the JSON line (both arms print the same one)."""
+    f = flops(w, "fwd") + flops(w, "bwd")
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+            "scale": w.scale, "counted_tflop_per_step": f / 1e12,
+            "l2": f"inputs larger than L2: each of q,k,v,dO is "
+                  f"{w.B * w.H * w.N * w.d * 2 / 2**20:.0f} MiB > {L2_BYTES / 2**20:.0f} MiB",
+            "parallelism": f"replicas x{world}"}
+
+
+def time_workload(w, steps: int, warmup: int) -> dict:
+    """Per-kernel times (ms, averaged) of `steps` forward + backward passes over workload w,
+    inputs resident, after `warmup` untimed ones; CUDA events on the launch stream."""
+    import torch
+    from exact_attention_tcgen05_gb300 import binding
+    from exact_attention_tcgen05_gb300 import inputs as I
+    q, k, v, do = (I.make_tensor(w, t).cuda() for t in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    delta = torch.empty_like(lse)
+    stream = torch.cuda.current_stream()
+    kern = (
+        lambda: binding.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, o=o, lse=lse),
+        lambda: binding.attn_bwd_preprocess(o, do, delta),
+        lambda: binding.attn_bwd_dkv(q, k, v, lse, delta, do, causal=w.causal, scale=w.scale,
+                                     dk=dk, dv=dv),
+        lambda: binding.attn_bwd_dq(q, k, v, lse, delta, do, causal=w.causal, scale=w.scale,
+                                    dq=dq),
+    )
+    for _ in range(warmup):
+        for fn in kern:
+            fn()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(stream)
+        for j, fn in enumerate(kern):
+            fn()
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    code, where = binding.attn_last_kernel_status()
+    if code != binding.ATTN_OK:
+        raise RuntimeError(f"{w.name}: a kernel reported status {code} (site {where:#x})")
+    out = {n: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)) / steps
+           for j, n in enumerate(("fwd", "delta", "dkv", "dq"))}
+    out["step"] = ev[0][0].elapsed_time(ev[-1][4]) / steps
+    del q, k, v, do, o, lse, dq, dk, dv, delta
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_workloads(args, peaks: dict, skip: str) -> dict:
+    """Forward and backward throughput of the other quoted workloads (the one the line is
+    about is skipped), measured after the main timed region, each on its own."""
+    from exact_attention_tcgen05_gb300 import inputs as I
+    burst = peaks["bf16_tflops"]
+    steps = max(10, min(args.steps, 30))
+    out = {}
+    for w in I.WORKLOADS:
+        if w.name == skip:
+            continue
+        t = time_workload(w, steps, max(3, args.warmup))
+        f_fwd, f_bwd = flops(w, "fwd"), flops(w, "bwd")
+        bwd_ms = t["delta"] + t["dkv"] + t["dq"]
+        fwd_tf = f_fwd / (t["fwd"] * 1e-3) / 1e12
+        bwd_tf = f_bwd / (bwd_ms * 1e-3) / 1e12
+        out[w.name] = {
+            "steps": steps, "ms_per_step": t["step"],
+            "step_tflops": (f_fwd + f_bwd) / (t["step"] * 1e-3) / 1e12,
+            "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+            "fwd_frac_of_burst": fwd_tf / burst, "bwd_frac_of_burst": bwd_tf / burst,
+            "kernels_ms": {n: t[n] for n in ("fwd", "delta", "dkv", "dq")}}
+    return out
+
+
 def run_ours(args) -> None:
     import torch
     from exact_attention_tcgen05_gb300 import binding
@@ -237,7 +379,7 @@ def run_ours(args) -> None:
     # --- device-timed region: inputs resident, per-kernel events on the launch stream.
     names = ("fwd", "delta", "dkv", "dq")
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    clocks = ClockSampler(local)
+    clocks = NvmlClockSampler.create(local) or ClockSampler(local)
     barrier(world)
     clocks.start()
     time.sleep(0.3)
@@ -315,6 +457,7 @@ def run_ours(args) -> None:
     dom_flops = flops(w, dominant)
     achieved = dom_flops / (avg[dominant] * 1e-3) / 1e12
     sustained = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    burst = peaks["bf16_tflops"]
     fwd_t = f_fwd / (avg["fwd"] * 1e-3) / 1e12
     bwd_ms = avg["delta"] + avg["dkv"] + avg["dq"]
     bwd_t = f_bwd / (bwd_ms * 1e-3) / 1e12
@@ -325,12 +468,7 @@ def run_ours(args) -> None:
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded N(0,1) inputs, see exact_attention_tcgen05_gb300/inputs.py)",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
-                   "causal": w.causal, "scale": w.scale,
-                   "counted_tflop_per_step": (f_fwd + f_bwd) / 1e12,
-                   "l2": f"inputs larger than L2: each of q,k,v,dO is "
-                         f"{w.B * w.H * w.N * w.d * 2 / 2**20:.0f} MiB > {L2_BYTES / 2**20:.0f} MiB",
-                   "parallelism": f"replicas x{world}"},
+        "config": config_of(w, world),
         "fwd_tflops": fwd_t, "bwd_tflops": bwd_t,
         "frac_of_peak": {"fwd": fwd_t / peaks["bf16_tflops"], "bwd": bwd_t / peaks["bf16_tflops"],
                          "peak_tflops": peaks["bf16_tflops"], "peak_source": peaks["source"],
@@ -339,15 +477,20 @@ def run_ours(args) -> None:
         "delta_kernel": {"achieved_gbs": delta_bytes / (avg["delta"] * 1e-3) / 1e9,
                          "peak_gbs": peaks["hbm_gbs"],
                          "frac": delta_bytes / (avg["delta"] * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+        # The kernels are timed inside a region of well under a second, so the burst peak
+        # (a GEMM timed alone) is the one to compare with, not the seconds-long sustained one.
         "roofline": {"kernel": dominant, "bound": "tensor", "achieved": achieved,
-                     "peak": sustained, "unit": "TFLOP/s", "frac": achieved / sustained,
-                     "peak_kind": f"bf16 sustained ({peaks['source']})",
+                     "peak": burst, "unit": "TFLOP/s", "frac": achieved / burst,
+                     "peak_kind": f"bf16 burst ({peaks['source']})",
+                     "frac_of_sustained": achieved / sustained,
                      "algorithmic_tflop_per_launch": dom_flops / 1e12, "traffic": traffic},
         "e2e": e2e, "clocks": clock_info, "gpu_launches": 4 * args.steps,
         "env": {"gpu": torch.cuda.get_device_name(), "torch": torch.__version__,
                 "cuda": torch.version.cuda,
                 "sm_count": torch.cuda.get_device_properties(0).multi_processor_count},
     }
+    if not args.no_workloads:
+        line["workloads"] = measure_workloads(args, peaks, w.name)
     if not args.no_decode:
         line["decode"] = measure_decode(args, peaks)
     if not args.no_varlen:
@@ -573,10 +716,10 @@ def run_reference(args) -> None:
         "steps": len(times), "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded, same generator as the CUDA arm)",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
-                   "causal": w.causal, "step": "one (b,h) slice, forward + backward"},
+        "config": config_of(w, 1),
         "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
-                         "sample": f"{len(times)} (b,h) slices of {w.name}, fp64 numpy oracle"},
+                         "sample": f"{len(times)} (b,h) slices of {w.name}, one slice "
+                                   f"forward + backward per step, fp64 numpy oracle"},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -593,6 +736,7 @@ def main() -> None:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true")
     ap.add_argument("--no-varlen", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
