@@ -663,7 +663,8 @@ def load_traffic(kernel: str, workload: str):
 # The source files each kernel is compiled from (a traffic record is valid only while
 # their contents match the hash stored with it).
 KERNEL_SOURCES = {
-    "fwd": ["fwd.cuh", "fwd_persistent.cuh", "schedule.h", "kernels_fwd.cu"],
+    "fwd": ["fwd.cuh", "fwd_persistent.cuh", "fwd_pair.cuh", "pair.cuh", "schedule.h",
+            "kernels_fwd.cu"],
     "delta": ["bwd_delta.cuh", "kernels_delta.cu"],
     "dkv": ["bwd_dkv.cuh", "bwd_dkv_persistent.cuh", "bwd_dq.cuh", "bwd_dq_persistent.cuh",
             "schedule.h", "kernels_dkv.cu"],

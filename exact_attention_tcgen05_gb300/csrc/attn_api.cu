@@ -110,10 +110,11 @@ attn_status encode_3d(CUtensorMap* m, const void* base, bool bf16, const cuuint6
 
 // [BH, N, d] 16-bit tensor, read as [64-column x 128-row] boxes with 128-byte swizzle;
 // rows past N read as zero.
-attn_status encode_map(CUtensorMap* m, const void* base, int BH, int N, int d, bool bf16) {
+attn_status encode_map(CUtensorMap* m, const void* base, int BH, int N, int d, bool bf16,
+                       int box_rows = 128) {
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * (cuuint64_t)d * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   return encode_3d(m, base, bf16, dims, strides, box);
 }
 
@@ -121,10 +122,10 @@ attn_status encode_map(CUtensorMap* m, const void* base, int BH, int N, int d, b
 // 128-byte swizzle: the same shared-memory image as a [64 x 128] box of the dense map.
 // Tokens past `total` read as zero.
 attn_status encode_map_packed(CUtensorMap* m, const void* base, int H, int total, int d,
-                              bool bf16) {
+                              bool bf16, int box_rows = 128) {
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)total};
   const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * (cuuint64_t)d * 2};
-  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
   return encode_3d(m, base, bf16, dims, strides, box);
 }
 
@@ -191,6 +192,8 @@ attn_status attn_fwd_qk(const void* q, const void* k, const void* v, void* o, fl
   if ((st = encode_map(&m.k, k, s.BH, Nk, d, s.bf16)) != ATTN_OK) return st;
   if ((st = encode_map(&m.v, v, s.BH, Nk, d, s.bf16)) != ATTN_OK) return st;
   m.d_o = m.v;
+  m.k64 = m.k;
+  if (d > 64 && (st = encode_map(&m.k64, k, s.BH, Nk, d, s.bf16, 64)) != ATTN_OK) return st;
   return from_cuda(attn::launch_fwd(m, s, o, lse, static_cast<cudaStream_t>(cuda_stream)));
 }
 
@@ -393,6 +396,9 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
   if ((st = encode_map_packed(&m.k, k, H, total_k, d, s.bf16)) != ATTN_OK) return st;
   if ((st = encode_map_packed(&m.v, v, H, total_k, d, s.bf16)) != ATTN_OK) return st;
   m.d_o = m.v;
+  m.k64 = m.k;
+  if (d > 64 && (st = encode_map_packed(&m.k64, k, H, total_k, d, s.bf16, 64)) != ATTN_OK)
+    return st;
   return from_cuda(attn::launch_fwd(m, s, o, lse, static_cast<cudaStream_t>(cuda_stream)));
 }
 
@@ -776,6 +782,9 @@ attn_status attn_last_kernel_status(void* cuda_stream, int* where) {
   }
   if (where != nullptr) *where = first;
   if (first == attn::kStatusBadSeqlens) return ATTN_ERR_INVALID_ARG;
+  // a kernel that found its launch unusable and did nothing (shared memory not aligned,
+  // the two tensor-memory allocations of a CTA pair at different addresses)
+  if (first == attn::kStatusSmemAlign || first == attn::kStatusPairTmem) return ATTN_ERR_CUDA;
   return first == 0 ? ATTN_OK : ATTN_ERR_TIMEOUT;
 }
 

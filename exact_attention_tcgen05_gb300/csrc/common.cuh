@@ -20,14 +20,17 @@ constexpr float kLn2 = 0.6931471805599453f;
 enum WaitSite : int {
   kWaitFwdQ = 0x11, kWaitFwdK, kWaitFwdV, kWaitFwdEmpty, kWaitFwdS, kWaitFwdP, kWaitFwdO,
   kWaitFwdDrain, kWaitFwdX, kWaitFwdQEmpty, kWaitFwdOFree,
+  kWaitFwdPeer,  // CTA pairs: rank 1's copies (forwarded to rank 0)
+  kWaitFwdExit,  // CTA pairs: the exit handshake
   kWaitDqQ = 0x21, kWaitDqK, kWaitDqV, kWaitDqEmpty, kWaitDqS, kWaitDqDP, kWaitDqDS,
   kWaitDqDone, kWaitDqDrain, kWaitDqSC, kWaitDqQFree, kWaitDqAccFree,
   kWaitDkvKV = 0x31, kWaitDkvQ, kWaitDkvDO, kWaitDkvEmpty, kWaitDkvS, kWaitDkvDP,
   kWaitDkvP, kWaitDkvDS, kWaitDkvDone, kWaitDkvDrain, kWaitDkvStats, kWaitDkvKVFree,
   kWaitDkvAccFree,
   kWaitDecFull = 0x41, kWaitDecDrain,
+  kErrPairTmem = kStatusPairTmem,  // CTA pairs: the two tensor-memory allocations differ
   kErrSeqlens = kStatusBadSeqlens,  // a packed batch's cu_seqlens hold a bad sequence
-  kErrSmemAlign = 0x7F  // dynamic shared memory not 1024-byte aligned (kernel skipped)
+  kErrSmemAlign = kStatusSmemAlign  // dynamic shared memory not 1024-byte aligned
 };
 
 // Bound of the waits that let a CTA's own in-flight work finish before it releases shared

@@ -4,6 +4,7 @@
 #include <vector>
 
 #include "fwd.cuh"
+#include "fwd_pair.cuh"
 #include "fwd_persistent.cuh"
 #include "launch.h"
 
@@ -72,6 +73,103 @@ static bool fwd_schedule(const Shape& s, int nqb, int G, ItemTable& out) {
   return true;
 }
 
+// The CTA-pair forward (fwd_pair.cuh) runs only when ATTN_FWD_PAIR = 1, in place of the
+// 128-column persistent forward; it gives the same bits. Measured on GB300 it is slower
+// (B4 H32 N4096 causal: 0.574 against 0.420 ms): the forward is bound by each tile's chain
+// S -> softmax -> P V, not by its copies or products, and the pair adds the wait for the
+// other CTA's P to that chain.
+static bool use_pair_fwd(const Shape& s) {
+  static const bool on = [] {
+    const char* e = std::getenv("ATTN_FWD_PAIR");
+    return e != nullptr && e[0] == '1';
+  }();
+  return on && s.d > 64 && use_persistent_fwd(s);
+}
+
+// Key blocks of pair item slot `x` (512 query rows; the geometry of fwd_pair_item_geom).
+static int fwd_pair_item_blocks(int nq, int nk, bool causal, int x) {
+  const int nsb = (nq + 4 * kTileM - 1) / (4 * kTileM);
+  if (x >= nsb) return 0;
+  const int nkb = (nk + kTileN - 1) / kTileN;
+  const int off = nk - nq;
+  const int q0 = (nsb - 1 - x) * 4 * kTileM;
+  int n = 0;
+  for (int t = 0; t < 2; ++t) {
+    const int r0 = q0 + t * 2 * kTileM;
+    if (r0 >= nq) continue;
+    const int last = std::min(r0 + 2 * kTileM, nq) - 1;
+    n = std::max(n, causal ? std::min(nkb, (last + off) / kTileN + 1) : nkb);
+  }
+  return n;
+}
+
+static bool fwd_pair_schedule(const Shape& s, int nsb, int G, ItemTable& out) {
+  const bool packed = s.vl.cu_q != nullptr;
+  const long long n_items = (long long)nsb * s.BH;
+  if (!item_table_applies(s.causal, packed, s.host_cu_q != nullptr, n_items, G)) return false;
+  static ItemTableCache cache;
+  const long long k[8] = {s.BH, s.N, s.Nk, s.d, G, nsb, s.causal ? 1 : 0,
+                          lengths_hash(s.host_cu_q, s.host_cu_k, s.vl_b)};
+  cache.get(k, G, n_items, out, [&](ItemTable& t) {
+    const long long kv_bytes =
+        packed ? 4LL * std::max(1, s.vl.total_k / std::max(1, s.vl_b)) * s.d : 4LL * s.Nk * s.d;
+    auto cost = [&](int bh, int x) -> long long {
+      int nq, nk;
+      slice_lengths(s, bh, nq, nk);
+      const int n = fwd_pair_item_blocks(nq, nk, s.causal, x);
+      return n > 0 ? n + 1 : 0;
+    };
+    greedy_item_table(s.BH, nsb, cost, item_table_window(s.BH, kv_bytes), G, t);
+  });
+  return true;
+}
+
+// Clusters of two CTAs of `kern` (320 threads, `smem` bytes each) that fit on the device at
+// once, asked of the runtime once per device: the persistent pair grid's size.
+template <class Kern>
+static int pair_clusters(Kern kern, int smem) {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return sm_count_fwd() / 2;
+  if (cached[dev] > 0) return cached[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (sm_count_fwd() / 2), 1, 1);
+  cfg.blockDim = dim3(320, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = sm_count_fwd() / 2;
+  }
+  n = std::min(n, kItemTableMaxCtas);
+  cached[dev] = n;
+  return n;
+}
+
+template <bool BF16, bool PACKED>
+static cudaError_t launch_fwd_pair(const Maps& m, const Shape& s, const FwdParams& p,
+                                   cudaStream_t st) {
+  using CP = FwdPairCfg<128>;
+  const int nsb_max = (s.N + 4 * kTileM - 1) / (4 * kTileM);
+  const long long n_items = (long long)nsb_max * s.BH;
+  auto kt = attn_fwd_pair_kernel<BF16, PACKED, ItemTable>;
+  auto ks = attn_fwd_pair_kernel<BF16, PACKED, FwdSerpentine>;
+  cudaError_t e = cudaFuncSetAttribute(kt, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       CP::kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, CP::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int G = (int)std::min<long long>(n_items, pair_clusters(ks, CP::kSmemBytes));
+  static thread_local ItemTable table;
+  if (fwd_pair_schedule(s, nsb_max, G, table))
+    kt<<<2 * G, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k64, m.v, p, (int)n_items, nsb_max,
+                                                    table);
+  else
+    ks<<<2 * G, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k64, m.v, p, (int)n_items, nsb_max,
+                                                    FwdSerpentine{});
+  return cudaGetLastError();
+}
+
 template <int D, bool BF16>
 static cudaError_t launch_fwd_t(const Maps& m, const Shape& s, void* o, float* lse,
                                 cudaStream_t st) {
@@ -94,6 +192,11 @@ static cudaError_t launch_fwd_t(const Maps& m, const Shape& s, void* o, float* l
   // Packed batches: s.N is the longest query sequence; blocks past a sequence's end are
   // skipped.
   const int nqb_max = (s.N + 2 * kTileM - 1) / (2 * kTileM);
+  if constexpr (D == 128) {
+    if (use_pair_fwd(s))
+      return s.vl.cu_q != nullptr ? launch_fwd_pair<BF16, true>(m, s, p, st)
+                                  : launch_fwd_pair<BF16, false>(m, s, p, st);
+  }
   if (use_persistent_fwd(s)) {
     using CP = FwdPCfg<D>;
     const long long n_items = (long long)nqb_max * s.BH;

@@ -12,6 +12,9 @@ namespace attn {
 // TMA descriptors of the [B*H, N, d] 16-bit tensors a kernel reads.
 struct Maps {
   CUtensorMap q, k, v, d_o;
+  // k read in [64-column x 64-row] boxes: the key halves of the CTA-pair forward (encoded
+  // by the forward entry points for the 128-column kernels)
+  CUtensorMap k64;
 };
 
 struct Shape {

@@ -13,6 +13,11 @@ namespace attn {
 
 // Status-word code of a kernel that found a malformed sequence in cu_seqlens.
 constexpr int kStatusBadSeqlens = 0x7E;
+// Status codes of a kernel that found its launch unusable and did nothing: the two
+// tensor-memory allocations of a CTA pair at different addresses; dynamic shared memory
+// not 1024-byte aligned.
+constexpr int kStatusPairTmem = 0x7D;
+constexpr int kStatusSmemAlign = 0x7F;
 
 struct Varlen {
   const int* cu_q;  // [B + 1] cumulative query lengths in device memory; null = dense

@@ -51,6 +51,15 @@
  *            caller's next synchronisation. Every pipeline wait inside the kernels
  *            is bounded; a wait that runs out records ATTN_ERR_TIMEOUT in the
  *            status word read by attn_last_kernel_status().
+ *   Environment (read once per process; every setting gives the same bits)
+ *            ATTN_WAIT_LIMIT_CYCLES  SM cycles one pipeline wait may take (default
+ *                                    2^31, about a second).
+ *            ATTN_FWD_PERSISTENT, ATTN_BWD_PERSISTENT = 0 / 1  force the one-CTA-per-item
+ *                                    or the persistent kernels (default: by shape).
+ *            ATTN_FWD_PAIR = 1       run the 128-column forward on CTA pairs (two SMs
+ *                                    sharing each K/V block through tcgen05 MMAs with
+ *                                    cta_group::2); off by default, since on the
+ *                                    measured shapes it is slower.
  */
 #ifndef ATTN_H
 #define ATTN_H

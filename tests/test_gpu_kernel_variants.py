@@ -2,7 +2,8 @@
 
 The forward, dK/dV and dQ kernels each exist as a persistent kernel (one CTA per SM walking
 many work items) and as one CTA per item; which one runs depends on the shape, and
-ATTN_FWD_PERSISTENT / ATTN_BWD_PERSISTENT = 0 / 1 force either. Both compute every tile in
+ATTN_FWD_PERSISTENT / ATTN_BWD_PERSISTENT = 0 / 1 force either. The 128-column forward also
+exists on CTA pairs (ATTN_FWD_PAIR = 1). Both compute every tile in
 the same order with the same rounding, so O, LSE, dQ, dK and dV must agree bit for bit.
 Each setting runs in a child process of its own (the variables are read once per process)
 on the same seeded inputs.
@@ -63,10 +64,10 @@ torch.save(out, sys.argv[2])
 """
 
 
-def _run(tmp_path, persistent):
-    path = str(tmp_path / f"run_{persistent}.pt")
+def _run(tmp_path, persistent, pair=0):
+    path = str(tmp_path / f"run_{persistent}_{pair}.pt")
     env = dict(os.environ, ATTN_FWD_PERSISTENT=str(persistent),
-               ATTN_BWD_PERSISTENT=str(persistent))
+               ATTN_BWD_PERSISTENT=str(persistent), ATTN_FWD_PAIR=str(pair))
     subprocess.run([sys.executable, "-c", CHILD, ROOT, path], env=env, check=True,
                    timeout=600)
     return torch.load(path)
@@ -75,6 +76,20 @@ def _run(tmp_path, persistent):
 def test_persistent_and_one_item_kernels_agree_bit_for_bit(tmp_path):
     a = _run(tmp_path, 1)
     b = _run(tmp_path, 0)
+    assert a.keys() == b.keys()
+    for name in a:
+        for what, x, y in zip(("O", "LSE", "dQ", "dK", "dV"), a[name], b[name]):
+            assert torch.equal(x, y), f"{name}: {what} differs"
+
+
+def test_cta_pair_forward_agrees_bit_for_bit(tmp_path):
+    """ATTN_FWD_PAIR = 1: the 128-column forward runs on CTA pairs (csrc/fwd_pair.cuh),
+    tcgen05 MMAs with .cta_group::2 over two SMs. Each S and P V element is computed from
+    the same operands in the same order as in the one-CTA kernel, so every output of the
+    cases above (dense d = 128 causal and full, ragged, more items than clusters, a packed
+    batch) must be the same bits; the d = 64 cases run the same kernels in both."""
+    a = _run(tmp_path, 1, pair=1)
+    b = _run(tmp_path, 1, pair=0)
     assert a.keys() == b.keys()
     for name in a:
         for what, x, y in zip(("O", "LSE", "dQ", "dK", "dV"), a[name], b[name]):

@@ -52,8 +52,11 @@ SITE_RANGE = {"fwd": (0x11, 0x1F), "dq": (0x21, 0x2F), "dkv": (0x31, 0x3F),
               "decode": (0x41, 0x4F)}
 
 
-def test_waits_that_run_out_are_reported_and_the_context_survives():
-    env = dict(os.environ, ATTN_WAIT_LIMIT_CYCLES="64")
+@pytest.mark.parametrize("pair", ["0", "1"], ids=["one_cta_forward", "cta_pair_forward"])
+def test_waits_that_run_out_are_reported_and_the_context_survives(pair):
+    # pair = "1": the forward runs on CTA pairs, whose abort path also drains the pair's
+    # MMAs on both CTAs and ends with the bounded exit handshake
+    env = dict(os.environ, ATTN_WAIT_LIMIT_CYCLES="64", ATTN_FWD_PAIR=pair)
     r = subprocess.run([sys.executable, "-c", CHILD], env=env, cwd=ROOT, capture_output=True,
                        text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
