@@ -194,6 +194,8 @@ attn_status attn_fwd_qk(const void* q, const void* k, const void* v, void* o, fl
   m.d_o = m.v;
   m.k64 = m.k;
   if (d > 64 && (st = encode_map(&m.k64, k, s.BH, Nk, d, s.bf16, 64)) != ATTN_OK) return st;
+  m.o = m.q;
+  if (d <= 64 && (st = encode_map(&m.o, o, s.BH, Nq, d, s.bf16, 32)) != ATTN_OK) return st;
   return from_cuda(attn::launch_fwd(m, s, o, lse, static_cast<cudaStream_t>(cuda_stream)));
 }
 
@@ -399,6 +401,7 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
   m.k64 = m.k;
   if (d > 64 && (st = encode_map_packed(&m.k64, k, H, total_k, d, s.bf16, 64)) != ATTN_OK)
     return st;
+  m.o = m.q;  // packed batches keep the row stores
   return from_cuda(attn::launch_fwd(m, s, o, lse, static_cast<cudaStream_t>(cuda_stream)));
 }
 

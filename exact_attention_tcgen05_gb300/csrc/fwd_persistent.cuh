@@ -92,16 +92,26 @@ struct FwdPCfg : FwdCfg<D> {
   // The barriers of the one-item kernel, then q_empty and o_free[2].
   static constexpr int kNumBars = B::kNumBars + 3;
   static constexpr int kOffMisc = B::kOffBar + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  // d = 64: each softmax warp stages its 32 rows of normalised O in shared memory (4 KiB,
+  // 128-byte swizzle) and writes them with one TMA store, so the epilogue's global writes
+  // run asynchronously instead of as 16-byte stores row by row (dense tensors; packed
+  // batches keep the row stores, since a tile may run past its sequence into the next one's
+  // rows).
+  static constexpr bool kStageO = (D == 64);
+  static constexpr int kOffO = ((kOffMisc + 16 + 1023) / 1024) * 1024;
+  static constexpr int kSmemBytes = (kStageO ? kOffO + 2 * B::kTileBytes : kOffMisc + 16) + 1024;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
 template <int D, bool BF16, bool PACKED, class Sched>
 __global__ void __launch_bounds__(320, 1)
     attn_fwd_persistent_kernel(const __grid_constant__ CUtensorMap map_q,
                                const __grid_constant__ CUtensorMap map_k,
-                               const __grid_constant__ CUtensorMap map_v, const FwdParams p,
+                               const __grid_constant__ CUtensorMap map_v,
+                               const __grid_constant__ CUtensorMap map_o, const FwdParams p,
                                int n_items, int nqb_max, const __grid_constant__ Sched sched) {
   using C = FwdPCfg<D>;
+  constexpr bool kTmaO = C::kStageO && !PACKED;
   constexpr int NS = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -501,7 +511,32 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before();
       warp_arrive(&o_free[t]);
       tb += nkv;
-      if (row < it.N) {
+      if constexpr (kTmaO) {
+        // Each warp stages its 32 rows of O / l in a 4 KiB buffer of its own (128-byte
+        // swizzle) and its lane 0 stores them with one TMA copy: no barrier beyond the warp.
+        // The buffer's previous store must have read it first.
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+        const float inv_l = 1.f / lr;
+        uint8_t* buf = smem + C::kOffO + (t * 4 + wq) * 4096;
+        const uint32_t rbase = smem_u32(buf) + lane * 128;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            w4[i] = pack2<BF16>(__uint_as_float(r[8 * v + 2 * i]) * inv_l,
+                                __uint_as_float(r[8 * v + 2 * i + 1]) * inv_l);
+          st_shared_v4(rbase + ((v ^ (lane & 7)) << 4), w4[0], w4[1], w4[2], w4[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&map_o, buf, 0, tile_row0 + wq * 32, it.sl.tma_bh);
+          bulk_commit_group();
+        }
+        if (row < it.N) p.lse[it.sl.stat0 + row] = (m + log2f(l)) * kLn2;
+      } else if (row < it.N) {
         const float inv_l = 1.f / lr;
         uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
                         (it.sl.q_elem0 + (size_t)row * it.sl.row_elems) * 2;
@@ -522,6 +557,9 @@ __global__ void __launch_bounds__(320, 1)
         p.lse[it.sl.stat0 + row] = (m + log2f(l)) * kLn2;
       }
     }
+    // the warp's last store must have finished with its buffer before shared memory is
+    // released
+    if (kTmaO && lane == 0) bulk_wait_all();
     tc_fence_before();
   }
 

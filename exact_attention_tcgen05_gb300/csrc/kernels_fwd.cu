@@ -207,16 +207,16 @@ static cudaError_t launch_fwd_t(const Maps& m, const Shape& s, void* o, float* l
                                      : attn_fwd_persistent_kernel<D, BF16, false, ItemTable>;
       e = cudaFuncSetAttribute(kt, cudaFuncAttributeMaxDynamicSharedMemorySize, CP::kSmemBytes);
       if (e != cudaSuccess) return e;
-      kt<<<grid, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, p, (int)n_items, nqb_max,
-                                                     table);
+      kt<<<grid, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, m.o, p, (int)n_items,
+                                                     nqb_max, table);
       return cudaGetLastError();
     }
     auto kp = s.vl.cu_q != nullptr ? attn_fwd_persistent_kernel<D, BF16, true, FwdSerpentine>
                                    : attn_fwd_persistent_kernel<D, BF16, false, FwdSerpentine>;
     e = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, CP::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kp<<<grid, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, p, (int)n_items, nqb_max,
-                                                   FwdSerpentine{});
+    kp<<<grid, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, m.o, p, (int)n_items,
+                                                   nqb_max, FwdSerpentine{});
     return cudaGetLastError();
   }
   dim3 grid(nqb_max, s.BH);

@@ -15,6 +15,9 @@ struct Maps {
   // k read in [64-column x 64-row] boxes: the key halves of the CTA-pair forward (encoded
   // by the forward entry points for the 128-column kernels)
   CUtensorMap k64;
+  // o written in [64-column x 32-row] boxes: the persistent forward's staged epilogue at
+  // d <= 64 (encoded by the dense forward entry point)
+  CUtensorMap o;
 };
 
 struct Shape {
