@@ -248,6 +248,16 @@ attn_status encode_bwd_maps(Maps* m, const void* q, const void* k, const void* v
   return encode_map(&m->d_o, dO, s.BH, s.N, s.d, s.bf16);
 }
 
+// The dK/dV outputs as TMA store targets (dense, d <= 64: the persistent kernel's staged
+// epilogue); otherwise unused and left as copies of the input maps.
+attn_status encode_dkv_out_maps(Maps* m, void* dk, void* dv, const Shape& s) {
+  m->dk = m->dv = m->k;
+  if (s.vl.cu_q != nullptr || s.d > 64) return ATTN_OK;
+  attn_status st = encode_map(&m->dk, dk, s.BH, s.Nk, s.d, s.bf16, 32);
+  if (st == ATTN_OK) st = encode_map(&m->dv, dv, s.BH, s.Nk, s.d, s.bf16, 32);
+  return st;
+}
+
 }  // namespace
 
 attn_status attn_bwd_dkv(const void* q, const void* k, const void* v, const float* lse,
@@ -266,6 +276,7 @@ attn_status attn_bwd_dkv(const void* q, const void* k, const void* v, const floa
   const Shape s = make_shape(B, H, N, d, dtype, causal, scale);
   Maps m;
   if ((st = encode_bwd_maps(&m, q, k, v, dO, s)) != ATTN_OK) return st;
+  if ((st = encode_dkv_out_maps(&m, dk, dv, s)) != ATTN_OK) return st;
   return from_cuda(attn::launch_dkv(m, s, q, k, v, dO, lse, delta, dk, dv,
                                     static_cast<cudaStream_t>(cuda_stream)));
 }
@@ -310,6 +321,7 @@ attn_status attn_bwd_qk(const void* q, const void* k, const void* v, const void*
   const Shape s = make_shape(B, H, Nq, d, dtype, causal, scale, Nk);
   Maps m;
   if ((st = encode_bwd_maps(&m, q, k, v, dO, s)) != ATTN_OK) return st;
+  if ((st = encode_dkv_out_maps(&m, dk, dv, s)) != ATTN_OK) return st;
   cudaStream_t cs = static_cast<cudaStream_t>(cuda_stream);
   float* delta = static_cast<float*>(workspace);
   cudaError_t e = attn::launch_delta(s, o, dO, delta, cs);
@@ -437,6 +449,7 @@ attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const v
   if ((st = encode_map_packed(&m.k, k, H, total_k, d, s.bf16)) != ATTN_OK) return st;
   if ((st = encode_map_packed(&m.v, v, H, total_k, d, s.bf16)) != ATTN_OK) return st;
   if ((st = encode_map_packed(&m.d_o, dO, H, total_q, d, s.bf16)) != ATTN_OK) return st;
+  if ((st = encode_dkv_out_maps(&m, dk, dv, s)) != ATTN_OK) return st;  // unused: packed
   cudaStream_t cs = static_cast<cudaStream_t>(cuda_stream);
   float* delta = static_cast<float*>(workspace);
   cudaError_t e = attn::launch_delta(s, o, dO, delta, cs);

@@ -68,14 +68,21 @@ struct DkvPCfg : DkvCfg<D> {
   // ds_full, acc_done, drain, stats_ready[2], kv_free, acc_free
   static constexpr int kNumBars = 1 + 2 * kQStages + 2 * kDOStages + 8 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  // d = 64: each elementwise warp stages its 32 rows of dV or dK in shared memory (4 KiB,
+  // 128-byte swizzle) and writes them with one TMA store, instead of 16-byte stores row by
+  // row (dense tensors; packed batches keep the row stores, since a key block may run past
+  // its sequence into the next one's rows).
+  static constexpr bool kStageOut = (D == 64);
+  static constexpr int kOffOut = ((kOffMisc + 16 + 1023) / 1024) * 1024;
+  static constexpr int kEnd = kStageOut ? kOffOut + 8 * 4096 : kOffMisc + 16;
   // 1024 bytes of slack to align the dynamic shared memory's base, where they fit in the
   // 227 KiB a CTA may take; otherwise none, and the kernel checks that the base is aligned
   // (it is on GB300: no static shared memory comes before it).
   static constexpr int kLimit = 227 * 1024;
-  static constexpr int kSlack = (kOffMisc + 16 + 1024 <= kLimit) ? 1024 : 0;
-  static constexpr int kSmemBytes =
-      (kOffMisc + 16 + kSlack) > B::kMinSmem ? (kOffMisc + 16 + kSlack) : B::kMinSmem;
+  static constexpr int kSlack = (kEnd + 1024 <= kLimit) ? 1024 : 0;
+  static constexpr int kSmemBytes = (kEnd + kSlack) > B::kMinSmem ? (kEnd + kSlack) : B::kMinSmem;
   static_assert(kSmemBytes <= kLimit, "shared memory");
+  static_assert(!kStageOut || kSlack == 1024, "the staging buffers need an aligned base");
 };
 
 template <int D, bool BF16, bool PACKED, class Sched>
@@ -84,9 +91,12 @@ __global__ void __launch_bounds__(320, 1)
                                    const __grid_constant__ CUtensorMap map_k,
                                    const __grid_constant__ CUtensorMap map_v,
                                    const __grid_constant__ CUtensorMap map_do,
+                                   const __grid_constant__ CUtensorMap map_dk,
+                                   const __grid_constant__ CUtensorMap map_dv,
                                    const BwdParams p, int n_pairs, int npairs, int nkb_max,
                                    const __grid_constant__ Sched sched) {
   using C = DkvPCfg<D>;
+  constexpr bool kTmaOut = C::kStageOut && !PACKED;
   constexpr int QS = C::kQStages, DS = C::kDOStages;
   // Rings of different depths release their slots separately (dO after the block's dV
   // product, Q after its dK product); at equal depths one release per block covers both
@@ -494,20 +504,55 @@ __global__ void __launch_bounds__(320, 1)
       // for the next item's first products (acc_free).
       if (!(ok = warp_wait(acc_done, items & 1, limit, abort_flag, kWaitDkvDone))) break;
       tc_fence_after();
-      uint8_t* dst = reinterpret_cast<uint8_t*>(g == 0 ? p.out1 : p.out0) +
-                     (it.sl.k_elem0 + (size_t)key * it.sl.row_elems) * 2;
       const uint32_t t_acc = tmem + lane_base + (g == 0 ? C::kColAcc0 : C::kColAcc1);
       const float mul = (g == 0) ? 1.f : p.scale;
+      if constexpr (kTmaOut) {
+        // All of the row into registers, the accumulators released at once (the next
+        // item's first products may overwrite them), then the row staged in this warp's
+        // buffer and the warp's 32 rows stored by one TMA copy once the buffer's previous
+        // store has read it.
+        uint32_t a[D];
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t a[32];
-        tmem_ld32(t_acc + cc * 32, a);
-        if (key < it.Nk) store_row32<BF16>(dst + cc * 64, a, mul, valid16(p.dh, cc * 32, 4));
+        for (int cc = 0; cc < D / 32; ++cc)
+          tmem_ld32(t_acc + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&a[cc * 32]));
+        tc_fence_before();
+        warp_arrive(acc_free);
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+        uint8_t* buf = smem + C::kOffOut + warp * 4096;
+        const uint32_t rbase = smem_u32(buf) + lane * 128;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            w4[i] = pack2<BF16>(__uint_as_float(a[8 * v + 2 * i]) * mul,
+                                __uint_as_float(a[8 * v + 2 * i + 1]) * mul);
+          st_shared_v4(rbase + ((v ^ (lane & 7)) << 4), w4[0], w4[1], w4[2], w4[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(g == 0 ? &map_dv : &map_dk, buf, 0, it.j0 + wq * 32, it.sl.tma_bh);
+          bulk_commit_group();
+        }
+      } else {
+        uint8_t* dst = reinterpret_cast<uint8_t*>(g == 0 ? p.out1 : p.out0) +
+                       (it.sl.k_elem0 + (size_t)key * it.sl.row_elems) * 2;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t a[32];
+          tmem_ld32(t_acc + cc * 32, a);
+          if (key < it.Nk) store_row32<BF16>(dst + cc * 64, a, mul, valid16(p.dh, cc * 32, 4));
+        }
+        tc_fence_before();
+        warp_arrive(acc_free);
       }
-      tc_fence_before();
-      warp_arrive(acc_free);
       ++items;
     }
+    // the warp's last store must have finished with its buffer before shared memory is
+    // released
+    if (kTmaOut && lane == 0) bulk_wait_all();
     tc_fence_before();
   }
 

@@ -115,8 +115,8 @@ static cudaError_t launch_dkv_t(const Maps& m, const Shape& s, const void* q, co
                                      : attn_bwd_dkv_persistent_kernel<D, BF16, false, ItemTable>;
       e = cudaFuncSetAttribute(kt, cudaFuncAttributeMaxDynamicSharedMemorySize, CP::kSmemBytes);
       if (e != cudaSuccess) return e;
-      kt<<<gt, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, m.d_o, p, (int)n_pairs,
-                                                   npairs, nkb_max, table);
+      kt<<<gt, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, m.d_o, m.dk, m.dv, p,
+                                                   (int)n_pairs, npairs, nkb_max, table);
       return cudaGetLastError();
     }
     auto kp = s.vl.cu_q != nullptr
@@ -125,8 +125,8 @@ static cudaError_t launch_dkv_t(const Maps& m, const Shape& s, const void* q, co
     e = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, CP::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = (int)std::min<long long>(n_pairs, sm_count_dkv());
-    kp<<<grid, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, m.d_o, p, (int)n_pairs,
-                                                   npairs, nkb_max, PairSchedule{});
+    kp<<<grid, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, m.d_o, m.dk, m.dv, p,
+                                                   (int)n_pairs, npairs, nkb_max, PairSchedule{});
     return cudaGetLastError();
   }
   // One CTA per 128-key block.

@@ -18,6 +18,9 @@ struct Maps {
   // o written in [64-column x 32-row] boxes: the persistent forward's staged epilogue at
   // d <= 64 (encoded by the dense forward entry point)
   CUtensorMap o;
+  // dk, dv written in [64-column x 32-row] boxes: the persistent dK/dV kernel's staged
+  // epilogue at d <= 64 (encoded by the dense backward entry points)
+  CUtensorMap dk, dv;
 };
 
 struct Shape {
