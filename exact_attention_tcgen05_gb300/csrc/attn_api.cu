@@ -90,14 +90,16 @@ EncodeFn get_encode() {
 // CUDA_ERROR_INVALID_CONTEXT. The thread is then bound to its current device's primary
 // context (what the runtime's own calls would do) and the encoding retried once.
 attn_status encode_3d(CUtensorMap* m, const void* base, bool bf16, const cuuint64_t (&dims)[3],
-                      const cuuint64_t (&strides)[2], const cuuint32_t (&box)[3]) {
+                      const cuuint64_t (&strides)[2], const cuuint32_t (&box)[3],
+                      bool swizzle = true) {
   EncodeFn enc = get_encode();
   if (enc == nullptr) return ATTN_ERR_CUDA;
   const cuuint32_t estr[3] = {1, 1, 1};
   auto encode = [&] {
     return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE,
+               swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   };
   CUresult r = encode();
@@ -116,6 +118,16 @@ attn_status encode_map(CUtensorMap* m, const void* base, int BH, int N, int d, b
   const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * (cuuint64_t)d * 2};
   const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   return encode_3d(m, base, bf16, dims, strides, box);
+}
+
+// [BH, N, d] 16-bit tensor as a TMA store target in unswizzled [32-column x 32-row] boxes
+// (64-byte rows in shared memory).
+attn_status encode_map_half_rows(CUtensorMap* m, const void* base, int BH, int N, int d,
+                                 bool bf16) {
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * (cuuint64_t)d * 2};
+  const cuuint32_t box[3] = {32, 32, 1};
+  return encode_3d(m, base, bf16, dims, strides, box, false);
 }
 
 // [total, H, d] packed 16-bit tensor, read as [64-column x 1-head x 128-token] boxes with
@@ -248,6 +260,14 @@ attn_status encode_bwd_maps(Maps* m, const void* q, const void* k, const void* v
   return encode_map(&m->d_o, dO, s.BH, s.N, s.d, s.bf16);
 }
 
+// The dQ output as a TMA store target (dense, d <= 64: the persistent kernel's staged
+// epilogue); otherwise unused and left as a copy of the q map.
+attn_status encode_dq_out_map(Maps* m, void* dq, const Shape& s) {
+  m->dq = m->q;
+  if (s.vl.cu_q != nullptr || s.d > 64) return ATTN_OK;
+  return encode_map_half_rows(&m->dq, dq, s.BH, s.N, s.d, s.bf16);
+}
+
 // The dK/dV outputs as TMA store targets (dense, d <= 64: the persistent kernel's staged
 // epilogue); otherwise unused and left as copies of the input maps.
 attn_status encode_dkv_out_maps(Maps* m, void* dk, void* dv, const Shape& s) {
@@ -296,6 +316,7 @@ attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const float
   const Shape s = make_shape(B, H, N, d, dtype, causal, scale);
   Maps m;
   if ((st = encode_bwd_maps(&m, q, k, v, dO, s)) != ATTN_OK) return st;
+  if ((st = encode_dq_out_map(&m, dq, s)) != ATTN_OK) return st;
   return from_cuda(
       attn::launch_dq(m, s, q, dO, lse, delta, dq, static_cast<cudaStream_t>(cuda_stream)));
 }
@@ -322,6 +343,7 @@ attn_status attn_bwd_qk(const void* q, const void* k, const void* v, const void*
   Maps m;
   if ((st = encode_bwd_maps(&m, q, k, v, dO, s)) != ATTN_OK) return st;
   if ((st = encode_dkv_out_maps(&m, dk, dv, s)) != ATTN_OK) return st;
+  if ((st = encode_dq_out_map(&m, dq, s)) != ATTN_OK) return st;
   cudaStream_t cs = static_cast<cudaStream_t>(cuda_stream);
   float* delta = static_cast<float*>(workspace);
   cudaError_t e = attn::launch_delta(s, o, dO, delta, cs);
@@ -450,6 +472,7 @@ attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const v
   if ((st = encode_map_packed(&m.v, v, H, total_k, d, s.bf16)) != ATTN_OK) return st;
   if ((st = encode_map_packed(&m.d_o, dO, H, total_q, d, s.bf16)) != ATTN_OK) return st;
   if ((st = encode_dkv_out_maps(&m, dk, dv, s)) != ATTN_OK) return st;  // unused: packed
+  if ((st = encode_dq_out_map(&m, dq, s)) != ATTN_OK) return st;        // unused: packed
   cudaStream_t cs = static_cast<cudaStream_t>(cuda_stream);
   float* delta = static_cast<float*>(workspace);
   cudaError_t e = attn::launch_delta(s, o, dO, delta, cs);

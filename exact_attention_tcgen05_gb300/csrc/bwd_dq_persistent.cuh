@@ -95,8 +95,14 @@ struct DqPCfg : DqCfg<D> {
   static constexpr bool kStageRows = D == 64;
   static constexpr int kOffStage = (kOffMisc + 16 + 127) / 128 * 128;
   static constexpr int kStageBytes = kStageRows ? 256 * (D * 2 + 8) : 0;
-  static constexpr int kEnd = kOffStage + kStageBytes + 1024;
+  // d = 64: each elementwise warp stages its 32 rows x 32 columns of dQ (64-byte rows,
+  // unswizzled, 2 KiB) and writes them with one TMA store, instead of 16-byte stores row
+  // by row (dense tensors; packed batches keep the row stores).
+  static constexpr bool kStageOut = D == 64;
+  static constexpr int kOffOut = (kOffStage + kStageBytes + 1023) / 1024 * 1024;
+  static constexpr int kEnd = (kStageOut ? kOffOut + 8 * 2048 : kOffStage + kStageBytes) + 1024;
   static constexpr int kSmemBytes = kEnd > B::kMinSmem ? kEnd : B::kMinSmem;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
 // A D-element 16-bit row from global memory into registers as packed pairs (zeros when
@@ -127,10 +133,12 @@ __global__ void __launch_bounds__(320, 1)
     attn_bwd_dq_persistent_kernel(const __grid_constant__ CUtensorMap map_q,
                                   const __grid_constant__ CUtensorMap map_k,
                                   const __grid_constant__ CUtensorMap map_v,
-                                  const __grid_constant__ CUtensorMap map_do, const BwdParams p,
+                                  const __grid_constant__ CUtensorMap map_do,
+                                  const __grid_constant__ CUtensorMap map_dq, const BwdParams p,
                                   int n_pairs, int npairs, int nb_max,
                                   const __grid_constant__ Sched sched) {
   using C = DqPCfg<D>;
+  constexpr bool kTmaOut = C::kStageOut && !PACKED;
   constexpr int NS = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -500,7 +508,32 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld32(t_acc + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&a[cc * 32]));
       tc_fence_before();
       warp_arrive(acc_free);
-      if (row < cur.N) {
+      if constexpr (kTmaOut) {
+        // The warp's 32 rows x 32 columns staged in its 2 KiB buffer (64-byte rows, no
+        // swizzle) and stored by one TMA copy once the buffer's previous store has read it.
+        // A group whose columns all lie past the head dimension has nothing to store.
+        if (g * (D / 2) < p.dh) {
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+          uint8_t* buf = smem + C::kOffOut + warp * 2048;
+          const uint32_t rbase = smem_u32(buf) + lane * 64;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              w4[i] = pack2<BF16>(__uint_as_float(a[8 * v + 2 * i]) * p.scale,
+                                  __uint_as_float(a[8 * v + 2 * i + 1]) * p.scale);
+            st_shared_v4(rbase + v * 16, w4[0], w4[1], w4[2], w4[3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&map_dq, buf, g * (D / 2), cur.i0 + wq * 32, cur.sl.tma_bh);
+            bulk_commit_group();
+          }
+        }
+      } else if (row < cur.N) {
         uint8_t* drow = reinterpret_cast<uint8_t*>(p.out0) +
                         (cur.sl.q_elem0 + (size_t)row * cur.sl.row_elems) * 2 + g * D;
 #pragma unroll
@@ -515,6 +548,9 @@ __global__ void __launch_bounds__(320, 1)
       dlt = dl_next;
     }
     if constexpr (C::kStageRows) cp_async_wait_all();  // no copy in flight at exit
+    // the warp's last store must have finished with its buffer before shared memory is
+    // released
+    if (kTmaOut && lane == 0) bulk_wait_all();
     tc_fence_before();
   }
 

@@ -121,7 +121,7 @@ static cudaError_t launch_dq_t(const Maps& m, const Shape& s, const void* q,
                                      : attn_bwd_dq_persistent_kernel<D, BF16, false, ItemTable>;
       e = cudaFuncSetAttribute(kt, cudaFuncAttributeMaxDynamicSharedMemorySize, CP::kSmemBytes);
       if (e != cudaSuccess) return e;
-      kt<<<gt, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, m.d_o, p, (int)n_pairs,
+      kt<<<gt, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, m.d_o, m.dq, p, (int)n_pairs,
                                                    npairs, nb_max, table);
       return cudaGetLastError();
     }
@@ -130,7 +130,7 @@ static cudaError_t launch_dq_t(const Maps& m, const Shape& s, const void* q,
     e = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, CP::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = (int)std::min<long long>(n_pairs, sm_count_dq());
-    kp<<<grid, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, m.d_o, p, (int)n_pairs,
+    kp<<<grid, CP::kThreads, CP::kSmemBytes, st>>>(m.q, m.k, m.v, m.d_o, m.dq, p, (int)n_pairs,
                                                    npairs, nb_max, PairSchedule{});
     return cudaGetLastError();
   }

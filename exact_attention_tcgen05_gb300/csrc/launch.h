@@ -21,6 +21,9 @@ struct Maps {
   // dk, dv written in [64-column x 32-row] boxes: the persistent dK/dV kernel's staged
   // epilogue at d <= 64 (encoded by the dense backward entry points)
   CUtensorMap dk, dv;
+  // dq written in unswizzled [32-column x 32-row] boxes: the persistent dQ kernel's staged
+  // epilogue at d <= 64 (encoded by the dense backward entry points)
+  CUtensorMap dq;
 };
 
 struct Shape {
