@@ -271,6 +271,16 @@ print(json.dumps({{"slices": done, "seconds": t_total}}))
                       f"{r['seconds']:.1f} s"}
 
 
+def workload_of(args):
+    """The workload named by --workload, or the shape given by --custom (smaller cases for
+    profiling: "B,H,N,d,dtype,causal|full", inputs drawn by the same generator)."""
+    from exact_attention_tcgen05_gb300 import inputs as I
+    if not args.custom:
+        return I.BY_NAME[args.workload]
+    B, H, N, d, dt, mask = args.custom.split(",")
+    return I.custom(int(B), int(H), int(N), int(d), dt, mask == "causal", seed=1002)
+
+
 def config_of(w, world: int) -> dict:
     """The `config` object of the JSON line (both arms print the same one)."""
     f = flops(w, "fwd") + flops(w, "bwd")
@@ -353,7 +363,7 @@ def run_ours(args) -> None:
     from exact_attention_tcgen05_gb300 import inputs as I
 
     rank, world, local = dist_setup()
-    w = I.BY_NAME[args.workload]
+    w = workload_of(args)
     w = replica_workload(w, rank)  # each rank: its own replica (weak scaling)
     binding.load()
     host = {t: I.make_tensor(w, t).pin_memory() for t in ("q", "k", "v", "do")}
@@ -698,7 +708,7 @@ def run_reference(args) -> None:
         return
     from exact_attention_tcgen05_gb300 import inputs as I
     import oracle.attention as OA
-    w = I.BY_NAME[args.workload]
+    w = workload_of(args)
     slices = I.sampled_slices(w, min(w.BH, args.steps + args.warmup))
     per_slice = (flops(w, "fwd") + flops(w, "bwd")) / w.BH
     times = []
@@ -733,6 +743,8 @@ def main() -> None:
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--custom", default=None,
+                    help="B,H,N,d,dtype,causal|full: a shape of one's own (profiling)")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

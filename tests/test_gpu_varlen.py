@@ -179,9 +179,12 @@ def test_bench_batch_sampled_against_the_oracle():
             ref = OA.attention_backward(_f64(q[q0:q1, h]), _f64(k[q0:q1, h]), _f64(v[q0:q1, h]),
                                         _f64(do[q0:q1, h]), True, w.scale)
             r = o_error(_f64(o[q0:q1, h]), ref["o"], w.torch_dtype)
-            record(f"{w.name} (sequences {b})", r)
+            r["lse_max"] = float(np.abs(lse[h, q0:q1].cpu().double().numpy() - ref["lse"]).max())
+            for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+                r[name] = rel_fro(_f64(got[q0:q1, h]), ref[name])
+            record(f"{w.name} (sequence {b})", r)
             assert r["o_excess"] <= 0, (b, h, r["o_max"])
-            assert np.abs(lse[h, q0:q1].cpu().double().numpy() - ref["lse"]).max() <= LSE_TOL
+            assert r["lse_max"] <= LSE_TOL
             for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
                 assert rel_fro(_f64(got[q0:q1, h]), ref[name]) <= GRAD_TOL, (b, h, name)
 
