@@ -44,8 +44,8 @@ struct DkvCfg : BwdCfg<D> {
       (kOffMisc + 16 + 1024) > B::kMinSmem ? (kOffMisc + 16 + 1024) : B::kMinSmem;
   // d = 64 (KV_TMEM): K_j and V_j also fit in tensor memory (d/2 columns of 16-bit pairs
   // each, after S^T, dP^T, dV and dK: 448 of 512), so S^T = K_j Q_i^T and dP^T = V_j dO_i^T
-  // run as TS products (A from tensor memory) at the full MMA rate instead of as SS
-  // products with M = N = 128, which take about twice as long. Each elementwise thread
+  // run as TS products (A from tensor memory), which read only B from shared memory
+  // (measured on GB300: B2 H32 N8192 d64 dK/dV 2.236 -> 2.049 ms). Each elementwise thread
   // copies its own key row there once, which costs start-up latency; the launcher picks
   // this form only when a key block meets enough query blocks. At d = 128 the four
   // accumulators fill all 512 columns.

@@ -2,16 +2,16 @@
 // CTAs on two SMs (a cluster of two) share every key block, and the pair's products are
 // tcgen05 MMAs with .cta_group::2 (M = 256 query rows, 128 in each CTA).
 //
-// Why (measured on GB300 with the one-CTA kernels): an MMA whose A and B both come from
-// shared memory (S = Q K^T) runs at about half the tensor core's rate when M = N = 128,
-// and a CTA needs 64 KiB of K/V per key block, which, with the softmax warps streaming
-// tensor memory, arrives at ~22 B/clk per SM. In a pair, each CTA holds half of the B
-// operand of each product - keys [64r, 64r + 64) of K_j for S, columns [64r, 64r + 64) of
-// V_j for P V (r = the CTA's rank) - so a key block costs each SM 32 KiB instead of 64, and
-// S runs as one M = 256 product whose shared-memory reads per SM are those of a full-rate
-// product. The method is that of fwd.cuh; only the distribution of the work changes (the
-// pages' Blackwell kernel, "FlashAttention·FA4·FP4", section HBM을 아낀 뒤에는 무엇이
-// 기다리는가, pairs SMs this way for its backward).
+// What the pairing changes: each CTA holds half of the B operand of each product - keys
+// [64r, 64r + 64) of K_j for S, columns [64r, 64r + 64) of V_j for P V (r = the CTA's rank)
+// - so a key block costs each SM 32 KiB of copies instead of 64, and each SM's tensor core
+// reads half as much B from shared memory per product. The method is that of fwd.cuh;
+// only the distribution of the work changes (the pages' Blackwell kernel,
+// "FlashAttention·FA4·FP4", section HBM을 아낀 뒤에는 무엇이 기다리는가, pairs SMs this way
+// for its backward). Measured on GB300 it is slower than the one-CTA forward (B4 H32 N4096
+// causal: 0.574 against 0.420 ms): the forward is bound by each tile's chain S -> softmax
+// -> P V, and the pair adds the wait for the other CTA's P to it. The launcher runs it only
+// on request (ATTN_FWD_PAIR = 1).
 //
 // Work: an item is 512 query rows (four 128-row blocks) of one (b, h) slice. Tile t
 // (t = 0, 1) of the pair is the 256 rows [q0 + 256t, q0 + 256t + 256); CTA r holds rows
