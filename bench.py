@@ -54,7 +54,7 @@ def load_peaks() -> dict:
 # clocks during the timed region
 # ------------------------------------------------------------------------------------
 class NvmlClockSampler:
-    """SM clock and clock-event reasons of one GPU polled every ~2 ms through NVML (the
+    """SM clock and clock-event reasons of one GPU polled every ~0.5 ms through NVML (the
     driver's management library, loaded with ctypes; reads only), so that even a timed
     region of a few tens of milliseconds gets a few dozen samples. start()/stop() as for
     ClockSampler; unavailable (None from create) where the library cannot be loaded."""
@@ -101,7 +101,7 @@ class NvmlClockSampler:
             ok = ok and self.reasons_fn(self.handle, ct.byref(rs)) == 0
             if ok:
                 self.samples.append((t, float(clk.value), int(rs.value)))
-            time.sleep(0.002)
+            time.sleep(0.0005)
 
     def start(self):
         self.thread.start()
@@ -116,7 +116,7 @@ class NvmlClockSampler:
                           if r & bit})
         return {"sm_mhz": statistics.median(c for _, c, _ in inside),
                 "sm_max_mhz": self.max_mhz, "samples": len(inside), "reasons": reasons,
-                "window": "NVML samples taken inside the timed region, every ~2 ms"}
+                "window": "NVML samples taken inside the timed region, every ~0.5 ms"}
 
 
 class ClockSampler:
