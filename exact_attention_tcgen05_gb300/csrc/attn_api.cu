@@ -35,15 +35,17 @@ Range range_of(const void* p, size_t bytes) {
 bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
 
 // Head dimensions the attention kernels take: multiples of 8 (16-byte rows for TMA) up to
-// 128; d <= 64 runs on the 64-column kernels, d > 64 on the 128-column ones, with the
-// columns past d read as zero.
-bool head_dim_ok(int d) { return d >= 8 && d <= 128 && d % 8 == 0; }
+// 128, and for the dense forward up to 256; d <= 64 runs on the 64-column kernels,
+// d <= 128 on the 128-column ones, d > 128 on the 256-column forward, with the columns
+// past d read as zero.
+constexpr int kMaxD = 128, kMaxDFwd = 256;
+bool head_dim_ok(int d, int max_d = kMaxD) { return d >= 8 && d <= max_d && d % 8 == 0; }
 
-attn_status check_shape(int B, int H, int N, int d, attn_dtype dtype) {
+attn_status check_shape(int B, int H, int N, int d, attn_dtype dtype, int max_d = kMaxD) {
   if (B < 1 || H < 1 || N < 1 || N > kMaxN) return ATTN_ERR_INVALID_ARG;
   if ((long long)B * H > kMaxBH) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_FP16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
-  if (!head_dim_ok(d)) return ATTN_ERR_UNSUPPORTED;
+  if (!head_dim_ok(d, max_d)) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
 }
 
@@ -181,9 +183,9 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N) {
 attn_status attn_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse,
                         int B, int H, int Nq, int Nk, int d, attn_dtype dtype, int causal,
                         float scale, void* cuda_stream) {
-  attn_status st = check_shape(B, H, Nq, d, dtype);
+  attn_status st = check_shape(B, H, Nq, d, dtype, kMaxDFwd);
   if (st != ATTN_OK) return st;
-  if ((st = check_shape(B, H, Nk, d, dtype)) != ATTN_OK) return st;
+  if ((st = check_shape(B, H, Nk, d, dtype, kMaxDFwd)) != ATTN_OK) return st;
   if (causal && Nk < Nq) return ATTN_ERR_INVALID_ARG;  // rows would see no key
   if ((st = check_scale(scale)) != ATTN_OK) return st;
   const void* ptrs[5] = {q, k, v, o, lse};
@@ -206,6 +208,8 @@ attn_status attn_fwd_qk(const void* q, const void* k, const void* v, void* o, fl
   m.d_o = m.v;
   m.k64 = m.k;
   if (d > 64 && (st = encode_map(&m.k64, k, s.BH, Nk, d, s.bf16, 64)) != ATTN_OK) return st;
+  m.v64 = m.v;
+  if (d > 128 && (st = encode_map(&m.v64, v, s.BH, Nk, d, s.bf16, 64)) != ATTN_OK) return st;
   m.o = m.q;
   if (d <= 64 && (st = encode_map(&m.o, o, s.BH, Nq, d, s.bf16, 32)) != ATTN_OK) return st;
   return from_cuda(attn::launch_fwd(m, s, o, lse, static_cast<cudaStream_t>(cuda_stream)));
@@ -435,6 +439,7 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
   m.k64 = m.k;
   if (d > 64 && (st = encode_map_packed(&m.k64, k, H, total_k, d, s.bf16, 64)) != ATTN_OK)
     return st;
+  m.v64 = m.v;  // (packed batches take d <= 128)
   m.o = m.q;  // packed batches keep the row stores
   return from_cuda(attn::launch_fwd(m, s, o, lse, static_cast<cudaStream_t>(cuda_stream)));
 }

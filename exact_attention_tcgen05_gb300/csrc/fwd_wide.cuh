@@ -1,0 +1,353 @@
+// fwd_wide.cuh - the attention forward for head dimensions above 128 (up to 256): the same
+// method as fwd.cuh (online softmax over key blocks, exp2 with the scale folded in, P
+// rounded to the input type for P V and O divided by the sum of those rounded values, the
+// conditional rescale, L = m + ln l) on a tile shape that fits a 256-column head.
+//
+// Why another shape: at d = 256 one 128-row tile needs 256 tensor-memory columns for O and
+// 128 for S, so the two-tile ping-pong of fwd.cuh (768 columns) does not fit in 512, and a
+// 128 x 256 K or V block takes 64 KiB of shared memory, so a ring of them beside a 64 KiB
+// Q tile leaves no room for a second stage. Here:
+//  * one CTA = one 128-row query tile of one (b, h) slice (grid: tiles x slices, the tiles
+//    of a head adjacent in launch order and longest first, as in fwd.cuh);
+//  * keys come in blocks of 64: S = scale Q K_j^T is a 128 x 64 product (N = 64), K_j and
+//    V_j take 32 KiB each and a two-stage ring of them 128 KiB, beside Q (64 KiB);
+//  * S is double buffered in tensor memory (2 x 64 columns) and O takes 256 columns, so
+//    S of block j + 1 runs on the tensor core while the softmax works on block j, and
+//    P V of block j (N = 256) follows as soon as P is in tensor memory (written over S as
+//    16-bit pairs, like the 128-column kernel);
+//  * warps 0-3: softmax, one query row per thread (64 scores a block); warp 4: TMA
+//    producer; warp 5: MMA issuer and tensor-memory owner.
+// Head dimensions between 136 and 248 run on the same kernel: TMA reads the columns past
+// d as zero, so every product sees exact zeros there, and only d columns are stored.
+#pragma once
+
+#include "fwd.cuh"
+
+namespace attn {
+
+struct FwdWCfg {
+  static constexpr int D = 256;
+  static constexpr int kBN = 64;                       // keys per block
+  static constexpr int kChunks = D / kBoxCols;         // 64-column boxes per row: 4
+  static constexpr int kQBytes = kChunks * kBoxBytes;  // 128 x 256 tile: 64 KiB
+  static constexpr int kKVBox = kBN * 128;             // one [64 rows x 64 cols] box: 8 KiB
+  static constexpr int kKVBytes = kChunks * kKVBox;    // 64 x 256 block: 32 KiB
+  static constexpr int kStages = 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kOffV = kOffK + kStages * kKVBytes;
+  static constexpr int kOffBar = kOffV + kStages * kKVBytes;
+  // q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_done, o_last, drain
+  static constexpr int kNumBars = 1 + 3 * kStages + 2 + 2 + 1 + 1 + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(kSmemBytes > 114 * 1024, "two CTAs could share an SM");
+  static constexpr int kThreads = 192;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS = 0;    // S buffer b at kColS + 64 b (P over its first 32)
+  static constexpr uint32_t kColO = 256;  // O: 256 columns
+};
+
+// S[128 x 64] = Q K^T over 256 columns: A = the Q tile (K-major, 16 KiB boxes), B = a K
+// block (K-major, 8 KiB boxes), 16 steps of 16 columns. Descriptors built once by the
+// caller; the start-address field is advanced by byte offset / 16.
+__device__ __forceinline__ void issue_s_wide(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < FwdWCfg::D / 16; ++kk) {
+    const uint32_t a_off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+    const uint32_t b_off = ((kk >> 2) * FwdWCfg::kKVBox + (kk & 3) * 32) >> 4;
+    mma_ss(d_tmem, a_desc + a_off, b_desc + b_off, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+template <bool BF16, bool PACKED>
+__global__ void __launch_bounds__(192, 1)
+    attn_fwd_wide_kernel(const __grid_constant__ CUtensorMap map_q,
+                         const __grid_constant__ CUtensorMap map_k64,
+                         const __grid_constant__ CUtensorMap map_v64, const FwdParams p) {
+  using C = FwdWCfg;
+  constexpr int NS = C::kStages;
+  constexpr int kBN = C::kBN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* v_full = k_full + NS;
+  uint64_t* kv_empty = v_full + NS;
+  uint64_t* s_full = kv_empty + NS;  // [2] per S buffer
+  uint64_t* p_full = s_full + 2;     // [2] per S buffer: P of the buffer's block is written
+  uint64_t* o_done = p_full + 2;     // every P V
+  // The last P V alone. When the softmax leaves its last block, two P V products can still
+  // be in flight (S(j) is issued before P V(j - 1)), so o_done's parity could name either.
+  uint64_t* o_last = o_done + 1;
+  uint64_t* drain = o_last + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+  const int bh = blockIdx.y;
+  SliceRows sl;
+  if (!slice_rows<PACKED>(p.vl, bh, p.N, p.Nk, p.dh, p.causal != 0, sl)) return;
+  const int N = sl.nq, Nk = sl.nk, off = sl.off;
+  const int nqb = (N + kTileM - 1) / kTileM;
+  if (PACKED && (int)blockIdx.x >= nqb) return;  // past this sequence's query tiles
+  const int q0 = (nqb - 1 - (int)blockIdx.x) * kTileM;  // longest first within a head
+  const int nkb = (Nk + kBN - 1) / kBN;
+  // causal: up to the block of the last key the tile's last row sees
+  const int n_kv = p.causal ? min(nkb, (q0 + kTileM - 1 + off) / kBN + 1) : nkb;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&p_full[b], 4);  // one arrival per softmax warp
+    }
+    mbar_init(o_done, 1);
+    mbar_init(o_last, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_holder, C::kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint64_t limit = p.wait_limit;
+
+  if (warp == 4) {
+    // ------------------------------ TMA producer ------------------------------
+    if (elect_one()) {
+      tma_prefetch_map(&map_q);
+      tma_prefetch_map(&map_k64);
+      tma_prefetch_map(&map_v64);
+      mbar_arrive_expect_tx(q_full, C::kQBytes);
+      for (int c = 0; c < C::kChunks; ++c)
+        tma_load_rows<PACKED>(smem + C::kOffQ + c * kBoxBytes, &map_q, q_full, c * kBoxCols, q0,
+                              sl, false);
+    }
+    __syncwarp();
+    int issued = 0;
+    for (int j = 0; j < n_kv; ++j) {
+      const int s = j % NS;
+      // Stage s held block j - NS: its S and P V products must be done (kv_empty completes
+      // once per block of the stage, after a copy issued past this wait).
+      if (j >= NS &&
+          !warp_wait(&kv_empty[s], ((j / NS) - 1) & 1, limit, abort_flag, kWaitFwdEmpty))
+        break;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(&k_full[s], C::kKVBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_rows<PACKED>(smem + C::kOffK + s * C::kKVBytes + c * C::kKVBox, &map_k64,
+                                &k_full[s], c * kBoxCols, j * kBN, sl, true);
+        mbar_arrive_expect_tx(&v_full[s], C::kKVBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_rows<PACKED>(smem + C::kOffV + s * C::kKVBytes + c * C::kKVBox, &map_v64,
+                                &v_full[s], c * kBoxCols, j * kBN, sl, true);
+      }
+      __syncwarp();
+      issued = j + 1;
+    }
+    if (*abort_flag) {
+      // Let every copy this CTA started land before its shared memory is released.
+      mbar_wait(q_full, 0, kDrainLimit, nullptr, kWaitFwdDrain);
+      for (int j = max(0, issued - NS); j < issued; ++j) {
+        mbar_wait(&k_full[j % NS], (j / NS) & 1, kDrainLimit, nullptr, kWaitFwdDrain);
+        mbar_wait(&v_full[j % NS], (j / NS) & 1, kDrainLimit, nullptr, kWaitFwdDrain);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------ MMA issuer --------------------------------
+    // Per block j: S(j + 1) into the other S buffer (its previous P was read by P V(j - 1),
+    // issued before it: the tensor core runs them in order), then P(j) V_j once the
+    // softmax has written P(j).
+    const uint32_t idesc_s = make_idesc(BF16, 128, kBN, false, false);
+    const uint32_t idesc_o = make_idesc(BF16, 128, C::D, false, true);
+    const uint64_t dq0 = make_sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
+    const uint64_t dk0 = make_sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
+    // V block: MN-major, 64-column boxes C::kKVBox apart along N, 8-row groups 1 KiB apart
+    const uint64_t dv0 = make_sdesc_sw128(smem_u32(smem + C::kOffV), C::kKVBox, 1024);
+    constexpr uint32_t kStep = C::kKVBytes >> 4;
+    auto issue_s = [&](int j) {
+      issue_s_wide(tmem + C::kColS + (j & 1) * 64, dq0, dk0 + (j % NS) * kStep, idesc_s);
+    };
+    auto issue_pv = [&](int j) {
+#pragma unroll
+      for (int kk = 0; kk < kBN / 16; ++kk)
+        mma_ts(tmem + C::kColO, tmem + C::kColS + (j & 1) * 64 + kk * 8,
+               dv0 + (j % NS) * kStep + ((kk * 2048) >> 4), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+    };
+    bool ok = warp_poll(q_full, 0, limit, abort_flag, kWaitFwdQ);
+    if (ok) ok = warp_poll(&k_full[0], 0, limit, abort_flag, kWaitFwdK);
+    if (ok) {
+      tc_fence_after();
+      if (elect_one()) {
+        issue_s(0);
+        mma_commit(&s_full[0]);
+      }
+      __syncwarp();
+    }
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const int jn = j + 1;
+      if (jn < n_kv) {
+        if (!(ok = warp_poll(&k_full[jn % NS], (jn / NS) & 1, limit, abort_flag, kWaitFwdK)))
+          break;
+        tc_fence_after();
+        if (elect_one()) {
+          issue_s(jn);
+          mma_commit(&s_full[jn & 1]);
+        }
+        __syncwarp();
+      }
+      if (!(ok = warp_poll(&v_full[j % NS], (j / NS) & 1, limit, abort_flag, kWaitFwdV))) break;
+      if (!(ok = warp_poll(&p_full[j & 1], (j >> 1) & 1, limit, abort_flag, kWaitFwdP))) break;
+      tc_fence_after();
+      if (elect_one()) {
+        issue_pv(j);
+        mma_commit(o_done);
+        mma_commit(&kv_empty[j % NS]);
+        if (j == n_kv - 1) mma_commit(o_last);
+      }
+      __syncwarp();
+    }
+    // Every MMA issued must finish before tensor memory is released.
+    if (elect_one()) mma_commit(drain);
+    __syncwarp();
+    mbar_wait(drain, 0, kDrainLimit, nullptr, kWaitFwdDrain);
+  } else {
+    // ------------------------------ softmax -----------------------------------
+    const int wq = warp;  // rows [32 wq, 32 wq + 32) of the tile: its tensor-memory lanes
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t t_o = tmem + lane_base + C::kColO;
+    const int row = q0 + wq * 32 + lane;  // query index of this thread
+    const float sl2 = p.scale_log2;
+    float m = -INFINITY;  // running max of scale*log2(e)*S (possibly stale by <= 8)
+    float l = 0.f;        // sum of exp2 values (fp32): defines L
+    float lr = 0.f;       // sum of the same values rounded to 16 bits: divides O
+    bool ok = true;
+    // O *= alpha in tensor memory, 64 columns at a time (the previous P V must be done).
+    auto rescale_o = [&](float alpha) {
+#pragma unroll 1
+      for (int cc = 0; cc < C::D / 64; ++cc) {
+        uint32_t r[64];
+        tmem_ld64(t_o + cc * 64, r);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+        tmem_st32(t_o + cc * 64, *reinterpret_cast<const uint32_t(*)[32]>(&r[0]));
+        tmem_st32(t_o + cc * 64 + 32, *reinterpret_cast<const uint32_t(*)[32]>(&r[32]));
+      }
+    };
+    for (int j = 0; j < n_kv; ++j) {
+      const uint32_t t_s = tmem + lane_base + C::kColS + (j & 1) * 64;
+      if (!(ok = warp_wait(&s_full[j & 1], (j >> 1) & 1, limit, abort_flag, kWaitFwdS))) break;
+      tc_fence_after();
+      uint32_t sr[kBN];
+      tmem_ld64(t_s, sr);
+      float* s = reinterpret_cast<float*>(sr);
+      const int kbase = j * kBN;
+      const bool diag = p.causal && (kbase + kBN - 1 > q0 + off);
+      if (diag || kbase + kBN > Nk) {
+        int lim = Nk - 1 - kbase;                           // last key in range
+        if (p.causal) lim = min(lim, row + off - kbase);    // last key this row sees
+#pragma unroll
+        for (int c = 0; c < kBN; ++c)
+          if (c > lim) s[c] = -INFINITY;
+      }
+      float mx[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) mx[u] = fmaxf(s[2 * u], s[2 * u + 1]);
+#pragma unroll
+      for (int c = 8; c < kBN; c += 8) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) mx[u] = fmax3(mx[u], s[c + 2 * u], s[c + 2 * u + 1]);
+      }
+      const float m_cand = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+      const bool need = m_cand > m + 8.0f;
+      float alpha = 1.f;
+      if (need) {
+        alpha = ex2(m - m_cand);  // 0 on the first block (m = -inf)
+        m = m_cand;
+      }
+      const float2 sl2x2 = make_float2(sl2, sl2);
+      const float2 neg_m2 = make_float2(-m, -m);
+      float2 sum[4];
+      float rsum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) sum[u] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int c2 = 0; c2 < kBN / 32; ++c2) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 x =
+              fma2(make_float2(s[c2 * 32 + 2 * i], s[c2 * 32 + 2 * i + 1]), sl2x2, neg_m2);
+          const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+          sum[i & 3] = add2(sum[i & 3], pp);
+          pk[i] = pack2<BF16>(pp.x, pp.y);
+          add_pair16<BF16>(rsum[(i & 1) * 2], rsum[(i & 1) * 2 + 1], pk[i]);
+        }
+        tmem_st16(t_s + c2 * 16, pk);  // P over the scores already read
+      }
+      const float2 sa = add2(add2(sum[0], sum[1]), add2(sum[2], sum[3]));
+      l = l * alpha + (sa.x + sa.y);
+      lr = lr * alpha + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        // Bring O to the new max once P V(j - 1) has landed. o_done is at most one phase
+        // past that product here: S(j) was committed after P V(j - 2).
+        if (!(ok = warp_wait(o_done, (j - 1) & 1, limit, abort_flag, kWaitFwdO))) break;
+        tc_fence_after();
+        rescale_o(alpha);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      warp_arrive(&p_full[j & 1]);
+    }
+    if (ok && warp_wait(o_last, 0, limit, abort_flag, kWaitFwdO)) {
+      tc_fence_after();
+      const float inv_l = 1.f / lr;
+      uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
+                      (sl.q_elem0 + (size_t)row * sl.row_elems) * 2;
+#pragma unroll 1
+      for (int cc = 0; cc < C::D / 64; ++cc) {
+        uint32_t r[64];
+        tmem_ld64(t_o + cc * 64, r);
+        if (row < N) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 128);
+          const int n16 = valid16(p.dh, cc * 64, 8);  // columns past dh are not stored
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              w4[i] = pack2<BF16>(__uint_as_float(r[8 * v + 2 * i]) * inv_l,
+                                  __uint_as_float(r[8 * v + 2 * i + 1]) * inv_l);
+            if (v < n16) dst[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
+      }
+      if (row < N) p.lse[sl.stat0 + row] = (m + log2f(l)) * kLn2;
+    }
+    tc_fence_before();
+  }
+
+  tmem_st_wait();  // no tensor-memory store in flight when memory is released
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace attn

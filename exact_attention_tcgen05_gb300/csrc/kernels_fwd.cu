@@ -6,6 +6,7 @@
 #include "fwd.cuh"
 #include "fwd_pair.cuh"
 #include "fwd_persistent.cuh"
+#include "fwd_wide.cuh"
 #include "launch.h"
 
 namespace attn {
@@ -224,7 +225,34 @@ static cudaError_t launch_fwd_t(const Maps& m, const Shape& s, void* o, float* l
   return cudaGetLastError();
 }
 
+// Head dims above 128: the 256-column forward (fwd_wide.cuh), one CTA per 128-row tile.
+template <bool BF16>
+static cudaError_t launch_fwd_wide(const Maps& m, const Shape& s, void* o, float* lse,
+                                   cudaStream_t st) {
+  using C = FwdWCfg;
+  auto kern = s.vl.cu_q != nullptr ? attn_fwd_wide_kernel<BF16, true>
+                                   : attn_fwd_wide_kernel<BF16, false>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  FwdParams p;
+  p.o = o;
+  p.lse = lse;
+  p.dh = s.d;
+  p.N = s.N;
+  p.Nk = s.Nk;
+  p.causal = s.causal ? 1 : 0;
+  p.scale_log2 = s.scale * kLog2e;
+  p.wait_limit = s.wait_limit;
+  p.vl = s.vl;
+  dim3 grid((s.N + kTileM - 1) / kTileM, s.BH);
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(m.q, m.k64, m.v64, p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_fwd(const Maps& m, const Shape& s, void* o, float* lse, cudaStream_t st) {
+  if (s.d > 128) return s.bf16 ? launch_fwd_wide<true>(m, s, o, lse, st)
+                                : launch_fwd_wide<false>(m, s, o, lse, st);
   if (s.d > 64) return s.bf16 ? launch_fwd_t<128, true>(m, s, o, lse, st)
                                 : launch_fwd_t<128, false>(m, s, o, lse, st);
   return s.bf16 ? launch_fwd_t<64, true>(m, s, o, lse, st)

@@ -12,9 +12,13 @@ namespace attn {
 // TMA descriptors of the [B*H, N, d] 16-bit tensors a kernel reads.
 struct Maps {
   CUtensorMap q, k, v, d_o;
-  // k read in [64-column x 64-row] boxes: the key halves of the CTA-pair forward (encoded
-  // by the forward entry points for the 128-column kernels)
+  // k read in [64-column x 64-row] boxes: the key halves of the CTA-pair forward, and the
+  // 64-key blocks of the forward for head dims above 128 (encoded by the forward entry
+  // points for d > 64)
   CUtensorMap k64;
+  // v read in [64-column x 64-row] boxes: the forward for head dims above 128 (encoded by
+  // the dense forward entry point for d > 128)
+  CUtensorMap v64;
   // o written in [64-column x 32-row] boxes: the persistent forward's staged epilogue at
   // d <= 64 (encoded by the dense forward entry point)
   CUtensorMap o;

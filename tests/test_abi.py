@@ -81,7 +81,7 @@ INVALID, UNSUPPORTED = 1, 2
     (dict(q=0), INVALID), (dict(o=0), INVALID), (dict(lse=L + 4), INVALID),
     (dict(k=K + 2), INVALID), (dict(B=0), INVALID), (dict(H=-1), INVALID),
     (dict(N=0), INVALID), (dict(N=(1 << 20) + 1), INVALID), (dict(B=300, H=300), INVALID),
-    (dict(d=100), UNSUPPORTED), (dict(d=256), UNSUPPORTED), (dict(d=136), UNSUPPORTED),
+    (dict(d=100), UNSUPPORTED), (dict(d=264), UNSUPPORTED), (dict(d=132), UNSUPPORTED),
     (dict(d=4), UNSUPPORTED), (dict(dt=2), INVALID),
     (dict(scale=0.0), INVALID), (dict(scale=-1.0), INVALID), (dict(scale=float("nan")), INVALID),
     (dict(scale=float("inf")), INVALID), (dict(o=Q), INVALID), (dict(o=K + 16), INVALID),
@@ -94,6 +94,7 @@ def test_fwd_rejects_bad_arguments(lib, kw, code):
 @pytest.mark.parametrize("kw,code", [
     (dict(dq=0), INVALID), (dict(ws=0), INVALID), (dict(dq=DK), INVALID), (dict(ws=Q), INVALID),
     (dict(dq=O + 32), INVALID), (dict(d=132), UNSUPPORTED), (dict(scale=0.0), INVALID),
+    (dict(d=256), UNSUPPORTED),  # head dims above 128: the forward only
     (dict(ws=WS + 8), INVALID),
 ])
 def test_bwd_rejects_bad_arguments(lib, kw, code):
