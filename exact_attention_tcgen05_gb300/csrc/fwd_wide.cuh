@@ -10,7 +10,9 @@
 //  * one CTA = one 128-row query tile of one (b, h) slice (grid: tiles x slices, the tiles
 //    of a head adjacent in launch order and longest first, as in fwd.cuh);
 //  * keys come in blocks of 64: S = scale Q K_j^T is a 128 x 64 product (N = 64), K_j and
-//    V_j take 32 KiB each and a two-stage ring of them 128 KiB, beside Q (64 KiB);
+//    V_j take 32 KiB each. K and V have rings of their own beside Q (64 KiB): three K
+//    stages, each free again once its S product is done, and two V stages, free once
+//    their P V is done, so the copies of K run two blocks ahead of those of V;
 //  * S is double buffered in tensor memory (2 x 64 columns) and O takes 256 columns, so
 //    S of block j + 1 runs on the tensor core while the softmax works on block j, and
 //    P V of block j (N = 256) follows as soon as P is in tensor memory (written over S as
@@ -32,13 +34,14 @@ struct FwdWCfg {
   static constexpr int kQBytes = kChunks * kBoxBytes;  // 128 x 256 tile: 64 KiB
   static constexpr int kKVBox = kBN * 128;             // one [64 rows x 64 cols] box: 8 KiB
   static constexpr int kKVBytes = kChunks * kKVBox;    // 64 x 256 block: 32 KiB
-  static constexpr int kStages = 2;
+  static constexpr int kKStages = 3, kVStages = 2;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBytes;
-  static constexpr int kOffV = kOffK + kStages * kKVBytes;
-  static constexpr int kOffBar = kOffV + kStages * kKVBytes;
-  // q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_done, o_last, drain
-  static constexpr int kNumBars = 1 + 3 * kStages + 2 + 2 + 1 + 1 + 1;
+  static constexpr int kOffV = kOffK + kKStages * kKVBytes;
+  static constexpr int kOffBar = kOffV + kVStages * kKVBytes;
+  // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2], p_full[2], o_done,
+  // o_last, drain
+  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 1 + 1 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -68,16 +71,17 @@ __global__ void __launch_bounds__(192, 1)
                          const __grid_constant__ CUtensorMap map_k64,
                          const __grid_constant__ CUtensorMap map_v64, const FwdParams p) {
   using C = FwdWCfg;
-  constexpr int NS = C::kStages;
+  constexpr int NK = C::kKStages, NV = C::kVStages;
   constexpr int kBN = C::kBN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
-  uint64_t* v_full = k_full + NS;
-  uint64_t* kv_empty = v_full + NS;
-  uint64_t* s_full = kv_empty + NS;  // [2] per S buffer
+  uint64_t* k_empty = k_full + NK;  // the stage's S product is done
+  uint64_t* v_full = k_empty + NK;
+  uint64_t* v_empty = v_full + NV;  // the stage's P V product is done
+  uint64_t* s_full = v_empty + NV;  // [2] per S buffer
   uint64_t* p_full = s_full + 2;     // [2] per S buffer: P of the buffer's block is written
   uint64_t* o_done = p_full + 2;     // every P V
   // The last P V alone. When the softmax leaves its last block, two P V products can still
@@ -102,10 +106,13 @@ __global__ void __launch_bounds__(192, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < NK; ++s) {
       mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < NV; ++s) {
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
@@ -139,34 +146,53 @@ __global__ void __launch_bounds__(192, 1)
                               sl, false);
     }
     __syncwarp();
-    int issued = 0;
-    for (int j = 0; j < n_kv; ++j) {
-      const int s = j % NS;
-      // Stage s held block j - NS: its S and P V products must be done (kv_empty completes
-      // once per block of the stage, after a copy issued past this wait).
-      if (j >= NS &&
-          !warp_wait(&kv_empty[s], ((j / NS) - 1) & 1, limit, abort_flag, kWaitFwdEmpty))
-        break;
+    // K(j) into stage j % NK once S(j - NK) is done; V(j) into stage j % NV once
+    // P V(j - NV) is done (each empty barrier completes once per block of its stage, after
+    // a copy issued past its wait). K runs NK - 1 blocks ahead of V.
+    int k_issued = 0, v_issued = 0;
+    auto load_k = [&](int j) -> bool {
+      const int s = j % NK;
+      if (j >= NK && !warp_wait(&k_empty[s], ((j / NK) - 1) & 1, limit, abort_flag,
+                                kWaitFwdEmpty))
+        return false;
       if (elect_one()) {
         mbar_arrive_expect_tx(&k_full[s], C::kKVBytes);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_rows<PACKED>(smem + C::kOffK + s * C::kKVBytes + c * C::kKVBox, &map_k64,
                                 &k_full[s], c * kBoxCols, j * kBN, sl, true);
+      }
+      __syncwarp();
+      k_issued = j + 1;
+      return true;
+    };
+    auto load_v = [&](int j) -> bool {
+      const int s = j % NV;
+      if (j >= NV && !warp_wait(&v_empty[s], ((j / NV) - 1) & 1, limit, abort_flag,
+                                kWaitFwdEmpty))
+        return false;
+      if (elect_one()) {
         mbar_arrive_expect_tx(&v_full[s], C::kKVBytes);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_rows<PACKED>(smem + C::kOffV + s * C::kKVBytes + c * C::kKVBox, &map_v64,
                                 &v_full[s], c * kBoxCols, j * kBN, sl, true);
       }
       __syncwarp();
-      issued = j + 1;
+      v_issued = j + 1;
+      return true;
+    };
+    bool ok = true;
+    for (int j = 0; ok && j < min(NK - 1, n_kv); ++j) ok = load_k(j);
+    for (int j = 0; ok && j < n_kv; ++j) {
+      if (j + NK - 1 < n_kv) ok = load_k(j + NK - 1);
+      if (ok) ok = load_v(j);
     }
     if (*abort_flag) {
       // Let every copy this CTA started land before its shared memory is released.
       mbar_wait(q_full, 0, kDrainLimit, nullptr, kWaitFwdDrain);
-      for (int j = max(0, issued - NS); j < issued; ++j) {
-        mbar_wait(&k_full[j % NS], (j / NS) & 1, kDrainLimit, nullptr, kWaitFwdDrain);
-        mbar_wait(&v_full[j % NS], (j / NS) & 1, kDrainLimit, nullptr, kWaitFwdDrain);
-      }
+      for (int j = max(0, k_issued - NK); j < k_issued; ++j)
+        mbar_wait(&k_full[j % NK], (j / NK) & 1, kDrainLimit, nullptr, kWaitFwdDrain);
+      for (int j = max(0, v_issued - NV); j < v_issued; ++j)
+        mbar_wait(&v_full[j % NV], (j / NV) & 1, kDrainLimit, nullptr, kWaitFwdDrain);
     }
   } else if (warp == 5) {
     // ------------------------------ MMA issuer --------------------------------
@@ -181,13 +207,13 @@ __global__ void __launch_bounds__(192, 1)
     const uint64_t dv0 = make_sdesc_sw128(smem_u32(smem + C::kOffV), C::kKVBox, 1024);
     constexpr uint32_t kStep = C::kKVBytes >> 4;
     auto issue_s = [&](int j) {
-      issue_s_wide(tmem + C::kColS + (j & 1) * 64, dq0, dk0 + (j % NS) * kStep, idesc_s);
+      issue_s_wide(tmem + C::kColS + (j & 1) * 64, dq0, dk0 + (j % NK) * kStep, idesc_s);
     };
     auto issue_pv = [&](int j) {
 #pragma unroll
       for (int kk = 0; kk < kBN / 16; ++kk)
         mma_ts(tmem + C::kColO, tmem + C::kColS + (j & 1) * 64 + kk * 8,
-               dv0 + (j % NS) * kStep + ((kk * 2048) >> 4), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+               dv0 + (j % NV) * kStep + ((kk * 2048) >> 4), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
     };
     bool ok = warp_poll(q_full, 0, limit, abort_flag, kWaitFwdQ);
     if (ok) ok = warp_poll(&k_full[0], 0, limit, abort_flag, kWaitFwdK);
@@ -196,28 +222,30 @@ __global__ void __launch_bounds__(192, 1)
       if (elect_one()) {
         issue_s(0);
         mma_commit(&s_full[0]);
+        mma_commit(&k_empty[0]);
       }
       __syncwarp();
     }
     for (int j = 0; ok && j < n_kv; ++j) {
       const int jn = j + 1;
       if (jn < n_kv) {
-        if (!(ok = warp_poll(&k_full[jn % NS], (jn / NS) & 1, limit, abort_flag, kWaitFwdK)))
+        if (!(ok = warp_poll(&k_full[jn % NK], (jn / NK) & 1, limit, abort_flag, kWaitFwdK)))
           break;
         tc_fence_after();
         if (elect_one()) {
           issue_s(jn);
           mma_commit(&s_full[jn & 1]);
+          mma_commit(&k_empty[jn % NK]);
         }
         __syncwarp();
       }
-      if (!(ok = warp_poll(&v_full[j % NS], (j / NS) & 1, limit, abort_flag, kWaitFwdV))) break;
+      if (!(ok = warp_poll(&v_full[j % NV], (j / NV) & 1, limit, abort_flag, kWaitFwdV))) break;
       if (!(ok = warp_poll(&p_full[j & 1], (j >> 1) & 1, limit, abort_flag, kWaitFwdP))) break;
       tc_fence_after();
       if (elect_one()) {
         issue_pv(j);
         mma_commit(o_done);
-        mma_commit(&kv_empty[j % NS]);
+        mma_commit(&v_empty[j % NV]);
         if (j == n_kv - 1) mma_commit(o_last);
       }
       __syncwarp();
