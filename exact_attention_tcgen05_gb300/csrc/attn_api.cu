@@ -35,10 +35,10 @@ Range range_of(const void* p, size_t bytes) {
 bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
 
 // Head dimensions the attention kernels take: multiples of 8 (16-byte rows for TMA) up to
-// 128, and for the dense forward up to 256; d <= 64 runs on the 64-column kernels,
-// d <= 128 on the 128-column ones, d > 128 on the 256-column forward, with the columns
-// past d read as zero.
-constexpr int kMaxD = 128, kMaxDFwd = 256;
+// 128, and for dense tensors (forward and backward) up to 256; d <= 64 runs on the
+// 64-column kernels, d <= 128 on the 128-column ones, d > 128 on the 256-column ones, with
+// the columns past d read as zero.
+constexpr int kMaxD = 128, kMaxDDense = 256;
 bool head_dim_ok(int d, int max_d = kMaxD) { return d >= 8 && d <= max_d && d % 8 == 0; }
 
 attn_status check_shape(int B, int H, int N, int d, attn_dtype dtype, int max_d = kMaxD) {
@@ -183,9 +183,9 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N) {
 attn_status attn_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse,
                         int B, int H, int Nq, int Nk, int d, attn_dtype dtype, int causal,
                         float scale, void* cuda_stream) {
-  attn_status st = check_shape(B, H, Nq, d, dtype, kMaxDFwd);
+  attn_status st = check_shape(B, H, Nq, d, dtype, kMaxDDense);
   if (st != ATTN_OK) return st;
-  if ((st = check_shape(B, H, Nk, d, dtype, kMaxDFwd)) != ATTN_OK) return st;
+  if ((st = check_shape(B, H, Nk, d, dtype, kMaxDDense)) != ATTN_OK) return st;
   if (causal && Nk < Nq) return ATTN_ERR_INVALID_ARG;  // rows would see no key
   if ((st = check_scale(scale)) != ATTN_OK) return st;
   const void* ptrs[5] = {q, k, v, o, lse};
@@ -223,7 +223,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
 
 attn_status attn_bwd_preprocess(const void* o, const void* dO, float* delta, int B, int H,
                                 int N, int d, attn_dtype dtype, void* cuda_stream) {
-  attn_status st = check_shape(B, H, N, d, dtype);
+  attn_status st = check_shape(B, H, N, d, dtype, kMaxDDense);
   if (st != ATTN_OK) return st;
   const void* ptrs[3] = {o, dO, delta};
   for (const void* p : ptrs)
@@ -261,7 +261,17 @@ attn_status encode_bwd_maps(Maps* m, const void* q, const void* k, const void* v
   if ((st = encode_map(&m->q, q, s.BH, s.N, s.d, s.bf16)) != ATTN_OK) return st;
   if ((st = encode_map(&m->k, k, s.BH, s.Nk, s.d, s.bf16)) != ATTN_OK) return st;
   if ((st = encode_map(&m->v, v, s.BH, s.Nk, s.d, s.bf16)) != ATTN_OK) return st;
-  return encode_map(&m->d_o, dO, s.BH, s.N, s.d, s.bf16);
+  if ((st = encode_map(&m->d_o, dO, s.BH, s.N, s.d, s.bf16)) != ATTN_OK) return st;
+  m->k64 = m->k;
+  m->v64 = m->v;
+  m->q64 = m->q;
+  m->do64 = m->d_o;
+  if (s.d <= 128) return ATTN_OK;
+  // head dims above 128: the streamed 64-row blocks of the 256-column backward
+  if ((st = encode_map(&m->k64, k, s.BH, s.Nk, s.d, s.bf16, 64)) != ATTN_OK) return st;
+  if ((st = encode_map(&m->v64, v, s.BH, s.Nk, s.d, s.bf16, 64)) != ATTN_OK) return st;
+  if ((st = encode_map(&m->q64, q, s.BH, s.N, s.d, s.bf16, 64)) != ATTN_OK) return st;
+  return encode_map(&m->do64, dO, s.BH, s.N, s.d, s.bf16, 64);
 }
 
 // The dQ output as a TMA store target (dense, d <= 64: the persistent kernel's staged
@@ -288,7 +298,7 @@ attn_status attn_bwd_dkv(const void* q, const void* k, const void* v, const floa
                          const float* delta, const void* dO, void* dk, void* dv, int B, int H,
                          int N, int d, attn_dtype dtype, int causal, float scale,
                          void* cuda_stream) {
-  attn_status st = check_shape(B, H, N, d, dtype);
+  attn_status st = check_shape(B, H, N, d, dtype, kMaxDDense);
   if (st != ATTN_OK) return st;
   if ((st = check_scale(scale)) != ATTN_OK) return st;
   if ((st = check_ptrs({q, k, v, lse, delta, dO, dk, dv})) != ATTN_OK) return st;
@@ -308,7 +318,7 @@ attn_status attn_bwd_dkv(const void* q, const void* k, const void* v, const floa
 attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const float* lse,
                         const float* delta, const void* dO, void* dq, int B, int H, int N,
                         int d, attn_dtype dtype, int causal, float scale, void* cuda_stream) {
-  attn_status st = check_shape(B, H, N, d, dtype);
+  attn_status st = check_shape(B, H, N, d, dtype, kMaxDDense);
   if (st != ATTN_OK) return st;
   if ((st = check_scale(scale)) != ATTN_OK) return st;
   if ((st = check_ptrs({q, k, v, lse, delta, dO, dq})) != ATTN_OK) return st;
@@ -329,9 +339,9 @@ attn_status attn_bwd_qk(const void* q, const void* k, const void* v, const void*
                         const float* lse, const void* dO, void* dq, void* dk, void* dv,
                         void* workspace, int B, int H, int Nq, int Nk, int d,
                         attn_dtype dtype, int causal, float scale, void* cuda_stream) {
-  attn_status st = check_shape(B, H, Nq, d, dtype);
+  attn_status st = check_shape(B, H, Nq, d, dtype, kMaxDDense);
   if (st != ATTN_OK) return st;
-  if ((st = check_shape(B, H, Nk, d, dtype)) != ATTN_OK) return st;
+  if ((st = check_shape(B, H, Nk, d, dtype, kMaxDDense)) != ATTN_OK) return st;
   if (causal && Nk < Nq) return ATTN_ERR_INVALID_ARG;
   if ((st = check_scale(scale)) != ATTN_OK) return st;
   if ((st = check_ptrs({q, k, v, o, lse, dO, dq, dk, dv, workspace})) != ATTN_OK) return st;

@@ -141,6 +141,21 @@ __device__ __forceinline__ bool warp_poll(uint64_t* bar, uint32_t parity, uint64
   return __all_sync(0xffffffffu, ok);
 }
 
+// D[128 x 64] = A B^T over 256 columns, both K-major with 128-byte swizzle: A a [128 x 256]
+// tile (four 16 KiB boxes of 64 columns), B a [64 x 256] block (four 8 KiB boxes), 16
+// steps of 16 columns (the score products of the kernels for head dims above 128).
+// Descriptors built once by the caller; the start-address field is advanced by byte
+// offset / 16.
+__device__ __forceinline__ void issue_rowdot_wide(uint32_t d_tmem, uint64_t a_desc,
+                                                  uint64_t b_desc, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < 256 / 16; ++kk) {
+    const uint32_t a_off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
+    const uint32_t b_off = ((kk >> 2) * (kBoxBytes / 2) + (kk & 3) * 32) >> 4;
+    mma_ss(d_tmem, a_desc + a_off, b_desc + b_off, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
 // A operand in tensor memory whose 16-bit pairs sit in two halves: columns [0, 64) of A in
 // [base, base + 32) and columns [64, 128) in [base + 64, base + 96). B is an MN-major
 // [128 x d] tile in shared memory. D[128 x d] (+)= A B.

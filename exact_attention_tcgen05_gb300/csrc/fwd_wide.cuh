@@ -52,19 +52,6 @@ struct FwdWCfg {
   static constexpr uint32_t kColO = 256;  // O: 256 columns
 };
 
-// S[128 x 64] = Q K^T over 256 columns: A = the Q tile (K-major, 16 KiB boxes), B = a K
-// block (K-major, 8 KiB boxes), 16 steps of 16 columns. Descriptors built once by the
-// caller; the start-address field is advanced by byte offset / 16.
-__device__ __forceinline__ void issue_s_wide(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                             uint32_t idesc) {
-#pragma unroll
-  for (int kk = 0; kk < FwdWCfg::D / 16; ++kk) {
-    const uint32_t a_off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
-    const uint32_t b_off = ((kk >> 2) * FwdWCfg::kKVBox + (kk & 3) * 32) >> 4;
-    mma_ss(d_tmem, a_desc + a_off, b_desc + b_off, idesc, kk > 0 ? 1u : 0u);
-  }
-}
-
 template <bool BF16, bool PACKED>
 __global__ void __launch_bounds__(192, 1)
     attn_fwd_wide_kernel(const __grid_constant__ CUtensorMap map_q,
@@ -207,7 +194,7 @@ __global__ void __launch_bounds__(192, 1)
     const uint64_t dv0 = make_sdesc_sw128(smem_u32(smem + C::kOffV), C::kKVBox, 1024);
     constexpr uint32_t kStep = C::kKVBytes >> 4;
     auto issue_s = [&](int j) {
-      issue_s_wide(tmem + C::kColS + (j & 1) * 64, dq0, dk0 + (j % NK) * kStep, idesc_s);
+      issue_rowdot_wide(tmem + C::kColS + (j & 1) * 64, dq0, dk0 + (j % NK) * kStep, idesc_s);
     };
     auto issue_pv = [&](int j) {
 #pragma unroll

@@ -32,6 +32,8 @@ static cudaError_t launch_delta_t(const Shape& s, const void* o, const void* dO,
 
 cudaError_t launch_delta(const Shape& s, const void* o, const void* dO, float* delta,
                          cudaStream_t st) {
+  if (s.d > 128) return s.bf16 ? launch_delta_t<256, true>(s, o, dO, delta, st)
+                                 : launch_delta_t<256, false>(s, o, dO, delta, st);
   if (s.d > 64) return s.bf16 ? launch_delta_t<128, true>(s, o, dO, delta, st)
                                 : launch_delta_t<128, false>(s, o, dO, delta, st);
   return s.bf16 ? launch_delta_t<64, true>(s, o, dO, delta, st)

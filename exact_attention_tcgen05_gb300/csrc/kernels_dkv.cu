@@ -4,6 +4,7 @@
 #include <vector>
 
 #include "bwd_dkv_persistent.cuh"
+#include "bwd_wide.cuh"
 #include "launch.h"
 
 namespace attn {
@@ -138,6 +139,19 @@ static cudaError_t launch_dkv_t(const Maps& m, const Shape& s, const void* q, co
 cudaError_t launch_dkv(const Maps& m, const Shape& s, const void* q, const void* k,
                        const void* v, const void* d_o, const float* lse, const float* delta,
                        void* dk, void* dv, cudaStream_t st) {
+  if (s.d > 128) {
+    // two passes (dK and dV together would need 512 accumulator columns): dV with K_j
+    // resident, then dK with K_j, V_j resident; Q_i, dO_i streamed in both
+    cudaError_t e = s.bf16 ? launch_bwd_wide<kWideDV, true>(m.k, m.k, m.q64, m.do64, s, lse,
+                                                            delta, dk, dv, st)
+                           : launch_bwd_wide<kWideDV, false>(m.k, m.k, m.q64, m.do64, s, lse,
+                                                             delta, dk, dv, st);
+    if (e != cudaSuccess) return e;
+    return s.bf16 ? launch_bwd_wide<kWideDK, true>(m.k, m.v, m.q64, m.do64, s, lse, delta, dk,
+                                                   dv, st)
+                  : launch_bwd_wide<kWideDK, false>(m.k, m.v, m.q64, m.do64, s, lse, delta, dk,
+                                                    dv, st);
+  }
   if (s.d > 64)
     return s.bf16 ? launch_dkv_t<128, true>(m, s, q, k, v, d_o, lse, delta, dk, dv, st)
                   : launch_dkv_t<128, false>(m, s, q, k, v, d_o, lse, delta, dk, dv, st);

@@ -16,9 +16,12 @@ struct Maps {
   // 64-key blocks of the forward for head dims above 128 (encoded by the forward entry
   // points for d > 64)
   CUtensorMap k64;
-  // v read in [64-column x 64-row] boxes: the forward for head dims above 128 (encoded by
-  // the dense forward entry point for d > 128)
+  // v read in [64-column x 64-row] boxes: the forward and backward for head dims above 128
+  // (encoded by the dense entry points for d > 128; k64 likewise for the backward)
   CUtensorMap v64;
+  // q and dO read in [64-column x 64-row] boxes: the dK/dV passes of the backward for head
+  // dims above 128 (encoded by the dense backward entry points for d > 128)
+  CUtensorMap q64, do64;
   // o written in [64-column x 32-row] boxes: the persistent forward's staged epilogue at
   // d <= 64 (encoded by the dense forward entry point)
   CUtensorMap o;

@@ -94,7 +94,7 @@ def test_fwd_rejects_bad_arguments(lib, kw, code):
 @pytest.mark.parametrize("kw,code", [
     (dict(dq=0), INVALID), (dict(ws=0), INVALID), (dict(dq=DK), INVALID), (dict(ws=Q), INVALID),
     (dict(dq=O + 32), INVALID), (dict(d=132), UNSUPPORTED), (dict(scale=0.0), INVALID),
-    (dict(d=256), UNSUPPORTED),  # head dims above 128: the forward only
+    (dict(d=264), UNSUPPORTED),
     (dict(ws=WS + 8), INVALID),
 ])
 def test_bwd_rejects_bad_arguments(lib, kw, code):
