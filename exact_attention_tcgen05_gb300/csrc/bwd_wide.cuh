@@ -20,11 +20,14 @@
 // each rounded once to the input type as the A operand of its product.
 //
 // Roles: warps 0-3 elementwise, one row per thread (TMEM lane); warp 4 TMA producer; warp
-// 5 MMA issuer and tensor-memory owner. Tensor memory: two S buffers (64 columns each),
-// two dP buffers (dQ, dK) and the 256-column accumulator, so the products of block b + 1
-// run while the elementwise warps work on block b. Streamed operands have rings of their
-// own, each stage freed by its last product: the one read by the accumulating product
-// (X: K_j in dQ, Q_i in dK; dO_i in dV) late, the other early.
+// 5 MMA issuer and tensor-memory owner. The first resident tile (Q_i or K_j) sits in shared
+// memory; the second (dO_i in dQ, V_j in dK) is copied by the elementwise threads, a row
+// each, into tensor memory, where it is the A operand of dP. That leaves shared memory for
+// three stages of X (the B operand of S) and two of Y (of dP; of the accumulation in dV),
+// each stage freed by its last product: X by the accumulation (dQ, dK) or by S (dV), Y by
+// dP (dQ, dK) or by the accumulation (dV). Tensor memory: S (two buffers in dV, where P
+// is written over S and nothing else needs columns), dP, the 256-column accumulator and
+// the copied tile: S(b + 1) runs while the elementwise warps finish block b.
 #pragma once
 
 #include "bwd_dq.cuh"
@@ -43,18 +46,19 @@ struct BwdWCfg {
   static constexpr int kBlkBox = kBN * 128;             // [64 x 64] box: 8 KiB
   static constexpr int kBlkBytes = kChunks * kBlkBox;   // streamed 64 x 256 block: 32 KiB
   static constexpr bool kDV = MODE == kWideDV;
-  static constexpr int kNumA = kDV ? 1 : 2;  // resident tiles
+  static constexpr bool kA2Tmem = !kDV;  // the second resident tile, in tensor memory
+  static constexpr int kSBufs = kDV ? 2 : 1;  // S buffers
   // Streamed X (the B operand of S) and Y (of dP, or of the accumulating product in dV)
-  static constexpr int kXStages = kDV ? 3 : 2;
-  static constexpr int kYStages = kDV ? 2 : 1;
+  static constexpr int kXStages = 3;
+  static constexpr int kYStages = 2;
   static constexpr int kOffA = 0;
-  static constexpr int kOffX = kOffA + kNumA * kTileBytes;
+  static constexpr int kOffX = kOffA + kTileBytes;
   static constexpr int kOffY = kOffX + kXStages * kBlkBytes;
   static constexpr int kOffStats = kOffY + kYStages * kBlkBytes;  // [2][-L log2 e x64, D x64]
   static constexpr int kOffBar = kOffStats + 2 * 128 * 4;
-  // a_full, x_full[XS], x_empty[XS], y_full[YS], y_empty[YS], s_full[2], dp_full[2],
-  // ds_full[2] (dV: p_full[2]), stats_ready[2], acc_last, drain
-  static constexpr int kNumBars = 1 + 2 * kXStages + 2 * kYStages + 2 + 2 + 2 + 2 + 1 + 1;
+  // a_full, a2_tmem, x_full[XS], x_empty[XS], y_full[YS], y_empty[YS], s_full[2], s_free,
+  // dp_full, ds_full[2] (dV: P written), stats_ready[2], acc_last, drain
+  static constexpr int kNumBars = 2 + 2 * kXStages + 2 * kYStages + 2 + 1 + 1 + 2 + 2 + 1 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -62,21 +66,33 @@ struct BwdWCfg {
   static constexpr int kThreads = 192;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0;     // S buffer b at 64 b (P over its first 32 in dV)
-  static constexpr uint32_t kColDP = 128;  // dP buffer b at 128 + 64 b (dS over its first 32)
-  static constexpr uint32_t kColAcc = 256;
+  static constexpr uint32_t kColDP = 64;   // dQ, dK: dP (dS over its first 32 columns)
+  static constexpr uint32_t kColAcc = 128;
+  static constexpr uint32_t kColA2 = 384;  // dQ, dK: dO_i or V_j as 16-bit pairs
 };
 
-// Maps: a1/a2 = resident tiles (128-row boxes), x/y = streamed blocks (64-row boxes).
+// D[128 x 64] = A B^T over 256 columns with A in tensor memory (16-bit pairs from column
+// a_tmem, 128 columns) and B a K-major [64 x 256] block (four 8 KiB boxes).
+__device__ __forceinline__ void issue_rowdot_ts_wide(uint32_t d_tmem, uint32_t a_tmem,
+                                                     uint64_t b_desc, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < 256 / 16; ++kk) {
+    const uint32_t b_off = ((kk >> 2) * (kBoxBytes / 2) + (kk & 3) * 32) >> 4;
+    mma_ts(d_tmem, a_tmem + kk * 8, b_desc + b_off, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// Maps: a1 = the resident tile in shared memory (128-row boxes), x/y = streamed blocks
+// (64-row boxes). dQ and dK read the second resident tile's rows from p.in_do / p.in_v.
 template <int MODE, bool BF16>
 __global__ void __launch_bounds__(192, 1)
     attn_bwd_wide_kernel(const __grid_constant__ CUtensorMap map_a1,
-                         const __grid_constant__ CUtensorMap map_a2,
                          const __grid_constant__ CUtensorMap map_x,
                          const __grid_constant__ CUtensorMap map_y, const BwdParams p) {
   using C = BwdWCfg<MODE>;
   constexpr bool kDV = C::kDV;
   constexpr bool kRowsAreQueries = MODE == kWideDQ;
-  constexpr int NX = C::kXStages, NY = C::kYStages;
+  constexpr int NX = C::kXStages, NY = C::kYStages, NB = C::kSBufs;
   constexpr int kBN = C::kBN;
   // Wait-site codes: the dQ kernel's for the dQ pass, the dK/dV kernel's for the others.
   constexpr int kSiteA = kRowsAreQueries ? kWaitDqQ : kWaitDkvKV;
@@ -92,13 +108,15 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* a_full = bars;
-  uint64_t* x_full = bars + 1;
+  uint64_t* a2_tmem = bars + 1;  // dQ, dK: every elementwise warp has copied its rows
+  uint64_t* x_full = bars + 2;
   uint64_t* x_empty = x_full + NX;
   uint64_t* y_full = x_empty + NX;
   uint64_t* y_empty = y_full + NY;
-  uint64_t* s_full = y_empty + NY;    // [2] per S buffer
-  uint64_t* dp_full = s_full + 2;     // [2] per dP buffer
-  uint64_t* ds_full = dp_full + 2;    // [2] dS (dV: P) of the buffer's block is written
+  uint64_t* s_full = y_empty + NY;    // [NB] per S buffer
+  uint64_t* s_free = s_full + 2;      // dQ, dK: S has been read (one buffer)
+  uint64_t* dp_full = s_free + 1;
+  uint64_t* ds_full = dp_full + 1;    // [NB] dS (dV: P) of the buffer's block is written
   uint64_t* stats_ready = ds_full + 2;  // [2] per statistics buffer
   uint64_t* acc_last = stats_ready + 2;  // the last accumulating product
   uint64_t* drain = acc_last + 1;
@@ -131,6 +149,7 @@ __global__ void __launch_bounds__(192, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(a_full, 1);
+    mbar_init(a2_tmem, 4);  // one arrival per elementwise warp
     for (int s = 0; s < NX; ++s) {
       mbar_init(&x_full[s], 1);
       mbar_init(&x_empty[s], 1);
@@ -141,10 +160,11 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&dp_full[b], 1);
       mbar_init(&ds_full[b], 4);      // one arrival per elementwise warp
       mbar_init(&stats_ready[b], 4);  // one arrival per elementwise warp
     }
+    mbar_init(s_free, 4);
+    mbar_init(dp_full, 1);
     mbar_init(acc_last, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -166,24 +186,20 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------ TMA producer ------------------------------
     if (elect_one()) {
       tma_prefetch_map(&map_a1);
-      if (!kDV) tma_prefetch_map(&map_a2);
       tma_prefetch_map(&map_x);
       tma_prefetch_map(&map_y);
-      mbar_arrive_expect_tx(a_full, C::kNumA * C::kTileBytes);
+      mbar_arrive_expect_tx(a_full, C::kTileBytes);
       for (int c = 0; c < C::kChunks; ++c)
         tma_load_rows<false>(smem + C::kOffA + c * kBoxBytes, &map_a1, a_full, c * kBoxCols, r0,
                              sl, a_keys);
-      if (!kDV)
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_rows<false>(smem + C::kOffA + C::kTileBytes + c * kBoxBytes, &map_a2, a_full,
-                               c * kBoxCols, r0, sl, a_keys);
     }
     __syncwarp();
     // X(b) into stage b % NX once the stage's previous block is released (x_empty), Y(b)
     // likewise; each empty barrier completes once per block of its stage, after a copy
-    // issued past its wait. The order never waits on a product that needs a later copy:
-    // dQ/dK: Y(b) (freed by dP(b - 1)) before X(b + 1) (freed by the accumulating product
-    // of b - 1, which follows dP(b)); dV: X two blocks ahead (freed by S), then Y(b).
+    // issued past its wait. Order: X(0), X(1), then Y(b), X(b + 2). It never waits on a
+    // product that needs a later copy: Y(b) waits for a product of block b - 2, X(b + 2)
+    // for one of block b - 1 (the accumulation in dQ/dK, S in dV), and neither of those
+    // needs more than X(b) and Y(b - 1).
     int x_issued = 0, y_issued = 0;
     auto load_x = [&](int b) -> bool {
       const int s = b % NX;
@@ -216,16 +232,11 @@ __global__ void __launch_bounds__(192, 1)
       return true;
     };
     bool ok = true;
-    constexpr int kLead = kDV ? NX - 1 : 1;  // X copies ahead of Y
+    constexpr int kLead = NX - 1;  // X copies ahead of Y
     for (int b = 0; ok && b < min(kLead, n); ++b) ok = load_x(b);
     for (int b = 0; ok && b < n; ++b) {
-      if constexpr (kDV) {
-        if (b + kLead < n) ok = load_x(b + kLead);
-        if (ok) ok = load_y(b);
-      } else {
-        ok = load_y(b);
-        if (ok && b + kLead < n) ok = load_x(b + kLead);
-      }
+      ok = load_y(b);
+      if (ok && b + kLead < n) ok = load_x(b + kLead);
     }
     if (*abort_flag) {
       // Let every copy this CTA started land before its shared memory is released.
@@ -237,27 +248,22 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp == 5) {
     // ------------------------------ MMA issuer --------------------------------
-    // Per block b: S(b + 1) (and dP(b + 1)) into the other buffers (their previous
-    // contents were last read by products issued before: the tensor core runs them in
-    // order), then the accumulating product of b once the elementwise warps are done.
+    // dV, per block b: S(b + 1) into the other S buffer (its previous P was read by the
+    // accumulation of b - 1, issued before: the tensor core runs them in order), then
+    // dV += P(b) Y(b) once P is written. dQ/dK, per block b: S(b + 1) once S(b) has been
+    // read (s_free), dQ/dK += dS(b) X(b) once dS is written, then dP(b + 1), which
+    // overwrites dS(b) after the product that reads it.
     const uint32_t idesc_s = make_idesc(BF16, 128, kBN, false, false);
     const uint32_t idesc_acc = make_idesc(BF16, 128, C::D, false, true);
     const uint64_t da1 = make_sdesc_sw128(smem_u32(smem + C::kOffA), 16, 1024);
-    const uint64_t da2 = da1 + (C::kTileBytes >> 4);
     const uint64_t dx0 = make_sdesc_sw128(smem_u32(smem + C::kOffX), 16, 1024);
     const uint64_t dy0 = make_sdesc_sw128(smem_u32(smem + C::kOffY), 16, 1024);
     // the accumulating product's B operand, MN-major: X (dQ, dK) or Y (dV)
     const uint64_t dacc0 =
         make_sdesc_sw128(smem_u32(smem + (kDV ? C::kOffY : C::kOffX)), C::kBlkBox, 1024);
     constexpr uint32_t kStep = C::kBlkBytes >> 4;
-    auto issue_s = [&](int b) {
-      issue_rowdot_wide(tmem + C::kColS + (b & 1) * 64, da1, dx0 + (b % NX) * kStep, idesc_s);
-    };
-    auto issue_dp = [&](int b) {
-      issue_rowdot_wide(tmem + C::kColDP + (b & 1) * 64, da2, dy0 + (b % NY) * kStep, idesc_s);
-    };
     auto issue_acc = [&](int b) {
-      const uint32_t a_col = (kDV ? C::kColS : C::kColDP) + (b & 1) * 64;
+      const uint32_t a_col = kDV ? C::kColS + (b & 1) * 64 : C::kColDP;
       const int stage = kDV ? b % NY : b % NX;
 #pragma unroll
       for (int kk = 0; kk < kBN / 16; ++kk)
@@ -265,38 +271,46 @@ __global__ void __launch_bounds__(192, 1)
                dacc0 + stage * kStep + ((kk * 2048) >> 4), idesc_acc,
                (b > 0 || kk > 0) ? 1u : 0u);
     };
-    // S(b) and, for dQ/dK, dP(b): waits for their operands, issue, commits.
-    auto issue_scores = [&](int b) -> bool {
+    auto issue_s = [&](int b) -> bool {
       if (!warp_poll(&x_full[b % NX], (b / NX) & 1, limit, abort_flag, kSiteX)) return false;
       tc_fence_after();
       if (elect_one()) {
-        issue_s(b);
-        mma_commit(&s_full[b & 1]);
+        issue_rowdot_wide(tmem + C::kColS + (b % NB) * 64, da1, dx0 + (b % NX) * kStep,
+                          idesc_s);
+        mma_commit(&s_full[b % NB]);
         if (kDV) mma_commit(&x_empty[b % NX]);  // dV: X is read by S alone
       }
       __syncwarp();
-      if constexpr (!kDV) {
-        if (!warp_poll(&y_full[b % NY], (b / NY) & 1, limit, abort_flag, kSiteY))
-          return false;
-        tc_fence_after();
-        if (elect_one()) {
-          issue_dp(b);
-          mma_commit(&dp_full[b & 1]);
-          mma_commit(&y_empty[b % NY]);  // dQ/dK: Y is read by dP alone
-        }
-        __syncwarp();
+      return true;
+    };
+    auto issue_dp = [&](int b) -> bool {
+      if (!warp_poll(&y_full[b % NY], (b / NY) & 1, limit, abort_flag, kSiteY)) return false;
+      tc_fence_after();
+      if (elect_one()) {
+        issue_rowdot_ts_wide(tmem + C::kColDP, tmem + C::kColA2, dy0 + (b % NY) * kStep,
+                             idesc_s);
+        mma_commit(dp_full);
+        mma_commit(&y_empty[b % NY]);  // dQ/dK: Y is read by dP alone
       }
+      __syncwarp();
       return true;
     };
     bool ok = warp_poll(a_full, 0, limit, abort_flag, kSiteA);
-    if (ok) ok = issue_scores(0);
+    if (ok && C::kA2Tmem) ok = warp_poll(a2_tmem, 0, limit, abort_flag, kSiteA);
+    if (ok) ok = issue_s(0);
+    if (ok && C::kA2Tmem) ok = issue_dp(0);
     for (int b = 0; ok && b < n; ++b) {
-      if (b + 1 < n && !(ok = issue_scores(b + 1))) break;
+      if (b + 1 < n) {
+        if (C::kA2Tmem &&
+            !(ok = warp_poll(s_free, b & 1, limit, abort_flag, kSiteS)))
+          break;
+        if (!(ok = issue_s(b + 1))) break;
+      }
       if constexpr (kDV) {
         if (!(ok = warp_poll(&y_full[b % NY], (b / NY) & 1, limit, abort_flag, kSiteY)))
           break;
       }
-      if (!(ok = warp_poll(&ds_full[b & 1], (b >> 1) & 1, limit, abort_flag, kSiteDS))) break;
+      if (!(ok = warp_poll(&ds_full[b % NB], (b / NB) & 1, limit, abort_flag, kSiteDS))) break;
       tc_fence_after();
       if (elect_one()) {
         issue_acc(b);
@@ -304,6 +318,7 @@ __global__ void __launch_bounds__(192, 1)
         if (b == n - 1) mma_commit(acc_last);
       }
       __syncwarp();
+      if (C::kA2Tmem && b + 1 < n && !(ok = issue_dp(b + 1))) break;
     }
     // Every MMA issued must finish before tensor memory is released.
     if (elect_one()) mma_commit(drain);
@@ -330,6 +345,18 @@ __global__ void __launch_bounds__(192, 1)
       return r_in < 64 ? -p.lse[sl.stat0 + q] * kLog2e : p.delta[sl.stat0 + q];
     };
     float stat_next = kRowsAreQueries ? 0.f : load_stat(0);
+    if constexpr (C::kA2Tmem) {
+      // This row of dO_i (dQ) or V_j (dK) into tensor memory (rows past the slice's end as
+      // zeros): the A operand of dP.
+      const uint8_t* gsrc = reinterpret_cast<const uint8_t*>(kRowsAreQueries ? p.in_do : p.in_v);
+      const size_t elem0 = kRowsAreQueries ? sl.q_elem0 : sl.k_elem0;
+      copy_row_to_tmem<C::D>(row < n_rows ? gsrc + (elem0 + (size_t)row * sl.row_elems) * 2
+                                          : nullptr,
+                             tmem + lane_base + C::kColA2, p.dh / 8);
+      tmem_st_wait();
+      tc_fence_before();
+      warp_arrive(a2_tmem);
+    }
     bool ok = true;
     for (int b = 0; b < n; ++b) {
       const float* st = stats + (b & 1) * 128;
@@ -344,11 +371,15 @@ __global__ void __launch_bounds__(192, 1)
           break;
       }
       // ---- P = exp2(S * scale * log2(e) - L * log2(e))
-      if (!(ok = warp_wait(&s_full[b & 1], (b >> 1) & 1, limit, abort_flag, kSiteS))) break;
+      if (!(ok = warp_wait(&s_full[b % NB], (b / NB) & 1, limit, abort_flag, kSiteS))) break;
       tc_fence_after();
-      const uint32_t t_s = tmem + lane_base + C::kColS + (b & 1) * 64;
+      const uint32_t t_s = tmem + lane_base + C::kColS + (b % NB) * 64;
       uint32_t sr[kBN];
       tmem_ld64(t_s, sr);
+      if constexpr (C::kA2Tmem) {
+        tc_fence_before();
+        warp_arrive(s_free);  // S(b) is in registers: S(b + 1) may overwrite it
+      }
       float* pr = reinterpret_cast<float*>(sr);
       if constexpr (kRowsAreQueries) {
         const float2 nl = make_float2(row_nl, row_nl);
@@ -398,10 +429,9 @@ __global__ void __launch_bounds__(192, 1)
         tmem_st16(t_s + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
       } else {
         // ---- dS = P * (dP - D), 16-bit pairs over dP: the A operand of the accumulation
-        if (!(ok = warp_wait(&dp_full[b & 1], (b >> 1) & 1, limit, abort_flag, kSiteDP)))
-          break;
+        if (!(ok = warp_wait(dp_full, b & 1, limit, abort_flag, kSiteDP))) break;
         tc_fence_after();
-        const uint32_t t_dp = tmem + lane_base + C::kColDP + (b & 1) * 64;
+        const uint32_t t_dp = tmem + lane_base + C::kColDP;
         uint32_t r[kBN];
         tmem_ld64(t_dp, r);
         if constexpr (kRowsAreQueries) {
@@ -436,7 +466,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      warp_arrive(&ds_full[b & 1]);
+      warp_arrive(&ds_full[b % NB]);
     }
     if (ok && warp_wait(acc_last, 0, limit, abort_flag, kSiteDone)) {
       tc_fence_after();
@@ -462,11 +492,12 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-// One pass of the kernel above: a1/a2 the resident 128-row tiles, x/y the streamed 64-row
-// blocks; one CTA per 128 rows (queries for dQ, keys for dK and dV) of each slice.
+// One pass of the kernel above: a1 the resident 128-row tile, x/y the streamed 64-row
+// blocks, a2_rows the tensor whose rows go to tensor memory (dO for dQ, V for dK); one CTA
+// per 128 rows (queries for dQ, keys for dK and dV) of each slice.
 template <int MODE, bool BF16>
-static cudaError_t launch_bwd_wide(const CUtensorMap& a1, const CUtensorMap& a2,
-                                   const CUtensorMap& x, const CUtensorMap& y, const Shape& s,
+static cudaError_t launch_bwd_wide(const CUtensorMap& a1, const CUtensorMap& x,
+                                   const CUtensorMap& y, const void* a2_rows, const Shape& s,
                                    const float* lse, const float* delta, void* out0,
                                    void* out1, cudaStream_t st) {
   using C = BwdWCfg<MODE>;
@@ -475,6 +506,8 @@ static cudaError_t launch_bwd_wide(const CUtensorMap& a1, const CUtensorMap& a2,
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   BwdParams p = {};
+  p.in_do = a2_rows;  // dQ: dO, rows copied into tensor memory
+  p.in_v = a2_rows;   // dK: V, likewise (dV: unused)
   p.lse = lse;
   p.delta = delta;
   p.out0 = out0;
@@ -489,7 +522,7 @@ static cudaError_t launch_bwd_wide(const CUtensorMap& a1, const CUtensorMap& a2,
   p.vl = s.vl;
   const int rows = MODE == kWideDQ ? s.N : s.Nk;
   dim3 grid((rows + kTileM - 1) / kTileM, s.BH);
-  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(a1, a2, x, y, p);
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(a1, x, y, p);
   return cudaGetLastError();
 }
 

@@ -145,9 +145,9 @@ cudaError_t launch_dq(const Maps& m, const Shape& s, const void* q, const void* 
                        const float* lse, const float* delta,
                       void* dq, cudaStream_t st) {
   if (s.d > 128)  // Q_i, dO_i resident; K_j, V_j streamed
-    return s.bf16 ? launch_bwd_wide<kWideDQ, true>(m.q, m.d_o, m.k64, m.v64, s, lse, delta, dq,
+    return s.bf16 ? launch_bwd_wide<kWideDQ, true>(m.q, m.k64, m.v64, d_o, s, lse, delta, dq,
                                                    nullptr, st)
-                  : launch_bwd_wide<kWideDQ, false>(m.q, m.d_o, m.k64, m.v64, s, lse, delta, dq,
+                  : launch_bwd_wide<kWideDQ, false>(m.q, m.k64, m.v64, d_o, s, lse, delta, dq,
                                                     nullptr, st);
   if (s.d > 64) return s.bf16 ? launch_dq_t<128, true>(m, s, q, d_o, lse, delta, dq, st)
                                 : launch_dq_t<128, false>(m, s, q, d_o, lse, delta, dq, st);
