@@ -335,12 +335,13 @@ def time_workload(w, steps: int, warmup: int) -> dict:
 
 def measure_workloads(args, peaks: dict, skip: str) -> dict:
     """Forward and backward throughput of the other quoted workloads (the one the line is
-    about is skipped), measured after the main timed region, each on its own."""
+    about is skipped) and of the head-dim-256 workload, measured after the main timed
+    region, each on its own."""
     from exact_attention_tcgen05_gb300 import inputs as I
     burst = peaks["bf16_tflops"]
     steps = max(10, min(args.steps, 30))
     out = {}
-    for w in I.WORKLOADS:
+    for w in I.WORKLOADS + I.HEAD_DIM_WORKLOADS:
         if w.name == skip:
             continue
         t = time_workload(w, steps, max(3, args.warmup))

@@ -70,7 +70,12 @@ WORKLOADS = [
     Workload("B2_H32_N8192_d64_bf16_full_spiked", 2, 32, 8192, 64, "bf16", False, 1004,
              qk_gain=4.0, spike=8.0, spike_frac=0.01, oracle_slices=2),
 ]
-BY_NAME = {w.name: w for w in WORKLOADS}
+# Beyond the quoted five: a head dim above 128 (the 256-column kernels), measured beside them.
+HEAD_DIM_WORKLOADS = [
+    Workload("B4_H16_N4096_d256_bf16_causal", 4, 16, 4096, 256, "bf16", True, 1005,
+             oracle_slices=2),
+]
+BY_NAME = {w.name: w for w in WORKLOADS + HEAD_DIM_WORKLOADS}
 
 
 def custom(B: int, H: int, N: int, d: int, dtype: str, causal: bool, seed: int,

@@ -96,3 +96,15 @@ def test_wide_single_key_gradients_vanish(d, dt):
         dq, dk = I.to_f64(run.dq[0, h]), I.to_f64(run.dk[0, h])
         assert np.all(np.abs(dq) <= w.scale * ds_max * np.abs(k) * (1 + 2.0 ** -7) + 1e-30)
         assert np.all(np.abs(dk) <= w.scale * ds_max * np.abs(q) * (1 + 2.0 ** -7) + 1e-30)
+
+
+def test_head_dim_workload_sampled():
+    """The head-dim-256 workload the benchmark times, at full size, on sampled slices."""
+    w = I.BY_NAME["B4_H16_N4096_d256_bf16_causal"]
+    run = run_gpu(w)
+    assert all_finite(run)
+    assert binding.attn_last_kernel_status() == (0, 0)
+    for b, h in I.sampled_slices(w):
+        res = compare_slice(w, run, b, h)
+        record(w.name, res)
+        assert_within(res, f"{w.name} slice {(b, h)}")
