@@ -70,3 +70,41 @@ def test_waits_that_run_out_are_reported_and_the_context_survives(pair):
         assert code == ATTN_ERR_TIMEOUT, (name, code, where)
         assert lo <= where <= hi, (name, hex(where))
     assert res["after"] == 45
+
+
+CHILD_WIDE = r"""
+import json
+import torch
+from exact_attention_tcgen05_gb300 import binding
+from exact_attention_tcgen05_gb300 import inputs as I
+
+w = I.custom(1, 2, 640, 256, "bf16", True, seed=5)
+q, k, v, do = (I.make_tensor(w, t).cuda() for t in ("q", "k", "v", "do"))
+out = {}
+o, lse = binding.attn_fwd(q, k, v, causal=True, scale=w.scale)
+out["fwd"] = binding.attn_last_kernel_status()
+delta = binding.attn_bwd_preprocess(o, do)
+binding.attn_bwd_dkv(q, k, v, lse, delta, do, causal=True, scale=w.scale)
+out["dkv"] = binding.attn_last_kernel_status()
+binding.attn_bwd_dq(q, k, v, lse, delta, do, causal=True, scale=w.scale)
+out["dq"] = binding.attn_last_kernel_status()
+torch.cuda.synchronize()
+out["after"] = int(torch.arange(10, device="cuda").sum().item())
+print(json.dumps(out))
+"""
+
+
+def test_wide_kernels_waits_that_run_out_are_reported_and_the_context_survives():
+    """The same for head dim 256: the 256-column forward and the three passes of the
+    256-column backward (the dK/dV passes report the dK/dV kernel's site codes)."""
+    env = dict(os.environ, ATTN_WAIT_LIMIT_CYCLES="64")
+    r = subprocess.run([sys.executable, "-c", CHILD_WIDE], env=env, cwd=ROOT,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    for name in ("fwd", "dkv", "dq"):
+        lo, hi = SITE_RANGE[name]
+        code, where = res[name]
+        assert code == ATTN_ERR_TIMEOUT, (name, code, where)
+        assert lo <= where <= hi, (name, hex(where))
+    assert res["after"] == 45
