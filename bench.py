@@ -271,6 +271,12 @@ print(json.dumps({{"slices": done, "seconds": t_total}}))
                       f"{r['seconds']:.1f} s"}
 
 
+def launches_per_step(w) -> int:
+    """Kernels one forward + backward step launches: forward, D, dK/dV (two passes, dV then
+    dK, for head dims above 128), dQ."""
+    return 5 if w.d > 128 else 4
+
+
 def workload_of(args):
     """The workload named by --workload, or the shape given by --custom (smaller cases for
     profiling: "B,H,N,d,dtype,causal|full", inputs drawn by the same generator)."""
@@ -495,7 +501,7 @@ def run_ours(args) -> None:
                      "peak_kind": f"bf16 burst ({peaks['source']})",
                      "frac_of_sustained": achieved / sustained,
                      "algorithmic_tflop_per_launch": dom_flops / 1e12, "traffic": traffic},
-        "e2e": e2e, "clocks": clock_info, "gpu_launches": 4 * args.steps,
+        "e2e": e2e, "clocks": clock_info, "gpu_launches": launches_per_step(w) * args.steps,
         "env": {"gpu": torch.cuda.get_device_name(), "torch": torch.__version__,
                 "cuda": torch.version.cuda,
                 "sm_count": torch.cuda.get_device_properties(0).multi_processor_count},
