@@ -84,7 +84,10 @@ __device__ __forceinline__ void issue_rowdot_ts_wide(uint32_t d_tmem, uint32_t a
 
 // Maps: a1 = the resident tile in shared memory (128-row boxes), x/y = streamed blocks
 // (64-row boxes). dQ and dK read the second resident tile's rows from p.in_do / p.in_v.
-template <int MODE, bool BF16>
+// PACKED: slices are (sequence, head) pairs of a packed batch (common.cuh, SliceRows); a
+// tile past its sequence's end does nothing, and a sequence with keys but no queries gets
+// zero key gradients.
+template <int MODE, bool BF16, bool PACKED>
 __global__ void __launch_bounds__(192, 1)
     attn_bwd_wide_kernel(const __grid_constant__ CUtensorMap map_a1,
                          const __grid_constant__ CUtensorMap map_x,
@@ -128,11 +131,12 @@ __global__ void __launch_bounds__(192, 1)
   const int lane = lane_id();
   const int bh = blockIdx.y;
   SliceRows sl;
-  if (!slice_rows<false>(p.vl, bh, p.N, p.Nk, p.dh, p.causal != 0, sl)) return;
+  if (!slice_rows<PACKED>(p.vl, bh, p.N, p.Nk, p.dh, p.causal != 0, sl)) return;
   const int N = sl.nq, Nk = sl.nk, off = sl.off;
   // Rows of this CTA and the streamed blocks it visits (b0 .. b0 + n - 1).
   const int n_rows = kRowsAreQueries ? N : Nk;
   const int n_tiles = (n_rows + kTileM - 1) / kTileM;
+  if (PACKED && (int)blockIdx.x >= n_tiles) return;  // past this sequence's rows
   const int r0 = (n_tiles - 1 - (int)blockIdx.x) * kTileM;  // longest first within a head
   int b0, n;
   if constexpr (kRowsAreQueries) {
@@ -144,7 +148,7 @@ __global__ void __launch_bounds__(192, 1)
     // queries from the block of the first query that sees the tile's first key
     const int nqb = (N + kBN - 1) / kBN;
     b0 = (p.causal && r0 > off) ? (r0 - off) / kBN : 0;
-    n = nqb - b0;  // >= 1: the last query sees every key (N_k >= N_q when causal)
+    n = nqb - b0;  // >= 1 unless the slice has no queries: the last query sees every key
   }
 
   if (threadIdx.x == 0) {
@@ -184,14 +188,14 @@ __global__ void __launch_bounds__(192, 1)
 
   if (warp == 4) {
     // ------------------------------ TMA producer ------------------------------
-    if (elect_one()) {
+    if (n > 0 && elect_one()) {
       tma_prefetch_map(&map_a1);
       tma_prefetch_map(&map_x);
       tma_prefetch_map(&map_y);
       mbar_arrive_expect_tx(a_full, C::kTileBytes);
       for (int c = 0; c < C::kChunks; ++c)
-        tma_load_rows<false>(smem + C::kOffA + c * kBoxBytes, &map_a1, a_full, c * kBoxCols, r0,
-                             sl, a_keys);
+        tma_load_rows<PACKED>(smem + C::kOffA + c * kBoxBytes, &map_a1, a_full, c * kBoxCols,
+                              r0, sl, a_keys);
     }
     __syncwarp();
     // X(b) into stage b % NX once the stage's previous block is released (x_empty), Y(b)
@@ -209,7 +213,7 @@ __global__ void __launch_bounds__(192, 1)
       if (elect_one()) {
         mbar_arrive_expect_tx(&x_full[s], C::kBlkBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_rows<false>(smem + C::kOffX + s * C::kBlkBytes + c * C::kBlkBox, &map_x,
+          tma_load_rows<PACKED>(smem + C::kOffX + s * C::kBlkBytes + c * C::kBlkBox, &map_x,
                                &x_full[s], c * kBoxCols, (b0 + b) * kBN, sl, x_keys);
       }
       __syncwarp();
@@ -224,7 +228,7 @@ __global__ void __launch_bounds__(192, 1)
       if (elect_one()) {
         mbar_arrive_expect_tx(&y_full[s], C::kBlkBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_rows<false>(smem + C::kOffY + s * C::kBlkBytes + c * C::kBlkBox, &map_y,
+          tma_load_rows<PACKED>(smem + C::kOffY + s * C::kBlkBytes + c * C::kBlkBox, &map_y,
                                &y_full[s], c * kBoxCols, (b0 + b) * kBN, sl, x_keys);
       }
       __syncwarp();
@@ -240,7 +244,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     if (*abort_flag) {
       // Let every copy this CTA started land before its shared memory is released.
-      mbar_wait(a_full, 0, kDrainLimit, nullptr, kSiteDrain);
+      if (n > 0) mbar_wait(a_full, 0, kDrainLimit, nullptr, kSiteDrain);
       for (int b = max(0, x_issued - NX); b < x_issued; ++b)
         mbar_wait(&x_full[b % NX], (b / NX) & 1, kDrainLimit, nullptr, kSiteDrain);
       for (int b = max(0, y_issued - NY); b < y_issued; ++b)
@@ -295,7 +299,7 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       return true;
     };
-    bool ok = warp_poll(a_full, 0, limit, abort_flag, kSiteA);
+    bool ok = n > 0 && warp_poll(a_full, 0, limit, abort_flag, kSiteA);
     if (ok && C::kA2Tmem) ok = warp_poll(a2_tmem, 0, limit, abort_flag, kSiteA);
     if (ok) ok = issue_s(0);
     if (ok && C::kA2Tmem) ok = issue_dp(0);
@@ -345,7 +349,7 @@ __global__ void __launch_bounds__(192, 1)
       return r_in < 64 ? -p.lse[sl.stat0 + q] * kLog2e : p.delta[sl.stat0 + q];
     };
     float stat_next = kRowsAreQueries ? 0.f : load_stat(0);
-    if constexpr (C::kA2Tmem) {
+    if (C::kA2Tmem && n > 0) {
       // This row of dO_i (dQ) or V_j (dK) into tensor memory (rows past the slice's end as
       // zeros): the A operand of dP.
       const uint8_t* gsrc = reinterpret_cast<const uint8_t*>(kRowsAreQueries ? p.in_do : p.in_v);
@@ -468,11 +472,17 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_before();
       warp_arrive(&ds_full[b % NB]);
     }
-    if (ok && warp_wait(acc_last, 0, limit, abort_flag, kSiteDone)) {
+    void* out = kRowsAreQueries || MODE == kWideDK ? p.out0 : p.out1;
+    const size_t elem0 = kRowsAreQueries ? sl.q_elem0 : sl.k_elem0;
+    uint8_t* drow = reinterpret_cast<uint8_t*>(out) + (elem0 + (size_t)row * sl.row_elems) * 2;
+    if (n == 0) {
+      // keys of a sequence without queries: no query sees them, so their gradients are zero
+      uint32_t z[32] = {};
+#pragma unroll 1
+      for (int cc = 0; cc < C::D / 32; ++cc)
+        if (row < n_rows) store_row32<BF16>(drow + cc * 64, z, 1.f, valid16(p.dh, cc * 32, 4));
+    } else if (ok && warp_wait(acc_last, 0, limit, abort_flag, kSiteDone)) {
       tc_fence_after();
-      void* out = kRowsAreQueries || MODE == kWideDK ? p.out0 : p.out1;
-      const size_t elem0 = kRowsAreQueries ? sl.q_elem0 : sl.k_elem0;
-      uint8_t* drow = reinterpret_cast<uint8_t*>(out) + (elem0 + (size_t)row * sl.row_elems) * 2;
       const float mul = kDV ? 1.f : p.scale;
 #pragma unroll 1
       for (int cc = 0; cc < C::D / 32; ++cc) {
@@ -494,14 +504,16 @@ __global__ void __launch_bounds__(192, 1)
 
 // One pass of the kernel above: a1 the resident 128-row tile, x/y the streamed 64-row
 // blocks, a2_rows the tensor whose rows go to tensor memory (dO for dQ, V for dK); one CTA
-// per 128 rows (queries for dQ, keys for dK and dV) of each slice.
+// per 128 rows (queries for dQ, keys for dK and dV) of each slice (packed batches: of the
+// longest sequence, the tiles past a shorter one's end returning at once).
 template <int MODE, bool BF16>
 static cudaError_t launch_bwd_wide(const CUtensorMap& a1, const CUtensorMap& x,
                                    const CUtensorMap& y, const void* a2_rows, const Shape& s,
                                    const float* lse, const float* delta, void* out0,
                                    void* out1, cudaStream_t st) {
   using C = BwdWCfg<MODE>;
-  auto kern = attn_bwd_wide_kernel<MODE, BF16>;
+  auto kern = s.vl.cu_q != nullptr ? attn_bwd_wide_kernel<MODE, BF16, true>
+                                   : attn_bwd_wide_kernel<MODE, BF16, false>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -520,7 +532,7 @@ static cudaError_t launch_bwd_wide(const CUtensorMap& a1, const CUtensorMap& x,
   p.scale_log2 = s.scale * kLog2e;
   p.wait_limit = s.wait_limit;
   p.vl = s.vl;
-  const int rows = MODE == kWideDQ ? s.N : s.Nk;
+  const int rows = MODE == kWideDQ ? s.N : s.Nk;  // packed: the longest sequence
   dim3 grid((rows + kTileM - 1) / kTileM, s.BH);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(a1, x, y, p);
   return cudaGetLastError();

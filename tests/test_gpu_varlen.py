@@ -27,6 +27,11 @@ CASES = [
     (3, 64, "bf16", True, (1000,), None),                         # one sequence
     (2, 64, "bf16", False, (1100, 40, 700), None),  # long enough for K, V in tensor memory
     (2, 96, "bf16", True, (300, 129, 64), (310, 200, 64)),  # a head dim of 96
+    # head dims above 128: the 256-column kernels
+    (2, 256, "bf16", True, (1, 130, 257, 64, 700), None),
+    (1, 192, "fp16", True, (129, 128, 383), (400, 128, 1000)),
+    (2, 256, "bf16", True, (0, 77, 0, 256), (0, 77, 40, 300)),   # keys without queries
+    (2, 256, "fp16", False, (200, 64, 1), (90, 300, 5)),
 ]
 
 
@@ -82,7 +87,7 @@ def test_packed_matches_oracle(case):
                     assert rel_fro(dvg[k0:k1, h], ref["dv"][k0:k1, h]) <= GRAD_TOL, where
 
 
-@pytest.mark.parametrize("d,causal", [(128, True), (64, False)])
+@pytest.mark.parametrize("d,causal", [(128, True), (64, False), (256, True), (200, False)])
 def test_equal_lengths_equal_the_dense_call_bit_for_bit(d, causal):
     """B sequences of one length N, packed, give exactly the bits of attn_fwd/attn_bwd on
     the [B, H, N, d] tensors (the same tiles in the same order)."""
