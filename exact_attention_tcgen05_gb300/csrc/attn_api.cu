@@ -35,10 +35,10 @@ Range range_of(const void* p, size_t bytes) {
 bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
 
 // Head dimensions the attention kernels take: multiples of 8 (16-byte rows for TMA) up to
-// 256 for the forward and backward of dense and packed tensors, up to 128 for the
-// host-buffer step; d <= 64 runs on the 64-column kernels, d <= 128 on the 128-column ones,
-// d > 128 on the 256-column ones, with the columns past d read as zero.
-constexpr int kMaxD = 128, kMaxDAttn = 256;
+// 256; d <= 64 runs on the 64-column kernels, d <= 128 on the 128-column ones, d > 128 on
+// the 256-column ones, with the columns past d read as zero. (Split-KV decoding checks
+// its own widths.)
+constexpr int kMaxD = 256;
 bool head_dim_ok(int d, int max_d = kMaxD) { return d >= 8 && d <= max_d && d % 8 == 0; }
 
 attn_status check_shape(int B, int H, int N, int d, attn_dtype dtype, int max_d = kMaxD) {
@@ -183,9 +183,9 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N) {
 attn_status attn_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse,
                         int B, int H, int Nq, int Nk, int d, attn_dtype dtype, int causal,
                         float scale, void* cuda_stream) {
-  attn_status st = check_shape(B, H, Nq, d, dtype, kMaxDAttn);
+  attn_status st = check_shape(B, H, Nq, d, dtype);
   if (st != ATTN_OK) return st;
-  if ((st = check_shape(B, H, Nk, d, dtype, kMaxDAttn)) != ATTN_OK) return st;
+  if ((st = check_shape(B, H, Nk, d, dtype)) != ATTN_OK) return st;
   if (causal && Nk < Nq) return ATTN_ERR_INVALID_ARG;  // rows would see no key
   if ((st = check_scale(scale)) != ATTN_OK) return st;
   const void* ptrs[5] = {q, k, v, o, lse};
@@ -223,7 +223,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
 
 attn_status attn_bwd_preprocess(const void* o, const void* dO, float* delta, int B, int H,
                                 int N, int d, attn_dtype dtype, void* cuda_stream) {
-  attn_status st = check_shape(B, H, N, d, dtype, kMaxDAttn);
+  attn_status st = check_shape(B, H, N, d, dtype);
   if (st != ATTN_OK) return st;
   const void* ptrs[3] = {o, dO, delta};
   for (const void* p : ptrs)
@@ -298,7 +298,7 @@ attn_status attn_bwd_dkv(const void* q, const void* k, const void* v, const floa
                          const float* delta, const void* dO, void* dk, void* dv, int B, int H,
                          int N, int d, attn_dtype dtype, int causal, float scale,
                          void* cuda_stream) {
-  attn_status st = check_shape(B, H, N, d, dtype, kMaxDAttn);
+  attn_status st = check_shape(B, H, N, d, dtype);
   if (st != ATTN_OK) return st;
   if ((st = check_scale(scale)) != ATTN_OK) return st;
   if ((st = check_ptrs({q, k, v, lse, delta, dO, dk, dv})) != ATTN_OK) return st;
@@ -318,7 +318,7 @@ attn_status attn_bwd_dkv(const void* q, const void* k, const void* v, const floa
 attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const float* lse,
                         const float* delta, const void* dO, void* dq, int B, int H, int N,
                         int d, attn_dtype dtype, int causal, float scale, void* cuda_stream) {
-  attn_status st = check_shape(B, H, N, d, dtype, kMaxDAttn);
+  attn_status st = check_shape(B, H, N, d, dtype);
   if (st != ATTN_OK) return st;
   if ((st = check_scale(scale)) != ATTN_OK) return st;
   if ((st = check_ptrs({q, k, v, lse, delta, dO, dq})) != ATTN_OK) return st;
@@ -339,9 +339,9 @@ attn_status attn_bwd_qk(const void* q, const void* k, const void* v, const void*
                         const float* lse, const void* dO, void* dq, void* dk, void* dv,
                         void* workspace, int B, int H, int Nq, int Nk, int d,
                         attn_dtype dtype, int causal, float scale, void* cuda_stream) {
-  attn_status st = check_shape(B, H, Nq, d, dtype, kMaxDAttn);
+  attn_status st = check_shape(B, H, Nq, d, dtype);
   if (st != ATTN_OK) return st;
-  if ((st = check_shape(B, H, Nk, d, dtype, kMaxDAttn)) != ATTN_OK) return st;
+  if ((st = check_shape(B, H, Nk, d, dtype)) != ATTN_OK) return st;
   if (causal && Nk < Nq) return ATTN_ERR_INVALID_ARG;
   if ((st = check_scale(scale)) != ATTN_OK) return st;
   if ((st = check_ptrs({q, k, v, o, lse, dO, dq, dk, dv, workspace})) != ATTN_OK) return st;
@@ -389,7 +389,7 @@ attn_status check_varlen(int B, int H, int total_q, int total_k, int max_q, int 
   if (cu_q == nullptr || cu_k == nullptr) return ATTN_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(cu_q) | reinterpret_cast<uintptr_t>(cu_k)) & 3u)
     return ATTN_ERR_INVALID_ARG;
-  if (!head_dim_ok(d, kMaxDAttn)) return ATTN_ERR_UNSUPPORTED;
+  if (!head_dim_ok(d)) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
 }
 

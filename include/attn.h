@@ -19,14 +19,12 @@
  *            lse and the backward workspace are contiguous [B, H, N] float32.
  *            Every pointer is a DEVICE pointer, 16-byte aligned.
  *   Sizes    B >= 1, H >= 1, 1 <= N <= 1048576, B*H <= 65535; d a multiple of 8 from 8
- *            to 256 for the forward and backward entry points (dense, N_q != N_k,
- *            packed, no-alloc and the backward stages), from 8 to 128 for
- *            attn_step_host, and 64 or 128 for split-KV decoding. The kernels are 64, 128 or 256 columns wide: a smaller
- *            d runs on the next width with the missing columns read as zero (exact: they
- *            add zeros to every product) and never written, so d = 96 costs what d = 128
- *            costs. The 256-column kernels take 128 query rows and 64-key blocks per step
- *            and run the dK/dV stage as two passes (dV, then dK), since the two
- *            accumulators do not fit in tensor memory together.
+ *            to 256 (split-KV decoding: d in {64, 128}). The kernels are 64, 128 or 256
+ *            columns wide: a smaller d runs on the next width with the missing columns
+ *            read as zero (exact: they add zeros to every product) and never written, so
+ *            d = 96 costs what d = 128 costs. The 256-column kernels take 128 query rows
+ *            and 64-key blocks per step and run the dK/dV stage as two passes (dV, then
+ *            dK), since the two accumulators do not fit in tensor memory together.
  *   Mask     causal != 0 masks key j for query i when j > i (top-left aligned,
  *            N_q = N_k, diagonal kept), so no row is ever fully masked.
  *   scale    the factor applied to Q K^T; finite and > 0 (the usual value is

@@ -207,7 +207,9 @@ def test_decode_rejects_bad_arguments(lib, kw, code):
 def test_step_host_rejects_bad_arguments(lib):
     need = lib.attn_step_host_scratch_bytes(1, 2, 256, 128, 2)
     assert need > 0 and lib.attn_step_host_scratch_bytes(1, 2, 256, 100, 2) == 0
-    assert lib.attn_step_host_scratch_bytes(1, 2, 256, 96, 2) > 0  # any multiple of 8 <= 128
+    assert lib.attn_step_host_scratch_bytes(1, 2, 256, 96, 2) > 0  # any multiple of 8 <= 256
+    assert lib.attn_step_host_scratch_bytes(1, 2, 256, 256, 2) > 0
+    assert lib.attn_step_host_scratch_bytes(1, 2, 256, 264, 2) == 0
 
     def call(scratch=WS, nbytes=need, chunks=2, d=128, scale=0.1, q=Q):
         return lib.attn_step_host(q, K, V, DO, O, L, DQ, DK, DV, scratch, nbytes, 1, 2, 256, d,

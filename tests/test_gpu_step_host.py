@@ -15,6 +15,7 @@ pytestmark = pytest.mark.gpu
     (1, 2, 256, 64, "fp16", False, 1),
     (2, 2, 513, 128, "bf16", False, 3),
     (1, 3, 128, 64, "bf16", True, 9),   # more chunks than slices (clamped)
+    (1, 3, 300, 256, "bf16", True, 2),  # the 256-column kernels
 ])
 def test_step_host_matches_device_path(B, H, N, d, dtype, causal, chunks):
     w = I.custom(B, H, N, d, dtype, causal, seed=N + chunks)
