@@ -36,8 +36,8 @@ bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
 
 // Head dimensions the attention kernels take: multiples of 8 (16-byte rows for TMA) up to
 // 256; d <= 64 runs on the 64-column kernels, d <= 128 on the 128-column ones, d > 128 on
-// the 256-column ones, with the columns past d read as zero. (Split-KV decoding checks
-// its own widths.)
+// the 256-column ones, with the columns past d read as zero. (Split-KV decoding takes
+// exactly 64, 128 or 256.)
 constexpr int kMaxD = 256;
 bool head_dim_ok(int d, int max_d = kMaxD) { return d >= 8 && d <= max_d && d % 8 == 0; }
 
@@ -731,7 +731,7 @@ constexpr int kMaxSplits = 65535;  // grid.x of the partial kernel
 attn_status check_decode(int B, int H, int Nk, int d, attn_dtype dtype, int splits) {
   attn_status st = check_shape(B, H, Nk, d, dtype);
   if (st != ATTN_OK) return st;
-  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;  // the decode kernels' widths
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;  // the kernels' widths
   if (splits < 1 || splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
@@ -751,7 +751,7 @@ attn::DecodeShape make_decode_shape(int B, int H, int Nk, int d, attn_dtype dtyp
 }  // namespace
 
 size_t attn_decode_workspace_bytes(int B, int H, int d, int num_splits) {
-  if (B <= 0 || H <= 0 || num_splits <= 0 || (d != 64 && d != 128)) return 0;
+  if (B <= 0 || H <= 0 || num_splits <= 0 || (d != 64 && d != 128 && d != 256)) return 0;
   return (size_t)4 * (size_t)B * (size_t)H * (size_t)num_splits * (size_t)(d + 4);
 }
 

@@ -18,8 +18,8 @@
 //    so several tens of KiB per SM are in flight without holding registers. Per
 //    sub-block: each warp forms eight scores (a lane multiplies D/32 elements, a
 //    butterfly of shuffles sums them), warp 0 updates the running max / sum and writes
-//    the exp2 weights, and every thread accumulates two output columns over a quarter
-//    (D = 128) or an eighth (D = 64) of the sub-block's keys. exp is exp2 with
+//    the exp2 weights, and every thread accumulates two output columns over a half
+//    (D = 256), a quarter (D = 128) or an eighth (D = 64) of the sub-block's keys. exp is exp2 with
 //    scale·log2(e) folded into the score ("Triton 05: Flash Attention", section
 //    2. exp -> exp2 트릭). The record written per split is (O~ [D], m, l) in fp32, m in
 //    natural-log units.
@@ -49,9 +49,10 @@ struct DecodeParams {
 
 template <int D>
 struct DecodeCfg {
-  // 64 KiB of stages (two sub-blocks of K and V at d = 128, four at d = 64): three CTAs
-  // fit on an SM, about 190 KiB of copies in flight per SM.
-  static constexpr int kStages = (D == 128) ? 2 : 4;
+  // 64 KiB of stages (one sub-block of K and V at d = 256, two at d = 128, four at d = 64):
+  // three CTAs fit on an SM, about 190 KiB of copies in flight per SM.
+  static constexpr int kStages = 64 * 1024 / (2 * kDecodeSub * D * 2);
+  static_assert(kStages >= 1, "one stage at least");
   static constexpr int kSubBytes = kDecodeSub * D * 2;  // one K (or V) sub-block
   static constexpr int kStageBytes = 2 * kSubBytes;     // K then V
   static constexpr int kOffScores = kStages * kStageBytes;           // float[64]
@@ -125,7 +126,13 @@ __global__ void __launch_bounds__(kDecodeThreads)
   float qv[kPerLane];
   {
     const uint8_t* qrow = reinterpret_cast<const uint8_t*>(p.q) + (size_t)bh * (D * 2);
-    if constexpr (kPerLane == 4) {
+    if constexpr (kPerLane == 8) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(qrow + lane * 16);
+      const float2 a = unpack2<BF16>(raw.x), b = unpack2<BF16>(raw.y);
+      const float2 c = unpack2<BF16>(raw.z), e = unpack2<BF16>(raw.w);
+      qv[0] = a.x; qv[1] = a.y; qv[2] = b.x; qv[3] = b.y;
+      qv[4] = c.x; qv[5] = c.y; qv[6] = e.x; qv[7] = e.y;
+    } else if constexpr (kPerLane == 4) {
       const uint2 raw = *reinterpret_cast<const uint2*>(qrow + lane * 8);
       const float2 a = unpack2<BF16>(raw.x), b = unpack2<BF16>(raw.y);
       qv[0] = a.x; qv[1] = a.y; qv[2] = b.x; qv[3] = b.y;
@@ -154,7 +161,13 @@ __global__ void __launch_bounds__(kDecodeThreads)
       const int key = warp + 8 * kk;
       float dot = 0.f;
       if (ok && key < nvalid) {
-        if constexpr (kPerLane == 4) {
+        if constexpr (kPerLane == 8) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(kst + key * (D * 2) + lane * 16);
+          const float2 a = unpack2<BF16>(raw.x), b = unpack2<BF16>(raw.y);
+          const float2 c = unpack2<BF16>(raw.z), e = unpack2<BF16>(raw.w);
+          dot = qv[0] * a.x + qv[1] * a.y + qv[2] * b.x + qv[3] * b.y + qv[4] * c.x +
+                qv[5] * c.y + qv[6] * e.x + qv[7] * e.y;
+        } else if constexpr (kPerLane == 4) {
           const uint2 raw = *reinterpret_cast<const uint2*>(kst + key * (D * 2) + lane * 8);
           const float2 a = unpack2<BF16>(raw.x), b = unpack2<BF16>(raw.y);
           dot = qv[0] * a.x + qv[1] * a.y + qv[2] * b.x + qv[3] * b.y;
@@ -255,7 +268,18 @@ __global__ void __launch_bounds__(256) attn_decode_merge_kernel(const float* par
     if (ms == -INFINITY) continue;  // empty split: the neutral state
     const float w = ex2((ms - m) * kLog2e);  // e^(m_s - m)
     l = fmaf(w, rec[D + 1], l);
-    if constexpr (kCols == 4) {
+    if constexpr (kCols == 8) {
+      const float4 x = *reinterpret_cast<const float4*>(rec + lane * 8);
+      const float4 y = *reinterpret_cast<const float4*>(rec + lane * 8 + 4);
+      u[0] = fmaf(w, x.x, u[0]);
+      u[1] = fmaf(w, x.y, u[1]);
+      u[2] = fmaf(w, x.z, u[2]);
+      u[3] = fmaf(w, x.w, u[3]);
+      u[4] = fmaf(w, y.x, u[4]);
+      u[5] = fmaf(w, y.y, u[5]);
+      u[6] = fmaf(w, y.z, u[6]);
+      u[7] = fmaf(w, y.w, u[7]);
+    } else if constexpr (kCols == 4) {
       const float4 x = *reinterpret_cast<const float4*>(rec + lane * 4);
       u[0] = fmaf(w, x.x, u[0]);
       u[1] = fmaf(w, x.y, u[1]);
@@ -269,7 +293,11 @@ __global__ void __launch_bounds__(256) attn_decode_merge_kernel(const float* par
   }
   const float inv = 1.f / l;
   uint8_t* orow = reinterpret_cast<uint8_t*>(o) + (size_t)bh * (D * 2);
-  if constexpr (kCols == 4) {
+  if constexpr (kCols == 8) {
+    *reinterpret_cast<uint4*>(orow + lane * 16) =
+        make_uint4(pack2<BF16>(u[0] * inv, u[1] * inv), pack2<BF16>(u[2] * inv, u[3] * inv),
+                   pack2<BF16>(u[4] * inv, u[5] * inv), pack2<BF16>(u[6] * inv, u[7] * inv));
+  } else if constexpr (kCols == 4) {
     *reinterpret_cast<uint2*>(orow + lane * 8) =
         make_uint2(pack2<BF16>(u[0] * inv, u[1] * inv), pack2<BF16>(u[2] * inv, u[3] * inv));
   } else {

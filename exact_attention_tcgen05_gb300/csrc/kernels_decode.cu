@@ -7,6 +7,7 @@ namespace attn {
 static_assert(kDecodeCtasPerSm == kDecodeCtasPerSmPublic, "one value for the split heuristic");
 static_assert(3 * (DecodeCfg<128>::kSmemBytes + 1024) <= 228 * 1024, "three CTAs per SM");
 static_assert(3 * (DecodeCfg<64>::kSmemBytes + 1024) <= 228 * 1024, "three CTAs per SM");
+static_assert(3 * (DecodeCfg<256>::kSmemBytes + 1024) <= 228 * 1024, "three CTAs per SM");
 
 int decode_chunk(int Nk, int splits) {
   const int per = (Nk + splits - 1) / splits;
@@ -46,6 +47,8 @@ static cudaError_t launch_decode_merge_t(const DecodeShape& s, const float* part
 
 cudaError_t launch_decode_partial(const DecodeShape& s, const void* q, const void* k,
                                   const void* v, float* partials, cudaStream_t st) {
+  if (s.d == 256) return s.bf16 ? launch_decode_partial_t<256, true>(s, q, k, v, partials, st)
+                                : launch_decode_partial_t<256, false>(s, q, k, v, partials, st);
   if (s.d == 128) return s.bf16 ? launch_decode_partial_t<128, true>(s, q, k, v, partials, st)
                                 : launch_decode_partial_t<128, false>(s, q, k, v, partials, st);
   return s.bf16 ? launch_decode_partial_t<64, true>(s, q, k, v, partials, st)
@@ -54,6 +57,8 @@ cudaError_t launch_decode_partial(const DecodeShape& s, const void* q, const voi
 
 cudaError_t launch_decode_merge(const DecodeShape& s, const float* partials, void* o,
                                 float* lse, cudaStream_t st) {
+  if (s.d == 256) return s.bf16 ? launch_decode_merge_t<256, true>(s, partials, o, lse, st)
+                                : launch_decode_merge_t<256, false>(s, partials, o, lse, st);
   if (s.d == 128) return s.bf16 ? launch_decode_merge_t<128, true>(s, partials, o, lse, st)
                                 : launch_decode_merge_t<128, false>(s, partials, o, lse, st);
   return s.bf16 ? launch_decode_merge_t<64, true>(s, partials, o, lse, st)

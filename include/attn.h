@@ -19,7 +19,7 @@
  *            lse and the backward workspace are contiguous [B, H, N] float32.
  *            Every pointer is a DEVICE pointer, 16-byte aligned.
  *   Sizes    B >= 1, H >= 1, 1 <= N <= 1048576, B*H <= 65535; d a multiple of 8 from 8
- *            to 256 (split-KV decoding: d in {64, 128}). The kernels are 64, 128 or 256
+ *            to 256 (split-KV decoding: d in {64, 128, 256}). The kernels are 64, 128 or 256
  *            columns wide: a smaller d runs on the next width with the missing columns
  *            read as zero (exact: they add zeros to every product) and never written, so
  *            d = 96 costs what d = 128 costs. The 256-column kernels take 128 query rows

@@ -70,6 +70,10 @@ CASES = [
     (2, 2, 1000, 64, "bf16", 7),
     (1, 2, 4113, 128, "bf16", 16),  # ragged last sub-block, several sub-blocks per split
     (1, 1, 3000, 128, "fp16", 1),   # one split over many sub-blocks (ring reuse)
+    (1, 2, 1, 256, "bf16", 1),      # d = 256: one stage of one sub-block
+    (2, 1, 64, 256, "fp16", 3),
+    (1, 2, 4113, 256, "bf16", 16),
+    (1, 1, 3000, 256, "fp16", 1),
 ]
 
 
