@@ -24,6 +24,7 @@
 #pragma once
 
 #include "fwd.cuh"
+#include "fwd_persistent.cuh"
 
 namespace attn {
 
@@ -353,6 +354,403 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       if (row < N) p.lse[sl.stat0 + row] = (m + log2f(l)) * kLn2;
+    }
+    tc_fence_before();
+  }
+
+  tmem_st_wait();  // no tensor-memory store in flight when memory is released
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// The same forward as a persistent kernel: one CTA per SM walks a list of items (128 query
+// rows of one (b, h) slice each), so the fixed cost of a CTA (launch, barriers, tensor
+// memory, the first copies, the last products, the epilogue) is paid once per SM instead of
+// once per tile. The K and V rings, the two S buffers and every barrier phase run on across
+// items (running counts kept alike by all roles); each item's first two K blocks are copied
+// before its Q, which waits for the previous item's last S product; the first P V of an
+// item waits until the previous item's epilogue has read O (o_free). The arithmetic of
+// every item is that of the kernel above: the outputs are bit-identical.
+
+struct FwdWPCfg : FwdWCfg {
+  // the barriers of the one-tile kernel, then q_empty and o_free
+  static constexpr int kNumBarsP = kNumBars + 2;
+  static constexpr int kOffMiscP = kOffBar + kNumBarsP * 8;
+  static constexpr int kSmemBytesP = kOffMiscP + 16 + 1024;
+  static_assert(kSmemBytesP <= 227 * 1024, "shared memory");
+};
+
+// One work item of the persistent kernel.
+struct FwdWItem {
+  SliceRows sl;
+  int N, Nk, off;
+  int q0;   // first query row of the tile within its slice
+  int n;    // key blocks (64 keys each) the tile sees
+};
+
+// Geometry of item `item` (nqb_max tiles per slice, longest first within a slice). False:
+// nothing to do (a tile past its sequence's end, or a malformed sequence).
+template <bool PACKED>
+__device__ __forceinline__ bool fwd_wide_item_geom(const FwdParams& p, int item, int nqb_max,
+                                                   FwdWItem& it) {
+  const int bh = item / nqb_max;
+  const int x = item - bh * nqb_max;
+  if (!slice_rows<PACKED>(p.vl, bh, p.N, p.Nk, p.dh, p.causal != 0, it.sl)) return false;
+  it.N = it.sl.nq;
+  it.Nk = it.sl.nk;
+  it.off = it.sl.off;
+  const int nqb = (it.N + kTileM - 1) / kTileM;
+  if (x >= nqb) return false;
+  it.q0 = (nqb - 1 - x) * kTileM;
+  const int nkb = (it.Nk + FwdWCfg::kBN - 1) / FwdWCfg::kBN;
+  it.n = p.causal ? min(nkb, (it.q0 + kTileM - 1 + it.off) / FwdWCfg::kBN + 1) : nkb;
+  return it.n > 0;
+}
+
+template <bool BF16, bool PACKED, class Sched>
+__global__ void __launch_bounds__(192, 1)
+    attn_fwd_wide_persistent_kernel(const __grid_constant__ CUtensorMap map_q,
+                                    const __grid_constant__ CUtensorMap map_k64,
+                                    const __grid_constant__ CUtensorMap map_v64,
+                                    const FwdParams p, int n_items, int nqb_max,
+                                    const __grid_constant__ Sched sched) {
+  using C = FwdWPCfg;
+  constexpr int NK = C::kKStages, NV = C::kVStages;
+  constexpr int kBN = C::kBN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + NK;
+  uint64_t* v_full = k_empty + NK;
+  uint64_t* v_empty = v_full + NV;
+  uint64_t* s_full = v_empty + NV;  // [2] per S buffer
+  uint64_t* p_full = s_full + 2;    // [2] per S buffer
+  uint64_t* o_done = p_full + 2;    // every P V
+  uint64_t* o_last = o_done + 1;    // the last P V of an item
+  uint64_t* drain = o_last + 1;
+  uint64_t* q_empty = drain + 1;    // every S of the item is done: Q may be replaced
+  uint64_t* o_free = q_empty + 1;   // the epilogue has read O
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMiscP);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMiscP + 4);
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+  const int G = gridDim.x, cta = blockIdx.x;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&p_full[b], 4);
+    }
+    mbar_init(o_done, 1);
+    mbar_init(o_last, 1);
+    mbar_init(drain, 1);
+    mbar_init(q_empty, 1);
+    mbar_init(o_free, 4);  // one arrival per softmax warp
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_holder, C::kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint64_t limit = p.wait_limit;
+
+  if (warp == 4) {
+    // ------------------------------ TMA producer ------------------------------
+    if (elect_one()) {
+      tma_prefetch_map(&map_q);
+      tma_prefetch_map(&map_k64);
+      tma_prefetch_map(&map_v64);
+    }
+    __syncwarp();
+    // Running counts of the copies issued: K and V blocks (one count per block of every
+    // item, in item order), Q tiles.
+    int k_issued = 0, v_issued = 0, q_loads = 0;
+    bool ok = true;
+    auto load_k = [&](const FwdWItem& it, int gb, int j) -> bool {
+      const int s = gb % NK;
+      if (gb >= NK &&
+          !warp_wait(&k_empty[s], ((gb / NK) - 1) & 1, limit, abort_flag, kWaitFwdEmpty))
+        return false;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(&k_full[s], C::kKVBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_rows<PACKED>(smem + C::kOffK + s * C::kKVBytes + c * C::kKVBox, &map_k64,
+                                &k_full[s], c * kBoxCols, j * kBN, it.sl, true);
+      }
+      __syncwarp();
+      k_issued = gb + 1;
+      return true;
+    };
+    auto load_v = [&](const FwdWItem& it, int gb, int j) -> bool {
+      const int s = gb % NV;
+      if (gb >= NV &&
+          !warp_wait(&v_empty[s], ((gb / NV) - 1) & 1, limit, abort_flag, kWaitFwdEmpty))
+        return false;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(&v_full[s], C::kKVBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_rows<PACKED>(smem + C::kOffV + s * C::kKVBytes + c * C::kKVBox, &map_v64,
+                                &v_full[s], c * kBoxCols, j * kBN, it.sl, true);
+      }
+      __syncwarp();
+      v_issued = gb + 1;
+      return true;
+    };
+    for (int k = 0; ok; ++k) {
+      const int item = fwd_sched_item(sched, k, G, cta, n_items);
+      if (item < 0) break;
+      FwdWItem it;
+      if (!fwd_wide_item_geom<PACKED>(p, item, nqb_max, it)) continue;
+      const int gb0 = v_issued;  // global index of the item's first block
+      constexpr int kLead = NK - 1;
+      for (int j = 0; ok && j < min(kLead, it.n); ++j) ok = load_k(it, gb0 + j, j);
+      if (!ok) break;
+      // The previous item's S products must be done with Q (q_empty completes once per
+      // item after its last S; its next completion needs the Q copied below).
+      if (q_loads > 0 &&
+          !(ok = warp_wait(q_empty, (q_loads - 1) & 1, limit, abort_flag, kWaitFwdQEmpty)))
+        break;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(q_full, C::kQBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_rows<PACKED>(smem + C::kOffQ + c * kBoxBytes, &map_q, q_full, c * kBoxCols,
+                                it.q0, it.sl, false);
+      }
+      __syncwarp();
+      ++q_loads;
+      for (int j = 0; ok && j < it.n; ++j) {
+        if (j + kLead < it.n) ok = load_k(it, gb0 + j + kLead, j + kLead);
+        if (ok) ok = load_v(it, gb0 + j, j);
+      }
+    }
+    if (*abort_flag) {
+      // Let every copy this CTA started land before its shared memory is released.
+      if (q_loads > 0) mbar_wait(q_full, (q_loads - 1) & 1, kDrainLimit, nullptr, kWaitFwdDrain);
+      for (int b = max(0, k_issued - NK); b < k_issued; ++b)
+        mbar_wait(&k_full[b % NK], (b / NK) & 1, kDrainLimit, nullptr, kWaitFwdDrain);
+      for (int b = max(0, v_issued - NV); b < v_issued; ++b)
+        mbar_wait(&v_full[b % NV], (b / NV) & 1, kDrainLimit, nullptr, kWaitFwdDrain);
+    }
+  } else if (warp == 5) {
+    // ------------------------------ MMA issuer --------------------------------
+    const uint32_t idesc_s = make_idesc(BF16, 128, kBN, false, false);
+    const uint32_t idesc_o = make_idesc(BF16, 128, C::D, false, true);
+    const uint64_t dq0 = make_sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
+    const uint64_t dk0 = make_sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
+    const uint64_t dv0 = make_sdesc_sw128(smem_u32(smem + C::kOffV), C::kKVBox, 1024);
+    constexpr uint32_t kStep = C::kKVBytes >> 4;
+    // S(b) into buffer b & 1 (its previous contents, P(b - 2), were read by P V(b - 2),
+    // issued before: the tensor core runs them in order)
+    auto issue_s = [&](int b) -> bool {
+      if (!warp_poll(&k_full[b % NK], (b / NK) & 1, limit, abort_flag, kWaitFwdK)) return false;
+      tc_fence_after();
+      if (elect_one()) {
+        issue_rowdot_wide(tmem + C::kColS + (b & 1) * 64, dq0, dk0 + (b % NK) * kStep, idesc_s);
+        mma_commit(&s_full[b & 1]);
+        mma_commit(&k_empty[b % NK]);
+      }
+      __syncwarp();
+      return true;
+    };
+    int gb = 0, items = 0;  // running counts: blocks and items
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int item = fwd_sched_item(sched, k, G, cta, n_items);
+      if (item < 0) break;
+      FwdWItem it;
+      if (!fwd_wide_item_geom<PACKED>(p, item, nqb_max, it)) continue;
+      const int n = it.n;
+      if (!(ok = warp_poll(q_full, items & 1, limit, abort_flag, kWaitFwdQ))) break;
+      if (!(ok = issue_s(gb))) break;
+      if (n == 1) {
+        if (elect_one()) mma_commit(q_empty);  // every S of the item issued
+        __syncwarp();
+      }
+      for (int j = 0; ok && j < n; ++j) {
+        const int b = gb + j;
+        if (j + 1 < n) {
+          if (!(ok = issue_s(b + 1))) break;
+          if (j + 2 == n) {
+            if (elect_one()) mma_commit(q_empty);
+            __syncwarp();
+          }
+        }
+        if (!(ok = warp_poll(&v_full[b % NV], (b / NV) & 1, limit, abort_flag, kWaitFwdV)))
+          break;
+        if (!(ok = warp_poll(&p_full[b & 1], (b >> 1) & 1, limit, abort_flag, kWaitFwdP)))
+          break;
+        // The item's first P V overwrites O: the previous item's epilogue must have read it
+        // (o_free: one completion per item, each after an o_last that follows this wait).
+        if (j == 0 && items > 0 &&
+            !(ok = warp_poll(o_free, (items - 1) & 1, limit, abort_flag, kWaitFwdOFree)))
+          break;
+        tc_fence_after();
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts(tmem + C::kColO, tmem + C::kColS + (b & 1) * 64 + kk * 8,
+                   dv0 + (b % NV) * kStep + ((kk * 2048) >> 4), idesc_o,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(o_done);
+          mma_commit(&v_empty[b % NV]);
+          if (j == n - 1) mma_commit(o_last);
+        }
+        __syncwarp();
+      }
+      gb += n;
+      ++items;
+    }
+    // Every MMA issued must finish before tensor memory is released.
+    if (elect_one()) mma_commit(drain);
+    __syncwarp();
+    mbar_wait(drain, 0, kDrainLimit, nullptr, kWaitFwdDrain);
+  } else {
+    // ------------------------------ softmax -----------------------------------
+    const int wq = warp;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t t_o = tmem + lane_base + C::kColO;
+    const float sl2 = p.scale_log2;
+    auto rescale_o = [&](float alpha) {
+#pragma unroll 1
+      for (int cc = 0; cc < C::D / 64; ++cc) {
+        uint32_t r[64];
+        tmem_ld64(t_o + cc * 64, r);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+        tmem_st32(t_o + cc * 64, *reinterpret_cast<const uint32_t(*)[32]>(&r[0]));
+        tmem_st32(t_o + cc * 64 + 32, *reinterpret_cast<const uint32_t(*)[32]>(&r[32]));
+      }
+    };
+    int gb = 0, items = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int item = fwd_sched_item(sched, k, G, cta, n_items);
+      if (item < 0) break;
+      FwdWItem it;
+      if (!fwd_wide_item_geom<PACKED>(p, item, nqb_max, it)) continue;
+      const int row = it.q0 + wq * 32 + lane;  // query index of this thread
+      float m = -INFINITY, l = 0.f, lr = 0.f;
+      for (int j = 0; j < it.n; ++j) {
+        const int b = gb + j;
+        const uint32_t t_s = tmem + lane_base + C::kColS + (b & 1) * 64;
+        if (!(ok = warp_wait(&s_full[b & 1], (b >> 1) & 1, limit, abort_flag, kWaitFwdS)))
+          break;
+        tc_fence_after();
+        uint32_t sr[kBN];
+        tmem_ld64(t_s, sr);
+        float* s = reinterpret_cast<float*>(sr);
+        const int kbase = j * kBN;
+        const bool diag = p.causal && (kbase + kBN - 1 > it.q0 + it.off);
+        if (diag || kbase + kBN > it.Nk) {
+          int lim = it.Nk - 1 - kbase;
+          if (p.causal) lim = min(lim, row + it.off - kbase);
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            if (c > lim) s[c] = -INFINITY;
+        }
+        float mx[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) mx[u] = fmaxf(s[2 * u], s[2 * u + 1]);
+#pragma unroll
+        for (int c = 8; c < kBN; c += 8) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) mx[u] = fmax3(mx[u], s[c + 2 * u], s[c + 2 * u + 1]);
+        }
+        const float m_cand = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+        const bool need = m_cand > m + 8.0f;
+        float alpha = 1.f;
+        if (need) {
+          alpha = ex2(m - m_cand);
+          m = m_cand;
+        }
+        const float2 sl2x2 = make_float2(sl2, sl2);
+        const float2 neg_m2 = make_float2(-m, -m);
+        float2 sum[4];
+        float rsum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) sum[u] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int c2 = 0; c2 < kBN / 32; ++c2) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 x =
+                fma2(make_float2(s[c2 * 32 + 2 * i], s[c2 * 32 + 2 * i + 1]), sl2x2, neg_m2);
+            const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+            sum[i & 3] = add2(sum[i & 3], pp);
+            pk[i] = pack2<BF16>(pp.x, pp.y);
+            add_pair16<BF16>(rsum[(i & 1) * 2], rsum[(i & 1) * 2 + 1], pk[i]);
+          }
+          tmem_st16(t_s + c2 * 16, pk);
+        }
+        const float2 sa = add2(add2(sum[0], sum[1]), add2(sum[2], sum[3]));
+        l = l * alpha + (sa.x + sa.y);
+        lr = lr * alpha + ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3]));
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          // o_done is at most one phase past P V(b - 1) here: S(b) was committed after
+          // P V(b - 2).
+          if (!(ok = warp_wait(o_done, (b - 1) & 1, limit, abort_flag, kWaitFwdO))) break;
+          tc_fence_after();
+          rescale_o(alpha);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        warp_arrive(&p_full[b & 1]);
+      }
+      if (!ok) break;
+      // Epilogue: O in four 64-column pieces, each normalised and stored as it is read;
+      // O is released (o_free) after the last read.
+      if (!(ok = warp_wait(o_last, items & 1, limit, abort_flag, kWaitFwdO))) break;
+      tc_fence_after();
+      const float inv_l = 1.f / lr;
+      uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
+                      (it.sl.q_elem0 + (size_t)row * it.sl.row_elems) * 2;
+#pragma unroll 1
+      for (int cc = 0; cc < C::D / 64; ++cc) {
+        uint32_t r[64];
+        tmem_ld64(t_o + cc * 64, r);
+        if (cc == C::D / 64 - 1) {
+          tc_fence_before();
+          warp_arrive(o_free);
+        }
+        if (row < it.N) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 128);
+          const int n16 = valid16(p.dh, cc * 64, 8);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              w4[i] = pack2<BF16>(__uint_as_float(r[8 * v + 2 * i]) * inv_l,
+                                  __uint_as_float(r[8 * v + 2 * i + 1]) * inv_l);
+            if (v < n16) dst[v] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
+      }
+      if (row < it.N) p.lse[it.sl.stat0 + row] = (m + log2f(l)) * kLn2;
+      gb += it.n;
+      ++items;
     }
     tc_fence_before();
   }

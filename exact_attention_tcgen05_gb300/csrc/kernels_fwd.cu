@@ -21,14 +21,22 @@ static int sm_count_fwd() {
 
 // Which forward: the persistent kernel (fwd_persistent.cuh) except at d = 64 with long
 // items (24 or more key blocks per item on average), where the one-item kernel's loop
-// measured about 5% faster and the fixed cost per item matters little. ATTN_FWD_PERSISTENT
-// = 0 / 1 forces one or the other (both give the same bits).
+// measured about 5% faster and the fixed cost per item matters little. Head dims above 128
+// (fwd_wide.cuh, 64-key blocks): the persistent kernel for items of fewer than 48 key
+// blocks on average (measured on GB300, d = 256 causal: B16 H16 N1024 0.189 -> 0.170 ms,
+// B4 H16 N4096 0.482 -> 0.466 ms), the one-tile kernel for longer ones (B4 H16 N4096 full
+// 0.833 against 0.877 ms, B1 H16 N16384 causal 1.60 against 1.67 ms).
+// ATTN_FWD_PERSISTENT = 0 / 1 forces one or the other (both give the same bits).
 static bool use_persistent_fwd(const Shape& s) {
   static const int forced = [] {
     const char* e = std::getenv("ATTN_FWD_PERSISTENT");
     return e == nullptr ? -1 : (e[0] == '0' ? 0 : 1);
   }();
   if (forced >= 0) return forced == 1;
+  if (s.d > 128) {
+    const int nkb64 = (s.Nk + 63) / 64;
+    return (s.causal ? (nkb64 + 1) / 2 : nkb64) < 48;
+  }
   const int nkb = (s.Nk + kTileN - 1) / kTileN;
   const int blocks_per_item = s.causal ? (nkb + 1) / 2 : nkb;
   return !(s.d <= 64 && blocks_per_item >= 24);
@@ -225,16 +233,47 @@ static cudaError_t launch_fwd_t(const Maps& m, const Shape& s, void* o, float* l
   return cudaGetLastError();
 }
 
-// Head dims above 128: the 256-column forward (fwd_wide.cuh), one CTA per 128-row tile.
+// Key blocks (64 keys) tile slot `x` of a slice with nq queries and nk keys sees in the
+// 256-column forward (the geometry of fwd_wide_item_geom); 0 past the slice's end.
+static int fwd_wide_item_blocks(int nq, int nk, bool causal, int x) {
+  const int nqb = (nq + kTileM - 1) / kTileM;
+  if (x >= nqb) return 0;
+  const int nkb = (nk + FwdWCfg::kBN - 1) / FwdWCfg::kBN;
+  const int q0 = (nqb - 1 - x) * kTileM;
+  return causal ? std::min(nkb, (q0 + kTileM - 1 + nk - nq) / FwdWCfg::kBN + 1) : nkb;
+}
+
+// The persistent 256-column forward's table (schedule.h), as for the 128-column one.
+static bool fwd_wide_schedule(const Shape& s, int nqb, int G, ItemTable& out) {
+  const bool packed = s.vl.cu_q != nullptr;
+  const long long n_items = (long long)nqb * s.BH;
+  if (!item_table_applies(s.causal, packed, s.host_cu_q != nullptr, n_items, G)) return false;
+  static ItemTableCache cache;
+  const long long k[8] = {s.BH, s.N, s.Nk, s.d, G, nqb, s.causal ? 1 : 0,
+                          lengths_hash(s.host_cu_q, s.host_cu_k, s.vl_b)};
+  cache.get(k, G, n_items, out, [&](ItemTable& t) {
+    const long long kv_bytes =
+        packed ? 4LL * std::max(1, s.vl.total_k / std::max(1, s.vl_b)) * s.d : 4LL * s.Nk * s.d;
+    auto cost = [&](int bh, int x) -> long long {
+      int nq, nk;
+      slice_lengths(s, bh, nq, nk);
+      const int n = fwd_wide_item_blocks(nq, nk, s.causal, x);
+      return n > 0 ? n + 1 : 0;
+    };
+    greedy_item_table(s.BH, nqb, cost, item_table_window(s.BH, kv_bytes), G, t);
+  });
+  return true;
+}
+
+// Head dims above 128: the 256-column forward (fwd_wide.cuh): the persistent kernel, or
+// with ATTN_FWD_PERSISTENT = 0 one CTA per 128-row tile (the same bits).
 template <bool BF16>
 static cudaError_t launch_fwd_wide(const Maps& m, const Shape& s, void* o, float* lse,
                                    cudaStream_t st) {
   using C = FwdWCfg;
   auto kern = s.vl.cu_q != nullptr ? attn_fwd_wide_kernel<BF16, true>
                                    : attn_fwd_wide_kernel<BF16, false>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
   FwdParams p;
   p.o = o;
   p.lse = lse;
@@ -245,7 +284,33 @@ static cudaError_t launch_fwd_wide(const Maps& m, const Shape& s, void* o, float
   p.scale_log2 = s.scale * kLog2e;
   p.wait_limit = s.wait_limit;
   p.vl = s.vl;
-  dim3 grid((s.N + kTileM - 1) / kTileM, s.BH);
+  const int nqb_max = (s.N + kTileM - 1) / kTileM;
+  if (use_persistent_fwd(s)) {
+    using CP = FwdWPCfg;
+    const long long n_items = (long long)nqb_max * s.BH;
+    const int grid = (int)std::min<long long>(n_items, sm_count_fwd());
+    static thread_local ItemTable table;
+    if (fwd_wide_schedule(s, nqb_max, grid, table)) {
+      auto kt = s.vl.cu_q != nullptr ? attn_fwd_wide_persistent_kernel<BF16, true, ItemTable>
+                                     : attn_fwd_wide_persistent_kernel<BF16, false, ItemTable>;
+      e = cudaFuncSetAttribute(kt, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               CP::kSmemBytesP);
+      if (e != cudaSuccess) return e;
+      kt<<<grid, CP::kThreads, CP::kSmemBytesP, st>>>(m.q, m.k64, m.v64, p, (int)n_items,
+                                                      nqb_max, table);
+      return cudaGetLastError();
+    }
+    auto ks = s.vl.cu_q != nullptr ? attn_fwd_wide_persistent_kernel<BF16, true, FwdSerpentine>
+                                   : attn_fwd_wide_persistent_kernel<BF16, false, FwdSerpentine>;
+    e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, CP::kSmemBytesP);
+    if (e != cudaSuccess) return e;
+    ks<<<grid, CP::kThreads, CP::kSmemBytesP, st>>>(m.q, m.k64, m.v64, p, (int)n_items,
+                                                    nqb_max, FwdSerpentine{});
+    return cudaGetLastError();
+  }
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(nqb_max, s.BH);
   kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(m.q, m.k64, m.v64, p);
   return cudaGetLastError();
 }

@@ -1,7 +1,7 @@
 """The persistent and the one-item kernels give the same bits.
 
-The forward, dK/dV and dQ kernels each exist as a persistent kernel (one CTA per SM walking
-many work items) and as one CTA per item; which one runs depends on the shape, and
+The forward (at every head dim), dK/dV and dQ kernels each exist as a persistent kernel (one
+CTA per SM walking many work items) and as one CTA per item; which one runs depends on the shape, and
 ATTN_FWD_PERSISTENT / ATTN_BWD_PERSISTENT = 0 / 1 force either. The 128-column forward also
 exists on CTA pairs (ATTN_FWD_PAIR = 1). Both compute every tile in
 the same order with the same rounding, so O, LSE, dQ, dK and dV must agree bit for bit.
@@ -29,7 +29,10 @@ for (B, H, N, d, dt, causal) in [(2, 3, 1000, 128, "bf16", True), (1, 4, 777, 64
                                  (3, 2, 2100, 64, "bf16", True), (1, 2, 4096, 64, "bf16", False),
                                  (1, 1, 300, 128, "fp16", False),
                                  # more causal items than SMs: the forward's scheduled order
-                                 (4, 16, 1280, 128, "bf16", True), (8, 8, 1024, 64, "fp16", True)]:
+                                 (4, 16, 1280, 128, "bf16", True), (8, 8, 1024, 64, "fp16", True),
+                                 # head dims above 128: the 256-column forward
+                                 (2, 3, 1000, 256, "bf16", True), (1, 2, 777, 192, "fp16", False),
+                                 (4, 8, 1280, 256, "bf16", True)]:
     w = I.custom(B, H, N, d, dt, causal, seed=N + d)
     q, k, v, do = (I.make_tensor(w, t).cuda() for t in ("q", "k", "v", "do"))
     o, lse = binding.attn_fwd(q, k, v, causal=causal, scale=w.scale)
@@ -49,6 +52,13 @@ o, lse = binding.attn_fwd_varlen(q, k, v, cq, cq, wv.max_q, wv.max_k, causal=Tru
 dq, dk, dv = binding.attn_bwd_varlen(q, k, v, o, lse, do, cq, cq, wv.max_q, wv.max_k,
                                      causal=True)
 out["packed_d64"] = tuple(x.cpu() for x in (o, lse, dq, dk, dv))
+wv = I.varlen(2, 256, "bf16", True, seed=6, seqlens_q=(500, 1, 900, 129))
+q, k, v, do = (I.make_varlen_tensor(wv, t).cuda() for t in ("q", "k", "v", "do"))
+cq = torch.tensor(wv.cu_q, dtype=torch.int32, device="cuda")
+o, lse = binding.attn_fwd_varlen(q, k, v, cq, cq, wv.max_q, wv.max_k, causal=True)
+dq, dk, dv = binding.attn_bwd_varlen(q, k, v, o, lse, do, cq, cq, wv.max_q, wv.max_k,
+                                     causal=True)
+out["packed_d256"] = tuple(x.cpu() for x in (o, lse, dq, dk, dv))
 # N_q = 640 against N_k = 1000 (bottom-right causal), more items than SMs in every kernel:
 # the scheduled orders with an offset
 wq = I.custom(4, 40, 640, 64, "bf16", True, seed=21)
