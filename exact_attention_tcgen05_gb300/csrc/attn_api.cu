@@ -212,7 +212,7 @@ attn_status attn_fwd_qk(const void* q, const void* k, const void* v, void* o, fl
   if (d > 128 && (st = encode_map(&m.v64, v, s.BH, Nk, d, s.bf16, 64)) != ATTN_OK) return st;
   m.o = m.q;
   if (d <= 64 && (st = encode_map(&m.o, o, s.BH, Nq, d, s.bf16, 32)) != ATTN_OK) return st;
-  return from_cuda(attn::launch_fwd(m, s, o, lse, static_cast<cudaStream_t>(cuda_stream)));
+  return from_cuda(attn::launch_fwd(m, s, q, o, lse, static_cast<cudaStream_t>(cuda_stream)));
 }
 
 attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
@@ -453,7 +453,7 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
   if (d > 128 && (st = encode_map_packed(&m.v64, v, H, total_k, d, s.bf16, 64)) != ATTN_OK)
     return st;
   m.o = m.q;  // packed batches keep the row stores
-  return from_cuda(attn::launch_fwd(m, s, o, lse, static_cast<cudaStream_t>(cuda_stream)));
+  return from_cuda(attn::launch_fwd(m, s, q, o, lse, static_cast<cudaStream_t>(cuda_stream)));
 }
 
 attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,

@@ -95,30 +95,6 @@ __device__ __forceinline__ void store_row32(uint8_t* dst, const uint32_t (&r)[32
     if (v < n16) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
 }
 
-// Copies one 16-bit row of n16 16-byte pieces from global memory (zeros past them, and
-// everywhere when src is null) into tensor-memory columns [t_col, t_col + D/2) of this
-// thread's lane as packed pairs (the layout of an A operand read from tensor memory). Every
-// lane of the warp calls it (the TMEM store is warp-collective).
-template <int D>
-__device__ __forceinline__ void copy_row_to_tmem(const uint8_t* src, uint32_t t_col,
-                                                 int n16 = D / 8) {
-  // Every load of the row is issued before the first tensor-memory store (the stores are
-  // ordering points for the compiler), so the row costs one memory latency, not D / 64.
-  uint32_t r[D / 2];
-#pragma unroll
-  for (int k = 0; k < D / 8; ++k) {
-    const uint4 v = (src && k < n16) ? *reinterpret_cast<const uint4*>(src + k * 16)
-                                     : make_uint4(0, 0, 0, 0);
-    r[4 * k] = v.x;
-    r[4 * k + 1] = v.y;
-    r[4 * k + 2] = v.z;
-    r[4 * k + 3] = v.w;
-  }
-#pragma unroll
-  for (int c = 0; c < D / 64; ++c)
-    tmem_st32(t_col + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(&r[32 * c]));
-}
-
 // K-major x K-major product over the head dimension: D[128 x 128] = A[128 x d] B[128 x d]^T.
 template <int D>
 __device__ __forceinline__ void issue_rowdot(uint32_t d_tmem, uint32_t a0, uint32_t b0,

@@ -20,14 +20,19 @@
 // each rounded once to the input type as the A operand of its product.
 //
 // Roles: warps 0-3 elementwise, one row per thread (TMEM lane); warp 4 TMA producer; warp
-// 5 MMA issuer and tensor-memory owner. The first resident tile (Q_i or K_j) sits in shared
-// memory; the second (dO_i in dQ, V_j in dK) is copied by the elementwise threads, a row
-// each, into tensor memory, where it is the A operand of dP. That leaves shared memory for
-// three stages of X (the B operand of S) and two of Y (of dP; of the accumulation in dV),
-// each stage freed by its last product: X by the accumulation (dQ, dK) or by S (dV), Y by
-// dP (dQ, dK) or by the accumulation (dV). Tensor memory: S (two buffers in dV, where P
-// is written over S and nothing else needs columns), dP, the 256-column accumulator and
-// the copied tile: S(b + 1) runs while the elementwise warps finish block b.
+// 5 MMA issuer and tensor-memory owner. In dQ and dK the first resident tile (Q_i or K_j)
+// sits in shared memory and the second (dO_i, V_j) is copied by the elementwise threads, a
+// row each, into tensor memory, where it is the A operand of dP; in dV the only resident
+// tile, K_j, is copied there likewise and is the A operand of S^T. An A operand in shared
+// memory is re-read for every 16-column step, which for these 64-column products costs
+// more shared-memory bandwidth than the B operand (measured on GB300: an S step with A in
+// shared memory issues in ~56 cycles, one with A in tensor memory in ~42). Shared memory
+// holds three stages of X (the B operand of S) and two of Y (of dP; of the accumulation
+// in dV), each stage freed by its last product: X by the accumulation (dQ, dK) or by S
+// (dV), Y by dP (dQ, dK) or by the accumulation (dV). Tensor memory: S (two buffers in
+// dV, where P is written over S and nothing else needs columns), dP, the 256-column
+// accumulator and the copied tile: S(b + 1) runs while the elementwise warps finish
+// block b.
 #pragma once
 
 #include "bwd_dq.cuh"
@@ -46,7 +51,8 @@ struct BwdWCfg {
   static constexpr int kBlkBox = kBN * 128;             // [64 x 64] box: 8 KiB
   static constexpr int kBlkBytes = kChunks * kBlkBox;   // streamed 64 x 256 block: 32 KiB
   static constexpr bool kDV = MODE == kWideDV;
-  static constexpr bool kA2Tmem = !kDV;  // the second resident tile, in tensor memory
+  static constexpr bool kA2Tmem = !kDV;  // dQ, dK: the second resident tile in tensor memory
+  static constexpr bool kA1Tmem = kDV;   // dV: the resident tile in tensor memory
   static constexpr int kSBufs = kDV ? 2 : 1;  // S buffers
   // Streamed X (the B operand of S) and Y (of dP, or of the accumulating product in dV)
   static constexpr int kXStages = 3;
@@ -68,19 +74,8 @@ struct BwdWCfg {
   static constexpr uint32_t kColS = 0;     // S buffer b at 64 b (P over its first 32 in dV)
   static constexpr uint32_t kColDP = 64;   // dQ, dK: dP (dS over its first 32 columns)
   static constexpr uint32_t kColAcc = 128;
-  static constexpr uint32_t kColA2 = 384;  // dQ, dK: dO_i or V_j as 16-bit pairs
+  static constexpr uint32_t kColA2 = 384;  // the copied tile (dO_i, V_j, K_j) as 16-bit pairs
 };
-
-// D[128 x 64] = A B^T over 256 columns with A in tensor memory (16-bit pairs from column
-// a_tmem, 128 columns) and B a K-major [64 x 256] block (four 8 KiB boxes).
-__device__ __forceinline__ void issue_rowdot_ts_wide(uint32_t d_tmem, uint32_t a_tmem,
-                                                     uint64_t b_desc, uint32_t idesc) {
-#pragma unroll
-  for (int kk = 0; kk < 256 / 16; ++kk) {
-    const uint32_t b_off = ((kk >> 2) * (kBoxBytes / 2) + (kk & 3) * 32) >> 4;
-    mma_ts(d_tmem, a_tmem + kk * 8, b_desc + b_off, idesc, kk > 0 ? 1u : 0u);
-  }
-}
 
 // Maps: a1 = the resident tile in shared memory (128-row boxes), x/y = streamed blocks
 // (64-row boxes). dQ and dK read the second resident tile's rows from p.in_do / p.in_v.
@@ -189,13 +184,15 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 4) {
     // ------------------------------ TMA producer ------------------------------
     if (n > 0 && elect_one()) {
-      tma_prefetch_map(&map_a1);
       tma_prefetch_map(&map_x);
       tma_prefetch_map(&map_y);
-      mbar_arrive_expect_tx(a_full, C::kTileBytes);
-      for (int c = 0; c < C::kChunks; ++c)
-        tma_load_rows<PACKED>(smem + C::kOffA + c * kBoxBytes, &map_a1, a_full, c * kBoxCols,
-                              r0, sl, a_keys);
+      if (!C::kA1Tmem) {
+        tma_prefetch_map(&map_a1);
+        mbar_arrive_expect_tx(a_full, C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_rows<PACKED>(smem + C::kOffA + c * kBoxBytes, &map_a1, a_full, c * kBoxCols,
+                                r0, sl, a_keys);
+      }
     }
     __syncwarp();
     // X(b) into stage b % NX once the stage's previous block is released (x_empty), Y(b)
@@ -244,7 +241,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     if (*abort_flag) {
       // Let every copy this CTA started land before its shared memory is released.
-      if (n > 0) mbar_wait(a_full, 0, kDrainLimit, nullptr, kSiteDrain);
+      if (n > 0 && !C::kA1Tmem) mbar_wait(a_full, 0, kDrainLimit, nullptr, kSiteDrain);
       for (int b = max(0, x_issued - NX); b < x_issued; ++b)
         mbar_wait(&x_full[b % NX], (b / NX) & 1, kDrainLimit, nullptr, kSiteDrain);
       for (int b = max(0, y_issued - NY); b < y_issued; ++b)
@@ -279,8 +276,12 @@ __global__ void __launch_bounds__(192, 1)
       if (!warp_poll(&x_full[b % NX], (b / NX) & 1, limit, abort_flag, kSiteX)) return false;
       tc_fence_after();
       if (elect_one()) {
-        issue_rowdot_wide(tmem + C::kColS + (b % NB) * 64, da1, dx0 + (b % NX) * kStep,
-                          idesc_s);
+        if constexpr (C::kA1Tmem)
+          issue_rowdot_ts_wide(tmem + C::kColS + (b % NB) * 64, tmem + C::kColA2,
+                               dx0 + (b % NX) * kStep, idesc_s);
+        else
+          issue_rowdot_wide(tmem + C::kColS + (b % NB) * 64, da1, dx0 + (b % NX) * kStep,
+                            idesc_s);
         mma_commit(&s_full[b % NB]);
         if (kDV) mma_commit(&x_empty[b % NX]);  // dV: X is read by S alone
       }
@@ -299,8 +300,8 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       return true;
     };
-    bool ok = n > 0 && warp_poll(a_full, 0, limit, abort_flag, kSiteA);
-    if (ok && C::kA2Tmem) ok = warp_poll(a2_tmem, 0, limit, abort_flag, kSiteA);
+    bool ok = n > 0 && (C::kA1Tmem || warp_poll(a_full, 0, limit, abort_flag, kSiteA));
+    if (ok) ok = warp_poll(a2_tmem, 0, limit, abort_flag, kSiteA);
     if (ok) ok = issue_s(0);
     if (ok && C::kA2Tmem) ok = issue_dp(0);
     for (int b = 0; ok && b < n; ++b) {
@@ -349,10 +350,11 @@ __global__ void __launch_bounds__(192, 1)
       return r_in < 64 ? -p.lse[sl.stat0 + q] * kLog2e : p.delta[sl.stat0 + q];
     };
     float stat_next = kRowsAreQueries ? 0.f : load_stat(0);
-    if (C::kA2Tmem && n > 0) {
-      // This row of dO_i (dQ) or V_j (dK) into tensor memory (rows past the slice's end as
-      // zeros): the A operand of dP.
-      const uint8_t* gsrc = reinterpret_cast<const uint8_t*>(kRowsAreQueries ? p.in_do : p.in_v);
+    if (n > 0) {
+      // This row of dO_i (dQ), V_j (dK) or K_j (dV) into tensor memory (rows past the
+      // slice's end as zeros): the A operand of dP (dQ, dK) or of S^T (dV).
+      const uint8_t* gsrc = reinterpret_cast<const uint8_t*>(
+          kRowsAreQueries ? p.in_do : (kDV ? p.in_k : p.in_v));
       const size_t elem0 = kRowsAreQueries ? sl.q_elem0 : sl.k_elem0;
       copy_row_to_tmem<C::D>(row < n_rows ? gsrc + (elem0 + (size_t)row * sl.row_elems) * 2
                                           : nullptr,
@@ -502,8 +504,9 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-// One pass of the kernel above: a1 the resident 128-row tile, x/y the streamed 64-row
-// blocks, a2_rows the tensor whose rows go to tensor memory (dO for dQ, V for dK); one CTA
+// One pass of the kernel above: a1 the resident 128-row tile (dQ, dK), x/y the streamed
+// 64-row blocks, a2_rows the tensor whose rows go to tensor memory (dO for dQ, V for dK, K
+// for dV); one CTA
 // per 128 rows (queries for dQ, keys for dK and dV) of each slice (packed batches: of the
 // longest sequence, the tiles past a shorter one's end returning at once).
 template <int MODE, bool BF16>
@@ -519,7 +522,8 @@ static cudaError_t launch_bwd_wide(const CUtensorMap& a1, const CUtensorMap& x,
   if (e != cudaSuccess) return e;
   BwdParams p = {};
   p.in_do = a2_rows;  // dQ: dO, rows copied into tensor memory
-  p.in_v = a2_rows;   // dK: V, likewise (dV: unused)
+  p.in_v = a2_rows;   // dK: V, likewise
+  p.in_k = a2_rows;   // dV: K, likewise
   p.lse = lse;
   p.delta = delta;
   p.out0 = out0;

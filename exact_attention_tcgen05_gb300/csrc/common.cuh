@@ -141,6 +141,30 @@ __device__ __forceinline__ bool warp_poll(uint64_t* bar, uint32_t parity, uint64
   return __all_sync(0xffffffffu, ok);
 }
 
+// Copies one 16-bit row of n16 16-byte pieces from global memory (zeros past them, and
+// everywhere when src is null) into tensor-memory columns [t_col, t_col + D/2) of this
+// thread's lane as packed pairs (the layout of an A operand read from tensor memory). Every
+// lane of the warp calls it (the TMEM store is warp-collective).
+template <int D>
+__device__ __forceinline__ void copy_row_to_tmem(const uint8_t* src, uint32_t t_col,
+                                                 int n16 = D / 8) {
+  // Every load of the row is issued before the first tensor-memory store (the stores are
+  // ordering points for the compiler), so the row costs one memory latency, not D / 64.
+  uint32_t r[D / 2];
+#pragma unroll
+  for (int k = 0; k < D / 8; ++k) {
+    const uint4 v = (src && k < n16) ? *reinterpret_cast<const uint4*>(src + k * 16)
+                                     : make_uint4(0, 0, 0, 0);
+    r[4 * k] = v.x;
+    r[4 * k + 1] = v.y;
+    r[4 * k + 2] = v.z;
+    r[4 * k + 3] = v.w;
+  }
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c)
+    tmem_st32(t_col + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(&r[32 * c]));
+}
+
 // D[128 x 64] = A B^T over 256 columns, both K-major with 128-byte swizzle: A a [128 x 256]
 // tile (four 16 KiB boxes of 64 columns), B a [64 x 256] block (four 8 KiB boxes), 16
 // steps of 16 columns (the score products of the kernels for head dims above 128).
@@ -153,6 +177,17 @@ __device__ __forceinline__ void issue_rowdot_wide(uint32_t d_tmem, uint64_t a_de
     const uint32_t a_off = ((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4;
     const uint32_t b_off = ((kk >> 2) * (kBoxBytes / 2) + (kk & 3) * 32) >> 4;
     mma_ss(d_tmem, a_desc + a_off, b_desc + b_off, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// D[128 x 64] = A B^T over 256 columns with A in tensor memory (16-bit pairs from column
+// a_tmem, 128 columns) and B a K-major [64 x 256] block (four 8 KiB boxes).
+__device__ __forceinline__ void issue_rowdot_ts_wide(uint32_t d_tmem, uint32_t a_tmem,
+                                                     uint64_t b_desc, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < 256 / 16; ++kk) {
+    const uint32_t b_off = ((kk >> 2) * (kBoxBytes / 2) + (kk & 3) * 32) >> 4;
+    mma_ts(d_tmem, a_tmem + kk * 8, b_desc + b_off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 

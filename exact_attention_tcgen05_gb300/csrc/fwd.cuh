@@ -38,6 +38,7 @@
 namespace attn {
 
 struct FwdParams {
+  const void* q;    // Q, for kernels that read its rows directly (the one-tile 256-column one)
   void* o;
   float* lse;
   int dh;           // head dimension of the tensors (<= D; columns past it read as zero)

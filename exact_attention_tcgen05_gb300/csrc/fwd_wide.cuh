@@ -50,6 +50,7 @@ struct FwdWCfg {
   static constexpr int kThreads = 192;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0;    // S buffer b at kColS + 64 b (P over its first 32)
+  static constexpr uint32_t kColQ = 128;  // one-tile kernel: Q as 16-bit pairs, 128 columns
   static constexpr uint32_t kColO = 256;  // O: 256 columns
 };
 
@@ -93,7 +94,7 @@ __global__ void __launch_bounds__(192, 1)
   const int n_kv = p.causal ? min(nkb, (q0 + kTileM - 1 + off) / kBN + 1) : nkb;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    mbar_init(q_full, 4);  // one arrival per softmax warp: its rows of Q are in tensor memory
     for (int s = 0; s < NK; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -125,13 +126,8 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 4) {
     // ------------------------------ TMA producer ------------------------------
     if (elect_one()) {
-      tma_prefetch_map(&map_q);
       tma_prefetch_map(&map_k64);
       tma_prefetch_map(&map_v64);
-      mbar_arrive_expect_tx(q_full, C::kQBytes);
-      for (int c = 0; c < C::kChunks; ++c)
-        tma_load_rows<PACKED>(smem + C::kOffQ + c * kBoxBytes, &map_q, q_full, c * kBoxCols, q0,
-                              sl, false);
     }
     __syncwarp();
     // K(j) into stage j % NK once S(j - NK) is done; V(j) into stage j % NV once
@@ -176,7 +172,6 @@ __global__ void __launch_bounds__(192, 1)
     }
     if (*abort_flag) {
       // Let every copy this CTA started land before its shared memory is released.
-      mbar_wait(q_full, 0, kDrainLimit, nullptr, kWaitFwdDrain);
       for (int j = max(0, k_issued - NK); j < k_issued; ++j)
         mbar_wait(&k_full[j % NK], (j / NK) & 1, kDrainLimit, nullptr, kWaitFwdDrain);
       for (int j = max(0, v_issued - NV); j < v_issued; ++j)
@@ -189,13 +184,13 @@ __global__ void __launch_bounds__(192, 1)
     // softmax has written P(j).
     const uint32_t idesc_s = make_idesc(BF16, 128, kBN, false, false);
     const uint32_t idesc_o = make_idesc(BF16, 128, C::D, false, true);
-    const uint64_t dq0 = make_sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
     const uint64_t dk0 = make_sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
     // V block: MN-major, 64-column boxes C::kKVBox apart along N, 8-row groups 1 KiB apart
     const uint64_t dv0 = make_sdesc_sw128(smem_u32(smem + C::kOffV), C::kKVBox, 1024);
     constexpr uint32_t kStep = C::kKVBytes >> 4;
-    auto issue_s = [&](int j) {
-      issue_rowdot_wide(tmem + C::kColS + (j & 1) * 64, dq0, dk0 + (j % NK) * kStep, idesc_s);
+    auto issue_s = [&](int j) {  // S = Q K^T with Q from tensor memory
+      issue_rowdot_ts_wide(tmem + C::kColS + (j & 1) * 64, tmem + C::kColQ,
+                           dk0 + (j % NK) * kStep, idesc_s);
     };
     auto issue_pv = [&](int j) {
 #pragma unroll
@@ -253,6 +248,16 @@ __global__ void __launch_bounds__(192, 1)
     float l = 0.f;        // sum of exp2 values (fp32): defines L
     float lr = 0.f;       // sum of the same values rounded to 16 bits: divides O
     bool ok = true;
+    {
+      // This thread's row of Q into tensor memory (rows past N as zeros): the A operand of
+      // S = Q K^T, read there by every S product without shared-memory traffic.
+      const uint8_t* qsrc = reinterpret_cast<const uint8_t*>(p.q) +
+                            (sl.q_elem0 + (size_t)row * sl.row_elems) * 2;
+      copy_row_to_tmem<C::D>(row < N ? qsrc : nullptr, tmem + lane_base + C::kColQ, p.dh / 8);
+      tmem_st_wait();
+      tc_fence_before();
+      warp_arrive(q_full);
+    }
     // O *= alpha in tensor memory, 64 columns at a time (the previous P V must be done).
     auto rescale_o = [&](float alpha) {
 #pragma unroll 1
@@ -377,8 +382,8 @@ __global__ void __launch_bounds__(192, 1)
 // every item is that of the kernel above: the outputs are bit-identical.
 
 struct FwdWPCfg : FwdWCfg {
-  // the barriers of the one-tile kernel, then q_empty and o_free
-  static constexpr int kNumBarsP = kNumBars + 2;
+  // the barriers of the one-tile kernel, then q_empty, o_free, q_tmem_full and q_smem_free
+  static constexpr int kNumBarsP = kNumBars + 4;
   static constexpr int kOffMiscP = kOffBar + kNumBarsP * 8;
   static constexpr int kSmemBytesP = kOffMiscP + 16 + 1024;
   static_assert(kSmemBytesP <= 227 * 1024, "shared memory");
@@ -436,6 +441,11 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* drain = o_last + 1;
   uint64_t* q_empty = drain + 1;    // every S of the item is done: Q may be replaced
   uint64_t* o_free = q_empty + 1;   // the epilogue has read O
+  // Q goes HBM -> shared memory (TMA, q_full) -> tensor memory (the softmax threads, a row
+  // each: q_tmem_full), where it is the A operand of every S of the item; the shared tile is
+  // then free for the next item's copy (q_smem_free).
+  uint64_t* q_tmem_full = o_free + 1;
+  uint64_t* q_smem_free = q_tmem_full + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMiscP);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMiscP + 4);
 
@@ -462,6 +472,8 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(drain, 1);
     mbar_init(q_empty, 1);
     mbar_init(o_free, 4);  // one arrival per softmax warp
+    mbar_init(q_tmem_full, 4);
+    mbar_init(q_smem_free, 4);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -526,10 +538,10 @@ __global__ void __launch_bounds__(192, 1)
       constexpr int kLead = NK - 1;
       for (int j = 0; ok && j < min(kLead, it.n); ++j) ok = load_k(it, gb0 + j, j);
       if (!ok) break;
-      // The previous item's S products must be done with Q (q_empty completes once per
-      // item after its last S; its next completion needs the Q copied below).
+      // The softmax threads must have copied the previous item's Q out of shared memory
+      // (q_smem_free completes once per item; its next completion needs the Q copied below).
       if (q_loads > 0 &&
-          !(ok = warp_wait(q_empty, (q_loads - 1) & 1, limit, abort_flag, kWaitFwdQEmpty)))
+          !(ok = warp_wait(q_smem_free, (q_loads - 1) & 1, limit, abort_flag, kWaitFwdQEmpty)))
         break;
       if (elect_one()) {
         mbar_arrive_expect_tx(q_full, C::kQBytes);
@@ -556,17 +568,17 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------ MMA issuer --------------------------------
     const uint32_t idesc_s = make_idesc(BF16, 128, kBN, false, false);
     const uint32_t idesc_o = make_idesc(BF16, 128, C::D, false, true);
-    const uint64_t dq0 = make_sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
     const uint64_t dk0 = make_sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
     const uint64_t dv0 = make_sdesc_sw128(smem_u32(smem + C::kOffV), C::kKVBox, 1024);
     constexpr uint32_t kStep = C::kKVBytes >> 4;
-    // S(b) into buffer b & 1 (its previous contents, P(b - 2), were read by P V(b - 2),
-    // issued before: the tensor core runs them in order)
+    // S(b) = Q K^T into buffer b & 1, Q from tensor memory (its previous contents, P(b - 2),
+    // were read by P V(b - 2), issued before: the tensor core runs them in order)
     auto issue_s = [&](int b) -> bool {
       if (!warp_poll(&k_full[b % NK], (b / NK) & 1, limit, abort_flag, kWaitFwdK)) return false;
       tc_fence_after();
       if (elect_one()) {
-        issue_rowdot_wide(tmem + C::kColS + (b & 1) * 64, dq0, dk0 + (b % NK) * kStep, idesc_s);
+        issue_rowdot_ts_wide(tmem + C::kColS + (b & 1) * 64, tmem + C::kColQ,
+                             dk0 + (b % NK) * kStep, idesc_s);
         mma_commit(&s_full[b & 1]);
         mma_commit(&k_empty[b % NK]);
       }
@@ -581,7 +593,7 @@ __global__ void __launch_bounds__(192, 1)
       FwdWItem it;
       if (!fwd_wide_item_geom<PACKED>(p, item, nqb_max, it)) continue;
       const int n = it.n;
-      if (!(ok = warp_poll(q_full, items & 1, limit, abort_flag, kWaitFwdQ))) break;
+      if (!(ok = warp_poll(q_tmem_full, items & 1, limit, abort_flag, kWaitFwdQ))) break;
       if (!(ok = issue_s(gb))) break;
       if (n == 1) {
         if (elect_one()) mma_commit(q_empty);  // every S of the item issued
@@ -651,6 +663,37 @@ __global__ void __launch_bounds__(192, 1)
       if (!fwd_wide_item_geom<PACKED>(p, item, nqb_max, it)) continue;
       const int row = it.q0 + wq * 32 + lane;  // query index of this thread
       float m = -INFINITY, l = 0.f, lr = 0.f;
+      {
+        // This thread's row of the item's Q: from the shared tile (four 128-byte-swizzled
+        // boxes of 64 columns) into tensor memory, once the previous item's S products are
+        // done with the tensor-memory copy (q_empty); then both copies are signalled.
+        if (!(ok = warp_wait(q_full, items & 1, limit, abort_flag, kWaitFwdQ))) break;
+        if (items > 0 &&
+            !(ok = warp_wait(q_empty, (items - 1) & 1, limit, abort_flag, kWaitFwdQEmpty)))
+          break;
+        tc_fence_after();
+        const int r_in = wq * 32 + lane;
+        const uint8_t* qrow = smem + C::kOffQ + r_in * 128;
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c) {
+          uint32_t r[32];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 v = *reinterpret_cast<const uint4*>(qrow + c * kBoxBytes +
+                                                           ((j ^ (r_in & 7)) << 4));
+            r[4 * j] = v.x;
+            r[4 * j + 1] = v.y;
+            r[4 * j + 2] = v.z;
+            r[4 * j + 3] = v.w;
+          }
+          tmem_st32(tmem + lane_base + C::kColQ + c * 32, r);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        fence_proxy_async_smem();  // the reads above before the next TMA copy into the tile
+        warp_arrive(q_tmem_full);
+        warp_arrive(q_smem_free);
+      }
       for (int j = 0; j < it.n; ++j) {
         const int b = gb + j;
         const uint32_t t_s = tmem + lane_base + C::kColS + (b & 1) * 64;

@@ -142,10 +142,10 @@ cudaError_t launch_dkv(const Maps& m, const Shape& s, const void* q, const void*
   if (s.d > 128) {
     // two passes (dK and dV together would need 512 accumulator columns): dV with K_j
     // resident, then dK with K_j, V_j resident; Q_i, dO_i streamed in both
-    cudaError_t e = s.bf16 ? launch_bwd_wide<kWideDV, true>(m.k, m.q64, m.do64, nullptr, s, lse,
+    cudaError_t e = s.bf16 ? launch_bwd_wide<kWideDV, true>(m.k, m.q64, m.do64, k, s, lse,
                                                             delta, dk, dv, st)
-                           : launch_bwd_wide<kWideDV, false>(m.k, m.q64, m.do64, nullptr, s,
-                                                             lse, delta, dk, dv, st);
+                           : launch_bwd_wide<kWideDV, false>(m.k, m.q64, m.do64, k, s, lse,
+                                                             delta, dk, dv, st);
     if (e != cudaSuccess) return e;
     return s.bf16 ? launch_bwd_wide<kWideDK, true>(m.k, m.q64, m.do64, v, s, lse, delta, dk, dv,
                                                    st)

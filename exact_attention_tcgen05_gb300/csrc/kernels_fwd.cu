@@ -22,10 +22,11 @@ static int sm_count_fwd() {
 // Which forward: the persistent kernel (fwd_persistent.cuh) except at d = 64 with long
 // items (24 or more key blocks per item on average), where the one-item kernel's loop
 // measured about 5% faster and the fixed cost per item matters little. Head dims above 128
-// (fwd_wide.cuh, 64-key blocks): the persistent kernel for items of fewer than 48 key
-// blocks on average (measured on GB300, d = 256 causal: B16 H16 N1024 0.189 -> 0.170 ms,
-// B4 H16 N4096 0.482 -> 0.466 ms), the one-tile kernel for longer ones (B4 H16 N4096 full
-// 0.833 against 0.877 ms, B1 H16 N16384 causal 1.60 against 1.67 ms).
+// (fwd_wide.cuh, 64-key blocks): the persistent kernel for causal items of fewer than 96
+// key blocks on average and other items of fewer than 48 (measured on GB300, d = 256:
+// causal B16 H16 N1024 0.200 -> 0.163 ms, B4 H16 N4096 0.432 -> 0.399 ms, B2 H16 N8192
+// 0.744 -> 0.724 ms), the one-tile kernel for longer ones (B4 H16 N4096 full 0.720
+// against 0.730 ms, B1 H16 N16384 causal 1.35 against 1.39 ms).
 // ATTN_FWD_PERSISTENT = 0 / 1 forces one or the other (both give the same bits).
 static bool use_persistent_fwd(const Shape& s) {
   static const int forced = [] {
@@ -35,7 +36,7 @@ static bool use_persistent_fwd(const Shape& s) {
   if (forced >= 0) return forced == 1;
   if (s.d > 128) {
     const int nkb64 = (s.Nk + 63) / 64;
-    return (s.causal ? (nkb64 + 1) / 2 : nkb64) < 48;
+    return s.causal ? (nkb64 + 1) / 2 < 96 : nkb64 < 48;
   }
   const int nkb = (s.Nk + kTileN - 1) / kTileN;
   const int blocks_per_item = s.causal ? (nkb + 1) / 2 : nkb;
@@ -189,6 +190,7 @@ static cudaError_t launch_fwd_t(const Maps& m, const Shape& s, void* o, float* l
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   FwdParams p;
+  p.q = nullptr;
   p.o = o;
   p.lse = lse;
   p.dh = s.d;
@@ -268,13 +270,14 @@ static bool fwd_wide_schedule(const Shape& s, int nqb, int G, ItemTable& out) {
 // Head dims above 128: the 256-column forward (fwd_wide.cuh): the persistent kernel, or
 // with ATTN_FWD_PERSISTENT = 0 one CTA per 128-row tile (the same bits).
 template <bool BF16>
-static cudaError_t launch_fwd_wide(const Maps& m, const Shape& s, void* o, float* lse,
-                                   cudaStream_t st) {
+static cudaError_t launch_fwd_wide(const Maps& m, const Shape& s, const void* q, void* o,
+                                   float* lse, cudaStream_t st) {
   using C = FwdWCfg;
   auto kern = s.vl.cu_q != nullptr ? attn_fwd_wide_kernel<BF16, true>
                                    : attn_fwd_wide_kernel<BF16, false>;
   cudaError_t e;
   FwdParams p;
+  p.q = q;
   p.o = o;
   p.lse = lse;
   p.dh = s.d;
@@ -315,9 +318,10 @@ static cudaError_t launch_fwd_wide(const Maps& m, const Shape& s, void* o, float
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd(const Maps& m, const Shape& s, void* o, float* lse, cudaStream_t st) {
-  if (s.d > 128) return s.bf16 ? launch_fwd_wide<true>(m, s, o, lse, st)
-                                : launch_fwd_wide<false>(m, s, o, lse, st);
+cudaError_t launch_fwd(const Maps& m, const Shape& s, const void* q, void* o, float* lse,
+                       cudaStream_t st) {
+  if (s.d > 128) return s.bf16 ? launch_fwd_wide<true>(m, s, q, o, lse, st)
+                                : launch_fwd_wide<false>(m, s, q, o, lse, st);
   if (s.d > 64) return s.bf16 ? launch_fwd_t<128, true>(m, s, o, lse, st)
                                 : launch_fwd_t<128, false>(m, s, o, lse, st);
   return s.bf16 ? launch_fwd_t<64, true>(m, s, o, lse, st)

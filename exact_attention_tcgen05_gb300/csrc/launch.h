@@ -62,7 +62,9 @@ inline void slice_lengths(const Shape& s, int bh, int& nq, int& nk) {
   if (nq < 0 || nq > s.vl.max_q || nk < 0 || nk > s.vl.max_k) nq = nk = 0;
 }
 
-cudaError_t launch_fwd(const Maps& m, const Shape& s, void* o, float* lse, cudaStream_t st);
+// q is the raw tensor map.q describes (the one-tile 256-column forward reads its rows).
+cudaError_t launch_fwd(const Maps& m, const Shape& s, const void* q, void* o, float* lse,
+                       cudaStream_t st);
 cudaError_t launch_delta(const Shape& s, const void* o, const void* dO, float* delta,
                          cudaStream_t st);
 // q and dO are the raw [B*H, N, d] tensors the maps describe (the dQ kernel reads its
