@@ -519,7 +519,7 @@ def run_ours(args) -> None:
 
 # Split-KV decoding, measured after the step (outside its timed region): one query row per
 # (b, h) against a K/V cache larger than L2, inputs resident, partial + merge per call.
-E2E_CHUNKS = 10  # chunks of (b, h) slices in the host-buffer step
+E2E_CHUNKS = 13  # chunks of (b, h) slices in the host-buffer step
 
 DECODE_WORKLOAD = dict(name="decode_B8_H32_Nk32768_d128_bf16", B=8, H=32, Nk=32768, d=128,
                        dtype="bf16", seed=2024)

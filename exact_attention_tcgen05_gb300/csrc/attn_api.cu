@@ -545,15 +545,18 @@ size_t step_set_bytes(long long slices, int N, int d) {
 }  // namespace
 
 namespace {
-// attn_step_host's two side streams and 3 x chunks events, per CUDA context (streams and
+// attn_step_host's two side streams and kNumEv x chunks events, per CUDA context (streams and
 // events belong to the context current when they are made), created on the first call in
 // that context and kept until the process exits: creating and destroying them on every
 // call costs time inside the step.
+// Per chunk: Q/K/V in, dO in, forward done, dK/dV done, all compute done, O/L out,
+// dK/dV out, dQ out.
+enum StepEvent { kEvQKV, kEvDO, kEvFwd, kEvDKV, kEvComp, kEvOutO, kEvOutKV, kEvOut, kNumEv };
 struct StepResources {
   CUcontext ctx = nullptr;
   cudaStream_t s_in = nullptr, s_out = nullptr;
   cudaEvent_t start = nullptr;
-  std::vector<cudaEvent_t> ev_in, ev_comp, ev_out;
+  std::vector<cudaEvent_t> ev[kNumEv];
 };
 std::mutex g_step_mu;
 std::vector<StepResources*> g_step_res;
@@ -608,19 +611,16 @@ cudaError_t step_resources(int chunks, StepResources** out) {
     }
     g_step_res.push_back(r);
   }
-  while ((int)r->ev_in.size() < chunks) {
-    cudaEvent_t a = nullptr, b = nullptr, c = nullptr;
-    cudaError_t e = new_event(&a);
-    if (e == cudaSuccess) e = new_event(&b);
-    if (e == cudaSuccess) e = new_event(&c);
+  while ((int)r->ev[0].size() < chunks) {
+    cudaEvent_t x[kNumEv] = {};
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < kNumEv && e == cudaSuccess; ++i) e = new_event(&x[i]);
     if (e != cudaSuccess) {
-      for (cudaEvent_t x : {a, b, c})
-        if (x) cudaEventDestroy(x);
+      for (cudaEvent_t y : x)
+        if (y) cudaEventDestroy(y);
       return e;
     }
-    r->ev_in.push_back(a);
-    r->ev_comp.push_back(b);
-    r->ev_out.push_back(c);
+    for (int i = 0; i < kNumEv; ++i) r->ev[i].push_back(x[i]);
   }
   *out = r;
   return cudaSuccess;
@@ -667,59 +667,89 @@ attn_status attn_step_host(const void* q, const void* k, const void* v, const vo
   if (e != cudaSuccess) return from_cuda(e);
   cudaStream_t s_in = res->s_in, s_out = res->s_out;
   cudaEvent_t start = res->start;
-  const std::vector<cudaEvent_t>& ev_in = res->ev_in;
-  const std::vector<cudaEvent_t>& ev_comp = res->ev_comp;
-  const std::vector<cudaEvent_t>& ev_out = res->ev_out;
+  const std::vector<cudaEvent_t>(&ev)[kNumEv] = res->ev;
   // The side streams start after the work already queued on the caller's stream.
   e = cudaEventRecord(start, cs);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(s_in, start, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, start, 0);
+  auto rec = [&](StepEvent k, int c, cudaStream_t st_) {
+    if (e == cudaSuccess) e = cudaEventRecord(ev[k][c], st_);
+  };
+  auto wait = [&](cudaStream_t st_, StepEvent k, int c) {  // no wait for c < 0
+    if (e == cudaSuccess && c >= 0) e = cudaStreamWaitEvent(st_, ev[k][c], 0);
+  };
+  auto h2d = [&](void* dst, const void* src, size_t bytes) {
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, s_in);
+  };
+  auto d2h = [&](void* dst, const void* src, size_t bytes) {
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, s_out);
+  };
+  auto run = [&](attn_status x) {
+    if (e == cudaSuccess && st == ATTN_OK) st = x;
+  };
 
-  for (int c = 0; c < chunks && e == cudaSuccess; ++c) {
+  // Chunk c uses buffer set c % kStepSets, which chunk p = c - kStepSets used before: each
+  // buffer is refilled only once p's last reader of it has run (inputs: p's backward;
+  // O/L, dK/dV, dQ: p's copies of them out). Each output leaves as soon as its kernel is
+  // done, so that the last chunk's O and dK/dV copies overlap its remaining kernels.
+  for (int c = 0; c < chunks && e == cudaSuccess && st == ATTN_OK; ++c) {
+    const int p = c - kStepSets;
     const long long b0 = bounds[c];
     const long long n = bounds[c + 1] - b0;
     uint8_t* set = static_cast<uint8_t*>(scratch) + (size_t)(c % kStepSets) * set_bytes;
-    uint8_t* dev[8];
+    uint8_t* dev[8];  // q, k, v, dO, o, dq, dk, dv
     for (int i = 0; i < 8; ++i) dev[i] = set + (size_t)i * up((size_t)per * row_t);
     float* d_lse = reinterpret_cast<float*>(set + 8 * up((size_t)per * row_t));
     float* d_delta = reinterpret_cast<float*>(set + 8 * up((size_t)per * row_t) +
                                               up((size_t)per * row_r));
     const size_t tb = (size_t)n * row_t, rb = (size_t)n * row_r;
     const size_t off_t = (size_t)b0 * row_t, off_r = (size_t)b0 * row_r;
-    // inputs of chunk c, once chunk c - kStepSets (same buffers) has been computed
-    if (c >= kStepSets) e = cudaStreamWaitEvent(s_in, ev_comp[c - kStepSets], 0);
-    const void* hin[4] = {q, k, v, dO};
-    for (int i = 0; i < 4 && e == cudaSuccess; ++i)
-      e = cudaMemcpyAsync(dev[i], static_cast<const uint8_t*>(hin[i]) + off_t, tb,
-                          cudaMemcpyHostToDevice, s_in);
-    if (e == cudaSuccess) e = cudaEventRecord(ev_in[c], s_in);
-    // compute chunk c once its inputs are in and chunk c - kStepSets's outputs have left
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev_in[c], 0);
-    if (e == cudaSuccess && c >= kStepSets)
-      e = cudaStreamWaitEvent(cs, ev_out[c - kStepSets], 0);
-    if (e == cudaSuccess) {
-      st = attn_fwd(dev[0], dev[1], dev[2], dev[4], d_lse, 1, (int)n, N, d, dtype, causal,
-                    scale, cs);
-      if (st == ATTN_OK)
-        st = attn_bwd(dev[0], dev[1], dev[2], dev[4], d_lse, dev[3], dev[5], dev[6], dev[7],
-                      d_delta, 1, (int)n, N, d, dtype, causal, scale, cs);
-      if (st != ATTN_OK) break;
-      e = cudaEventRecord(ev_comp[c], cs);
-    }
-    // outputs of chunk c
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, ev_comp[c], 0);
-    void* hout[4] = {o, dq, dk, dv};
-    const int dsrc[4] = {4, 5, 6, 7};
-    for (int i = 0; i < 4 && e == cudaSuccess; ++i)
-      e = cudaMemcpyAsync(static_cast<uint8_t*>(hout[i]) + off_t, dev[dsrc[i]], tb,
-                          cudaMemcpyDeviceToHost, s_out);
+    auto host_at = [&](const void* base) { return static_cast<const uint8_t*>(base) + off_t; };
+    auto host_out = [&](void* base, size_t off) { return static_cast<uint8_t*>(base) + off; };
+    const int ni = (int)n;
+    // inputs: Q, K, V (the forward's), then dO
+    wait(s_in, kEvComp, p);
+    h2d(dev[0], host_at(q), tb);
+    h2d(dev[1], host_at(k), tb);
+    h2d(dev[2], host_at(v), tb);
+    rec(kEvQKV, c, s_in);
+    h2d(dev[3], host_at(dO), tb);
+    rec(kEvDO, c, s_in);
+    // forward, then the backward's three kernels, on the caller's stream
+    wait(cs, kEvQKV, c);
+    wait(cs, kEvOutO, p);
     if (e == cudaSuccess)
-      e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse) + off_r, d_lse, rb,
-                          cudaMemcpyDeviceToHost, s_out);
-    if (e == cudaSuccess) e = cudaEventRecord(ev_out[c], s_out);
+      run(attn_fwd(dev[0], dev[1], dev[2], dev[4], d_lse, 1, ni, N, d, dtype, causal, scale,
+                   cs));
+    rec(kEvFwd, c, cs);
+    wait(cs, kEvDO, c);
+    if (e == cudaSuccess && st == ATTN_OK)
+      run(attn_bwd_preprocess(dev[4], dev[3], d_delta, 1, ni, N, d, dtype, cs));
+    wait(cs, kEvOutKV, p);
+    if (e == cudaSuccess && st == ATTN_OK)
+      run(attn_bwd_dkv(dev[0], dev[1], dev[2], d_lse, d_delta, dev[3], dev[6], dev[7], 1, ni,
+                       N, d, dtype, causal, scale, cs));
+    rec(kEvDKV, c, cs);
+    wait(cs, kEvOut, p);
+    if (e == cudaSuccess && st == ATTN_OK)
+      run(attn_bwd_dq(dev[0], dev[1], dev[2], d_lse, d_delta, dev[3], dev[5], 1, ni, N, d,
+                      dtype, causal, scale, cs));
+    rec(kEvComp, c, cs);
+    // outputs, each after its kernel
+    wait(s_out, kEvFwd, c);
+    d2h(host_out(o, off_t), dev[4], tb);
+    d2h(host_out(lse, off_r), d_lse, rb);
+    rec(kEvOutO, c, s_out);
+    wait(s_out, kEvDKV, c);
+    d2h(host_out(dk, off_t), dev[6], tb);
+    d2h(host_out(dv, off_t), dev[7], tb);
+    rec(kEvOutKV, c, s_out);
+    wait(s_out, kEvComp, c);
+    d2h(host_out(dq, off_t), dev[5], tb);
+    rec(kEvOut, c, s_out);
   }
   // The caller's stream completes after the last copy out.
-  if (e == cudaSuccess && st == ATTN_OK) e = cudaStreamWaitEvent(cs, ev_out[chunks - 1], 0);
+  if (st == ATTN_OK) wait(cs, kEvOut, chunks - 1);
   if (st != ATTN_OK) return st;
   return from_cuda(e);
 }

@@ -256,7 +256,9 @@ attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const 
  * consecutive slices whose sizes ramp up and down (weights 1, 2, 3, 3, ..., 3, 2, 1): the
  * first upload and the last chunk's compute and download overlap nothing, so those chunks
  * are short. While chunk c is computed on cuda_stream, the inputs of chunk c + 1 are
- * copied in and the outputs of chunk c - 1 copied out on two side streams. The side
+ * copied in and the outputs of chunk c - 1 copied out on two side streams. Within a chunk
+ * the forward waits only for Q, K and V (dO follows), and each output leaves as soon as
+ * its kernel is done: O and L after the forward, dK and dV after their kernel, dQ last. The side
  * streams and the call's events are made on the first call in a CUDA context and kept for
  * later calls there until the process exits; a lock orders the enqueueing of concurrent
  * calls, whose copies then share the side streams. Results are identical to attn_fwd +
