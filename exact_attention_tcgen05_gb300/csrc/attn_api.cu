@@ -143,6 +143,17 @@ attn_status encode_map_packed(CUtensorMap* m, const void* base, int H, int total
   return encode_3d(m, base, bf16, dims, strides, box);
 }
 
+// ATTN_TEST_STALL = 1: every kernel's copies are withheld, so that its pipeline waits run
+// out (after ATTN_WAIT_LIMIT_CYCLES) on phases that never complete - the failure tests'
+// way to exercise the bounded waits and the abort paths without a fault.
+int test_stall() {
+  static const int v = [] {
+    const char* e = std::getenv("ATTN_TEST_STALL");
+    return (e != nullptr && e[0] == '1') ? 1 : 0;
+  }();
+  return v;
+}
+
 Shape make_shape(int B, int H, int N, int d, attn_dtype dtype, int causal, float scale,
                  int Nk = -1) {
   Shape s;
@@ -154,6 +165,7 @@ Shape make_shape(int B, int H, int N, int d, attn_dtype dtype, int causal, float
   s.causal = causal != 0;
   s.scale = scale;
   s.wait_limit = wait_limit_cycles();
+  s.stall = test_stall();
   s.vl = attn::Varlen{};  // dense tensors
   return s;
 }
@@ -776,6 +788,7 @@ attn::DecodeShape make_decode_shape(int B, int H, int Nk, int d, attn_dtype dtyp
   s.bf16 = dtype == ATTN_BF16;
   s.scale = scale;
   s.wait_limit = wait_limit_cycles();
+  s.stall = test_stall();
   return s;
 }
 }  // namespace

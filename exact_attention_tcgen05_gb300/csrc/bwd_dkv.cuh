@@ -134,7 +134,9 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = *tmem_holder;
   const uint64_t limit = p.wait_limit;
 
-  if (warp == 8) {
+  if (warp == 8 && p.stall) {
+    // Failure tests: the producer withholds every copy; the consumers' waits run out.
+  } else if (warp == 8) {
     // TMA producer. The warp runs converged (waits in every lane); the elected lane issues.
     if (elect_one()) {
       tma_prefetch_map(&map_q);
@@ -205,8 +207,8 @@ __global__ void __launch_bounds__(320, 1)
       else
         issue_rowdot_d<D>(tmem + C::kColDP, dv, ddo + stage * kStageStep, idesc_st);
     };
-    bool ok = warp_poll(kv_full, 0, limit, abort_flag, kWaitDkvKV) &&
-              warp_poll(&q_full[0], 0, limit, abort_flag, kWaitDkvQ);
+    bool ok = warp_wait(kv_full, 0, limit, abort_flag, kWaitDkvKV) &&
+              warp_wait(&q_full[0], 0, limit, abort_flag, kWaitDkvQ);
     if (ok) {
       tc_fence_after();
       if (elect_one()) {
@@ -214,7 +216,7 @@ __global__ void __launch_bounds__(320, 1)
         mma_commit(s_full);
       }
       __syncwarp();
-      ok = warp_poll(&do_full[0], 0, limit, abort_flag, kWaitDkvDO);
+      ok = warp_wait(&do_full[0], 0, limit, abort_flag, kWaitDkvDO);
     }
     if (ok) {
       tc_fence_after();
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(320, 1)
       const int s = it % NS;
       const int in = it + 1;
       const int sn = in % NS;
-      if (!(ok = warp_poll(p_full, it & 1, limit, abort_flag, kWaitDkvP))) break;
+      if (!(ok = warp_wait(p_full, it & 1, limit, abort_flag, kWaitDkvP))) break;
       tc_fence_after();
       // dV_j += P^T dO_i
       if (elect_one())
@@ -236,7 +238,7 @@ __global__ void __launch_bounds__(320, 1)
                              idesc_acc, it > 0);
       __syncwarp();
       if (in < n) {
-        if (!(ok = warp_poll(&q_full[sn], (in / NS) & 1, limit, abort_flag, kWaitDkvQ))) break;
+        if (!(ok = warp_wait(&q_full[sn], (in / NS) & 1, limit, abort_flag, kWaitDkvQ))) break;
         tc_fence_after();
         if (elect_one()) {
           issue_st(sn);
@@ -244,7 +246,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         __syncwarp();
       }
-      if (!(ok = warp_poll(ds_full, it & 1, limit, abort_flag, kWaitDkvDS))) break;
+      if (!(ok = warp_wait(ds_full, it & 1, limit, abort_flag, kWaitDkvDS))) break;
       tc_fence_after();
       // dK_j += dS^T Q_i
       if (elect_one())
@@ -252,7 +254,7 @@ __global__ void __launch_bounds__(320, 1)
                              idesc_acc, it > 0);
       __syncwarp();
       if (in < n) {
-        if (!(ok = warp_poll(&do_full[sn], (in / NS) & 1, limit, abort_flag, kWaitDkvDO)))
+        if (!(ok = warp_wait(&do_full[sn], (in / NS) & 1, limit, abort_flag, kWaitDkvDO)))
           break;
         tc_fence_after();
         if (elect_one()) {

@@ -166,7 +166,9 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = *tmem_holder;
   const uint64_t limit = p.wait_limit;
 
-  if (warp == 8) {
+  if (warp == 8 && p.stall) {
+    // Failure tests: the producer withholds every copy; the consumers' waits run out.
+  } else if (warp == 8) {
     // TMA producer: K_j, V_j per item, and the Q/dO ring continued across items.
     if (elect_one()) {
       tma_prefetch_map(&map_q);
@@ -302,8 +304,8 @@ __global__ void __launch_bounds__(320, 1)
       const int n = it.n;
       // K_j, V_j of this item (kv_full: one completion per item; the next copy needs the
       // kv_free committed below) and its first Q block.
-      if (!(ok = warp_poll(kv_full, items & 1, limit, abort_flag, kWaitDkvKV) &&
-                 warp_poll(&q_full[tb % QS], (tb / QS) & 1, limit, abort_flag, kWaitDkvQ)))
+      if (!(ok = warp_wait(kv_full, items & 1, limit, abort_flag, kWaitDkvKV) &&
+                 warp_wait(&q_full[tb % QS], (tb / QS) & 1, limit, abort_flag, kWaitDkvQ)))
         break;
       // S^T overwrites the previous item's last P^T, read by a dV product the tensor core
       // runs before this one; dP^T likewise the last dS^T, read by the last dK product.
@@ -313,7 +315,7 @@ __global__ void __launch_bounds__(320, 1)
         mma_commit(s_full);
       }
       __syncwarp();
-      if (!(ok = warp_poll(&do_full[tb % DS], (tb / DS) & 1, limit, abort_flag, kWaitDkvDO)))
+      if (!(ok = warp_wait(&do_full[tb % DS], (tb / DS) & 1, limit, abort_flag, kWaitDkvDO)))
         break;
       tc_fence_after();
       if (elect_one()) {
@@ -325,12 +327,12 @@ __global__ void __launch_bounds__(320, 1)
       for (int t = 0; ok && t < n; ++t) {
         const int b = tb + t, bn = b + 1;
         const int sq = b % QS, sqn = bn % QS, sd = b % DS, sdn = bn % DS;
-        if (!(ok = warp_poll(p_full, b & 1, limit, abort_flag, kWaitDkvP))) break;
+        if (!(ok = warp_wait(p_full, b & 1, limit, abort_flag, kWaitDkvP))) break;
         // The first accumulating products of an item overwrite dV and dK: the previous
         // item's epilogue must have read them (acc_free: one completion per item, each
         // after an acc_done that follows this wait).
         if (t == 0 && items > 0 &&
-            !(ok = warp_poll(acc_free, (items - 1) & 1, limit, abort_flag, kWaitDkvAccFree)))
+            !(ok = warp_wait(acc_free, (items - 1) & 1, limit, abort_flag, kWaitDkvAccFree)))
           break;
         tc_fence_after();
         // dV_j += P^T dO_i, the last reader of dO_i's slot
@@ -340,7 +342,7 @@ __global__ void __launch_bounds__(320, 1)
         __syncwarp();
         if constexpr (kSplit) commit(&do_empty[sd]);
         if (t + 1 < n) {
-          if (!(ok = warp_poll(&q_full[sqn], (bn / QS) & 1, limit, abort_flag, kWaitDkvQ)))
+          if (!(ok = warp_wait(&q_full[sqn], (bn / QS) & 1, limit, abort_flag, kWaitDkvQ)))
             break;
           tc_fence_after();
           if (elect_one()) {
@@ -349,7 +351,7 @@ __global__ void __launch_bounds__(320, 1)
           }
           __syncwarp();
         }
-        if (!(ok = warp_poll(ds_full, b & 1, limit, abort_flag, kWaitDkvDS))) break;
+        if (!(ok = warp_wait(ds_full, b & 1, limit, abort_flag, kWaitDkvDS))) break;
         tc_fence_after();
         // dK_j += dS^T Q_i, the last reader of Q_i's slot
         if (elect_one())
@@ -358,7 +360,7 @@ __global__ void __launch_bounds__(320, 1)
         __syncwarp();
         if constexpr (kSplit) commit(&q_empty[sq]);
         if (t + 1 < n) {
-          if (!(ok = warp_poll(&do_full[sdn], (bn / DS) & 1, limit, abort_flag, kWaitDkvDO)))
+          if (!(ok = warp_wait(&do_full[sdn], (bn / DS) & 1, limit, abort_flag, kWaitDkvDO)))
             break;
           tc_fence_after();
           if (elect_one()) {

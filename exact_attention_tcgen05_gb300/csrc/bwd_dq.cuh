@@ -42,6 +42,7 @@ struct BwdParams {
   float scale;
   float scale_log2;    // scale * log2(e)
   unsigned long long wait_limit;
+  int stall;           // failure tests: the TMA producer withholds every copy
   Varlen vl;           // packed variable-length batch (vl.cu_q == nullptr: dense)
 };
 
@@ -182,7 +183,9 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = *tmem_holder;
   const uint64_t limit = p.wait_limit;
 
-  if (warp == 8) {
+  if (warp == 8 && p.stall) {
+    // Failure tests: the producer withholds every copy; the consumers' waits run out.
+  } else if (warp == 8) {
     // TMA producer. The warp runs converged (waits in every lane); the elected lane issues.
     if (elect_one()) {
       tma_prefetch_map(&map_k);
@@ -226,8 +229,8 @@ __global__ void __launch_bounds__(320, 1)
     constexpr uint32_t kStageStep = C::kTileBytes >> 4;
     const uint32_t tq = tmem + C::kColQ;
     const uint32_t tdo = tmem + C::kColDO;
-    bool ok = warp_poll(qdo_tmem, 0, limit, abort_flag, kWaitDqQ) &&
-              warp_poll(&k_full[0], 0, limit, abort_flag, kWaitDqK);
+    bool ok = warp_wait(qdo_tmem, 0, limit, abort_flag, kWaitDqQ) &&
+              warp_wait(&k_full[0], 0, limit, abort_flag, kWaitDqK);
     if (ok) {
       tc_fence_after();
       if (elect_one()) {
@@ -235,7 +238,7 @@ __global__ void __launch_bounds__(320, 1)
         mma_commit(s_full);
       }
       __syncwarp();
-      ok = warp_poll(&v_full[0], 0, limit, abort_flag, kWaitDqV);
+      ok = warp_wait(&v_full[0], 0, limit, abort_flag, kWaitDqV);
     }
     if (ok) {
       tc_fence_after();
@@ -251,8 +254,8 @@ __global__ void __launch_bounds__(320, 1)
       const int sn = jn % NS;
       if (jn < n) {
         // S of the next block overwrites S once the softmax warps have read it.
-        if (!(ok = warp_poll(&k_full[sn], (jn / NS) & 1, limit, abort_flag, kWaitDqK) &&
-                   warp_poll(s_free, j & 1, limit, abort_flag, kWaitDqSC)))
+        if (!(ok = warp_wait(&k_full[sn], (jn / NS) & 1, limit, abort_flag, kWaitDqK) &&
+                   warp_wait(s_free, j & 1, limit, abort_flag, kWaitDqSC)))
           break;
         tc_fence_after();
         if (elect_one()) {
@@ -261,7 +264,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         __syncwarp();
       }
-      if (!(ok = warp_poll(ds_full, j & 1, limit, abort_flag, kWaitDqDS))) break;
+      if (!(ok = warp_wait(ds_full, j & 1, limit, abort_flag, kWaitDqDS))) break;
       tc_fence_after();
       // dQ_i += dS K_j (dS read from tensor memory, over dP)
       if (elect_one())
@@ -269,7 +272,7 @@ __global__ void __launch_bounds__(320, 1)
                              idesc_acc, j > 0);
       __syncwarp();
       if (jn < n) {
-        if (!(ok = warp_poll(&v_full[sn], (jn / NS) & 1, limit, abort_flag, kWaitDqV))) break;
+        if (!(ok = warp_wait(&v_full[sn], (jn / NS) & 1, limit, abort_flag, kWaitDqV))) break;
         tc_fence_after();
         if (elect_one()) {
           issue_rowdot_ts_d<D>(tmem + C::kColDP, tdo, dv + sn * kStageStep, idesc_sq);

@@ -190,7 +190,9 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = *tmem_holder;
   const uint64_t limit = p.wait_limit;
 
-  if (warp == 8) {
+  if (warp == 8 && p.stall) {
+    // Failure tests: the producer withholds every copy; the consumers' waits run out.
+  } else if (warp == 8) {
     // TMA producer: the K/V ring, continued across items.
     if (elect_one()) {
       tma_prefetch_map(&map_k);
@@ -256,11 +258,11 @@ __global__ void __launch_bounds__(320, 1)
       const int n = it.n;
       // Q_i and dO_i of this item in tensor memory (qdo_tmem: one completion per item; the
       // next needs qdo_free of this item, committed below after this wait).
-      if (!(ok = warp_poll(qdo_tmem, items & 1, limit, abort_flag, kWaitDqQ))) break;
-      if (!(ok = warp_poll(&k_full[tb % NS], (tb / NS) & 1, limit, abort_flag, kWaitDqK)))
+      if (!(ok = warp_wait(qdo_tmem, items & 1, limit, abort_flag, kWaitDqQ))) break;
+      if (!(ok = warp_wait(&k_full[tb % NS], (tb / NS) & 1, limit, abort_flag, kWaitDqK)))
         break;
       // S overwrites the previous item's last S, which the elementwise warps have read.
-      if (tb > 0 && !(ok = warp_poll(s_free, (tb - 1) & 1, limit, abort_flag, kWaitDqSC)))
+      if (tb > 0 && !(ok = warp_wait(s_free, (tb - 1) & 1, limit, abort_flag, kWaitDqSC)))
         break;
       tc_fence_after();
       if (elect_one()) {
@@ -270,7 +272,7 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       // dP overwrites the previous item's last dP / dS: read by the elementwise warps and
       // by the last dQ product, which the tensor core runs before this one.
-      if (!(ok = warp_poll(&v_full[tb % NS], (tb / NS) & 1, limit, abort_flag, kWaitDqV)))
+      if (!(ok = warp_wait(&v_full[tb % NS], (tb / NS) & 1, limit, abort_flag, kWaitDqV)))
         break;
       tc_fence_after();
       if (elect_one()) {
@@ -283,8 +285,8 @@ __global__ void __launch_bounds__(320, 1)
         const int b = tb + j, bn = b + 1;
         const int s = b % NS, sn = bn % NS;
         if (j + 1 < n) {
-          if (!(ok = warp_poll(&k_full[sn], (bn / NS) & 1, limit, abort_flag, kWaitDqK) &&
-                     warp_poll(s_free, b & 1, limit, abort_flag, kWaitDqSC)))
+          if (!(ok = warp_wait(&k_full[sn], (bn / NS) & 1, limit, abort_flag, kWaitDqK) &&
+                     warp_wait(s_free, b & 1, limit, abort_flag, kWaitDqSC)))
             break;
           tc_fence_after();
           if (elect_one()) {
@@ -293,12 +295,12 @@ __global__ void __launch_bounds__(320, 1)
           }
           __syncwarp();
         }
-        if (!(ok = warp_poll(ds_full, b & 1, limit, abort_flag, kWaitDqDS))) break;
+        if (!(ok = warp_wait(ds_full, b & 1, limit, abort_flag, kWaitDqDS))) break;
         // The first dQ product of an item overwrites the accumulator: the previous item's
         // epilogue must have read it (acc_free: one completion per item, each after an
         // acc_done that follows this wait).
         if (j == 0 && items > 0 &&
-            !(ok = warp_poll(acc_free, (items - 1) & 1, limit, abort_flag, kWaitDqAccFree)))
+            !(ok = warp_wait(acc_free, (items - 1) & 1, limit, abort_flag, kWaitDqAccFree)))
           break;
         tc_fence_after();
         if (elect_one())
@@ -306,7 +308,7 @@ __global__ void __launch_bounds__(320, 1)
                                idesc_acc, j > 0);
         __syncwarp();
         if (j + 1 < n) {
-          if (!(ok = warp_poll(&v_full[sn], (bn / NS) & 1, limit, abort_flag, kWaitDqV)))
+          if (!(ok = warp_wait(&v_full[sn], (bn / NS) & 1, limit, abort_flag, kWaitDqV)))
             break;
           tc_fence_after();
           if (elect_one()) {

@@ -181,7 +181,9 @@ __global__ void __launch_bounds__(192, 1)
   // Row of the resident tiles and of the streamed blocks in the slice: queries or keys.
   const bool a_keys = !kRowsAreQueries, x_keys = kRowsAreQueries;
 
-  if (warp == 4) {
+  if (warp == 4 && p.stall) {
+    // Failure tests: the producer withholds every copy; the consumers' waits run out.
+  } else if (warp == 4) {
     // ------------------------------ TMA producer ------------------------------
     if (n > 0 && elect_one()) {
       tma_prefetch_map(&map_x);
@@ -273,7 +275,7 @@ __global__ void __launch_bounds__(192, 1)
                (b > 0 || kk > 0) ? 1u : 0u);
     };
     auto issue_s = [&](int b) -> bool {
-      if (!warp_poll(&x_full[b % NX], (b / NX) & 1, limit, abort_flag, kSiteX)) return false;
+      if (!warp_wait(&x_full[b % NX], (b / NX) & 1, limit, abort_flag, kSiteX)) return false;
       tc_fence_after();
       if (elect_one()) {
         if constexpr (C::kA1Tmem)
@@ -289,7 +291,7 @@ __global__ void __launch_bounds__(192, 1)
       return true;
     };
     auto issue_dp = [&](int b) -> bool {
-      if (!warp_poll(&y_full[b % NY], (b / NY) & 1, limit, abort_flag, kSiteY)) return false;
+      if (!warp_wait(&y_full[b % NY], (b / NY) & 1, limit, abort_flag, kSiteY)) return false;
       tc_fence_after();
       if (elect_one()) {
         issue_rowdot_ts_wide(tmem + C::kColDP, tmem + C::kColA2, dy0 + (b % NY) * kStep,
@@ -300,22 +302,22 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       return true;
     };
-    bool ok = n > 0 && (C::kA1Tmem || warp_poll(a_full, 0, limit, abort_flag, kSiteA));
-    if (ok) ok = warp_poll(a2_tmem, 0, limit, abort_flag, kSiteA);
+    bool ok = n > 0 && (C::kA1Tmem || warp_wait(a_full, 0, limit, abort_flag, kSiteA));
+    if (ok) ok = warp_wait(a2_tmem, 0, limit, abort_flag, kSiteA);
     if (ok) ok = issue_s(0);
     if (ok && C::kA2Tmem) ok = issue_dp(0);
     for (int b = 0; ok && b < n; ++b) {
       if (b + 1 < n) {
         if (C::kA2Tmem &&
-            !(ok = warp_poll(s_free, b & 1, limit, abort_flag, kSiteS)))
+            !(ok = warp_wait(s_free, b & 1, limit, abort_flag, kSiteS)))
           break;
         if (!(ok = issue_s(b + 1))) break;
       }
       if constexpr (kDV) {
-        if (!(ok = warp_poll(&y_full[b % NY], (b / NY) & 1, limit, abort_flag, kSiteY)))
+        if (!(ok = warp_wait(&y_full[b % NY], (b / NY) & 1, limit, abort_flag, kSiteY)))
           break;
       }
-      if (!(ok = warp_poll(&ds_full[b % NB], (b / NB) & 1, limit, abort_flag, kSiteDS))) break;
+      if (!(ok = warp_wait(&ds_full[b % NB], (b / NB) & 1, limit, abort_flag, kSiteDS))) break;
       tc_fence_after();
       if (elect_one()) {
         issue_acc(b);
@@ -535,6 +537,7 @@ static cudaError_t launch_bwd_wide(const CUtensorMap& a1, const CUtensorMap& x,
   p.scale = s.scale;
   p.scale_log2 = s.scale * kLog2e;
   p.wait_limit = s.wait_limit;
+  p.stall = s.stall;
   p.vl = s.vl;
   const int rows = MODE == kWideDQ ? s.N : s.Nk;  // packed: the longest sequence
   dim3 grid((rows + kTileM - 1) / kTileM, s.BH);

@@ -133,14 +133,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
   return __all_sync(0xffffffffu, ok);
 }
 
-// Warp-uniform bounded poll (non-suspending test_wait in every lane): for the converged
-// MMA-issuing warps.
-__device__ __forceinline__ bool warp_poll(uint64_t* bar, uint32_t parity, uint64_t limit,
-                                          volatile int* abort, int where) {
-  const bool ok = mbar_poll(bar, parity, limit, abort, where);
-  return __all_sync(0xffffffffu, ok);
-}
-
 // Copies one 16-bit row of n16 16-byte pieces from global memory (zeros past them, and
 // everywhere when src is null) into tensor-memory columns [t_col, t_col + D/2) of this
 // thread's lane as packed pairs (the layout of an A operand read from tensor memory). Every

@@ -45,6 +45,7 @@ struct DecodeParams {
   int chunk;          // keys per split (multiple of kDecodeSub)
   float scale_log2;   // scale * log2(e)
   unsigned long long wait_limit;
+  int stall;          // failure tests: thread 0 withholds every copy
 };
 
 template <int D>
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
     bulk_load(st, kbase + (size_t)i * C::kSubBytes, bytes, &full[s]);
     bulk_load(st + C::kSubBytes, vbase + (size_t)i * C::kSubBytes, bytes, &full[s]);
   };
-  if (threadIdx.x == 0)
+  if (threadIdx.x == 0 && !p.stall)  // failure tests: no copies, so the waits run out
     for (int i = 0; i < min(NS, nsub); ++i) issue(i);
 
   // This lane's slice of q, as floats.

@@ -47,6 +47,7 @@ struct FwdParams {
   int causal;
   float scale_log2; // scale * log2(e)
   unsigned long long wait_limit;
+  int stall;        // failure tests: the TMA producer withholds every copy
   Varlen vl;        // packed variable-length batch (vl.cu_q == nullptr: dense)
 };
 
@@ -147,7 +148,9 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = *tmem_holder;
   const uint64_t limit = p.wait_limit;
 
-  if (warp == 8) {
+  if (warp == 8 && p.stall) {
+    // Failure tests: the producer withholds every copy; the consumers' waits run out.
+  } else if (warp == 8) {
     // ------------------------------ TMA producer ------------------------------
     // Converged warp (waits in every lane); the elected lane issues the copies.
     if (elect_one()) {
@@ -213,8 +216,8 @@ __global__ void __launch_bounds__(320, 1)
                dv0 + stage * kStep + ((kk * 2048) >> 4), idesc_o, (acc || kk > 0) ? 1u : 0u);
     };
 
-    bool ok = warp_poll(q_full, 0, limit, abort_flag, kWaitFwdQ);
-    if (ok) ok = warp_poll(&k_full[0], 0, limit, abort_flag, kWaitFwdK);
+    bool ok = warp_wait(q_full, 0, limit, abort_flag, kWaitFwdQ);
+    if (ok) ok = warp_wait(&k_full[0], 0, limit, abort_flag, kWaitFwdK);
     if (ok) {
       tc_fence_after();
       if (elect_one()) {
@@ -237,12 +240,12 @@ __global__ void __launch_bounds__(320, 1)
         for (int t = 0; t < 2 && ok; ++t) {
           if (jn >= nkv[t]) continue;
           if (!next_k_ready) {
-            if (!(ok = warp_poll(&k_full[sn], (jn / C::kStages) & 1, limit, abort_flag,
+            if (!(ok = warp_wait(&k_full[sn], (jn / C::kStages) & 1, limit, abort_flag,
                                  kWaitFwdK)))
               break;
             next_k_ready = true;
           }
-          if (!(ok = warp_poll(&s_free[t], j & 1, limit, abort_flag, kWaitFwdX))) break;
+          if (!(ok = warp_wait(&s_free[t], j & 1, limit, abort_flag, kWaitFwdX))) break;
           tc_fence_after();
           if (elect_one()) {
             issue_s(t, sn);
@@ -251,11 +254,11 @@ __global__ void __launch_bounds__(320, 1)
           __syncwarp();
         }
         if (!ok) break;
-        if (!(ok = warp_poll(&v_full[s], (j / C::kStages) & 1, limit, abort_flag, kWaitFwdV)))
+        if (!(ok = warp_wait(&v_full[s], (j / C::kStages) & 1, limit, abort_flag, kWaitFwdV)))
           break;
         for (int t = 0; t < 2 && ok; ++t) {
           if (j >= nkv[t]) continue;
-          if (!(ok = warp_poll(&p_full[t], j & 1, limit, abort_flag, kWaitFwdP))) break;
+          if (!(ok = warp_wait(&p_full[t], j & 1, limit, abort_flag, kWaitFwdP))) break;
           tc_fence_after();
           if (elect_one()) {
             issue_pv(t, s, j > 0);
@@ -271,7 +274,7 @@ __global__ void __launch_bounds__(320, 1)
     } else {
       for (int j = 0; ok && j < n_kv; ++j) {
         const int s = j % C::kStages;
-        if (!(ok = warp_poll(&v_full[s], (j / C::kStages) & 1, limit, abort_flag, kWaitFwdV)))
+        if (!(ok = warp_wait(&v_full[s], (j / C::kStages) & 1, limit, abort_flag, kWaitFwdV)))
           break;
         tc_fence_after();
         const int jn = j + 1;
@@ -279,7 +282,7 @@ __global__ void __launch_bounds__(320, 1)
         bool next_k_ready = false;
         for (int t = 0; t < 2 && ok; ++t) {
           if (j >= nkv[t]) continue;
-          if (!(ok = warp_poll(&p_full[t], j & 1, limit, abort_flag, kWaitFwdP))) break;
+          if (!(ok = warp_wait(&p_full[t], j & 1, limit, abort_flag, kWaitFwdP))) break;
           tc_fence_after();
           if (elect_one()) {
             issue_pv(t, s, j > 0);
@@ -288,7 +291,7 @@ __global__ void __launch_bounds__(320, 1)
           __syncwarp();
           if (jn < nkv[t]) {
             if (!next_k_ready) {
-              if (!(ok = warp_poll(&k_full[sn], (jn / C::kStages) & 1, limit, abort_flag,
+              if (!(ok = warp_wait(&k_full[sn], (jn / C::kStages) & 1, limit, abort_flag,
                                    kWaitFwdK)))
                 break;
               tc_fence_after();

@@ -193,6 +193,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
 
   if (!pair_ok) {
     // no work: fall through to the exit handshake
+  } else if (warp == 8 && p.stall) {
+    // Failure tests: the producer withholds every copy; the consumers' waits run out.
   } else if (warp == 8) {
     // ------------------------------ TMA producer (both CTAs) ------------------------------
     if (elect_one()) {
@@ -318,7 +320,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     };
     // both this CTA's copy and rank 1's (forwarded) of one stage
     auto wait_stage = [&](uint64_t* own, uint64_t* peer, uint32_t parity, int where) {
-      return warp_poll(own, parity, limit, abort_flag, where) &&
+      return warp_wait(own, parity, limit, abort_flag, where) &&
              __all_sync(0xffffffffu,
                         mbar_poll_cluster(peer, parity, limit, abort_flag, kWaitFwdPeer));
     };

@@ -163,7 +163,9 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = *tmem_holder;
   const uint64_t limit = p.wait_limit;
 
-  if (warp == 8) {
+  if (warp == 8 && p.stall) {
+    // Failure tests: the producer withholds every copy; the consumers' waits run out.
+  } else if (warp == 8) {
     // ------------------------------ TMA producer ------------------------------
     if (elect_one()) {
       tma_prefetch_map(&map_q);
@@ -259,9 +261,9 @@ __global__ void __launch_bounds__(320, 1)
       FwdItem it;
       if (!fwd_item_geom<D, PACKED>(p, item, nqb_max, it)) continue;
       const int n_kv = it.n_kv;
-      if (!(ok = warp_poll(q_full, q_used & 1, limit, abort_flag, kWaitFwdQ))) break;
+      if (!(ok = warp_wait(q_full, q_used & 1, limit, abort_flag, kWaitFwdQ))) break;
       ++q_used;
-      if (!(ok = warp_poll(&k_full[kv_base % NS], (kv_base / NS) & 1, limit, abort_flag,
+      if (!(ok = warp_wait(&k_full[kv_base % NS], (kv_base / NS) & 1, limit, abort_flag,
                            kWaitFwdK)))
         break;
       // First S of each tile. It overwrites S_t: at d = 128 the previous P over S_t was read
@@ -271,7 +273,7 @@ __global__ void __launch_bounds__(320, 1)
       for (int t = 0; t < 2 && ok; ++t) {
         if (it.nkv[t] == 0) continue;
         if (C::kOwnP && tb[t] > 0 &&
-            !(ok = warp_poll(&s_free[t], (tb[t] - 1) & 1, limit, abort_flag, kWaitFwdX)))
+            !(ok = warp_wait(&s_free[t], (tb[t] - 1) & 1, limit, abort_flag, kWaitFwdX)))
           break;
         tc_fence_after();
         if (elect_one()) {
@@ -293,11 +295,11 @@ __global__ void __launch_bounds__(320, 1)
       for (int t = 0; t < 2 && ok; ++t) {
             if (jn >= it.nkv[t]) continue;
             if (!next_k_ready) {
-              if (!(ok = warp_poll(&k_full[sn], (bn / NS) & 1, limit, abort_flag, kWaitFwdK)))
+              if (!(ok = warp_wait(&k_full[sn], (bn / NS) & 1, limit, abort_flag, kWaitFwdK)))
                 break;
               next_k_ready = true;
             }
-            if (!(ok = warp_poll(&s_free[t], (tb[t] + j) & 1, limit, abort_flag, kWaitFwdX)))
+            if (!(ok = warp_wait(&s_free[t], (tb[t] + j) & 1, limit, abort_flag, kWaitFwdX)))
               break;
             tc_fence_after();
             if (elect_one()) {
@@ -308,7 +310,7 @@ __global__ void __launch_bounds__(320, 1)
           }
           if (!ok) break;
           if (jn == n_kv - 1) commit(q_empty);
-          if (!(ok = warp_poll(&v_full[s], (b / NS) & 1, limit, abort_flag, kWaitFwdV))) break;
+          if (!(ok = warp_wait(&v_full[s], (b / NS) & 1, limit, abort_flag, kWaitFwdV))) break;
           #pragma unroll
       for (int t = 0; t < 2 && ok; ++t) {
             if (j >= it.nkv[t]) continue;
@@ -316,10 +318,10 @@ __global__ void __launch_bounds__(320, 1)
             // item must have read it (o_free: one completion per item of the tile, each
             // after a P V issued past this wait).
             if (j == 0 && ti[t] > 0 &&
-                !(ok = warp_poll(&o_free[t], (ti[t] - 1) & 1, limit, abort_flag,
+                !(ok = warp_wait(&o_free[t], (ti[t] - 1) & 1, limit, abort_flag,
                                  kWaitFwdOFree)))
               break;
-            if (!(ok = warp_poll(&p_full[t], (tb[t] + j) & 1, limit, abort_flag, kWaitFwdP)))
+            if (!(ok = warp_wait(&p_full[t], (tb[t] + j) & 1, limit, abort_flag, kWaitFwdP)))
               break;
             tc_fence_after();
             if (elect_one()) {
@@ -329,17 +331,17 @@ __global__ void __launch_bounds__(320, 1)
             __syncwarp();
           }
         } else {
-          if (!(ok = warp_poll(&v_full[s], (b / NS) & 1, limit, abort_flag, kWaitFwdV))) break;
+          if (!(ok = warp_wait(&v_full[s], (b / NS) & 1, limit, abort_flag, kWaitFwdV))) break;
           tc_fence_after();
           bool next_k_ready = false;
           #pragma unroll
       for (int t = 0; t < 2 && ok; ++t) {
             if (j >= it.nkv[t]) continue;
             if (j == 0 && ti[t] > 0 &&
-                !(ok = warp_poll(&o_free[t], (ti[t] - 1) & 1, limit, abort_flag,
+                !(ok = warp_wait(&o_free[t], (ti[t] - 1) & 1, limit, abort_flag,
                                  kWaitFwdOFree)))
               break;
-            if (!(ok = warp_poll(&p_full[t], (tb[t] + j) & 1, limit, abort_flag, kWaitFwdP)))
+            if (!(ok = warp_wait(&p_full[t], (tb[t] + j) & 1, limit, abort_flag, kWaitFwdP)))
               break;
             tc_fence_after();
             if (elect_one()) {
@@ -349,7 +351,7 @@ __global__ void __launch_bounds__(320, 1)
             __syncwarp();
             if (jn < it.nkv[t]) {
               if (!next_k_ready) {
-                if (!(ok = warp_poll(&k_full[sn], (bn / NS) & 1, limit, abort_flag,
+                if (!(ok = warp_wait(&k_full[sn], (bn / NS) & 1, limit, abort_flag,
                                      kWaitFwdK)))
                   break;
                 tc_fence_after();

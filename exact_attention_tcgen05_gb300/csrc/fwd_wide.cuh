@@ -123,7 +123,9 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = *tmem_holder;
   const uint64_t limit = p.wait_limit;
 
-  if (warp == 4) {
+  if (warp == 4 && p.stall) {
+    // Failure tests: the producer withholds every copy; the consumers' waits run out.
+  } else if (warp == 4) {
     // ------------------------------ TMA producer ------------------------------
     if (elect_one()) {
       tma_prefetch_map(&map_k64);
@@ -198,8 +200,8 @@ __global__ void __launch_bounds__(192, 1)
         mma_ts(tmem + C::kColO, tmem + C::kColS + (j & 1) * 64 + kk * 8,
                dv0 + (j % NV) * kStep + ((kk * 2048) >> 4), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
     };
-    bool ok = warp_poll(q_full, 0, limit, abort_flag, kWaitFwdQ);
-    if (ok) ok = warp_poll(&k_full[0], 0, limit, abort_flag, kWaitFwdK);
+    bool ok = warp_wait(q_full, 0, limit, abort_flag, kWaitFwdQ);
+    if (ok) ok = warp_wait(&k_full[0], 0, limit, abort_flag, kWaitFwdK);
     if (ok) {
       tc_fence_after();
       if (elect_one()) {
@@ -212,7 +214,7 @@ __global__ void __launch_bounds__(192, 1)
     for (int j = 0; ok && j < n_kv; ++j) {
       const int jn = j + 1;
       if (jn < n_kv) {
-        if (!(ok = warp_poll(&k_full[jn % NK], (jn / NK) & 1, limit, abort_flag, kWaitFwdK)))
+        if (!(ok = warp_wait(&k_full[jn % NK], (jn / NK) & 1, limit, abort_flag, kWaitFwdK)))
           break;
         tc_fence_after();
         if (elect_one()) {
@@ -222,8 +224,8 @@ __global__ void __launch_bounds__(192, 1)
         }
         __syncwarp();
       }
-      if (!(ok = warp_poll(&v_full[j % NV], (j / NV) & 1, limit, abort_flag, kWaitFwdV))) break;
-      if (!(ok = warp_poll(&p_full[j & 1], (j >> 1) & 1, limit, abort_flag, kWaitFwdP))) break;
+      if (!(ok = warp_wait(&v_full[j % NV], (j / NV) & 1, limit, abort_flag, kWaitFwdV))) break;
+      if (!(ok = warp_wait(&p_full[j & 1], (j >> 1) & 1, limit, abort_flag, kWaitFwdP))) break;
       tc_fence_after();
       if (elect_one()) {
         issue_pv(j);
@@ -487,7 +489,9 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = *tmem_holder;
   const uint64_t limit = p.wait_limit;
 
-  if (warp == 4) {
+  if (warp == 4 && p.stall) {
+    // Failure tests: the producer withholds every copy; the consumers' waits run out.
+  } else if (warp == 4) {
     // ------------------------------ TMA producer ------------------------------
     if (elect_one()) {
       tma_prefetch_map(&map_q);
@@ -574,7 +578,7 @@ __global__ void __launch_bounds__(192, 1)
     // S(b) = Q K^T into buffer b & 1, Q from tensor memory (its previous contents, P(b - 2),
     // were read by P V(b - 2), issued before: the tensor core runs them in order)
     auto issue_s = [&](int b) -> bool {
-      if (!warp_poll(&k_full[b % NK], (b / NK) & 1, limit, abort_flag, kWaitFwdK)) return false;
+      if (!warp_wait(&k_full[b % NK], (b / NK) & 1, limit, abort_flag, kWaitFwdK)) return false;
       tc_fence_after();
       if (elect_one()) {
         issue_rowdot_ts_wide(tmem + C::kColS + (b & 1) * 64, tmem + C::kColQ,
@@ -593,7 +597,7 @@ __global__ void __launch_bounds__(192, 1)
       FwdWItem it;
       if (!fwd_wide_item_geom<PACKED>(p, item, nqb_max, it)) continue;
       const int n = it.n;
-      if (!(ok = warp_poll(q_tmem_full, items & 1, limit, abort_flag, kWaitFwdQ))) break;
+      if (!(ok = warp_wait(q_tmem_full, items & 1, limit, abort_flag, kWaitFwdQ))) break;
       if (!(ok = issue_s(gb))) break;
       if (n == 1) {
         if (elect_one()) mma_commit(q_empty);  // every S of the item issued
@@ -608,14 +612,14 @@ __global__ void __launch_bounds__(192, 1)
             __syncwarp();
           }
         }
-        if (!(ok = warp_poll(&v_full[b % NV], (b / NV) & 1, limit, abort_flag, kWaitFwdV)))
+        if (!(ok = warp_wait(&v_full[b % NV], (b / NV) & 1, limit, abort_flag, kWaitFwdV)))
           break;
-        if (!(ok = warp_poll(&p_full[b & 1], (b >> 1) & 1, limit, abort_flag, kWaitFwdP)))
+        if (!(ok = warp_wait(&p_full[b & 1], (b >> 1) & 1, limit, abort_flag, kWaitFwdP)))
           break;
         // The item's first P V overwrites O: the previous item's epilogue must have read it
         // (o_free: one completion per item, each after an o_last that follows this wait).
         if (j == 0 && items > 0 &&
-            !(ok = warp_poll(o_free, (items - 1) & 1, limit, abort_flag, kWaitFwdOFree)))
+            !(ok = warp_wait(o_free, (items - 1) & 1, limit, abort_flag, kWaitFwdOFree)))
           break;
         tc_fence_after();
         if (elect_one()) {

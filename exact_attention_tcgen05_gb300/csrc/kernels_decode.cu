@@ -32,6 +32,7 @@ static cudaError_t launch_decode_partial_t(const DecodeShape& s, const void* q, 
   p.chunk = decode_chunk(s.Nk, s.splits);
   p.scale_log2 = s.scale * kLog2e;
   p.wait_limit = s.wait_limit;
+  p.stall = s.stall;
   dim3 grid(s.splits, s.BH);
   kern<<<grid, kDecodeThreads, C::kSmemBytes, st>>>(p);
   return cudaGetLastError();

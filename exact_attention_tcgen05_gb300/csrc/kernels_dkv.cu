@@ -104,6 +104,7 @@ static cudaError_t launch_dkv_t(const Maps& m, const Shape& s, const void* q, co
   p.scale = s.scale;
   p.scale_log2 = s.scale * kLog2e;
   p.wait_limit = s.wait_limit;
+  p.stall = s.stall;
   const int nkb_max = (s.Nk + kTileN - 1) / kTileN;  // packed batches: the longest sequence
   if (use_persistent_dkv(s, kv_tmem)) {
     using CP = DkvPCfg<D>;

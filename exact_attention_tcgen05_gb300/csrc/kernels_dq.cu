@@ -110,6 +110,7 @@ static cudaError_t launch_dq_t(const Maps& m, const Shape& s, const void* q,
   p.scale = s.scale;
   p.scale_log2 = s.scale * kLog2e;
   p.wait_limit = s.wait_limit;
+  p.stall = s.stall;
   const int nb_max = (s.N + kTileM - 1) / kTileM;  // packed batches: the longest sequence
   if (use_persistent_dq(s)) {
     using CP = DqPCfg<D>;

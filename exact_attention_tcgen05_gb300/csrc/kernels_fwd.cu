@@ -199,6 +199,7 @@ static cudaError_t launch_fwd_t(const Maps& m, const Shape& s, void* o, float* l
   p.causal = s.causal ? 1 : 0;
   p.scale_log2 = s.scale * kLog2e;
   p.wait_limit = s.wait_limit;
+  p.stall = s.stall;
   p.vl = s.vl;
   // Packed batches: s.N is the longest query sequence; blocks past a sequence's end are
   // skipped.
@@ -286,6 +287,7 @@ static cudaError_t launch_fwd_wide(const Maps& m, const Shape& s, const void* q,
   p.causal = s.causal ? 1 : 0;
   p.scale_log2 = s.scale * kLog2e;
   p.wait_limit = s.wait_limit;
+  p.stall = s.stall;
   p.vl = s.vl;
   const int nqb_max = (s.N + kTileM - 1) / kTileM;
   if (use_persistent_fwd(s)) {

@@ -39,6 +39,7 @@ struct Shape {
   bool bf16, causal;
   float scale;
   unsigned long long wait_limit;  // SM cycles one pipeline wait may take
+  int stall = 0;  // failure tests: each kernel's copies are withheld (ATTN_TEST_STALL = 1)
   Varlen vl;     // packed variable-length batch; vl.cu_q == nullptr for dense tensors
   // Packed batches: HOST copies of vl.cu_q / vl.cu_k ([vl_b + 1] each), or null. Used only
   // to order the persistent kernels' work items (schedule.h); the kernels read the device
@@ -84,6 +85,7 @@ struct DecodeShape {
   bool bf16;
   float scale;
   unsigned long long wait_limit;
+  int stall = 0;
 };
 // Resident CTAs of the decode partial kernel per SM (its shared-memory footprint).
 constexpr int kDecodeCtasPerSmPublic = 3;

@@ -99,7 +99,7 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
 }
 
 // Bounded waits with cluster-scope acquire, for barriers that receive arrivals from the
-// other CTA of the pair (as mbar_poll / mbar_wait otherwise).
+// other CTA of the pair (as mbar_wait otherwise).
 __device__ __forceinline__ bool mbar_poll_cluster(uint64_t* bar, uint32_t parity,
                                                   uint64_t limit, volatile int* abort,
                                                   int where) {

@@ -62,6 +62,9 @@
  *                                    sharing each K/V block through tcgen05 MMAs with
  *                                    cta_group::2); off by default, since on the
  *                                    measured shapes it is slower.
+ *            For failure tests only: ATTN_TEST_STALL = 1 makes every kernel withhold
+ *            its copies, so that its waits run out after ATTN_WAIT_LIMIT_CYCLES and
+ *            every call reports ATTN_ERR_TIMEOUT (no results are computed).
  */
 #ifndef ATTN_H
 #define ATTN_H
