@@ -7,8 +7,8 @@ wait on never complete, so their waits run out after the pipeline limit
 record the site of the first wait that gave up, let the products it issued finish (those
 drain waits have their own, fixed bound), release its memory and return. The test checks
 that attn_last_kernel_status reports ATTN_ERR_TIMEOUT with a site code of the right
-kernel after each call, for the one-CTA-per-item, persistent, CTA-pair, 256-column and
-decode kernels, and that the CUDA context is still usable afterwards.
+kernel after each call, for the one-CTA-per-item, persistent, CTA-pair, 256-column,
+packed-batch and decode kernels, and that the CUDA context is still usable afterwards.
 
 A second check runs the kernels with the limit cut to 64 cycles and nothing withheld. The
 waits suspend, and the hardware may hold a suspended wait until its phase completes, so a
@@ -49,6 +49,14 @@ out["dq"] = binding.attn_last_kernel_status()
 qd = I.make_tensor(I.custom(1, 2, 1, d, "bf16", False, seed=4), "q").cuda()
 binding.attn_decode(qd, k, v, num_splits=2)
 out["decode"] = binding.attn_last_kernel_status()
+# a packed batch of two sequences (the PACKED instantiations), host offsets given
+cu = torch.tensor([0, 300, 768], dtype=torch.int32)
+pq, pk, pv, pdo = (x[0].transpose(0, 1).contiguous() for x in (q, k, v, do))
+po, plse = binding.attn_fwd_varlen(pq, pk, pv, cu, cu, 468, 468, causal=True, scale=w.scale)
+out["fwd_varlen"] = binding.attn_last_kernel_status()
+binding.attn_bwd_varlen(pq, pk, pv, po, plse, pdo, cu, cu, 468, 468, causal=True,
+                        scale=w.scale)
+out["bwd_varlen"] = binding.attn_last_kernel_status()
 torch.cuda.synchronize()
 out["after"] = int(torch.arange(10, device="cuda").sum().item())
 print(json.dumps(out))
@@ -57,7 +65,10 @@ print(json.dumps(out))
 # The site codes of each kernel's waits (kernel * 16 + site, csrc/common.cuh); the dK/dV
 # passes of the 256-column backward report the dK/dV kernel's codes.
 SITE_RANGE = {"fwd": (0x11, 0x1F), "dq": (0x21, 0x2F), "dkv": (0x31, 0x3F),
-              "decode": (0x41, 0x4F)}
+              "decode": (0x41, 0x4F), "fwd_varlen": (0x11, 0x1F),
+              # the packed backward runs D (no waits), then dK/dV, then dQ: the status
+              # word keeps the first wait that ran out, the dK/dV or the dQ kernel's
+              "bwd_varlen": (0x21, 0x3F)}
 
 
 def run_child(d, **env_over):
